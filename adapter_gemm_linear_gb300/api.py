@@ -1,0 +1,247 @@
+"""PyTorch-facing binding of the C ABI: tensors in, pointers out.
+
+Every function here only marshals arguments: torch allocates device memory
+and provides the stream, the C library (liblora.so) does all the work.
+Names follow include/lora.h without the ``lora_`` prefix.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import LORA_BLOCK_ROWS, LORA_BF16, LORA_FP32, STATUS_NAMES
+
+_TORCH_DTYPE = {LORA_BF16: torch.bfloat16, LORA_FP32: torch.float32}
+_LORA_DTYPE = {torch.bfloat16: LORA_BF16, torch.float32: LORA_FP32}
+
+
+class LoraError(RuntimeError):
+    """A C-ABI call returned a status other than LORA_OK."""
+
+    def __init__(self, status: int, what: str):
+        self.status = int(status)
+        self.name = STATUS_NAMES.get(self.status, str(status))
+        msg = _lib.lib().lora_status_string(self.status).decode()
+        super().__init__(f"{what}: {self.name} ({msg})")
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise LoraError(status, what)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def lora_dtype(dtype: torch.dtype) -> int:
+    if dtype not in _LORA_DTYPE:
+        raise TypeError(f"unsupported dtype {dtype}; use torch.bfloat16 or torch.float32")
+    return _LORA_DTYPE[dtype]
+
+
+def status_string(status: int) -> str:
+    return _lib.lib().lora_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(_lib.lib().lora_abi_version())
+
+
+def pool_slot_bytes(K: int, N: int, rank: int, dtype: torch.dtype = torch.bfloat16) -> int:
+    return int(_lib.lib().lora_pool_slot_bytes(K, N, rank, lora_dtype(dtype)))
+
+
+def pool_arena_bytes(K: int, N: int, num_blocks: int, dtype: torch.dtype = torch.bfloat16) -> int:
+    return int(_lib.lib().lora_pool_arena_bytes(K, N, num_blocks, lora_dtype(dtype)))
+
+
+class LoraPool:
+    """One projection's paged adapter pool (lora_pool_create & co.).
+
+    Device memory (two arenas of ``num_blocks`` 16-row blocks, the block
+    table, ranks and scales) is allocated here with torch and handed to the
+    library, which keeps only host metadata.
+    """
+
+    def __init__(self, K: int, N: int, max_slots: int, max_rank: int, num_blocks: int,
+                 dtype: torch.dtype = torch.bfloat16, device=None, free_list_seed: int = 0,
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.device = torch.device(device if device is not None else "cuda")
+        self.dtype = dtype
+        self.K, self.N = int(K), int(N)
+        self.max_slots, self.max_rank, self.num_blocks = int(max_slots), int(max_rank), int(num_blocks)
+        bps = max(1, self.max_rank // LORA_BLOCK_ROWS)
+        self.a_arena = torch.empty((num_blocks, LORA_BLOCK_ROWS, K), dtype=dtype, device=self.device)
+        self.bt_arena = torch.empty((num_blocks, LORA_BLOCK_ROWS, N), dtype=dtype, device=self.device)
+        self.block_table = torch.empty((max_slots, bps), dtype=torch.int32, device=self.device)
+        self.ranks = torch.empty((max_slots,), dtype=torch.int32, device=self.device)
+        self.scales = torch.empty((max_slots,), dtype=torch.float32, device=self.device)
+        desc = _lib.PoolDesc(
+            lora_dtype(dtype), self.K, self.N, self.max_slots, self.max_rank, self.num_blocks,
+            _ptr(self.a_arena), _ptr(self.bt_arena), _ptr(self.block_table), _ptr(self.ranks),
+            _ptr(self.scales), int(free_list_seed))
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _check(_lib.lib().lora_pool_create(ctypes.byref(desc), _stream_handle(stream),
+                                               ctypes.byref(handle)), "lora_pool_create")
+        self._handle = handle
+
+    @property
+    def handle(self) -> int:
+        if self._handle is None:
+            raise RuntimeError("pool is closed")
+        return self._handle.value
+
+    def load(self, slot: int, A: torch.Tensor, B: torch.Tensor, alpha: float,
+             stream: Optional[torch.cuda.Stream] = None) -> None:
+        """lora_pool_load_slot: A [r, K], B [N, r] in the pool dtype, on the
+        host or on this pool's device."""
+        r = int(A.shape[0])
+        if A.shape != (r, self.K) or B.shape != (self.N, r):
+            raise ValueError(f"A {tuple(A.shape)} / B {tuple(B.shape)} do not match K={self.K}, N={self.N}")
+        A = A.to(self.dtype).contiguous()
+        B = B.to(self.dtype).contiguous()
+        on_dev = A.is_cuda
+        if on_dev != B.is_cuda:
+            raise ValueError("A and B must both be on the host or both on the device")
+        with torch.cuda.device(self.device):
+            st = stream if stream is not None else torch.cuda.current_stream()
+            _check(_lib.lib().lora_pool_load_slot(self.handle, int(slot), r, float(alpha), _ptr(A), _ptr(B),
+                                                  1 if on_dev else 0, int(st.cuda_stream)),
+                   f"lora_pool_load_slot(slot={slot}, rank={r})")
+            if on_dev:
+                A.record_stream(st)
+                B.record_stream(st)
+
+    def unload(self, slot: int, stream: Optional[torch.cuda.Stream] = None) -> None:
+        with torch.cuda.device(self.device):
+            _check(_lib.lib().lora_pool_unload_slot(self.handle, int(slot), _stream_handle(stream)),
+                   f"lora_pool_unload_slot(slot={slot})")
+
+    def slot_info(self, slot: int) -> Tuple[int, float, List[int]]:
+        r = ctypes.c_int32()
+        s = ctypes.c_float()
+        blocks = (ctypes.c_int32 * self.block_table.shape[1])()
+        _check(_lib.lib().lora_pool_slot_info(self.handle, int(slot), ctypes.byref(r), ctypes.byref(s),
+                                              blocks), "lora_pool_slot_info")
+        return int(r.value), float(s.value), list(blocks)
+
+    @property
+    def free_blocks(self) -> int:
+        return int(_lib.lib().lora_pool_free_blocks(self.handle))
+
+    def close(self) -> None:
+        if getattr(self, "_handle", None) is not None:
+            _lib.lib().lora_pool_destroy(self._handle.value)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def segment_rows(ids, num_slots: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """lora_segment_rows on host ids -> (perm, seg_offsets, seg_adapter)."""
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    M = int(ids.size)
+    perm = np.empty(max(M, 1), np.int32)
+    offs = np.empty(M + 1, np.int32)
+    adp = np.empty(max(M, 1), np.int32)
+    n = ctypes.c_int32()
+    _check(_lib.lib().lora_segment_rows(ids.ctypes.data if M else None, M, int(num_slots),
+                                        perm.ctypes.data, offs.ctypes.data, adp.ctypes.data,
+                                        ctypes.byref(n)), "lora_segment_rows")
+    S = int(n.value)
+    return perm[:M].copy(), offs[:S + 1].copy(), adp[:S].copy()
+
+
+class LinearCall:
+    """Prepared arguments of one lora_linear_forward call.
+
+    Building the ctypes argument block once and re-issuing it keeps the
+    per-call host cost to one foreign call; the tensors passed in must stay
+    alive (this object holds references to them).
+    """
+
+    def __init__(self, x: torch.Tensor, projections: Sequence[Tuple[torch.Tensor, LoraPool, torch.Tensor]],
+                 row_adapter: Optional[torch.Tensor] = None,
+                 seg_offsets: Optional[torch.Tensor] = None, seg_adapter: Optional[torch.Tensor] = None,
+                 perm: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+        if x.dim() != 2 or x.stride(1) != 1:
+            raise ValueError("x must be a row-major 2-D tensor")
+        if (row_adapter is None) == (seg_offsets is None and seg_adapter is None):
+            if row_adapter is not None or x.shape[0] > 0:
+                raise ValueError("give either row_adapter or (seg_offsets, seg_adapter)")
+        dt = lora_dtype(x.dtype)
+        self._keep = [x, row_adapter, seg_offsets, seg_adapter, perm]
+        projs = (_lib.Proj * len(projections))()
+        for i, (W, pool, out) in enumerate(projections):
+            if out.dim() != 2 or out.stride(1) != 1:
+                raise ValueError("out must be a row-major 2-D tensor")
+            projs[i] = _lib.Proj(_ptr(W), pool.handle, _ptr(out), int(out.stride(0)))
+            self._keep += [W, pool, out]
+        self._projs = projs
+        for t in (row_adapter, seg_offsets, seg_adapter, perm):
+            if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+                raise ValueError("index tensors must be contiguous int32")
+        num_segs = 0 if seg_adapter is None else int(seg_adapter.numel())
+        self.args = _lib.ForwardArgs(
+            dt, int(x.shape[0]), int(x.shape[1]), _ptr(x), int(x.stride(0)), len(projections),
+            ctypes.cast(projs, ctypes.POINTER(_lib.Proj)), _ptr(row_adapter), _ptr(seg_offsets),
+            _ptr(seg_adapter), _ptr(perm), num_segs, None, 0)
+        need = int(_lib.lib().lora_forward_workspace_bytes(ctypes.byref(self.args)))
+        if need == 0:
+            # the arguments failed validation: the forward reports why (it
+            # validates before touching the device, so nothing is launched)
+            st = _lib.lib().lora_linear_forward(ctypes.byref(self.args), None)
+            raise LoraError(st if st else 1, "lora_linear_forward")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        if workspace.numel() * workspace.element_size() < need:
+            raise LoraError(12, f"workspace has {workspace.numel()} bytes, needs {need}")
+        self.workspace = workspace
+        self.workspace_bytes = need
+        self.args.workspace = _ptr(workspace)
+        self.args.workspace_bytes = workspace.numel() * workspace.element_size()
+        self.device = x.device
+        self._fn = _lib.lib().lora_linear_forward
+        self._argref = ctypes.byref(self.args)
+
+    def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        st = self._fn(self._argref, _stream_handle(stream))
+        if st != 0:
+            raise LoraError(st, "lora_linear_forward")
+
+
+def linear_forward(x: torch.Tensor, projections, row_adapter=None, seg_offsets=None,
+                   seg_adapter=None, perm=None, workspace=None,
+                   stream: Optional[torch.cuda.Stream] = None) -> None:
+    """lora_linear_forward: out_p = x W_p^T + per-row (alpha_i/r_i) B_i (A_i x).
+
+    ``projections`` is a sequence of (W [N, K], LoraPool, out [M, >=N]).
+    Rows reach adapters through ``row_adapter`` (device int32 [M], -1 = none)
+    or through sorted segments (``seg_offsets``, ``seg_adapter``, optional
+    ``perm``; device int32).
+    """
+    LinearCall(x, projections, row_adapter, seg_offsets, seg_adapter, perm, workspace)(stream)
+
+
+def device_status(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
+    """lora_get_device_status -> (status, detail); clears the word."""
+    d = ctypes.c_int32(0)
+    st = _lib.lib().lora_get_device_status(_stream_handle(stream), ctypes.byref(d))
+    return int(st), int(d.value)

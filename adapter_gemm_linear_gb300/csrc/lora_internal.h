@@ -1,0 +1,90 @@
+// Internal declarations shared by the host library and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "lora.h"
+
+// Host-side pool metadata.  Device state (table, ranks, scales, arenas) lives
+// in caller memory; the vectors here mirror it so that loads and unloads can
+// be validated without reading the device.
+struct lora_pool {
+    lora_pool_desc_t d;
+    int bps;                       // blocks per slot = max_rank / 16
+    int device;                    // CUDA device the pool was created on
+    std::vector<int32_t> free_list;  // stack: back() is handed out next
+    std::vector<int32_t> rank;       // [max_slots], 0 = empty
+    std::vector<float> scale;        // [max_slots]
+    std::vector<int32_t> table;      // [max_slots * bps], -1 = unused
+};
+
+namespace lora {
+
+constexpr int kMaxRankLimit = 1024;               // largest pool max_rank
+constexpr int kMaxBlocksPerSlot = kMaxRankLimit / LORA_BLOCK_ROWS;
+
+// Codes kernels record in the per-device status word (first error wins).
+enum DeviceError : uint32_t {
+    kDevOk = 0,
+    kDevBadAdapter = 1,   // id outside [-1, max_slots); detail = row
+    kDevEmptySlot = 2,    // row names a slot with rank 0; detail = row
+    kDevBadBlock = 3,     // table entry outside [0, num_blocks) or bad rank; detail = slot
+    kDevBadSegment = 4,   // segment offsets out of order / range, or perm row out of range
+    kDevTimeout = 5,      // a bounded mbarrier wait ran out; detail = kernel site
+};
+
+// Device address of this device's status word (a 64-bit word holding
+// code << 32 | detail).  Looked up once per device.
+cudaError_t device_status_ptr(unsigned long long **out);
+
+// Element size of a dtype.
+inline size_t dtype_bytes(lora_dtype_t t) { return t == LORA_FP32 ? 4 : 2; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Per-projection view handed to the kernel launchers.
+struct ProjView {
+    const void *W;
+    void *out;
+    int32_t N, ldo;
+    const void *a_arena, *bt_arena;
+    const int32_t *table;
+    const int32_t *ranks;
+    const float *scales;
+    int32_t max_slots, bps, num_blocks, max_rank;
+    float *V;              // workspace: [M][max_rank] fp32
+};
+
+struct ForwardPlan {
+    lora_dtype_t dtype;
+    int32_t M, K, ldx;
+    const void *x;
+    const int32_t *row_slot;  // per-row slot ids (device)
+    int n_proj;
+    ProjView proj[LORA_MAX_PROJ];
+    unsigned long long *status;
+};
+
+// Workspace layout of one forward call.
+struct WorkspaceLayout {
+    size_t row_slot_off;          // int32[M] (segment mode only)
+    size_t v_off[LORA_MAX_PROJ];  // fp32[M][max_rank]
+    size_t total;
+};
+
+// Launchers (lora_kernels.cu).
+cudaError_t launch_segments_to_rows(int32_t M, const int32_t *seg_offsets,
+                                    const int32_t *seg_adapter, const int32_t *perm,
+                                    int32_t num_segs, int32_t *row_slot,
+                                    unsigned long long *status, cudaStream_t stream);
+// Copy a device-resident adapter (A [rank][K], B [N][rank]) into the blocks
+// `blocks` (host array of ceil(rank/16) ids), transposing B into B^T rows and
+// zeroing the tail rows of the last block.
+cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32_t *blocks,
+                                const void *A, const void *B, cudaStream_t stream);
+cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream);
+
+}  // namespace lora

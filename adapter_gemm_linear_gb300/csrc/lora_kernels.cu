@@ -1,0 +1,303 @@
+// Device status word, row-map and pool-copy kernels, and the SIMT
+// (CUDA-core) forward path used for fp32 inputs.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "lora_internal.h"
+#include "lora_device.cuh"
+
+namespace lora {
+
+// ---------------------------------------------------------------------------
+// per-device status word
+// ---------------------------------------------------------------------------
+
+__device__ unsigned long long g_lora_status;
+
+cudaError_t device_status_ptr(unsigned long long **out) {
+    static std::mutex mu;
+    static unsigned long long *cache[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_lora_status);
+        if (e != cudaSuccess) return e;
+        cache[dev] = static_cast<unsigned long long *>(p);
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// segments -> per-row slot ids
+// ---------------------------------------------------------------------------
+
+__global__ void segments_to_rows_kernel(int32_t M, const int32_t *__restrict__ off,
+                                        const int32_t *__restrict__ seg_adapter,
+                                        const int32_t *__restrict__ perm, int32_t S,
+                                        int32_t *__restrict__ row_slot,
+                                        unsigned long long *status) {
+    const int32_t p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p <= S && p < S + 1) {
+        // offsets must be non-decreasing within [0, M]
+        const int32_t o = off[p];
+        const bool bad = o < 0 || o > M || (p > 0 && off[p - 1] > o);
+        if (bad) record_error(status, kDevBadSegment, static_cast<uint32_t>(p));
+    }
+    if (p >= M) return;
+    // last segment s with off[s] <= p
+    int32_t lo = 0, hi = S;  // search in [0, S]
+    if (off[0] > p) return;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= p) lo = mid; else hi = mid - 1;
+    }
+    const int32_t s = lo;
+    if (s >= S || p >= off[s + 1]) return;
+    const int32_t row = perm ? perm[p] : p;
+    if (row < 0 || row >= M) {
+        record_error(status, kDevBadSegment, static_cast<uint32_t>(p));
+        return;
+    }
+    row_slot[row] = seg_adapter[s];
+}
+
+cudaError_t launch_segments_to_rows(int32_t M, const int32_t *seg_offsets,
+                                    const int32_t *seg_adapter, const int32_t *perm,
+                                    int32_t num_segs, int32_t *row_slot,
+                                    unsigned long long *status, cudaStream_t stream) {
+    const int32_t n = (M > num_segs + 1 ? M : num_segs + 1);
+    const int threads = 256;
+    segments_to_rows_kernel<<<(n + threads - 1) / threads, threads, 0, stream>>>(
+        M, seg_offsets, seg_adapter, perm, num_segs, row_slot, status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// device-to-device adapter load: A rows and transposed B into pool blocks
+// ---------------------------------------------------------------------------
+
+struct ScatterBlocks {
+    int32_t b[kMaxBlocksPerSlot];
+};
+
+template <typename T>
+__global__ void pool_scatter_kernel(const T *__restrict__ A, const T *__restrict__ B, int32_t rank,
+                                    int32_t K, int32_t N, T *__restrict__ a_arena,
+                                    T *__restrict__ bt_arena, ScatterBlocks blocks) {
+    const int32_t t = blockIdx.y;
+    const int32_t row = blockIdx.z;
+    const int32_t j = t * LORA_BLOCK_ROWS + row;
+    const size_t b = static_cast<size_t>(blocks.b[t]);
+    T *a_dst = a_arena + (b * LORA_BLOCK_ROWS + row) * static_cast<size_t>(K);
+    T *bt_dst = bt_arena + (b * LORA_BLOCK_ROWS + row) * static_cast<size_t>(N);
+    const int32_t stride = gridDim.x * blockDim.x;
+    for (int32_t k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += stride)
+        a_dst[k] = j < rank ? A[static_cast<size_t>(j) * K + k] : from_float<T>(0.0f);
+    for (int32_t n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += stride)
+        bt_dst[n] = j < rank ? B[static_cast<size_t>(n) * rank + j] : from_float<T>(0.0f);
+}
+
+cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32_t *blocks,
+                                const void *A, const void *B, cudaStream_t stream) {
+    const int nb = (rank + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
+    ScatterBlocks sb;
+    for (int t = 0; t < kMaxBlocksPerSlot; ++t) sb.b[t] = t < nb ? blocks[t] : 0;
+    dim3 grid(8, nb, LORA_BLOCK_ROWS);
+    const lora_pool_desc_t &d = pool->d;
+    if (d.dtype == LORA_FP32)
+        pool_scatter_kernel<float><<<grid, 256, 0, stream>>>(
+            static_cast<const float *>(A), static_cast<const float *>(B), rank, d.K, d.N,
+            static_cast<float *>(d.a_arena), static_cast<float *>(d.bt_arena), sb);
+    else
+        pool_scatter_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), rank,
+            d.K, d.N, static_cast<__nv_bfloat16 *>(d.a_arena),
+            static_cast<__nv_bfloat16 *>(d.bt_arena), sb);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// SIMT shrink: V[m, 16t + j] = sum_k A_i[16t + j, k] x[m, k]
+// grid (M, blocks per slot), 128 threads; each CTA one row x one 16-row block
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(128)
+shrink_simt_kernel(const T *__restrict__ x, int32_t ldx, int32_t K, const int32_t *__restrict__ row_slot,
+                   const T *__restrict__ a_arena, const int32_t *__restrict__ table,
+                   const int32_t *__restrict__ ranks, int32_t max_slots, int32_t bps,
+                   int32_t num_blocks, float *__restrict__ V, int32_t ldv,
+                   unsigned long long *status) {
+    const int32_t m = blockIdx.x;
+    const int32_t t = blockIdx.y;
+    int32_t r;
+    float s;
+    const int32_t i = resolve_slot(row_slot[m], m, ranks, nullptr, max_slots, bps, &r, &s, status,
+                                   t == 0 && threadIdx.x == 0);
+    if (i < 0 || t * LORA_BLOCK_ROWS >= r) return;
+    const int32_t b = table[i * bps + t];
+    if (b < 0 || b >= num_blocks) {
+        if (threadIdx.x == 0) record_error(status, kDevBadBlock, static_cast<uint32_t>(i));
+        return;
+    }
+    constexpr int VE = VecTraits<T>::kElems;
+    const T *A = a_arena + static_cast<size_t>(b) * LORA_BLOCK_ROWS * K;
+    const T *xr = x + static_cast<size_t>(m) * ldx;
+    float acc[LORA_BLOCK_ROWS];
+#pragma unroll
+    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = 0.0f;
+    for (int32_t k = threadIdx.x * VE; k < K; k += blockDim.x * VE) {
+        float xv[VE];
+        VecTraits<T>::load(xr + k, xv);
+#pragma unroll
+        for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
+            float av[VE];
+            VecTraits<T>::load(A + static_cast<size_t>(j) * K + k, av);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) acc[j] = fmaf(av[e], xv[e], acc[j]);
+        }
+    }
+    __shared__ float red[4][LORA_BLOCK_ROWS];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
+        float v = acc[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[warp][j] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < LORA_BLOCK_ROWS) {
+        const float v = red[0][threadIdx.x] + red[1][threadIdx.x] + red[2][threadIdx.x] +
+                        red[3][threadIdx.x];
+        V[static_cast<size_t>(m) * ldv + t * LORA_BLOCK_ROWS + threadIdx.x] = v;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// SIMT GEMM with the expand fused into the epilogue:
+// out[m, n] = sum_k x[m,k] W[n,k] + s_i * sum_j Bt_i[j, n] V[m, j]
+// 64x64 tile, 256 threads, 4x4 outputs per thread (rows ty+16a, cols tx+16b)
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+gemm_lora_simt_kernel(const T *__restrict__ x, int32_t ldx, const T *__restrict__ W, int32_t M,
+                      int32_t N, int32_t K, T *__restrict__ out, int32_t ldo,
+                      const int32_t *__restrict__ row_slot, const T *__restrict__ bt_arena,
+                      const int32_t *__restrict__ table, const int32_t *__restrict__ ranks,
+                      const float *__restrict__ scales, int32_t max_slots, int32_t bps,
+                      int32_t num_blocks, const float *__restrict__ V, int32_t ldv,
+                      unsigned long long *status) {
+    constexpr int BM = 64, BN = 64, BK = 16;
+    __shared__ float xs[BK][BM + 4];
+    __shared__ float wsm[BK][BN + 4];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int32_t m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] = 0.0f;
+
+    const int lr = threadIdx.x >> 2;        // 0..63: tile row loaded by this thread
+    const int lk = (threadIdx.x & 3) * 4;   // 0,4,8,12: first k of its 4
+    for (int32_t k0 = 0; k0 < K; k0 += BK) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int32_t k = k0 + lk + e;
+            const int32_t m = m0 + lr, n = n0 + lr;
+            xs[lk + e][lr] = (m < M && k < K) ? to_float(x[static_cast<size_t>(m) * ldx + k]) : 0.0f;
+            wsm[lk + e][lr] = (n < N && k < K) ? to_float(W[static_cast<size_t>(n) * K + k]) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) av[a] = xs[kk][ty + 16 * a];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) bv[c] = wsm[kk][tx + 16 * c];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(av[a], bv[c], acc[a][c]);
+        }
+        __syncthreads();
+    }
+
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int32_t m = m0 + ty + 16 * a;
+        if (m >= M) continue;
+        int32_t r;
+        float s;
+        const int32_t i = resolve_slot(row_slot[m], m, ranks, scales, max_slots, bps, &r, &s,
+                                       status, false);
+        float lo[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (i >= 0) {
+            const float *vr = V + static_cast<size_t>(m) * ldv;
+            for (int32_t j = 0; j < r; ++j) {
+                const int32_t b = table[i * bps + (j >> 4)];
+                if (b < 0 || b >= num_blocks) {
+                    record_error(status, kDevBadBlock, static_cast<uint32_t>(i));
+                    lo[0] = lo[1] = lo[2] = lo[3] = 0.0f;
+                    s = 0.0f;
+                    break;
+                }
+                const T *btr = bt_arena + (static_cast<size_t>(b) * LORA_BLOCK_ROWS + (j & 15)) * N;
+                const float v = vr[j];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int32_t n = n0 + tx + 16 * c;
+                    if (n < N) lo[c] = fmaf(to_float(btr[n]), v, lo[c]);
+                }
+            }
+        } else {
+            s = 0.0f;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int32_t n = n0 + tx + 16 * c;
+            if (n < N) out[static_cast<size_t>(m) * ldo + n] = from_float<T>(fmaf(s, lo[c], acc[a][c]));
+        }
+    }
+}
+
+template <typename T>
+static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t stream) {
+    for (int p = 0; p < plan.n_proj; ++p) {
+        const ProjView &v = plan.proj[p];
+        dim3 sgrid(plan.M, v.bps);
+        shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
+            static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
+            static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
+            v.V, v.max_rank, plan.status);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        dim3 ggrid((v.N + 63) / 64, (plan.M + 63) / 64);
+        gemm_lora_simt_kernel<T><<<ggrid, 256, 0, stream>>>(
+            static_cast<const T *>(plan.x), plan.ldx, static_cast<const T *>(v.W), plan.M, v.N,
+            plan.K, static_cast<T *>(v.out), v.ldo, plan.row_slot,
+            static_cast<const T *>(v.bt_arena), v.table, v.ranks, v.scales, v.max_slots, v.bps,
+            v.num_blocks, v.V, v.max_rank, plan.status);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream) {
+    if (plan.dtype == LORA_FP32) return launch_forward_simt<float>(plan, stream);
+    return launch_forward_simt<__nv_bfloat16>(plan, stream);
+}
+
+}  // namespace lora

@@ -1,0 +1,199 @@
+"""GPU parity: lora_linear_forward (through the C ABI) against the float64
+oracle on the same seeded inputs.
+
+Small cases span several output tiles with ragged tails in M, N and K; the
+five named workloads run at full size with the oracle evaluated on every row
+(small ones) or on sampled rows (large ones).  Integer-valued cases must be
+bit-exact; mutation cases check that the tolerance is not vacuous.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import lora_harness as H
+from workloads import make_config, synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _sample_rows(wl, n=48, seed=0):
+    """Rows to check at full size: both ends, segment boundaries, base-only
+    rows, and a seeded random sample."""
+    rng = np.random.default_rng(seed)
+    rows = {0, wl.M - 1}
+    if wl.seg_offsets is not None:
+        for o in wl.seg_offsets[1:-1]:
+            rows.update({int(o) - 1, int(o)})
+    base = np.nonzero(wl.row_adapter < 0)[0]
+    rows.update(int(r) for r in base[:4])
+    rows.update(int(r) for r in rng.choice(wl.M, size=min(n, wl.M), replace=False))
+    return np.array(sorted(r for r in rows if 0 <= r < wl.M), dtype=np.int64)
+
+
+@pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
+@pytest.mark.parametrize("shape", [(300, 520, 392), (130, 1024, 264), (1, 64, 8), (257, 136, 1000)])
+def test_small_mixed_ranks(shape, mode):
+    M, K, N = shape
+    wl = synth(M=M, K=K, Ns=[N], num_slots=7, rank_choices=(1, 7, 16, 33, 64), seed=M + K + N)
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, mode)[0]
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0), f"{shape} {mode}")
+
+
+def test_presorted_segments_without_perm():
+    wl = synth(M=333, K=256, Ns=[200], num_slots=9, rank_choices=(8, 16, 48), mode="sgmv", seed=5)
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, "sorted")[0]
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0), "sorted")
+
+
+@pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
+def test_integer_exact_bitwise(mode):
+    """Small-integer inputs with scale 2: every partial sum is an exact
+    integer, so the bf16 output bits must equal the oracle's rounded bits.
+    Mixed ranks up to 128 in shuffled pool blocks pin the block-table gather
+    and the row->adapter indexing exactly."""
+    wl = synth(M=200, K=256, Ns=[136, 64], num_slots=11, rank_choices=(1, 8, 16, 17, 64, 128),
+               integer=True, seed=21, none_frac=0.15)
+    pools = H.make_pools(wl, DEV, extra_blocks=13)
+    outs = H.forward(wl, pools, mode)
+    for p in range(2):
+        want = H.oracle_bf16_bits(H.oracle_rows(wl, p))
+        got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), f"projection {p}: {np.sum(got != want)} outputs differ"
+
+
+def test_tiny_fp32_full():
+    wl = make_config("tiny_fp32")
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, "bgmv")[0]
+    H.assert_close("fp32", out, H.oracle_rows(wl, 0), "tiny_fp32")
+
+
+def test_decode_bgmv_full():
+    wl = make_config("decode_bgmv")
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, "bgmv")[0]
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0), "decode_bgmv")
+
+
+def test_prefill_sgmv_sampled():
+    wl = make_config("prefill_sgmv")
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, "sorted")[0]
+    rows = _sample_rows(wl)
+    H.assert_close("bf16", out[rows], H.oracle_rows(wl, 0, rows), "prefill_sgmv")
+    assert not np.isnan(out).any()
+
+
+def test_decode_70b_qv_sampled():
+    wl = make_config("decode_70b_qv")
+    pools = H.make_pools(wl, DEV)
+    outs = H.forward(wl, pools, "bgmv")
+    rows = _sample_rows(wl, n=64)
+    for p in range(2):
+        H.assert_close("bf16", outs[p][rows], H.oracle_rows(wl, p, rows), f"decode_70b_qv p{p}")
+        assert not np.isnan(outs[p]).any()
+
+
+def test_slora_mixed_sampled():
+    wl = make_config("slora_mixed")
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, "bgmv")[0]
+    rows = _sample_rows(wl, n=64)
+    H.assert_close("bf16", out[rows], H.oracle_rows(wl, 0, rows), "slora_mixed")
+    assert not np.isnan(out).any()
+
+
+@pytest.mark.parametrize("cfg", ["tiny_fp32", "decode_bgmv", "slora_mixed"])
+def test_mutations_fail_tolerance(cfg):
+    """Outputs computed with a wrong assignment or scale must fail the
+    tolerance against the true oracle: (i) every id forced to -1, (ii) ids
+    rotated to another slot, (iii) every scale halved."""
+    wl = make_config(cfg)
+    rows = _sample_rows(wl, n=32) if wl.M > 64 else np.arange(wl.M)
+    ref = H.oracle_rows(wl, 0, rows)
+    ids = wl.row_adapter
+    none = np.full_like(ids, -1)
+    used = wl.used_slots
+    rot = ids.copy()
+    for k, s in enumerate(used):
+        rot[ids == s] = used[(k + 1) % used.size]
+    pools = H.make_pools(wl, DEV)
+    out_none = H.forward(wl, pools, "bgmv", ids=none)[0]
+    out_rot = H.forward(wl, pools, "bgmv", ids=rot)[0]
+    half = H.make_pools(wl, DEV, alpha_scale=0.5)
+    out_half = H.forward(wl, half, "bgmv")[0]
+    for name, out in (("none", out_none), ("rotated", out_rot), ("half scale", out_half)):
+        assert H.fails_tolerance(wl.dtype, out[rows], ref), f"{cfg}: mutation '{name}' passed"
+
+
+def test_base_only_and_empty():
+    wl = synth(M=96, K=128, Ns=[72], num_slots=3, seed=9)
+    pools = H.make_pools(wl, DEV)
+    none = np.full(wl.M, -1, np.int32)
+    out = H.forward(wl, pools, "bgmv", ids=none)[0]
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0, ids=none), "all base-only")
+    # M = 0 is a no-op
+    wl0 = synth(M=0, K=128, Ns=[72], num_slots=3, seed=9)
+    assert H.forward(wl0, pools, "bgmv")[0].shape == (0, 72)
+
+
+def test_device_source_load_matches_host_load():
+    wl = synth(M=64, K=192, Ns=[96], num_slots=5, rank_choices=(3, 16, 40), seed=13)
+    ph = H.make_pools(wl, DEV, src="host")[0]
+    pd = H.make_pools(wl, DEV, src="device")[0]
+    torch.cuda.synchronize()
+    for s in wl.used_slots:
+        rh, sh, bh = ph.slot_info(int(s))
+        rd, sd, bd = pd.slot_info(int(s))
+        assert (rh, sh, bh) == (rd, sd, bd)
+        A, B = wl.adapter(0, int(s))
+        r = int(wl.ranks[s])
+        for t in range(-(-r // 16)):
+            rows = min(16, r - 16 * t)
+            for pool in (ph, pd):
+                blk = pool.a_arena[bh[t]].float().cpu().numpy()
+                assert np.array_equal(blk[:rows], A[16 * t:16 * t + rows])
+                assert not blk[rows:].any()
+                blt = pool.bt_arena[bh[t]].float().cpu().numpy()
+                assert np.array_equal(blt[:rows], B.T[16 * t:16 * t + rows])
+                assert not blt[rows:].any()
+
+
+def test_unload_reload_and_errors():
+    from adapter_gemm_linear_gb300 import LoraError, device_status
+    wl = synth(M=40, K=64, Ns=[48], num_slots=4, rank_choices=(16, 32), seed=17, none_frac=0.0)
+    pool = H.make_pools(wl, DEV, slots=range(4))[0]
+    free0 = pool.free_blocks
+    r2 = pool.slot_info(2)[0]
+    pool.unload(2)
+    assert pool.free_blocks == free0 + -(-r2 // 16)
+    with pytest.raises(LoraError):
+        pool.unload(2)
+    # a row that names the empty slot gets no correction and is reported
+    device_status()
+    ids = wl.row_adapter.copy()
+    out = H.forward(wl, [pool], "bgmv", ids=ids)[0]
+    st, detail = device_status()
+    assert (st != 0) == bool((ids == 2).any())
+    ids_ref = np.where(ids == 2, -1, ids)
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0, ids=ids_ref), "empty slot rows -> base")
+    # out-of-range id
+    bad = ids_ref.copy()
+    bad[5] = 99
+    out = H.forward(wl, [pool], "bgmv", ids=bad)[0]
+    st, detail = device_status()
+    assert st == 7 and detail == 5
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0, ids=np.where(bad == 99, -1, bad)), "bad id")
+    # reload
+    A, B = wl.adapter(0, 2)
+    pool.load(2, torch.from_numpy(A).to(torch.bfloat16), torch.from_numpy(B).to(torch.bfloat16),
+              float(wl.alphas[2]))
+    assert pool.free_blocks == free0
+    out = H.forward(wl, [pool], "bgmv")[0]
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0), "after reload")
+    assert device_status()[0] == 0
