@@ -181,7 +181,7 @@ class LinearCall:
                  row_adapter: Optional[torch.Tensor] = None,
                  seg_offsets: Optional[torch.Tensor] = None, seg_adapter: Optional[torch.Tensor] = None,
                  perm: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
-        if x.dim() != 2 or x.stride(1) != 1:
+        if x.dim() != 2 or (x.numel() > 0 and x.stride(1) != 1):
             raise ValueError("x must be a row-major 2-D tensor")
         if (row_adapter is None) == (seg_offsets is None and seg_adapter is None):
             if row_adapter is not None or x.shape[0] > 0:
@@ -190,17 +190,19 @@ class LinearCall:
         self._keep = [x, row_adapter, seg_offsets, seg_adapter, perm]
         projs = (_lib.Proj * len(projections))()
         for i, (W, pool, out) in enumerate(projections):
-            if out.dim() != 2 or out.stride(1) != 1:
+            if out.dim() != 2 or (out.numel() > 0 and out.stride(1) != 1):
                 raise ValueError("out must be a row-major 2-D tensor")
-            projs[i] = _lib.Proj(_ptr(W), pool.handle, _ptr(out), int(out.stride(0)))
+            ldo = int(out.stride(0)) if out.numel() > 0 else int(out.shape[1])
+            projs[i] = _lib.Proj(_ptr(W), pool.handle, _ptr(out), ldo)
             self._keep += [W, pool, out]
         self._projs = projs
         for t in (row_adapter, seg_offsets, seg_adapter, perm):
             if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
                 raise ValueError("index tensors must be contiguous int32")
         num_segs = 0 if seg_adapter is None else int(seg_adapter.numel())
+        ldx = int(x.stride(0)) if x.numel() > 0 else int(x.shape[1])
         self.args = _lib.ForwardArgs(
-            dt, int(x.shape[0]), int(x.shape[1]), _ptr(x), int(x.stride(0)), len(projections),
+            dt, int(x.shape[0]), int(x.shape[1]), _ptr(x), ldx, len(projections),
             ctypes.cast(projs, ctypes.POINTER(_lib.Proj)), _ptr(row_adapter), _ptr(seg_offsets),
             _ptr(seg_adapter), _ptr(perm), num_segs, None, 0)
         need = int(_lib.lib().lora_forward_workspace_bytes(ctypes.byref(self.args)))

@@ -87,4 +87,8 @@ cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32
                                 const void *A, const void *B, cudaStream_t stream);
 cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream);
 
+// Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
+cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+int choose_tc_bn(int32_t M, int32_t N);
+
 }  // namespace lora

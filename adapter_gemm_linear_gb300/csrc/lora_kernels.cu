@@ -295,9 +295,27 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
     return cudaSuccess;
 }
 
+// bf16: CUDA-core shrink, then the tensor-core GEMM with the fused expand.
+static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t stream) {
+    using T = __nv_bfloat16;
+    for (int p = 0; p < plan.n_proj; ++p) {
+        const ProjView &v = plan.proj[p];
+        dim3 sgrid(plan.M, v.bps);
+        shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
+            static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
+            static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
+            v.V, v.max_rank, plan.status);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        e = launch_gemm_lora_tc(plan, v, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream) {
     if (plan.dtype == LORA_FP32) return launch_forward_simt<float>(plan, stream);
-    return launch_forward_simt<__nv_bfloat16>(plan, stream);
+    return launch_forward_tc(plan, stream);
 }
 
 }  // namespace lora
