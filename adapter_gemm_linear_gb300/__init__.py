@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     LoraPool,
     abi_version,
     device_status,
+    kernel_launches,
     linear_forward,
     pool_arena_bytes,
     pool_slot_bytes,

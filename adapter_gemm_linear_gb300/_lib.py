@@ -79,6 +79,8 @@ class ForwardArgs(ctypes.Structure):
         ("num_segs", ctypes.c_int32),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("stage_events", ctypes.POINTER(ctypes.c_void_p)),
+        ("num_stage_events", ctypes.c_int32),
     ]
 
 
@@ -108,6 +110,7 @@ SIGNATURES = [
     ("lora_get_device_status", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("lora_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("lora_abi_version", ctypes.c_int32, []),
+    ("lora_kernel_launches", ctypes.c_uint64, []),
 ]
 
 _lock = threading.Lock()

@@ -204,7 +204,8 @@ class LinearCall:
         self.args = _lib.ForwardArgs(
             dt, int(x.shape[0]), int(x.shape[1]), _ptr(x), ldx, len(projections),
             ctypes.cast(projs, ctypes.POINTER(_lib.Proj)), _ptr(row_adapter), _ptr(seg_offsets),
-            _ptr(seg_adapter), _ptr(perm), num_segs, None, 0)
+            _ptr(seg_adapter), _ptr(perm), num_segs, None, 0, None, 0)
+        self.n_proj = len(projections)
         need = int(_lib.lib().lora_forward_workspace_bytes(ctypes.byref(self.args)))
         if need == 0:
             # the arguments failed validation: the forward reports why (it
@@ -223,10 +224,34 @@ class LinearCall:
         self._fn = _lib.lib().lora_linear_forward
         self._argref = ctypes.byref(self.args)
 
+    def set_stage_events(self, events: Optional[Sequence[torch.cuda.Event]]) -> None:
+        """Have the next calls record ``events`` (1 + 2*n_proj timing events)
+        at the stage boundaries on the launching stream; None turns it off."""
+        if events is None:
+            self._events = None
+            self.args.stage_events = None
+            self.args.num_stage_events = 0
+            return
+        if len(events) != 1 + 2 * self.n_proj:
+            raise ValueError(f"need {1 + 2 * self.n_proj} events")
+        handles = []
+        for ev in events:
+            if not ev.cuda_event:
+                ev.record()  # torch creates the event lazily on first record
+            handles.append(ev.cuda_event)
+        self._events = (events, (ctypes.c_void_p * len(handles))(*handles))
+        self.args.stage_events = ctypes.cast(self._events[1], ctypes.POINTER(ctypes.c_void_p))
+        self.args.num_stage_events = len(handles)
+
     def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> None:
         st = self._fn(self._argref, _stream_handle(stream))
         if st != 0:
             raise LoraError(st, "lora_linear_forward")
+
+
+def kernel_launches() -> int:
+    """lora_kernel_launches: kernels the library launched in this process."""
+    return int(_lib.lib().lora_kernel_launches())
 
 
 def linear_forward(x: torch.Tensor, projections, row_adapter=None, seg_offsets=None,

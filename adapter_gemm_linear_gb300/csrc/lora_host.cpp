@@ -6,10 +6,15 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <new>
 #include <vector>
 
 #include "lora_internal.h"
+
+static std::atomic<uint64_t> g_kernel_launches{0};
+
+void lora::count_launches(int n) { g_kernel_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
 using lora::align_up;
 using lora::dtype_bytes;
@@ -51,6 +56,8 @@ lora_status_t push_slot(lora_pool *p, int32_t slot, cudaStream_t st) {
 extern "C" {
 
 int32_t lora_abi_version(void) { return LORA_ABI_VERSION; }
+
+uint64_t lora_kernel_launches(void) { return g_kernel_launches.load(std::memory_order_relaxed); }
 
 const char *lora_status_string(lora_status_t s) {
     switch (s) {
@@ -307,6 +314,11 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
             if (a->seg_offsets || a->seg_adapter || a->num_segs) return LORA_ERR_INVALID_ARG;
         }
     }
+    if (a->num_stage_events != 0 &&
+        (a->num_stage_events != 1 + 2 * a->n_proj || !a->stage_events))
+        return LORA_ERR_INVALID_ARG;
+    if (a->num_stage_events == 0 && a->stage_events) return LORA_ERR_INVALID_ARG;
+    plan->stage_events = a->stage_events;
     plan->dtype = a->dtype;
     plan->M = a->M;
     plan->K = a->K;
@@ -372,6 +384,9 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
     if (lora::device_status_ptr(&plan.status) != cudaSuccess) return LORA_ERR_CUDA;
     for (int i = 0; i < plan.n_proj; ++i) plan.proj[i].V = reinterpret_cast<float *>(base + ws.v_off[i]);
     cudaStream_t st = as_stream(stream);
+    if (plan.stage_events &&
+        cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[0]), st) != cudaSuccess)
+        return LORA_ERR_CUDA;
     if (args->row_adapter) {
         if (!aligned16(args->row_adapter)) return LORA_ERR_ALIGNMENT;
         plan.row_slot = args->row_adapter;
@@ -379,10 +394,12 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
         int32_t *row_slot = reinterpret_cast<int32_t *>(base + ws.row_slot_off);
         if (cudaMemsetAsync(row_slot, 0xFF, sizeof(int32_t) * plan.M, st) != cudaSuccess)
             return LORA_ERR_CUDA;
-        if (args->num_segs > 0 &&
-            lora::launch_segments_to_rows(plan.M, args->seg_offsets, args->seg_adapter, args->perm,
-                                          args->num_segs, row_slot, plan.status, st) != cudaSuccess)
-            return LORA_ERR_CUDA;
+        if (args->num_segs > 0) {
+            if (lora::launch_segments_to_rows(plan.M, args->seg_offsets, args->seg_adapter, args->perm,
+                                              args->num_segs, row_slot, plan.status, st) != cudaSuccess)
+                return LORA_ERR_CUDA;
+            lora::count_launches(1);
+        }
         plan.row_slot = row_slot;
     }
     return lora::launch_forward(plan, st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;

@@ -66,7 +66,11 @@ struct ForwardPlan {
     int n_proj;
     ProjView proj[LORA_MAX_PROJ];
     unsigned long long *status;
+    void *const *stage_events;  // NULL or 1 + 2*n_proj cudaEvent_t
 };
+
+// Count of kernels launched by the library (lora_kernel_launches).
+void count_launches(int n);
 
 // Workspace layout of one forward call.
 struct WorkspaceLayout {

@@ -110,6 +110,7 @@ cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32
     const int nb = (rank + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
     ScatterBlocks sb;
     for (int t = 0; t < kMaxBlocksPerSlot; ++t) sb.b[t] = t < nb ? blocks[t] : 0;
+    count_launches(1);
     dim3 grid(8, nb, LORA_BLOCK_ROWS);
     const lora_pool_desc_t &d = pool->d;
     if (d.dtype == LORA_FP32)
@@ -283,6 +284,10 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
             v.V, v.max_rank, plan.status);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        if (plan.stage_events) {
+            e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[1 + 2 * p]), stream);
+            if (e != cudaSuccess) return e;
+        }
         dim3 ggrid((v.N + 63) / 64, (plan.M + 63) / 64);
         gemm_lora_simt_kernel<T><<<ggrid, 256, 0, stream>>>(
             static_cast<const T *>(plan.x), plan.ldx, static_cast<const T *>(v.W), plan.M, v.N,
@@ -291,6 +296,11 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
             v.num_blocks, v.V, v.max_rank, plan.status);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        count_launches(2);
+        if (plan.stage_events) {
+            e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[2 + 2 * p]), stream);
+            if (e != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }
@@ -307,8 +317,17 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
             v.V, v.max_rank, plan.status);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        if (plan.stage_events) {
+            e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[1 + 2 * p]), stream);
+            if (e != cudaSuccess) return e;
+        }
         e = launch_gemm_lora_tc(plan, v, stream);
         if (e != cudaSuccess) return e;
+        count_launches(2);
+        if (plan.stage_events) {
+            e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[2 + 2 * p]), stream);
+            if (e != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }

@@ -1,0 +1,516 @@
+#!/usr/bin/env python
+"""Benchmark of the multi-adapter LoRA linear layer (lora_linear_forward) on GB300.
+
+One step = one lora_linear_forward call over one batch: the shrink kernel
+(V = A_i x per row), the tensor-core base GEMM with the expand fused in its
+epilogue, for every projection of the workload.  Prints ONE JSON line per
+workload (default: the decode BGMV workload, 64 rows of q_proj 4096->4096
+with 32 rank-16 adapters).
+
+Timing: W warm-up steps, then K steps; L2 is flushed (a 2 x L2 write)
+before every step, outside the timed intervals; each step is bracketed by
+CUDA events on the launching stream and the step times are summed.  The
+dominant kernel's roofline uses stage events the library records around each
+kernel on the same stream.  `e2e` repeats the measurement through the C ABI
+with pinned host buffers: the host->device copy of x and the row ids and the
+device->host copy of the outputs are inside each timed step.
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+row sample of the same workload (the reference arm of this comparison).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "adapted tokens/s per LoRA linear; TC util (base GEMM) and HBM GB/s (LoRA path)"
+DEFAULT_CONFIG = "decode_bgmv"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_SOURCES = ["tc_gemm.cu", "sm100_ptx.cuh", "lora_device.cuh", "lora_internal.h"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: ~1.5 s of GPU work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["lora", "reference"], default="lora")
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
+                    help="workload name, or 'all' for one line per workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the oracle baseline")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "adapter_gemm_linear_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """dram bytes per launch of the GEMM kernel from a committed ncu capture,
+    if it was taken on the current kernel source."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None
+    src = gemm_source_hash()
+    for e in entries.get("entries", []):
+        if e.get("workload") == workload and e.get("source_hash") == src:
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        smax = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            for name, v in zip(names, s[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(self.samples)}
+
+
+def workload_stats(wl):
+    """Distinct adapters, adapted rows and rank sums the byte counts need."""
+    ids = wl.row_adapter
+    used = wl.used_slots
+    adapted = ids[ids >= 0]
+    return {
+        "distinct": int(used.size),
+        "adapted_rows": int(adapted.size),
+        "sum_r_distinct": int(sum(int(wl.ranks[s]) for s in used)),
+        "sum_r_rows": int(sum(int(wl.ranks[s]) for s in adapted)),
+    }
+
+
+def algorithmic(wl):
+    """Per-call algorithmic bytes and flops of each kernel stage.
+
+    GEMM (per projection): W, x and out once, plus the fused expand's
+    adapter B^T rows (each distinct adapter once) and V reads; flops 2MNK
+    plus the expand's 2 r N per adapted row.  Shrink: each distinct
+    adapter's A rows once, x rows of adapted rows, V writes.
+    """
+    eb = 2 if wl.dtype == "bf16" else 4
+    st = workload_stats(wl)
+    M, K = wl.M, wl.K
+    out = {"gemm_bytes": 0, "gemm_flops": 0, "shrink_bytes": 0, "shrink_flops": 0, "per_proj": []}
+    for p in wl.projections:
+        N = p.N
+        gb = (N * K + M * K + M * N) * eb + st["sum_r_distinct"] * N * eb + st["sum_r_rows"] * 4
+        gf = 2 * M * N * K + 2 * st["sum_r_rows"] * N
+        sb = st["sum_r_distinct"] * K * eb + st["adapted_rows"] * K * eb + st["sum_r_rows"] * 4
+        sf = 2 * st["sum_r_rows"] * K
+        out["gemm_bytes"] += gb
+        out["gemm_flops"] += gf
+        out["shrink_bytes"] += sb
+        out["shrink_flops"] += sf
+        out["per_proj"].append({"N": N, "gemm_bytes": gb, "gemm_flops": gf})
+    out.update(st)
+    return out
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def build_case(wl, device):
+    import torch
+    from adapter_gemm_linear_gb300 import LinearCall, LoraPool
+
+    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    max_rank = max(16, -(-int(wl.ranks.max()) // 16) * 16)
+    used = set(int(s) for s in wl.used_slots)
+    pools = []
+    for p, proj in enumerate(wl.projections):
+        pool = LoraPool(wl.K, proj.N, wl.num_slots, max_rank, wl.blocks_needed(), dtype=td,
+                        device=device, free_list_seed=wl.free_list_seed + p)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1234 + p)
+        for s in range(wl.num_slots):
+            r = int(wl.ranks[s])
+            if s in used or wl.num_slots <= 256:
+                A, B = wl.adapter(p, s)
+                pool.load(s, torch.from_numpy(A).to(td), torch.from_numpy(B).to(td), float(wl.alphas[s]))
+            else:
+                # resident but unused by this batch: device-random contents
+                A = (torch.randn(r, wl.K, device=device, generator=gen) * 0.02).to(td)
+                B = (torch.randn(proj.N, r, device=device, generator=gen) * 0.02).to(td)
+                pool.load(s, A, B, float(wl.alphas[s]))
+        pools.append(pool)
+    x = torch.from_numpy(wl.x).to(td).to(device)
+    Ws = [torch.from_numpy(p.W).to(td).to(device) for p in wl.projections]
+    outs = [torch.empty((wl.M, p.N), dtype=td, device=device) for p in wl.projections]
+    if wl.mode == "sgmv":
+        offs = torch.from_numpy(wl.seg_offsets).to(device)
+        adp = torch.from_numpy(wl.seg_adapter).to(device)
+        call = LinearCall(x, list(zip(Ws, pools, outs)), seg_offsets=offs, seg_adapter=adp)
+        ids = None
+    else:
+        ids = torch.from_numpy(wl.row_adapter).to(device)
+        call = LinearCall(x, list(zip(Ws, pools, outs)), row_adapter=ids)
+    torch.cuda.synchronize(device)
+    return {"pools": pools, "x": x, "Ws": Ws, "outs": outs, "ids": ids, "call": call}
+
+
+def time_device(case, wl, steps, warmup, flush, clocks_index):
+    import torch
+    from adapter_gemm_linear_gb300 import kernel_launches
+
+    call = case["call"]
+    n_ev = 1 + 2 * len(wl.projections)
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    stage = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    for ev in stage:  # materialise the raw events before the timed region
+        for e in ev:
+            e.record()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(clocks_index)
+    time.sleep(0.3)
+    n0 = kernel_launches()
+    for i in range(steps):
+        flush.zero_()
+        call.set_stage_events(stage[i])
+        starts[i].record()
+        call()
+        ends[i].record()
+    torch.cuda.synchronize()
+    launches = kernel_launches() - n0
+    clocks = sampler.stop()
+    call.set_stage_events(None)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    n_proj = len(wl.projections)
+    shrink_ms = [sum(ev[2 * p].elapsed_time(ev[2 * p + 1]) for p in range(n_proj)) for ev in stage]
+    gemm_ms = [sum(ev[2 * p + 1].elapsed_time(ev[2 * p + 2]) for p in range(n_proj)) for ev in stage]
+    return {"step_ms": step_ms, "shrink_ms": shrink_ms, "gemm_ms": gemm_ms, "launches": launches,
+            "clocks": clocks}
+
+
+def time_e2e(case, wl, steps, flush, device):
+    """Through the C ABI with pinned host buffers; copies inside each step."""
+    import torch
+
+    call = case["call"]
+    x_host = torch.from_numpy(wl.x).to(case["x"].dtype).pin_memory()
+    ids_host = None if case["ids"] is None else torch.from_numpy(wl.row_adapter).pin_memory()
+    outs_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in case["outs"]]
+    h2d = x_host.numel() * x_host.element_size() + (0 if ids_host is None else ids_host.numel() * 4)
+    d2h = sum(o.numel() * o.element_size() for o in outs_host)
+    total_ms = 0.0
+    for i in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        case["x"].copy_(x_host, non_blocking=True)
+        if ids_host is not None:
+            case["ids"].copy_(ids_host, non_blocking=True)
+        call()
+        for o, oh in zip(case["outs"], outs_host):
+            oh.copy_(o, non_blocking=True)
+        e.record()
+        e.synchronize()
+        total_ms += s.elapsed_time(e)
+    return {"ms": total_ms, "h2d": h2d, "d2h": d2h}
+
+
+def cpu_baseline(wl, seconds):
+    import oracle
+
+    rows = np.arange(wl.M)
+    cores = oracle.usable_cores()
+    done = 0
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        for p in range(len(wl.projections)):
+            oracle.workload_forward(wl, p, rows=rows, threads=cores)
+        done += rows.size
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} pass(es) of all {wl.M} rows x {len(wl.projections)} projection(s), "
+                      f"float64 oracle, {cores} threads, {dt:.1f} s"}
+
+
+def run_gpu(cfg_name, args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from workloads import make_config
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    import __graft_entry__
+    __graft_entry__.build()
+    wl = make_config(cfg_name)
+    case = build_case(wl, device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    if args.steps is None:
+        # about 1.5 s of forwards plus flushes
+        case["call"]()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(20):
+            flush.zero_()
+            case["call"]()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t) / 20
+        steps = int(min(20000, max(50, 1.5 / max(per, 1e-6))))
+    else:
+        steps = args.steps
+    warmup = max(3, args.warmup)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    dev_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[local_rank]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local_rank
+    res = time_device(case, wl, steps, warmup, flush, dev_index)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = sum(res["step_ms"])
+    gemm_ms = sum(res["gemm_ms"])
+    shrink_ms = sum(res["shrink_ms"])
+    e2e_steps = max(3, min(steps, 200))
+    e2e = time_e2e(case, wl, e2e_steps, flush, device)
+    if world > 1:
+        t = torch.tensor([total_ms, e2e["ms"]], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    else:
+        e2e_ms = e2e["ms"]
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    alg = algorithmic(wl)
+    tokens = wl.M * steps * world
+    value = tokens / (total_ms / 1e3)
+    # dominant kernel: the GEMM (compare stage time shares)
+    gemm_avg_s = gemm_ms / steps / 1e3
+    shrink_avg_s = shrink_ms / steps / 1e3
+    ai = alg["gemm_flops"] / alg["gemm_bytes"]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if ai > ridge:
+        achieved = alg["gemm_flops"] / gemm_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        achieved = alg["gemm_bytes"] / gemm_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = ncu_traffic(wl.name)
+    roof["kernel"] = "tc_gemm_lora_kernel"
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
+    roof["algorithmic_bytes_per_call"] = alg["gemm_bytes"]
+    roof["algorithmic_flops_per_call"] = alg["gemm_flops"]
+    roof["time_share"] = round(gemm_ms / total_ms, 3) if total_ms else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": round(total_ms / steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": {
+            "workload": wl.name, "M": wl.M, "K": wl.K, "N": [p.N for p in wl.projections],
+            "slots": wl.num_slots, "ranks": sorted(set(int(r) for r in wl.ranks)),
+            "mode": wl.mode, "distinct_adapters": alg["distinct"], "adapted_rows": alg["adapted_rows"],
+            "l2": "flushed before every step (2 x L2 write, outside the timed intervals)",
+            "launch": "eager, per-step CUDA events on the launching stream",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": roof,
+        "lora_path": {
+            "shrink_us": round(shrink_avg_s * 1e6, 3),
+            "shrink_gbs": round(alg["shrink_bytes"] / shrink_avg_s / 1e9, 1) if shrink_avg_s > 0 else None,
+            "shrink_frac_hbm": round(alg["shrink_bytes"] / shrink_avg_s / 1e9 / peaks["hbm_gbs"], 4)
+            if shrink_avg_s > 0 else None,
+            "gemm_us": round(gemm_avg_s * 1e6, 3),
+            "gemm_tc_frac": round(alg["gemm_flops"] / gemm_avg_s / 1e12 / peaks["bf16_tflops"], 4),
+            "gemm_hbm_frac": round(alg["gemm_bytes"] / gemm_avg_s / 1e9 / peaks["hbm_gbs"], 4),
+        },
+        "e2e": {"value": round(wl.M * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": int(res["launches"]),
+        "clocks": res["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    for pool in case["pools"]:
+        pool.close()
+    return line
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(cfg_name, args):
+    import oracle
+    from workloads import make_config
+
+    wl = make_config(cfg_name)
+    cores = oracle.usable_cores()
+    oracle.build()
+    steps = args.steps if args.steps is not None else 10
+    warmup = max(3, args.warmup)
+    # calibrate: time of one row through every projection
+    t = time.perf_counter()
+    for p in range(len(wl.projections)):
+        oracle.workload_forward(wl, p, rows=[0], threads=1)
+    row_s = max(time.perf_counter() - t, 1e-4)
+    budget = 90.0  # seconds of oracle work for the whole run
+    rows_per_step = int(max(1, min(wl.M, budget * cores / (steps + warmup) / row_s)))
+    rng = np.random.default_rng(0)
+
+    def step():
+        rows = rng.choice(wl.M, size=rows_per_step, replace=False)
+        for p in range(len(wl.projections)):
+            oracle.workload_forward(wl, p, rows=rows, threads=cores)
+
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = rows_per_step * steps / dt
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "tokens/s",
+        "n_gpus": 1,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": round(dt / steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": [p.N for p in wl.projections],
+                   "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} random rows of {wl.M} per step, float64 oracle, "
+                                   f"{cores} threads"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from workloads import CONFIG_NAMES
+    names = list(CONFIG_NAMES[1:]) if args.config == "all" else [args.config]
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        for name in names:
+            print(json.dumps(run_reference(name, args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        for name in names:
+            line = run_gpu(name, args, rank, world, local_rank)
+            if line is not None:
+                print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -223,6 +223,13 @@ typedef struct lora_forward_args {
     int32_t num_segs;
     void *workspace;          /* device scratch, >= lora_forward_workspace_bytes */
     size_t workspace_bytes;
+    /* Optional profiling hook: NULL, or 1 + 2*n_proj cudaEvent_t handles
+     * (created by the caller).  The forward records event 0 on `stream`
+     * before its first kernel, event 1+2p after projection p's shrink kernel
+     * and event 2+2p after its GEMM, so elapsed times between them are the
+     * stage durations on the launching stream. */
+    void *const *stage_events;
+    int32_t num_stage_events; /* 0, or exactly 1 + 2*n_proj */
 } lora_forward_args_t;
 
 /* Scratch bytes lora_linear_forward needs for these arguments (depends on
@@ -256,6 +263,10 @@ const char *lora_status_string(lora_status_t status);
 
 /* LORA_ABI_VERSION of the library. */
 int32_t lora_abi_version(void);
+
+/* Kernels this library has launched in this process (all devices), for
+ * accounting in benchmarks. */
+uint64_t lora_kernel_launches(void);
 
 #ifdef __cplusplus
 }

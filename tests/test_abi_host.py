@@ -102,7 +102,7 @@ def test_forward_validation_without_device(L):
         d = dict(dtype=0, M=4, K=64, x=0x3000, ldx=64, n_proj=1,
                  proj=ctypes.cast(projs, ctypes.POINTER(Proj)), row_adapter=0x4000,
                  seg_offsets=None, seg_adapter=None, perm=None, num_segs=0,
-                 workspace=None, workspace_bytes=0)
+                 workspace=None, workspace_bytes=0, stage_events=None, num_stage_events=0)
         d.update(kw)
         return ForwardArgs(**d)
 
@@ -120,3 +120,6 @@ def test_forward_validation_without_device(L):
     # both index forms at once
     assert fwd(ctypes.byref(args(seg_offsets=0x5000, num_segs=1)), None) == 1
     assert L.lora_forward_workspace_bytes(ctypes.byref(args())) == 0
+    # stage events: count must be 1 + 2*n_proj
+    assert fwd(ctypes.byref(args(num_stage_events=2)), None) == 1
+    assert L.lora_kernel_launches() == 0
