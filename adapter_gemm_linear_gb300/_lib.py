@@ -107,6 +107,7 @@ SIGNATURES = [
       ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("lora_forward_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(ForwardArgs)]),
     ("lora_linear_forward", ctypes.c_int, [ctypes.POINTER(ForwardArgs), ctypes.c_void_p]),
+    ("lora_linear_forward_noalloc", ctypes.c_int, [ctypes.POINTER(ForwardArgs), ctypes.c_void_p]),
     ("lora_get_device_status", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("lora_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("lora_abi_version", ctypes.c_int32, []),

@@ -251,6 +251,43 @@ size_t lora_forward_workspace_bytes(const lora_forward_args_t *args);
 lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream);
 
 /*
+ * Size of the scratch array behind lora_linear_forward_noalloc: 16 MiB.
+ */
+#define LORA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * lora_linear_forward for callers that cannot allocate device memory.
+ * (The pages have no counterpart of this entry point; it exists for
+ * integration.)  Some callers have no way to obtain scratch memory: a
+ * plugin inside a host framework that owns the whole device memory budget
+ * and hands out none, a process that reserves all of its memory at start-up
+ * under a fixed cap, or a latency-critical loop that must not call
+ * cudaMalloc because an allocation can stall or synchronise the device.
+ * This entry point takes the same arguments as lora_linear_forward; the
+ * caller still provides x, W, the pools, the row ids or segments and the
+ * outputs, but `workspace` and `workspace_bytes` are ignored.  Instead the
+ * forward uses a scratch array of LORA_NOALLOC_SCRATCH_BYTES that the
+ * library keeps in the memory of every device that loads it, for the life
+ * of the process.  Nothing is allocated: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ * Limits and rules:
+ *  - Returns LORA_ERR_WORKSPACE, launching nothing, when the call needs more
+ *    scratch than LORA_NOALLOC_SCRATCH_BYTES (lora_forward_workspace_bytes
+ *    gives the need: per projection M*max_rank*4 bytes plus, with segments,
+ *    M*4 bytes, each rounded up to 256).
+ *  - The first call on a device looks up that device's copy of the array
+ *    (with the device current), so make that first call before starting
+ *    any stream capture on the device.
+ *  - Every call on a device shares the one array, and the array keeps
+ *    whatever the last call left in it; the forward itself resets what must
+ *    start from a known value.  Calls whose work overlaps on the GPU (for
+ *    example on two streams without ordering between them) race on the
+ *    array and may corrupt each other's results: order them on one stream.
+ * Other errors are those of lora_linear_forward.
+ */
+lora_status_t lora_linear_forward_noalloc(const lora_forward_args_t *args, void *stream);
+
+/*
  * Wait for `stream`, then read and clear this device's status word.
  * Returns LORA_OK when no kernel recorded an error, else ADAPTER_ID,
  * SEGMENTS, DEVICE_INDEX or DEVICE_TIMEOUT; *detail (may be NULL) receives
