@@ -46,7 +46,7 @@ class PoolDesc(ctypes.Structure):
         ("max_rank", ctypes.c_int32),
         ("num_blocks", ctypes.c_int32),
         ("a_arena", ctypes.c_void_p),
-        ("bt_arena", ctypes.c_void_p),
+        ("b_arena", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p),
         ("ranks", ctypes.c_void_p),
         ("scales", ctypes.c_void_p),

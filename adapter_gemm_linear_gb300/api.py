@@ -70,8 +70,8 @@ def pool_arena_bytes(K: int, N: int, num_blocks: int, dtype: torch.dtype = torch
 class LoraPool:
     """One projection's paged adapter pool (lora_pool_create & co.).
 
-    Device memory (two arenas of ``num_blocks`` 16-row blocks, the block
-    table, ranks and scales) is allocated here with torch and handed to the
+    Device memory (A-arena [num_blocks, 16, K] and B-arena [num_blocks, N, 16],
+    the block table, ranks and scales) is allocated here with torch and handed to the
     library, which keeps only host metadata.
     """
 
@@ -84,13 +84,13 @@ class LoraPool:
         self.max_slots, self.max_rank, self.num_blocks = int(max_slots), int(max_rank), int(num_blocks)
         bps = max(1, self.max_rank // LORA_BLOCK_ROWS)
         self.a_arena = torch.empty((num_blocks, LORA_BLOCK_ROWS, K), dtype=dtype, device=self.device)
-        self.bt_arena = torch.empty((num_blocks, LORA_BLOCK_ROWS, N), dtype=dtype, device=self.device)
+        self.b_arena = torch.empty((num_blocks, N, LORA_BLOCK_ROWS), dtype=dtype, device=self.device)
         self.block_table = torch.empty((max_slots, bps), dtype=torch.int32, device=self.device)
         self.ranks = torch.empty((max_slots,), dtype=torch.int32, device=self.device)
         self.scales = torch.empty((max_slots,), dtype=torch.float32, device=self.device)
         desc = _lib.PoolDesc(
             lora_dtype(dtype), self.K, self.N, self.max_slots, self.max_rank, self.num_blocks,
-            _ptr(self.a_arena), _ptr(self.bt_arena), _ptr(self.block_table), _ptr(self.ranks),
+            _ptr(self.a_arena), _ptr(self.b_arena), _ptr(self.block_table), _ptr(self.ranks),
             _ptr(self.scales), int(free_list_seed))
         handle = ctypes.c_void_p()
         with torch.cuda.device(self.device):

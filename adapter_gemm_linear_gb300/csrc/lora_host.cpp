@@ -99,9 +99,9 @@ lora_status_t lora_pool_create(const lora_pool_desc_t *desc, void *stream, lora_
         return LORA_ERR_INVALID_ARG;
     if (d.max_rank % LORA_BLOCK_ROWS != 0 || d.max_rank > lora::kMaxRankLimit)
         return LORA_ERR_RANK;
-    if (!d.a_arena || !d.bt_arena || !d.block_table || !d.ranks || !d.scales)
+    if (!d.a_arena || !d.b_arena || !d.block_table || !d.ranks || !d.scales)
         return LORA_ERR_INVALID_ARG;
-    if (!aligned16(d.a_arena) || !aligned16(d.bt_arena) || !aligned16(d.block_table) ||
+    if (!aligned16(d.a_arena) || !aligned16(d.b_arena) || !aligned16(d.block_table) ||
         !aligned16(d.ranks) || !aligned16(d.scales))
         return LORA_ERR_ALIGNMENT;
     if (d.K % vec_elems(d.dtype) || d.N % vec_elems(d.dtype)) return LORA_ERR_ALIGNMENT;
@@ -198,34 +198,35 @@ lora_status_t lora_pool_load_slot(lora_pool_t *pool, int32_t slot, int32_t rank,
     if (src_on_device) {
         e = lora::launch_pool_scatter(p, rank, blocks.data(), A, B, st);
     } else {
-        // B [N][rank] -> B^T [rank][N] on the host, then one copy per block
-        std::vector<unsigned char> bt;
+        // per block t: A rows 16t.. (contiguous) and B columns 16t..16t+15
+        // gathered on the host into the block's [N][16] layout
+        std::vector<unsigned char> bblk;
         try {
-            bt.resize(static_cast<size_t>(rank) * N * eb);
+            bblk.resize(N * LORA_BLOCK_ROWS * eb);
         } catch (...) {
             return LORA_ERR_INVALID_ARG;
         }
-        const unsigned char *src = static_cast<const unsigned char *>(B);
-        for (size_t n = 0; n < N; ++n)
-            for (size_t j = 0; j < static_cast<size_t>(rank); ++j)
-                memcpy(&bt[(j * N + n) * eb], src + (n * rank + j) * eb, eb);
-        unsigned char *a_arena = static_cast<unsigned char *>(p->d.a_arena);
-        unsigned char *bt_arena = static_cast<unsigned char *>(p->d.bt_arena);
         const unsigned char *a_src = static_cast<const unsigned char *>(A);
+        const unsigned char *b_src = static_cast<const unsigned char *>(B);
+        unsigned char *a_arena = static_cast<unsigned char *>(p->d.a_arena);
+        unsigned char *b_arena = static_cast<unsigned char *>(p->d.b_arena);
         for (int t = 0; t < nb && e == cudaSuccess; ++t) {
             const size_t b = static_cast<size_t>(blocks[t]);
             const size_t j0 = static_cast<size_t>(t) * LORA_BLOCK_ROWS;
             const size_t rows = std::min<size_t>(LORA_BLOCK_ROWS, rank - j0);
             unsigned char *a_dst = a_arena + b * LORA_BLOCK_ROWS * K * eb;
-            unsigned char *bt_dst = bt_arena + b * LORA_BLOCK_ROWS * N * eb;
             e = cudaMemcpyAsync(a_dst, a_src + j0 * K * eb, rows * K * eb, cudaMemcpyHostToDevice, st);
-            if (e == cudaSuccess)
-                e = cudaMemcpyAsync(bt_dst, &bt[j0 * N * eb], rows * N * eb, cudaMemcpyHostToDevice, st);
-            if (e == cudaSuccess && rows < LORA_BLOCK_ROWS) {
+            if (e == cudaSuccess && rows < LORA_BLOCK_ROWS)
                 e = cudaMemsetAsync(a_dst + rows * K * eb, 0, (LORA_BLOCK_ROWS - rows) * K * eb, st);
-                if (e == cudaSuccess)
-                    e = cudaMemsetAsync(bt_dst + rows * N * eb, 0, (LORA_BLOCK_ROWS - rows) * N * eb, st);
-            }
+            if (e != cudaSuccess) break;
+            // the previous block's copy must finish before the staging buffer is reused
+            e = cudaStreamSynchronize(st);
+            if (e != cudaSuccess) break;
+            memset(bblk.data(), 0, bblk.size());
+            for (size_t n = 0; n < N; ++n)
+                memcpy(&bblk[n * LORA_BLOCK_ROWS * eb], b_src + (n * rank + j0) * eb, rows * eb);
+            e = cudaMemcpyAsync(b_arena + b * N * LORA_BLOCK_ROWS * eb, bblk.data(), bblk.size(),
+                                cudaMemcpyHostToDevice, st);
         }
         // the host staging buffer dies with this scope
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -346,7 +347,7 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         v.N = d.N;
         v.ldo = pj.ldo;
         v.a_arena = d.a_arena;
-        v.bt_arena = d.bt_arena;
+        v.b_arena = d.b_arena;
         v.table = d.block_table;
         v.ranks = d.ranks;
         v.scales = d.scales;
@@ -361,6 +362,20 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     // slot ids of every pool must mean the same adapters
     for (int i = 1; i < a->n_proj; ++i)
         if (a->proj[i].pool->d.max_slots != a->proj[0].pool->d.max_slots) return LORA_ERR_INVALID_ARG;
+    // split-K scratch of the tensor-core GEMM, shared by the projections
+    // (their GEMMs run one after the other on the stream)
+    size_t y32 = 0, cnt = 0;
+    if (a->dtype == LORA_BF16 && a->M > 0) {
+        for (int i = 0; i < a->n_proj; ++i) {
+            const lora::TcPlan tp = lora::plan_tc(a->M, a->proj[i].pool->d.N, a->K);
+            y32 = std::max(y32, tp.y32_bytes);
+            cnt = std::max(cnt, tp.counter_bytes);
+        }
+    }
+    ws->y32_off = off;
+    off += align_up(y32, 256);
+    ws->counter_off = off;
+    off += align_up(cnt, 256);
     ws->total = off;
     return LORA_OK;
 }
@@ -383,6 +398,8 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
     unsigned char *base = static_cast<unsigned char *>(args->workspace);
     if (lora::device_status_ptr(&plan.status) != cudaSuccess) return LORA_ERR_CUDA;
     for (int i = 0; i < plan.n_proj; ++i) plan.proj[i].V = reinterpret_cast<float *>(base + ws.v_off[i]);
+    plan.y32 = reinterpret_cast<float *>(base + ws.y32_off);
+    plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);
     cudaStream_t st = as_stream(stream);
     if (plan.stage_events &&
         cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[0]), st) != cudaSuccess)

@@ -50,7 +50,7 @@ struct ProjView {
     const void *W;
     void *out;
     int32_t N, ldo;
-    const void *a_arena, *bt_arena;
+    const void *a_arena, *b_arena;
     const int32_t *table;
     const int32_t *ranks;
     const float *scales;
@@ -67,6 +67,8 @@ struct ForwardPlan {
     ProjView proj[LORA_MAX_PROJ];
     unsigned long long *status;
     void *const *stage_events;  // NULL or 1 + 2*n_proj cudaEvent_t
+    float *y32;                 // workspace: split-K accumulator
+    int32_t *counters;          // workspace: split-K tile counters
 };
 
 // Count of kernels launched by the library (lora_kernel_launches).
@@ -76,7 +78,18 @@ void count_launches(int n);
 struct WorkspaceLayout {
     size_t row_slot_off;          // int32[M] (segment mode only)
     size_t v_off[LORA_MAX_PROJ];  // fp32[M][max_rank]
+    size_t y32_off;               // fp32[M][N] split-K accumulator (largest projection)
+    size_t counter_off;           // int32 per output tile (split-K)
     size_t total;
+};
+
+// Tensor-core GEMM launch plan (tc_gemm.cu): orientation, tile width, split-K.
+struct TcPlan {
+    bool swap;            // W rows on the TMEM lanes, tokens as the MMA's N
+    int bn;               // MMA N (tokens when swapped, output columns otherwise)
+    int num_kb, kb_per_split, splits;
+    int tiles_a, tiles_b, units, grid;
+    size_t y32_bytes, counter_bytes;
 };
 
 // Launchers (lora_kernels.cu).
@@ -85,14 +98,15 @@ cudaError_t launch_segments_to_rows(int32_t M, const int32_t *seg_offsets,
                                     int32_t num_segs, int32_t *row_slot,
                                     unsigned long long *status, cudaStream_t stream);
 // Copy a device-resident adapter (A [rank][K], B [N][rank]) into the blocks
-// `blocks` (host array of ceil(rank/16) ids), transposing B into B^T rows and
-// zeroing the tail rows of the last block.
+// `blocks` (host array of ceil(rank/16) ids) in the arena layouts of
+// lora_pool_desc_t, zeroing the entries past `rank` in the last block.
 cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32_t *blocks,
                                 const void *A, const void *B, cudaStream_t stream);
 cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream);
 
 // Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
-cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
-int choose_tc_bn(int32_t M, int32_t N);
+TcPlan plan_tc(int32_t M, int32_t N, int32_t K);
+cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, float *y32, int32_t *counters,
+                                cudaStream_t stream);
 
 }  // namespace lora

@@ -91,18 +91,19 @@ struct ScatterBlocks {
 template <typename T>
 __global__ void pool_scatter_kernel(const T *__restrict__ A, const T *__restrict__ B, int32_t rank,
                                     int32_t K, int32_t N, T *__restrict__ a_arena,
-                                    T *__restrict__ bt_arena, ScatterBlocks blocks) {
+                                    T *__restrict__ b_arena, ScatterBlocks blocks) {
     const int32_t t = blockIdx.y;
     const int32_t row = blockIdx.z;
     const int32_t j = t * LORA_BLOCK_ROWS + row;
     const size_t b = static_cast<size_t>(blocks.b[t]);
     T *a_dst = a_arena + (b * LORA_BLOCK_ROWS + row) * static_cast<size_t>(K);
-    T *bt_dst = bt_arena + (b * LORA_BLOCK_ROWS + row) * static_cast<size_t>(N);
+    T *b_dst = b_arena + b * static_cast<size_t>(N) * LORA_BLOCK_ROWS + row;
     const int32_t stride = gridDim.x * blockDim.x;
     for (int32_t k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += stride)
         a_dst[k] = j < rank ? A[static_cast<size_t>(j) * K + k] : from_float<T>(0.0f);
     for (int32_t n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += stride)
-        bt_dst[n] = j < rank ? B[static_cast<size_t>(n) * rank + j] : from_float<T>(0.0f);
+        b_dst[static_cast<size_t>(n) * LORA_BLOCK_ROWS] =
+            j < rank ? B[static_cast<size_t>(n) * rank + j] : from_float<T>(0.0f);
 }
 
 cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32_t *blocks,
@@ -116,12 +117,12 @@ cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32
     if (d.dtype == LORA_FP32)
         pool_scatter_kernel<float><<<grid, 256, 0, stream>>>(
             static_cast<const float *>(A), static_cast<const float *>(B), rank, d.K, d.N,
-            static_cast<float *>(d.a_arena), static_cast<float *>(d.bt_arena), sb);
+            static_cast<float *>(d.a_arena), static_cast<float *>(d.b_arena), sb);
     else
         pool_scatter_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), rank,
             d.K, d.N, static_cast<__nv_bfloat16 *>(d.a_arena),
-            static_cast<__nv_bfloat16 *>(d.bt_arena), sb);
+            static_cast<__nv_bfloat16 *>(d.b_arena), sb);
     return cudaGetLastError();
 }
 
@@ -185,7 +186,7 @@ shrink_simt_kernel(const T *__restrict__ x, int32_t ldx, int32_t K, const int32_
 
 // ---------------------------------------------------------------------------
 // SIMT GEMM with the expand fused into the epilogue:
-// out[m, n] = sum_k x[m,k] W[n,k] + s_i * sum_j Bt_i[j, n] V[m, j]
+// out[m, n] = sum_k x[m,k] W[n,k] + s_i * sum_j B_i[n, j] V[m, j]
 // 64x64 tile, 256 threads, 4x4 outputs per thread (rows ty+16a, cols tx+16b)
 // ---------------------------------------------------------------------------
 
@@ -193,7 +194,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 gemm_lora_simt_kernel(const T *__restrict__ x, int32_t ldx, const T *__restrict__ W, int32_t M,
                       int32_t N, int32_t K, T *__restrict__ out, int32_t ldo,
-                      const int32_t *__restrict__ row_slot, const T *__restrict__ bt_arena,
+                      const int32_t *__restrict__ row_slot, const T *__restrict__ b_arena,
                       const int32_t *__restrict__ table, const int32_t *__restrict__ ranks,
                       const float *__restrict__ scales, int32_t max_slots, int32_t bps,
                       int32_t num_blocks, const float *__restrict__ V, int32_t ldv,
@@ -254,12 +255,12 @@ gemm_lora_simt_kernel(const T *__restrict__ x, int32_t ldx, const T *__restrict_
                     s = 0.0f;
                     break;
                 }
-                const T *btr = bt_arena + (static_cast<size_t>(b) * LORA_BLOCK_ROWS + (j & 15)) * N;
+                const T *bb = b_arena + static_cast<size_t>(b) * N * LORA_BLOCK_ROWS + (j & 15);
                 const float v = vr[j];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int32_t n = n0 + tx + 16 * c;
-                    if (n < N) lo[c] = fmaf(to_float(btr[n]), v, lo[c]);
+                    if (n < N) lo[c] = fmaf(to_float(bb[static_cast<size_t>(n) * LORA_BLOCK_ROWS]), v, lo[c]);
                 }
             }
         } else {
@@ -292,7 +293,7 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
         gemm_lora_simt_kernel<T><<<ggrid, 256, 0, stream>>>(
             static_cast<const T *>(plan.x), plan.ldx, static_cast<const T *>(v.W), plan.M, v.N,
             plan.K, static_cast<T *>(v.out), v.ldo, plan.row_slot,
-            static_cast<const T *>(v.bt_arena), v.table, v.ranks, v.scales, v.max_slots, v.bps,
+            static_cast<const T *>(v.b_arena), v.table, v.ranks, v.scales, v.max_slots, v.bps,
             v.num_blocks, v.V, v.max_rank, plan.status);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -321,7 +322,7 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
             e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[1 + 2 * p]), stream);
             if (e != cudaSuccess) return e;
         }
-        e = launch_gemm_lora_tc(plan, v, stream);
+        e = launch_gemm_lora_tc(plan, v, plan.y32, plan.counters, stream);
         if (e != cudaSuccess) return e;
         count_launches(2);
         if (plan.stage_events) {

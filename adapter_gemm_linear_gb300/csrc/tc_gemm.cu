@@ -1,25 +1,35 @@
-// Base GEMM on the 5th-generation tensor cores (tcgen05, accumulator in
-// TMEM, operands staged by TMA) with the LoRA expand fused into the
-// epilogue:
+// Base GEMM on the 5th-generation tensor cores (tcgen05, fp32 accumulators in
+// TMEM, operands staged by TMA) with the LoRA expand fused into the epilogue:
 //
-//   out[m, n] = round( sum_k x[m,k] W[n,k]  +  s_i * sum_j Bt_i[j,n] V[m,j] )
+//   out[m, n] = round( sum_k x[m,k] W[n,k]  +  s_i * sum_j B_i[n,j] V[m,j] )
 //
 // where i is row m's adapter slot (none: no second term), V = A_i x is the
-// rank-r intermediate (fp32, produced by the shrink kernel), Bt_i are the
-// adapter's B^T rank-rows gathered through the pool's block table, and
-// s_i = alpha_i / r_i.  The correction is added to the fp32 accumulator, so
-// each output is rounded to bf16 exactly once.
+// rank-r intermediate (fp32, from the shrink kernel), B_i's entries are
+// gathered through the pool's block table, and s_i = alpha_i / r_i.  The
+// correction is added to the fp32 accumulator, so each output is rounded to
+// bf16 exactly once.
 //
-// One CTA computes one 128 x BN output tile.  Warp roles:
-//   warp 0      TMA producer: x tile [128 x 64] and W tile [BN x 64] per
-//               k-block into a STAGES-deep shared-memory ring (128-byte
-//               swizzle), completion counted on the stage's `full` barrier;
+// Persistent kernel: one CTA per SM walks a list of work units; a unit is an
+// output tile (and, for split-K, one K range of it).  Two orientations:
+//   non-swapped  (large M): the MMA's M = 128 token rows of x, its N = BN
+//                columns of W; TMEM lane = token, TMEM column = output column.
+//   swapped      (small M): the MMA's M = 128 rows of W (output columns), its
+//                N = BN tokens; TMEM lane = output column, column = token.  With
+//                few tokens this puts W's rows on the 128 lanes, and split-K
+//                spreads each tile's K range over several CTAs so that ~all
+//                SMs stream W.  Partial tiles are summed with fp32 reductions
+//                into an L2-resident buffer; the CTA that finishes a tile last
+//                (per-tile counter) applies the correction and stores it.
+// Warp roles:
+//   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per
+//               k-block into a shared-memory ring (128-byte swizzle);
 //   warp 1      TMEM allocator and MMA issuer: 4 tcgen05.mma (K = 16 each)
-//               per k-block into a 128 x BN fp32 TMEM accumulator, then
-//               tcgen05.commit frees the stage (`empty` barrier);
-//   warps 2-5   epilogue: each warp owns one 32-lane quarter of TMEM (= 32
-//               output rows), reads 32 columns at a time with tcgen05.ld,
-//               adds the row's LoRA correction and stores bf16.
+//               per k-block into one of two TMEM accumulators, so the next
+//               unit's MMAs overlap the previous unit's epilogue;
+//   warps 2-9   epilogue: each warp may read one 32-lane quarter of TMEM
+//               (two warps per quarter, alternating 32-column chunks), reads
+//               32 columns at a time with tcgen05.ld, adds the correction and
+//               stores bf16.
 // Every barrier wait is bounded in time; a wait that runs out records
 // kDevTimeout in the status word and the CTA unwinds without hanging.
 #include <cuda.h>
@@ -38,36 +48,69 @@ namespace lora {
 
 namespace {
 
-constexpr int kBM = 128;               // tile rows (UMMA M)
+constexpr int kBM = 128;               // rows of the A operand per tile (UMMA M)
 constexpr int kBK = 64;                // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;             // K of one tcgen05.mma for 16-bit inputs
-constexpr int kThreads = 192;          // 6 warps
+constexpr int kEpiWarps = 8;   // two per TMEM lane quarter
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kRingBudget = 196 * 1024;  // shared memory for the operand ring
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr int kEpiBarrier = 1;         // named barrier of the epilogue warps
 
 struct TcParams {
-    int32_t M, N, K, num_kb;
+    int32_t M, N, K;
+    int32_t num_kb, kb_per_split, splits;
+    int32_t tiles_a, tiles_b, num_units;
     __nv_bfloat16 *out;
     int32_t ldo;
     const int32_t *row_slot;
-    const __nv_bfloat16 *bt_arena;
+    const __nv_bfloat16 *b_arena;
     const int32_t *table;
     const int32_t *ranks;
     const float *scales;
     int32_t max_slots, bps, num_blocks;
     const float *V;
     int32_t ldv;
+    float *y32;         // split-K accumulator [M][N], zero on entry (splits > 1)
+    int32_t *counters;  // per tile, zero on entry (splits > 1)
     unsigned long long *status;
 };
 
 template <int BN>
-__host__ __device__ constexpr uint32_t tmem_cols() {
-    return BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
-}
+struct Cfg {
+    static constexpr uint32_t kABytes = kBM * kBK * 2;
+    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr int kStages0 = kRingBudget / static_cast<int>(kABytes + kBBytes);
+    static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
+    static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
+                                        : 2 * BN <= 256 ? 256 : 512;
+    // ring + barriers + TMEM address + flags + per-token metadata, plus alignment slack
+    static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) +
+                                    (2 * kStages + 4) * 8 + 16 + BN * 12;
+    static_assert(kStages >= 2, "ring too small");
+};
 
-template <int BN, int STAGES>
-constexpr size_t smem_bytes() {
-    return 1024 /* alignment slack */ + static_cast<size_t>(STAGES) * (kBM + BN) * kBK * 2 +
-           (2 * STAGES + 1) * 8 + 16;
+struct Unit {
+    int32_t ta, tb, ks;
+};
+
+// Units are numbered with the split fastest; for the swapped orientation the
+// token tiles of one W tile come next (so they run at the same time and share
+// the W tile through L2), for the non-swapped one the x tiles of one W tile.
+template <bool SWAP>
+__device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
+    Unit w;
+    w.ks = u % p.splits;
+    const int32_t r = u / p.splits;
+    if (SWAP) {
+        w.tb = r % p.tiles_b;
+        w.ta = r / p.tiles_b;
+    } else {
+        w.ta = r % p.tiles_a;
+        w.tb = r / p.tiles_a;
+    }
+    return w;
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &q, float *v) {
@@ -84,46 +127,418 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int BN, int STAGES>
+__device__ __forceinline__ void epi_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(kEpiThreads) : "memory");
+}
+
+// --------------------------------------------------------------- producer
+
+template <bool SWAP, int BN>
+__device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUtensorMap *tma_b,
+                                             const TcParams &p, uint8_t *sA, uint8_t *sB,
+                                             uint64_t *full, uint64_t *empty,
+                                             volatile uint32_t *abort_flag) {
+    using namespace sm100;
+    using C = Cfg<BN>;
+    int32_t it = 0;
+    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        const Unit w = decode_unit<SWAP>(u, p);
+        const int32_t kb0 = w.ks * p.kb_per_split;
+        const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+        for (int32_t kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = it % C::kStages;
+            const uint32_t ph = (it / C::kStages) & 1;
+            if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimitNs)) {
+                record_error(p.status, kDevTimeout, 1);
+                *abort_flag = 1;
+            }
+            if (*abort_flag) return;
+            mbar_arrive_expect_tx(&full[s], C::kABytes + C::kBBytes);
+            tma_load_2d(sA + s * C::kABytes, tma_a, kb * kBK, w.ta * kBM, &full[s]);
+            tma_load_2d(sB + s * C::kBBytes, tma_b, kb * kBK, w.tb * BN, &full[s]);
+        }
+    }
+}
+
+// --------------------------------------------------------------- MMA issuer
+
+template <bool SWAP, int BN>
+__device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
+                                        uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
+                                        uint32_t tmem_base, volatile uint32_t *abort_flag) {
+    using namespace sm100;
+    using C = Cfg<BN>;
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+    int32_t it = 0, t = 0;
+    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
+        const Unit w = decode_unit<SWAP>(u, p);
+        const int32_t kb0 = w.ks * p.kb_per_split;
+        const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+        const int b = t & 1;
+        bool ok = mbar_wait_bounded(&tmem_empty[b], ((t >> 1) & 1) ^ 1, kWaitLimitNs);
+        if (!ok) record_error(p.status, kDevTimeout, 2);
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + b * BN;
+        for (int32_t kb = kb0; kb < kb1 && ok; ++kb, ++it) {
+            const int s = it % C::kStages;
+            const uint32_t ph = (it / C::kStages) & 1;
+            if (!mbar_wait_bounded(&full[s], ph, kWaitLimitNs)) {
+                record_error(p.status, kDevTimeout, 3);
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t a_addr = smem_u32(sA + s * C::kABytes);
+            const uint32_t b_addr = smem_u32(sB + s * C::kBBytes);
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+                mma_bf16_f32(d, desc_kmajor_sw128(a_addr + k * kUmmaK * 2),
+                             desc_kmajor_sw128(b_addr + k * kUmmaK * 2), idesc,
+                             (kb > kb0 || k > 0) ? 1u : 0u);
+            mma_commit(&empty[s]);
+        }
+        if (!ok || *abort_flag) {
+            *abort_flag = 1;
+            mbar_arrive(&tmem_full[b]);  // wake the epilogue so it can unwind
+            return;
+        }
+        mma_commit(&tmem_full[b]);
+    }
+}
+
+// --------------------------------------------------------------- epilogue
+
+// AND of `v` over the epilogue threads, also a barrier among them.
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "n"(kEpiBarrier), "n"(kEpiThreads)
+        : "memory");
+    return r != 0;
+}
+
+// Swapped orientation: this thread owns output column n; the 32 values in
+// acc are tokens m0 .. m0+31 (meta_* hold their slot, rank, scale).  For one
+// token all lanes of the warp use the same adapter: the B rows they read are
+// 32 consecutive 32-byte pieces and the V values are a broadcast.
+__device__ __forceinline__ void swap_finish_chunk(const TcParams &p, int32_t n, bool n_ok, int32_t m0,
+                                                  const int32_t *meta_slot, const int32_t *meta_rank,
+                                                  const float *meta_scale, float (&acc)[32]) {
+    if (!n_ok) return;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const int32_t slot = meta_slot[e];
+        if (slot < 0) continue;
+        const int32_t r = meta_rank[e];
+        const float *vrow = p.V + static_cast<size_t>(m0 + e) * p.ldv;
+        const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;
+        float lo0 = 0.0f, lo1 = 0.0f, lo2 = 0.0f, lo3 = 0.0f;
+        bool bad = false;
+#pragma unroll 1
+        for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
+            const int32_t blk = trow[jb];
+            if (blk < 0 || blk >= p.num_blocks) {
+                record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
+                bad = true;
+                break;
+            }
+            const uint4 *bsrc = reinterpret_cast<const uint4 *>(
+                p.b_arena + (static_cast<size_t>(blk) * p.N + n) * LORA_BLOCK_ROWS);
+            const float4 *vsrc = reinterpret_cast<const float4 *>(vrow + jb * LORA_BLOCK_ROWS);
+            const uint4 q0 = __ldg(bsrc), q1 = __ldg(bsrc + 1);
+            const float4 v0 = vsrc[0], v1 = vsrc[1], v2 = vsrc[2], v3 = vsrc[3];
+            float bv[16];
+            unpack_bf16x8(q0, bv);
+            unpack_bf16x8(q1, bv + 8);
+            lo0 = fmaf(bv[0], v0.x, lo0);
+            lo1 = fmaf(bv[1], v0.y, lo1);
+            lo2 = fmaf(bv[2], v0.z, lo2);
+            lo3 = fmaf(bv[3], v0.w, lo3);
+            lo0 = fmaf(bv[4], v1.x, lo0);
+            lo1 = fmaf(bv[5], v1.y, lo1);
+            lo2 = fmaf(bv[6], v1.z, lo2);
+            lo3 = fmaf(bv[7], v1.w, lo3);
+            lo0 = fmaf(bv[8], v2.x, lo0);
+            lo1 = fmaf(bv[9], v2.y, lo1);
+            lo2 = fmaf(bv[10], v2.z, lo2);
+            lo3 = fmaf(bv[11], v2.w, lo3);
+            lo0 = fmaf(bv[12], v3.x, lo0);
+            lo1 = fmaf(bv[13], v3.y, lo1);
+            lo2 = fmaf(bv[14], v3.z, lo2);
+            lo3 = fmaf(bv[15], v3.w, lo3);
+        }
+        if (!bad) acc[e] = fmaf(meta_scale[e], (lo0 + lo1) + (lo2 + lo3), acc[e]);
+    }
+}
+
+// Non-swapped orientation: this thread owns token row m (adapter slot, rank
+// r, scale s); the 32 values in acc are output columns n0 .. n0+31.  The
+// correction for 8 columns at a time keeps 8 independent accumulators.
+__device__ __forceinline__ void rows_finish_chunk(const TcParams &p, int32_t slot, int32_t r, float s,
+                                                  int32_t m, int32_t n0, float (&acc)[32]) {
+    if (slot < 0 || n0 >= p.N) return;
+    const float *vrow = p.V + static_cast<size_t>(m) * p.ldv;
+    const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;
+    float lo[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) lo[e] = 0.0f;
+#pragma unroll 1
+    for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
+        const int32_t blk = trow[jb];
+        if (blk < 0 || blk >= p.num_blocks) {
+            record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
+            return;
+        }
+        float v[16];
+        const float4 *vsrc = reinterpret_cast<const float4 *>(vrow + jb * LORA_BLOCK_ROWS);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float4 q = vsrc[g];
+            v[4 * g] = q.x;
+            v[4 * g + 1] = q.y;
+            v[4 * g + 2] = q.z;
+            v[4 * g + 3] = q.w;
+        }
+        const uint4 *bsrc = reinterpret_cast<const uint4 *>(
+            p.b_arena + (static_cast<size_t>(blk) * p.N + n0) * LORA_BLOCK_ROWS);
+        const int valid = min(32, p.N - n0);  // a multiple of 8
+#pragma unroll
+        for (int eg = 0; eg < 4; ++eg) {
+            if (eg * 8 >= valid) break;
+            // columns n0 + 8eg .. +7: 16 B values each, as 2 x 16 bytes
+            uint4 q[8][2];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                q[e][0] = __ldg(bsrc + 2 * (eg * 8 + e));
+                q[e][1] = __ldg(bsrc + 2 * (eg * 8 + e) + 1);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t word = w == 0 ? q[e][h].x : w == 1 ? q[e][h].y : w == 2 ? q[e][h].z : q[e][h].w;
+                        lo[eg * 8 + e] = fmaf(__uint_as_float(word << 16), v[h * 8 + 2 * w], lo[eg * 8 + e]);
+                        lo[eg * 8 + e] = fmaf(__uint_as_float(word & 0xFFFF0000u), v[h * 8 + 2 * w + 1],
+                                              lo[eg * 8 + e]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = fmaf(s, lo[e], acc[e]);
+}
+
+__device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]) {
+    uint32_t raw[32];
+    sm100::tmem_ld_32x32b_x32(taddr, raw);
+    sm100::tmem_ld_wait(raw);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(raw[e]);
+}
+
+// Epilogue warps: warp w (2..2+kEpiWarps-1) may access TMEM lane quarter
+// w % 4; the kEpiWarps / 4 warps sharing a quarter take turns over the
+// 32-column chunks.
+template <bool SWAP, int BN>
+__device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_full, uint64_t *tmem_empty,
+                                             uint32_t tmem_base, volatile uint32_t *abort_flag,
+                                             volatile uint32_t *last_flag, int32_t *meta_slot,
+                                             int32_t *meta_rank, float *meta_scale) {
+    using namespace sm100;
+    constexpr int kGroups = kEpiWarps / 4;
+    constexpr int kChunks = BN / 32;
+    const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
+    const int warp = threadIdx.x >> 5;
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int grp = (warp - 2) >> 2;  // which of the warps sharing the quarter
+    const int lane = threadIdx.x & 31;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int32_t t = 0;
+    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
+        const Unit w = decode_unit<SWAP>(u, p);
+        const int b = t & 1;
+        if (SWAP) {
+            // slot, rank and scale of this unit's tokens (the previous unit is
+            // done with the arrays: every unit ends with a barrier)
+            for (int e = et; e < BN; e += kEpiThreads) {
+                const int32_t m = w.tb * BN + e;
+                int32_t r = 0, slot = -1;
+                float s = 0.0f;
+                if (m < p.M)
+                    slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s,
+                                        p.status, false);
+                meta_slot[e] = slot;
+                meta_rank[e] = r;
+                meta_scale[e] = s;
+            }
+        }
+        bool ok = mbar_wait_bounded(&tmem_full[b], (t >> 1) & 1, kWaitLimitNs);
+        if (!ok) {
+            record_error(p.status, kDevTimeout, 4);
+            *abort_flag = 1;
+        }
+        if (!epi_all(ok && !*abort_flag)) return;  // uniform over the epilogue warps
+        tc_fence_after_sync();
+        const uint32_t col0 = lane_addr + b * BN;
+
+        if (SWAP) {
+            const int32_t n = w.ta * kBM + q * 32 + lane;
+            const bool n_ok = n < p.N;
+            if (p.splits == 1) {
+#pragma unroll 1
+                for (int c = grp; c < kChunks; c += kGroups) {
+                    float acc[32];
+                    load_tmem_chunk(col0 + c * 32, acc);
+                    const int32_t m0 = w.tb * BN + c * 32;
+                    swap_finish_chunk(p, n, n_ok, m0, meta_slot + c * 32, meta_rank + c * 32,
+                                      meta_scale + c * 32, acc);
+                    if (n_ok) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (m0 + e < p.M)
+                                p.out[static_cast<size_t>(m0 + e) * p.ldo + n] = __float2bfloat16_rn(acc[e]);
+                    }
+                    __syncwarp();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tmem_empty[b]);
+            } else {
+                // partial tile: reduce into the fp32 buffer
+#pragma unroll 1
+                for (int c = grp; c < kChunks; c += kGroups) {
+                    float acc[32];
+                    load_tmem_chunk(col0 + c * 32, acc);
+                    const int32_t m0 = w.tb * BN + c * 32;
+                    if (n_ok) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (m0 + e < p.M) atomicAdd(p.y32 + static_cast<size_t>(m0 + e) * p.N + n, acc[e]);
+                    }
+                    __syncwarp();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tmem_empty[b]);
+                __threadfence();
+                epi_sync();
+                if (et == 0) {
+                    const int32_t old = atomicAdd(p.counters + (w.ta * p.tiles_b + w.tb), 1);
+                    *last_flag = (old == p.splits - 1) ? 1u : 0u;
+                }
+                epi_sync();
+                const bool last = *last_flag != 0;
+                if (last) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int c = grp; c < kChunks; c += kGroups) {
+                        const int32_t m0 = w.tb * BN + c * 32;
+                        float acc[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            acc[e] = (n_ok && m0 + e < p.M) ? __ldcg(p.y32 + static_cast<size_t>(m0 + e) * p.N + n)
+                                                            : 0.0f;
+                        swap_finish_chunk(p, n, n_ok, m0, meta_slot + c * 32, meta_rank + c * 32,
+                                          meta_scale + c * 32, acc);
+                        if (n_ok) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (m0 + e < p.M)
+                                    p.out[static_cast<size_t>(m0 + e) * p.ldo + n] = __float2bfloat16_rn(acc[e]);
+                        }
+                    }
+                }
+            }
+        } else {
+            const int32_t m = w.ta * kBM + q * 32 + lane;
+            int32_t r = 0, slot = -1;
+            float s = 0.0f;
+            if (m < p.M)
+                slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s, p.status,
+                                    false);
+#pragma unroll 1
+            for (int c = grp; c < kChunks; c += kGroups) {
+                float acc[32];
+                load_tmem_chunk(col0 + c * 32, acc);
+                const int32_t n0 = w.tb * BN + c * 32;
+                rows_finish_chunk(p, slot, r, s, m, n0, acc);
+                if (m < p.M) {
+                    __nv_bfloat16 *dst = p.out + static_cast<size_t>(m) * p.ldo + n0;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (n0 + g * 8 < p.N) {
+                            uint4 v;
+                            v.x = pack_bf16x2(acc[g * 8 + 0], acc[g * 8 + 1]);
+                            v.y = pack_bf16x2(acc[g * 8 + 2], acc[g * 8 + 3]);
+                            v.z = pack_bf16x2(acc[g * 8 + 4], acc[g * 8 + 5]);
+                            v.w = pack_bf16x2(acc[g * 8 + 6], acc[g * 8 + 7]);
+                            *reinterpret_cast<uint4 *>(dst + g * 8) = v;
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tmem_empty[b]);
+        }
+        epi_sync();  // metadata and last_flag are rewritten by the next unit
+    }
+}
+
+// --------------------------------------------------------------- kernel
+
+template <bool SWAP, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                     const TcParams p) {
     using namespace sm100;
-    constexpr uint32_t kABytes = kBM * kBK * 2;
-    constexpr uint32_t kBBytes = BN * kBK * 2;
-    constexpr uint32_t kCols = tmem_cols<BN>();
-
+    using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * kBBytes);
-    uint64_t *empty = full + STAGES;
-    uint64_t *tmem_full = empty + STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_full + 1);
+    uint8_t *sB = smem + C::kStages * C::kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tmem_full = empty + C::kStages;   // [2]
+    uint64_t *tmem_empty = tmem_full + 2;       // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
+    volatile uint32_t *last_flag = tmem_slot + 2;
+    int32_t *meta_slot = reinterpret_cast<int32_t *>(tmem_slot + 4);
+    int32_t *meta_rank = meta_slot + BN;
+    float *meta_scale = reinterpret_cast<float *>(meta_rank + BN);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int32_t m0 = blockIdx.x * kBM;
-    const int32_t n0 = blockIdx.y * BN;
-
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(tmem_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tmem_full[b], 1);
+            mbar_init(&tmem_empty[b], kEpiWarps);
+        }
         *abort_flag = 0;
+        *last_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tmx);
-        prefetch_tensormap(&tmw);
+        prefetch_tensormap(&tma_a);
+        prefetch_tensormap(&tma_b);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kCols);
+        tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -132,136 +547,20 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_consta
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            for (int32_t kb = 0; kb < p.num_kb; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (kb / STAGES) & 1;
-                if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimitNs)) {
-                    record_error(p.status, kDevTimeout, 1);
-                    *abort_flag = 1;
-                    break;
-                }
-                if (*abort_flag) break;
-                mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
-                tma_load_2d(sA + s * kABytes, &tmx, kb * kBK, m0, &full[s]);
-                tma_load_2d(sB + s * kBBytes, &tmw, kb * kBK, n0, &full[s]);
-            }
-        }
+        if (lane == 0) run_producer<SWAP, BN>(&tma_a, &tma_b, p, sA, sB, full, empty, abort_flag);
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
-            bool ok = true;
-            for (int32_t kb = 0; kb < p.num_kb; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (kb / STAGES) & 1;
-                if (!mbar_wait_bounded(&full[s], ph, kWaitLimitNs) || *abort_flag) {
-                    if (!*abort_flag) record_error(p.status, kDevTimeout, 2);
-                    *abort_flag = 1;
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t a_addr = smem_u32(sA + s * kABytes);
-                const uint32_t b_addr = smem_u32(sB + s * kBBytes);
-#pragma unroll
-                for (int k = 0; k < kBK / kUmmaK; ++k) {
-                    mma_bf16_f32(tmem_base, desc_kmajor_sw128(a_addr + k * kUmmaK * 2),
-                                 desc_kmajor_sw128(b_addr + k * kUmmaK * 2), idesc,
-                                 (kb > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit(&empty[s]);
-            }
-            if (ok)
-                mma_commit(tmem_full);
-            else
-                mbar_arrive(tmem_full);
-        }
+        if (lane == 0)
+            run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
     } else {
-        // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int32_t m = m0 + q * 32 + lane;
-        bool ok = mbar_wait_bounded(tmem_full, 0, kWaitLimitNs);
-        if (!ok) record_error(p.status, kDevTimeout, 3);
-        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-        tc_fence_after_sync();
-        if (ok) {
-            int32_t r = 0;
-            float s = 0.0f;
-            int32_t slot = -1;
-            if (m < p.M)
-                slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s,
-                                    p.status, false);
-            const float *vrow = p.V + static_cast<size_t>(m < p.M ? m : 0) * p.ldv;
-            const int32_t *trow = p.table + static_cast<size_t>(slot < 0 ? 0 : slot) * p.bps;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t raw[32];
-                tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 32, raw);
-                tmem_ld_wait(raw);
-                float acc[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(raw[e]);
-                const int32_t nc = n0 + c * 32;
-                if (slot >= 0 && nc < p.N) {
-                    float lo[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) lo[e] = 0.0f;
-                    bool bad = false;
-#pragma unroll 1
-                    for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
-                        const int32_t b = trow[jb];
-                        if (b < 0 || b >= p.num_blocks) {
-                            record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
-                            bad = true;
-                            break;
-                        }
-                        const int32_t jn = min(LORA_BLOCK_ROWS, r - jb * LORA_BLOCK_ROWS);
-                        const __nv_bfloat16 *bt =
-                            p.bt_arena + static_cast<size_t>(b) * LORA_BLOCK_ROWS * p.N + nc;
-#pragma unroll 1
-                        for (int32_t jj = 0; jj < jn; ++jj) {
-                            const float v = vrow[jb * LORA_BLOCK_ROWS + jj];
-                            const uint4 *src = reinterpret_cast<const uint4 *>(bt + static_cast<size_t>(jj) * p.N);
-#pragma unroll
-                            for (int g = 0; g < 4; ++g) {
-                                if (nc + g * 8 < p.N) {
-                                    float bv[8];
-                                    unpack_bf16x8(__ldg(src + g), bv);
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) lo[g * 8 + e] = fmaf(bv[e], v, lo[g * 8 + e]);
-                                }
-                            }
-                        }
-                    }
-                    if (!bad) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) acc[e] = fmaf(s, lo[e], acc[e]);
-                    }
-                }
-                if (m < p.M) {
-                    __nv_bfloat16 *dst = p.out + static_cast<size_t>(m) * p.ldo + nc;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (nc + g * 8 < p.N) {
-                            uint4 w;
-                            w.x = pack_bf16x2(acc[g * 8 + 0], acc[g * 8 + 1]);
-                            w.y = pack_bf16x2(acc[g * 8 + 2], acc[g * 8 + 3]);
-                            w.z = pack_bf16x2(acc[g * 8 + 4], acc[g * 8 + 5]);
-                            w.w = pack_bf16x2(acc[g * 8 + 6], acc[g * 8 + 7]);
-                            *reinterpret_cast<uint4 *>(dst + g * 8) = w;
-                        }
-                    }
-                }
-                __syncwarp();
-            }
-        }
+        run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, meta_slot,
+                               meta_rank, meta_scale);
     }
 
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, kCols);
+        tmem_dealloc(tmem_base, C::kTmemCols);
     }
 }
 
@@ -303,17 +602,17 @@ int sm_count() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
     if (!cache[dev]) {
         int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n > 0 ? n : 148;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
     }
     return cache[dev];
 }
 
-template <int BN, int STAGES>
-cudaError_t launch_tile(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
-    auto kernel = tc_gemm_lora_kernel<BN, STAGES>;
-    constexpr size_t smem = smem_bytes<BN, STAGES>();
-    // the shared-memory opt-in is a per-device function attribute
+template <bool SWAP, int BN>
+cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, float *y32,
+                           int32_t *counters, cudaStream_t stream) {
+    using C = Cfg<BN>;
+    auto kernel = tc_gemm_lora_kernel<SWAP, BN>;
     static std::mutex mu;
     static bool done[128] = {};
     int dev = 0;
@@ -322,25 +621,30 @@ cudaError_t launch_tile(const ForwardPlan &plan, const ProjView &v, cudaStream_t
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!done[dev]) {
+        if (!done[dev]) {  // the shared-memory opt-in is a per-device function attribute
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem));
+                                     static_cast<int>(C::kSmem));
             if (e != cudaSuccess) return e;
             done[dev] = true;
         }
     }
-    CUtensorMap tmx, tmw;
-    if (!make_tmap_bf16(&tmx, plan.x, plan.M, plan.K, plan.ldx, kBM)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16(&tmw, v.W, v.N, plan.K, plan.K, BN)) return cudaErrorInvalidValue;
+    CUtensorMap tx, tw;
+    if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, SWAP ? BN : kBM)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, SWAP ? kBM : BN)) return cudaErrorInvalidValue;
     TcParams p;
     p.M = plan.M;
     p.N = v.N;
     p.K = plan.K;
-    p.num_kb = (plan.K + kBK - 1) / kBK;
+    p.num_kb = tp.num_kb;
+    p.kb_per_split = tp.kb_per_split;
+    p.splits = tp.splits;
+    p.tiles_a = tp.tiles_a;
+    p.tiles_b = tp.tiles_b;
+    p.num_units = tp.units;
     p.out = static_cast<__nv_bfloat16 *>(v.out);
     p.ldo = v.ldo;
     p.row_slot = plan.row_slot;
-    p.bt_arena = static_cast<const __nv_bfloat16 *>(v.bt_arena);
+    p.b_arena = static_cast<const __nv_bfloat16 *>(v.b_arena);
     p.table = v.table;
     p.ranks = v.ranks;
     p.scales = v.scales;
@@ -349,39 +653,75 @@ cudaError_t launch_tile(const ForwardPlan &plan, const ProjView &v, cudaStream_t
     p.num_blocks = v.num_blocks;
     p.V = v.V;
     p.ldv = v.max_rank;
+    p.y32 = y32;
+    p.counters = counters;
     p.status = plan.status;
-    dim3 grid((plan.M + kBM - 1) / kBM, (v.N + BN - 1) / BN);
-    kernel<<<grid, kThreads, smem, stream>>>(tmx, tmw, p);
+    if (tp.splits > 1) {
+        e = cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(plan.M) * v.N, stream);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(counters, 0, sizeof(int32_t) * static_cast<size_t>(tp.tiles_a) * tp.tiles_b,
+                                stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (SWAP) {
+        kernel<<<tp.grid, kThreads, C::kSmem, stream>>>(tw, tx, p);
+    } else {
+        kernel<<<tp.grid, kThreads, C::kSmem, stream>>>(tx, tw, p);
+    }
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// Tile width: fewest waves of CTAs over the SMs, weighting each tile by its
-// width plus a fixed per-tile cost.
-int choose_tc_bn(int32_t M, int32_t N) {
+// Orientation, tile width and split-K factor for an M x N x K problem.
+TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
+    TcPlan t{};
     const int sms = sm_count();
-    const int mt = (M + kBM - 1) / kBM;
-    int best = 256;
-    long best_cost = -1;
-    for (int bn : {256, 128, 64}) {
-        const long tiles = static_cast<long>(mt) * ((N + bn - 1) / bn);
-        const long waves = (tiles + sms - 1) / sms;
-        const long cost = waves * (bn + 32);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = bn;
-        }
+    t.num_kb = (K + kBK - 1) / kBK;
+    t.swap = M <= 512;
+    if (t.swap) {
+        // tokens per tile at most 128, so an x tile is never larger than a W tile
+        t.bn = M <= 32 ? 32 : M <= 64 ? 64 : 128;
+        t.tiles_a = (N + kBM - 1) / kBM;
+        t.tiles_b = (M + t.bn - 1) / t.bn;
+        const int tiles = t.tiles_a * t.tiles_b;
+        int s = tiles >= sms ? 1 : sms / tiles;
+        s = s < 1 ? 1 : s;
+        const int max_s = t.num_kb / 4 > 0 ? t.num_kb / 4 : 1;
+        if (s > max_s) s = max_s;
+        if (s > 16) s = 16;
+        t.kb_per_split = (t.num_kb + s - 1) / s;
+        t.splits = (t.num_kb + t.kb_per_split - 1) / t.kb_per_split;
+    } else {
+        t.tiles_a = (M + kBM - 1) / kBM;
+        const long u256 = static_cast<long>(t.tiles_a) * ((N + 255) / 256);
+        const long u128 = static_cast<long>(t.tiles_a) * ((N + 127) / 128);
+        const long c256 = ((u256 + sms - 1) / sms) * (256 + 32);
+        const long c128 = ((u128 + sms - 1) / sms) * (128 + 32);
+        t.bn = c256 <= c128 ? 256 : 128;
+        t.tiles_b = (N + t.bn - 1) / t.bn;
+        t.splits = 1;
+        t.kb_per_split = t.num_kb;
     }
-    return best;
+    t.units = t.tiles_a * t.tiles_b * t.splits;
+    t.grid = t.units < sms ? t.units : sms;
+    t.y32_bytes = t.splits > 1 ? sizeof(float) * static_cast<size_t>(M) * N : 0;
+    t.counter_bytes = t.splits > 1 ? sizeof(int32_t) * static_cast<size_t>(t.tiles_a) * t.tiles_b : 0;
+    return t;
 }
 
-cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
-    switch (choose_tc_bn(plan.M, v.N)) {
-        case 256: return launch_tile<256, 4>(plan, v, stream);
-        case 128: return launch_tile<128, 6>(plan, v, stream);
-        default: return launch_tile<64, 8>(plan, v, stream);
+cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, float *y32, int32_t *counters,
+                                cudaStream_t stream) {
+    const TcPlan tp = plan_tc(plan.M, v.N, plan.K);
+    if (tp.swap) {
+        switch (tp.bn) {
+            case 32: return launch_variant<true, 32>(plan, v, tp, y32, counters, stream);
+            case 64: return launch_variant<true, 64>(plan, v, tp, y32, counters, stream);
+            default: return launch_variant<true, 128>(plan, v, tp, y32, counters, stream);
+        }
     }
+    if (tp.bn == 128) return launch_variant<false, 128>(plan, v, tp, y32, counters, stream);
+    return launch_variant<false, 256>(plan, v, tp, y32, counters, stream);
 }
 
 }  // namespace lora

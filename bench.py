@@ -157,7 +157,7 @@ def algorithmic(wl):
     """Per-call algorithmic bytes and flops of each kernel stage.
 
     GEMM (per projection): W, x and out once, plus the fused expand's
-    adapter B^T rows (each distinct adapter once) and V reads; flops 2MNK
+    adapter B rows (each distinct adapter once) and V reads; flops 2MNK
     plus the expand's 2 r N per adapted row.  Shrink: each distinct
     adapter's A rows once, x rows of adapted rows, V writes.
     """

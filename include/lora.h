@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define LORA_ABI_VERSION 1
+#define LORA_ABI_VERSION 2
 #define LORA_BLOCK_ROWS 16
 #define LORA_MAX_PROJ 4
 
@@ -77,24 +77,24 @@ typedef enum lora_dtype {
 /* ---------------------------------------------------------------------- */
 
 /*
- * Description of one projection's adapter pool.  Block b holds rank-rows
- * of one adapter in both arenas: A rows (width K) at
- * a_arena[b*16*K .. (b+1)*16*K) and B^T rows (width N) at
- * bt_arena[b*16*N .. (b+1)*16*N), row-major, in `dtype`.  Slot s of rank r
- * uses blocks block_table[s*(max_rank/16) + t] for t < ceil(r/16); rank-row
- * j of the adapter is row j%16 of block t = j/16.  Rows of a slot's last
- * block beyond its rank are zero.  ranks[s] = 0 marks an empty slot, and
- * scales[s] = alpha/r (fp32).  Unused table entries are -1.
+ * Description of one projection's adapter pool.  Block b holds 16 rank
+ * indices j (16t <= j < 16t+16) of one adapter in both arenas, in `dtype`:
+ *   a_arena[(b*16 + jj)*K + k]  = A_i[16t + jj][k]   (16 rows of A, width K)
+ *   b_arena[(b*N + n)*16 + jj]  = B_i[n][16t + jj]   (N rows of 16 B values)
+ * Slot s of rank r uses blocks block_table[s*(max_rank/16) + t] for
+ * t < ceil(r/16).  Entries of a slot's last block beyond its rank are zero.
+ * ranks[s] = 0 marks an empty slot, and scales[s] = alpha/r (fp32).  Unused
+ * table entries are -1.
  */
 typedef struct lora_pool_desc {
     lora_dtype_t dtype;
     int32_t K;            /* in-features: width of A rows; multiple of 8 (bf16) / 4 (fp32) */
-    int32_t N;            /* out-features: width of B^T rows; same rule */
+    int32_t N;            /* out-features: rows of B; same rule */
     int32_t max_slots;    /* adapters that can be resident at once (>= 1) */
     int32_t max_rank;     /* largest rank accepted; multiple of 16, <= 1024 */
     int32_t num_blocks;   /* blocks in each arena (>= 1) */
     void *a_arena;        /* device, num_blocks*16*K elements */
-    void *bt_arena;       /* device, num_blocks*16*N elements */
+    void *b_arena;        /* device, num_blocks*N*16 elements */
     int32_t *block_table; /* device, max_slots*(max_rank/16) int32 */
     int32_t *ranks;       /* device, max_slots int32 */
     float *scales;        /* device, max_slots fp32 */
@@ -120,8 +120,8 @@ lora_status_t lora_pool_destroy(lora_pool_t *pool);
  * Load adapter (A [rank][K] row-major, B [N][rank] row-major, both in the
  * pool dtype) into empty slot `slot` with scale alpha/rank.  Takes
  * ceil(rank/16) blocks from the free list, copies A's rank-rows and B's
- * columns (as B^T rows) into them, zeroes the unused tail rows of the last
- * block, and writes the slot's table row, rank and scale.  The pages call
+ * columns into them (16 of each per block), zeroes the unused tail of the
+ * last block, and writes the slot's table row, rank and scale.  The pages call
  * this activating an adapter into a GPU slot ("LoRA Adapters: Many Models
  * in One", §"Three tiers of storage"; "S-LoRA…", §"Unified paging").
  * src_on_device = 0: A and B are host memory; the call returns once the

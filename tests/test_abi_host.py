@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.lora_abi_version() == 1
+    assert L.lora_abi_version() == 2
     from adapter_gemm_linear_gb300._lib import STATUS_NAMES
     texts = {L.lora_status_string(c).decode() for c in STATUS_NAMES}
     assert len(texts) == len(STATUS_NAMES) and all(texts)
@@ -79,13 +79,13 @@ def test_pool_create_validation_without_device(L):
 
     def desc(**kw):
         d = dict(dtype=0, K=64, N=64, max_slots=4, max_rank=16, num_blocks=8,
-                 a_arena=0x10000, bt_arena=0x20000, block_table=0x30000, ranks=0x40000,
+                 a_arena=0x10000, b_arena=0x20000, block_table=0x30000, ranks=0x40000,
                  scales=0x50000, free_list_seed=0)
         d.update(kw)
         return PoolDesc(**d)
 
     assert L.lora_pool_create(ctypes.byref(desc(a_arena=None)), None, ctypes.byref(out)) == 1
-    assert L.lora_pool_create(ctypes.byref(desc(bt_arena=0x20008)), None, ctypes.byref(out)) == 2
+    assert L.lora_pool_create(ctypes.byref(desc(b_arena=0x20008)), None, ctypes.byref(out)) == 2
     assert L.lora_pool_create(ctypes.byref(desc(K=60)), None, ctypes.byref(out)) == 2
     assert L.lora_pool_create(ctypes.byref(desc(max_rank=20)), None, ctypes.byref(out)) == 4
     assert L.lora_pool_create(ctypes.byref(desc(max_rank=2048)), None, ctypes.byref(out)) == 4

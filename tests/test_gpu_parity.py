@@ -34,7 +34,8 @@ def _sample_rows(wl, n=48, seed=0):
 
 
 @pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
-@pytest.mark.parametrize("shape", [(300, 520, 392), (130, 1024, 264), (1, 64, 8), (257, 136, 1000)])
+@pytest.mark.parametrize("shape", [(300, 520, 392), (130, 1024, 264), (1, 64, 8), (257, 136, 1000),
+                                   (64, 2048, 520), (17, 4096, 136), (600, 256, 200), (520, 1024, 2056)])
 def test_small_mixed_ranks(shape, mode):
     M, K, N = shape
     wl = synth(M=M, K=K, Ns=[N], num_slots=7, rank_choices=(1, 7, 16, 33, 64), seed=M + K + N)
@@ -64,6 +65,22 @@ def test_integer_exact_bitwise(mode):
         want = H.oracle_bf16_bits(H.oracle_rows(wl, p))
         got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         assert np.array_equal(got, want), f"projection {p}: {np.sum(got != want)} outputs differ"
+
+
+@pytest.mark.parametrize("shape", [(64, 2048, (264, 520)), (37, 1024, (1032,)), (700, 192, (136,))])
+def test_integer_exact_split_k_and_orientations(shape):
+    """Bit-exact through the split-K reduction (few tokens, long K: several
+    CTAs share each output tile) and the non-swapped orientation (many
+    tokens)."""
+    M, K, Ns = shape
+    wl = synth(M=M, K=K, Ns=list(Ns), num_slots=6, rank_choices=(4, 16, 32), integer=True,
+               seed=M + K, none_frac=0.2)
+    pools = H.make_pools(wl, DEV)
+    outs = H.forward(wl, pools, "bgmv")
+    for p in range(len(Ns)):
+        want = H.oracle_bf16_bits(H.oracle_rows(wl, p))
+        got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), f"{shape} projection {p}: {np.sum(got != want)} outputs differ"
 
 
 def test_tiny_fp32_full():
@@ -159,9 +176,9 @@ def test_device_source_load_matches_host_load():
                 blk = pool.a_arena[bh[t]].float().cpu().numpy()
                 assert np.array_equal(blk[:rows], A[16 * t:16 * t + rows])
                 assert not blk[rows:].any()
-                blt = pool.bt_arena[bh[t]].float().cpu().numpy()
-                assert np.array_equal(blt[:rows], B.T[16 * t:16 * t + rows])
-                assert not blt[rows:].any()
+                blb = pool.b_arena[bh[t]].float().cpu().numpy()  # [N, 16]
+                assert np.array_equal(blb[:, :rows], B[:, 16 * t:16 * t + rows])
+                assert not blb[:, rows:].any()
 
 
 def test_unload_reload_and_errors():
