@@ -321,6 +321,7 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     if (a->num_stage_events == 0 && a->stage_events) return LORA_ERR_INVALID_ARG;
     plan->stage_events = a->stage_events;
     plan->dtype = a->dtype;
+    plan->v_parts = 1;
     plan->M = a->M;
     plan->K = a->K;
     plan->ldx = a->ldx;
@@ -357,21 +358,25 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         v.max_rank = d.max_rank;
         v.V = nullptr;
         ws->v_off[i] = off;
-        off += align_up(sizeof(float) * static_cast<size_t>(a->M) * d.max_rank, 256);
+        off += align_up(sizeof(float) * static_cast<size_t>(a->M) * d.max_rank * plan->v_parts, 256);
     }
     // slot ids of every pool must mean the same adapters
     for (int i = 1; i < a->n_proj; ++i)
         if (a->proj[i].pool->d.max_slots != a->proj[0].pool->d.max_slots) return LORA_ERR_INVALID_ARG;
     // split-K scratch of the tensor-core GEMM, shared by the projections
     // (their GEMMs run one after the other on the stream)
-    size_t y32 = 0, cnt = 0;
+    size_t y32 = 0, cnt = 0, shr = 0;
     if (a->dtype == LORA_BF16 && a->M > 0) {
         for (int i = 0; i < a->n_proj; ++i) {
             const lora::TcPlan tp = lora::plan_tc(a->M, a->proj[i].pool->d.N, a->K);
             y32 = std::max(y32, tp.y32_bytes);
             cnt = std::max(cnt, tp.counter_bytes);
+            if (lora::shrink_grouped_supported(a->M, a->proj[i].pool->d.max_slots))
+                shr = std::max(shr, lora::shrink_workspace_bytes(a->M, a->K, a->proj[i].pool->d.max_rank));
         }
     }
+    ws->shrink_off = off;
+    off += align_up(shr, 256);
     ws->y32_off = off;
     off += align_up(y32, 256);
     ws->counter_off = off;
@@ -399,6 +404,7 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
     if (lora::device_status_ptr(&plan.status) != cudaSuccess) return LORA_ERR_CUDA;
     for (int i = 0; i < plan.n_proj; ++i) plan.proj[i].V = reinterpret_cast<float *>(base + ws.v_off[i]);
     plan.y32 = reinterpret_cast<float *>(base + ws.y32_off);
+    plan.shrink_scratch = base + ws.shrink_off;
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);
     cudaStream_t st = as_stream(stream);
     if (plan.stage_events &&

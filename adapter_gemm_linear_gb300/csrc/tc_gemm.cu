@@ -72,22 +72,27 @@ struct TcParams {
     int32_t max_slots, bps, num_blocks;
     const float *V;
     int32_t ldv;
+    int32_t v_parts;        // 1 or 2 partial planes of V, summed here
+    size_t v_part_stride;   // elements between the planes
     float *y32;         // split-K accumulator [M][N], zero on entry (splits > 1)
     int32_t *counters;  // per tile, zero on entry (splits > 1)
     unsigned long long *status;
 };
 
-template <int BN>
+template <bool SWAP, int BN>
 struct Cfg {
     static constexpr uint32_t kABytes = kBM * kBK * 2;
     static constexpr uint32_t kBBytes = BN * kBK * 2;
-    static constexpr int kStages0 = kRingBudget / static_cast<int>(kABytes + kBBytes);
+    // swapped orientation: the LoRA correction of a tile, fp32 [BN tokens][128 columns]
+    static constexpr int kCorrBytes = SWAP ? BN * kBM * 4 : 0;
+    static constexpr int kStages0 = (kRingBudget - kCorrBytes) / static_cast<int>(kABytes + kBBytes);
     static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
     static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                         : 2 * BN <= 256 ? 256 : 512;
-    // ring + barriers + TMEM address + flags + per-token metadata, plus alignment slack
-    static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) +
-                                    (2 * kStages + 4) * 8 + 16 + BN * 12;
+    // ring + correction tile + barriers + TMEM address + flags + per-token
+    // metadata (slot, rank, scale, order), plus alignment slack
+    static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kCorrBytes +
+                                    (2 * kStages + 4) * 8 + 16 + BN * 16;
     static_assert(kStages >= 2, "ring too small");
 };
 
@@ -139,7 +144,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                                              uint64_t *full, uint64_t *empty,
                                              volatile uint32_t *abort_flag) {
     using namespace sm100;
-    using C = Cfg<BN>;
+    using C = Cfg<SWAP, BN>;
     int32_t it = 0;
     for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         const Unit w = decode_unit<SWAP>(u, p);
@@ -167,7 +172,7 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
                                         uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
                                         uint32_t tmem_base, volatile uint32_t *abort_flag) {
     using namespace sm100;
-    using C = Cfg<BN>;
+    using C = Cfg<SWAP, BN>;
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
     int32_t it = 0, t = 0;
     for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
@@ -222,60 +227,6 @@ __device__ __forceinline__ bool epi_all(bool v) {
     return r != 0;
 }
 
-// Swapped orientation: this thread owns output column n; the 32 values in
-// acc are tokens m0 .. m0+31 (meta_* hold their slot, rank, scale).  For one
-// token all lanes of the warp use the same adapter: the B rows they read are
-// 32 consecutive 32-byte pieces and the V values are a broadcast.
-__device__ __forceinline__ void swap_finish_chunk(const TcParams &p, int32_t n, bool n_ok, int32_t m0,
-                                                  const int32_t *meta_slot, const int32_t *meta_rank,
-                                                  const float *meta_scale, float (&acc)[32]) {
-    if (!n_ok) return;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-        const int32_t slot = meta_slot[e];
-        if (slot < 0) continue;
-        const int32_t r = meta_rank[e];
-        const float *vrow = p.V + static_cast<size_t>(m0 + e) * p.ldv;
-        const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;
-        float lo0 = 0.0f, lo1 = 0.0f, lo2 = 0.0f, lo3 = 0.0f;
-        bool bad = false;
-#pragma unroll 1
-        for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
-            const int32_t blk = trow[jb];
-            if (blk < 0 || blk >= p.num_blocks) {
-                record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
-                bad = true;
-                break;
-            }
-            const uint4 *bsrc = reinterpret_cast<const uint4 *>(
-                p.b_arena + (static_cast<size_t>(blk) * p.N + n) * LORA_BLOCK_ROWS);
-            const float4 *vsrc = reinterpret_cast<const float4 *>(vrow + jb * LORA_BLOCK_ROWS);
-            const uint4 q0 = __ldg(bsrc), q1 = __ldg(bsrc + 1);
-            const float4 v0 = vsrc[0], v1 = vsrc[1], v2 = vsrc[2], v3 = vsrc[3];
-            float bv[16];
-            unpack_bf16x8(q0, bv);
-            unpack_bf16x8(q1, bv + 8);
-            lo0 = fmaf(bv[0], v0.x, lo0);
-            lo1 = fmaf(bv[1], v0.y, lo1);
-            lo2 = fmaf(bv[2], v0.z, lo2);
-            lo3 = fmaf(bv[3], v0.w, lo3);
-            lo0 = fmaf(bv[4], v1.x, lo0);
-            lo1 = fmaf(bv[5], v1.y, lo1);
-            lo2 = fmaf(bv[6], v1.z, lo2);
-            lo3 = fmaf(bv[7], v1.w, lo3);
-            lo0 = fmaf(bv[8], v2.x, lo0);
-            lo1 = fmaf(bv[9], v2.y, lo1);
-            lo2 = fmaf(bv[10], v2.z, lo2);
-            lo3 = fmaf(bv[11], v2.w, lo3);
-            lo0 = fmaf(bv[12], v3.x, lo0);
-            lo1 = fmaf(bv[13], v3.y, lo1);
-            lo2 = fmaf(bv[14], v3.z, lo2);
-            lo3 = fmaf(bv[15], v3.w, lo3);
-        }
-        if (!bad) acc[e] = fmaf(meta_scale[e], (lo0 + lo1) + (lo2 + lo3), acc[e]);
-    }
-}
-
 // Non-swapped orientation: this thread owns token row m (adapter slot, rank
 // r, scale s); the 32 values in acc are output columns n0 .. n0+31.  The
 // correction for 8 columns at a time keeps 8 independent accumulators.
@@ -298,7 +249,11 @@ __device__ __forceinline__ void rows_finish_chunk(const TcParams &p, int32_t slo
         const float4 *vsrc = reinterpret_cast<const float4 *>(vrow + jb * LORA_BLOCK_ROWS);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            const float4 q = vsrc[g];
+            float4 q = vsrc[g];
+            if (p.v_parts > 1) {
+                const float4 w2 = vsrc[g + p.v_part_stride / 4];
+                q.x += w2.x; q.y += w2.y; q.z += w2.z; q.w += w2.w;
+            }
             v[4 * g] = q.x;
             v[4 * g + 1] = q.y;
             v[4 * g + 2] = q.z;
@@ -344,6 +299,83 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
     for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(raw[e]);
 }
 
+// Swapped orientation, before the tile's accumulator is ready: the LoRA
+// correction of the whole tile, corr[e][n_local] = s * sum_j B[n][j] V[m][j]
+// for the unit's tokens m = m0 + e and output columns n = n0 + n_local.
+// Tokens are walked in adapter order (meta_order), so each thread loads its
+// 32-byte piece of an adapter's B rows once per 16-rank block and applies it
+// to every token of that adapter.  The two halves of the epilogue threads take
+// alternate adapters; each (token, column) has one writer.
+template <int BN>
+__device__ __forceinline__ void build_correction(const TcParams &p, int32_t n0, int32_t m0, const int32_t *meta_slot,
+                                                 const int32_t *meta_rank, const float *meta_scale,
+                                                 const int32_t *meta_order, float *corr) {
+    const int et = threadIdx.x - 64;
+    const int n_local = et % kBM;
+    const int half = et / kBM;
+    const int32_t n = n0 + n_local;
+    const bool n_ok = n < p.N;
+    int g = 0;
+    for (int a = 0; a < BN;) {
+        const int e0 = meta_order[a];
+        const int32_t slot = meta_slot[e0];
+        if (slot < 0) break;  // tokens without an adapter are ordered last
+        int b = a + 1;
+        while (b < BN && meta_slot[meta_order[b]] == slot) ++b;
+        if ((g % (kEpiThreads / kBM)) == half && n_ok) {
+            const int32_t r = meta_rank[e0];
+            const float s = meta_scale[e0];
+            const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;
+            bool ok = true;
+            for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb)
+                ok &= (trow[jb] >= 0 && trow[jb] < p.num_blocks);
+            if (!ok) {
+                record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
+            } else {
+#pragma unroll 1
+                for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
+                    const uint4 *bsrc = reinterpret_cast<const uint4 *>(
+                        p.b_arena + (static_cast<size_t>(trow[jb]) * p.N + n) * LORA_BLOCK_ROWS);
+                    float bv[16];
+                    unpack_bf16x8(__ldg(bsrc), bv);
+                    unpack_bf16x8(__ldg(bsrc + 1), bv + 8);
+#pragma unroll 2
+                    for (int i = a; i < b; ++i) {
+                        const int e = meta_order[i];
+                        const float4 *vsrc = reinterpret_cast<const float4 *>(
+                            p.V + static_cast<size_t>(m0 + e) * p.ldv + jb * LORA_BLOCK_ROWS);
+                        float4 v0 = vsrc[0], v1 = vsrc[1], v2 = vsrc[2], v3 = vsrc[3];
+                        if (p.v_parts > 1) {
+                            const float4 *vs2 = vsrc + p.v_part_stride / 4;
+                            const float4 w0 = vs2[0], w1 = vs2[1], w2 = vs2[2], w3 = vs2[3];
+                            v0.x += w0.x; v0.y += w0.y; v0.z += w0.z; v0.w += w0.w;
+                            v1.x += w1.x; v1.y += w1.y; v1.z += w1.z; v1.w += w1.w;
+                            v2.x += w2.x; v2.y += w2.y; v2.z += w2.z; v2.w += w2.w;
+                            v3.x += w3.x; v3.y += w3.y; v3.z += w3.z; v3.w += w3.w;
+                        }
+                        float d0 = bv[0] * v0.x, d1 = bv[1] * v0.y, d2 = bv[2] * v0.z, d3 = bv[3] * v0.w;
+                        d0 = fmaf(bv[4], v1.x, d0);
+                        d1 = fmaf(bv[5], v1.y, d1);
+                        d2 = fmaf(bv[6], v1.z, d2);
+                        d3 = fmaf(bv[7], v1.w, d3);
+                        d0 = fmaf(bv[8], v2.x, d0);
+                        d1 = fmaf(bv[9], v2.y, d1);
+                        d2 = fmaf(bv[10], v2.z, d2);
+                        d3 = fmaf(bv[11], v2.w, d3);
+                        d0 = fmaf(bv[12], v3.x, d0);
+                        d1 = fmaf(bv[13], v3.y, d1);
+                        d2 = fmaf(bv[14], v3.z, d2);
+                        d3 = fmaf(bv[15], v3.w, d3);
+                        corr[e * kBM + n_local] = fmaf(s, (d0 + d1) + (d2 + d3), corr[e * kBM + n_local]);
+                    }
+                }
+            }
+        }
+        ++g;
+        a = b;
+    }
+}
+
 // Epilogue warps: warp w (2..2+kEpiWarps-1) may access TMEM lane quarter
 // w % 4; the kEpiWarps / 4 warps sharing a quarter take turns over the
 // 32-column chunks.
@@ -351,7 +383,8 @@ template <bool SWAP, int BN>
 __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_full, uint64_t *tmem_empty,
                                              uint32_t tmem_base, volatile uint32_t *abort_flag,
                                              volatile uint32_t *last_flag, int32_t *meta_slot,
-                                             int32_t *meta_rank, float *meta_scale) {
+                                             int32_t *meta_rank, float *meta_scale, int32_t *meta_order,
+                                             float *corr) {
     using namespace sm100;
     constexpr int kGroups = kEpiWarps / 4;
     constexpr int kChunks = BN / 32;
@@ -380,6 +413,27 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                 meta_scale[e] = s;
             }
         }
+        // the split that owns the correction of a swapped tile builds it now,
+        // while the tile's MMAs run
+        const bool owns = SWAP && (p.splits == 1 || w.ks == 0);
+        if (SWAP) {
+            epi_sync();
+            if (owns) {
+                for (int e = et; e < BN; e += kEpiThreads) {
+                    const int32_t key = meta_slot[e] < 0 ? 0x7fffffff : meta_slot[e];
+                    int rnk = 0;
+                    for (int e2 = 0; e2 < BN; ++e2) {
+                        const int32_t k2 = meta_slot[e2] < 0 ? 0x7fffffff : meta_slot[e2];
+                        rnk += (k2 < key) || (k2 == key && e2 < e);
+                    }
+                    meta_order[rnk] = e;
+                }
+                for (int i = et; i < BN * kBM; i += kEpiThreads) corr[i] = 0.0f;
+                epi_sync();
+                build_correction<BN>(p, w.ta * kBM, w.tb * BN, meta_slot, meta_rank, meta_scale, meta_order, corr);
+                epi_sync();
+            }
+        }
         bool ok = mbar_wait_bounded(&tmem_full[b], (t >> 1) & 1, kWaitLimitNs);
         if (!ok) {
             record_error(p.status, kDevTimeout, 4);
@@ -398,8 +452,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                     float acc[32];
                     load_tmem_chunk(col0 + c * 32, acc);
                     const int32_t m0 = w.tb * BN + c * 32;
-                    swap_finish_chunk(p, n, n_ok, m0, meta_slot + c * 32, meta_rank + c * 32,
-                                      meta_scale + c * 32, acc);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] += corr[(c * 32 + e) * kBM + q * 32 + lane];
                     if (n_ok) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
@@ -418,6 +472,10 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                     float acc[32];
                     load_tmem_chunk(col0 + c * 32, acc);
                     const int32_t m0 = w.tb * BN + c * 32;
+                    if (owns) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[e] += corr[(c * 32 + e) * kBM + q * 32 + lane];
+                    }
                     if (n_ok) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
@@ -446,8 +504,6 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                         for (int e = 0; e < 32; ++e)
                             acc[e] = (n_ok && m0 + e < p.M) ? __ldcg(p.y32 + static_cast<size_t>(m0 + e) * p.N + n)
                                                             : 0.0f;
-                        swap_finish_chunk(p, n, n_ok, m0, meta_slot + c * 32, meta_rank + c * 32,
-                                          meta_scale + c * 32, acc);
                         if (n_ok) {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
@@ -501,13 +557,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                     const TcParams p) {
     using namespace sm100;
-    using C = Cfg<BN>;
+    using C = Cfg<SWAP, BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::kStages * C::kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes);
+    float *corr = reinterpret_cast<float *>(sB + C::kStages * C::kBBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes + C::kCorrBytes);
     uint64_t *empty = full + C::kStages;
     uint64_t *tmem_full = empty + C::kStages;   // [2]
     uint64_t *tmem_empty = tmem_full + 2;       // [2]
@@ -517,6 +574,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     int32_t *meta_slot = reinterpret_cast<int32_t *>(tmem_slot + 4);
     int32_t *meta_rank = meta_slot + BN;
     float *meta_scale = reinterpret_cast<float *>(meta_rank + BN);
+    int32_t *meta_order = reinterpret_cast<int32_t *>(meta_scale + BN);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -553,7 +611,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
             run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
     } else {
         run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, meta_slot,
-                               meta_rank, meta_scale);
+                               meta_rank, meta_scale, meta_order, corr);
     }
 
     tc_fence_before_sync();
@@ -611,7 +669,7 @@ int sm_count() {
 template <bool SWAP, int BN>
 cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, float *y32,
                            int32_t *counters, cudaStream_t stream) {
-    using C = Cfg<BN>;
+    using C = Cfg<SWAP, BN>;
     auto kernel = tc_gemm_lora_kernel<SWAP, BN>;
     static std::mutex mu;
     static bool done[128] = {};
@@ -653,6 +711,8 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.num_blocks = v.num_blocks;
     p.V = v.V;
     p.ldv = v.max_rank;
+    p.v_parts = plan.v_parts;
+    p.v_part_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.y32 = y32;
     p.counters = counters;
     p.status = plan.status;
