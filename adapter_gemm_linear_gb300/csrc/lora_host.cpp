@@ -365,18 +365,14 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         if (a->proj[i].pool->d.max_slots != a->proj[0].pool->d.max_slots) return LORA_ERR_INVALID_ARG;
     // split-K scratch of the tensor-core GEMM, shared by the projections
     // (their GEMMs run one after the other on the stream)
-    size_t y32 = 0, cnt = 0, shr = 0;
+    size_t y32 = 0, cnt = 0;
     if (a->dtype == LORA_BF16 && a->M > 0) {
         for (int i = 0; i < a->n_proj; ++i) {
             const lora::TcPlan tp = lora::plan_tc(a->M, a->proj[i].pool->d.N, a->K);
             y32 = std::max(y32, tp.y32_bytes);
             cnt = std::max(cnt, tp.counter_bytes);
-            if (lora::shrink_grouped_supported(a->M, a->proj[i].pool->d.max_slots))
-                shr = std::max(shr, lora::shrink_workspace_bytes(a->M, a->K, a->proj[i].pool->d.max_rank));
         }
     }
-    ws->shrink_off = off;
-    off += align_up(shr, 256);
     ws->y32_off = off;
     off += align_up(y32, 256);
     ws->counter_off = off;
@@ -404,7 +400,6 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
     if (lora::device_status_ptr(&plan.status) != cudaSuccess) return LORA_ERR_CUDA;
     for (int i = 0; i < plan.n_proj; ++i) plan.proj[i].V = reinterpret_cast<float *>(base + ws.v_off[i]);
     plan.y32 = reinterpret_cast<float *>(base + ws.y32_off);
-    plan.shrink_scratch = base + ws.shrink_off;
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);
     cudaStream_t st = as_stream(stream);
     if (plan.stage_events &&

@@ -70,7 +70,6 @@ struct ForwardPlan {
     float *y32;                 // workspace: split-K accumulator
     int32_t *counters;          // workspace: split-K tile counters
     int v_parts;                // partial planes of V the shrink writes (1 or 2)
-    void *shrink_scratch;       // workspace: grouped-shrink partials
 };
 
 // Count of kernels launched by the library (lora_kernel_launches).
@@ -80,7 +79,6 @@ void count_launches(int n);
 struct WorkspaceLayout {
     size_t row_slot_off;          // int32[M] (segment mode only)
     size_t v_off[LORA_MAX_PROJ];  // fp32[M][max_rank]
-    size_t shrink_off;            // grouped-shrink partial planes and counters (largest projection)
     size_t y32_off;               // fp32[M][N] split-K accumulator (largest projection)
     size_t counter_off;           // int32 per output tile (split-K)
     size_t total;
@@ -106,14 +104,6 @@ cudaError_t launch_segments_to_rows(int32_t M, const int32_t *seg_offsets,
 cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32_t *blocks,
                                 const void *A, const void *B, cudaStream_t stream);
 cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream);
-
-// Grouped shrink for bf16 (shrink.cu): scratch it needs and launch.
-size_t shrink_workspace_bytes(int32_t M, int32_t K, int32_t max_rank);
-bool shrink_grouped_supported(int32_t M, int32_t max_slots);
-cudaError_t launch_shrink_grouped(const ForwardPlan &plan, const ProjView &v, void *scratch,
-                                  cudaStream_t stream);
-// Rows above which the per-row shrink kernel is used instead of the grouped one.
-constexpr int32_t kGroupedShrinkMaxRows = 1024;
 
 // Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K);

@@ -311,17 +311,12 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
     using T = __nv_bfloat16;
     for (int p = 0; p < plan.n_proj; ++p) {
         const ProjView &v = plan.proj[p];
-        cudaError_t e;
-        if (shrink_grouped_supported(plan.M, v.max_slots)) {
-            e = launch_shrink_grouped(plan, v, plan.shrink_scratch, stream);
-        } else {
-            dim3 sgrid(plan.M, v.bps);
-            shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
-                static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
-                static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
-                v.V, v.max_rank, plan.status);
-            e = cudaGetLastError();
-        }
+        dim3 sgrid(plan.M, v.bps);
+        shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
+            static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
+            static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
+            v.V, v.max_rank, plan.status);
+        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (plan.stage_events) {
             e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[1 + 2 * p]), stream);

@@ -8,10 +8,12 @@ workload (default: the decode BGMV workload, 64 rows of q_proj 4096->4096
 with 32 rank-16 adapters).
 
 Timing: W warm-up steps, then K steps; L2 is flushed (a 2 x L2 write)
-before every step, outside the timed intervals; each step is bracketed by
-CUDA events on the launching stream and the step times are summed.  The
-dominant kernel's roofline uses stage events the library records around each
-kernel on the same stream.  `e2e` repeats the measurement through the C ABI
+before every step, outside the timed intervals.  The timed steps replay one
+forward call captured in a CUDA graph (the launch mode of a decode server),
+each replay bracketed by CUDA events on the launching stream; step times are
+summed.  The dominant kernel's roofline uses stage events the library
+records around each kernel in an eager pass over the same K steps; the eager
+step rate is reported beside the graph one.  `e2e` repeats the measurement through the C ABI
 with pinned host buffers: the host->device copy of x and the row ids and the
 device->host copy of the outputs are inside each timed step.
 
@@ -222,6 +224,10 @@ def build_case(wl, device):
 
 
 def time_device(case, wl, steps, warmup, flush, clocks_index):
+    """Eager pass with per-stage events (kernel durations for the roofline),
+    then the timed pass: one forward captured in a CUDA graph and replayed
+    once per step, an L2 flush before each replay, events around each replay
+    on the launching stream."""
     import torch
     from adapter_gemm_linear_gb300 import kernel_launches
 
@@ -231,32 +237,57 @@ def time_device(case, wl, steps, warmup, flush, clocks_index):
         flush.zero_()
         call()
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    # ---- eager pass: stage durations of every kernel
     stage = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
-    for ev in stage:  # materialise the raw events before the timed region
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for ev in stage:  # materialise the raw events before timing
         for e in ev:
             e.record()
     torch.cuda.synchronize()
-    sampler = ClockSampler(clocks_index)
-    time.sleep(0.3)
-    n0 = kernel_launches()
     for i in range(steps):
         flush.zero_()
         call.set_stage_events(stage[i])
-        starts[i].record()
+        e_starts[i].record()
         call()
-        ends[i].record()
+        e_ends[i].record()
     torch.cuda.synchronize()
-    launches = kernel_launches() - n0
-    clocks = sampler.stop()
     call.set_stage_events(None)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     n_proj = len(wl.projections)
     shrink_ms = [sum(ev[2 * p].elapsed_time(ev[2 * p + 1]) for p in range(n_proj)) for ev in stage]
     gemm_ms = [sum(ev[2 * p + 1].elapsed_time(ev[2 * p + 2]) for p in range(n_proj)) for ev in stage]
-    return {"step_ms": step_ms, "shrink_ms": shrink_ms, "gemm_ms": gemm_ms, "launches": launches,
-            "clocks": clocks}
+    eager_ms = [s.elapsed_time(e) for s, e in zip(e_starts, e_ends)]
+    # ---- timed pass: CUDA graph of one forward
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    n_cap = kernel_launches()
+    with torch.cuda.graph(graph):
+        call()
+    kernels_per_call = kernel_launches() - n_cap
+    for _ in range(warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(clocks_index)
+    time.sleep(0.3)
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record()
+        graph.replay()
+        ends[i].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    del graph
+    return {"step_ms": step_ms, "eager_ms": eager_ms, "shrink_ms": shrink_ms, "gemm_ms": gemm_ms,
+            "launches": kernels_per_call * steps, "kernels_per_call": kernels_per_call, "clocks": clocks}
 
 
 def time_e2e(case, wl, steps, flush, device):
@@ -399,7 +430,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
             "slots": wl.num_slots, "ranks": sorted(set(int(r) for r in wl.ranks)),
             "mode": wl.mode, "distinct_adapters": alg["distinct"], "adapted_rows": alg["adapted_rows"],
             "l2": "flushed before every step (2 x L2 write, outside the timed intervals)",
-            "launch": "eager, per-step CUDA events on the launching stream",
+            "launch": "CUDA graph of one lora_linear_forward call, replayed per step; events around each replay",
             "parallelism": f"replicas x{world}",
         },
         "roofline": roof,
@@ -415,6 +446,9 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         "e2e": {"value": round(wl.M * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": int(res["launches"]),
+        "kernels_per_step": int(res["kernels_per_call"]),
+        "eager": {"value": round(tokens / (sum(res["eager_ms"]) / 1e3), 1), "unit": "tokens/s",
+                  "ms_per_step": round(sum(res["eager_ms"]) / steps, 5)},
         "clocks": res["clocks"],
     }
     if not args.no_cpu_baseline:
