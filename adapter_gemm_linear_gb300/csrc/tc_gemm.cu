@@ -302,14 +302,48 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
 // Swapped orientation, before the tile's accumulator is ready: the LoRA
 // correction of the whole tile, corr[e][n_local] = s * sum_j B[n][j] V[m][j]
 // for the unit's tokens m = m0 + e and output columns n = n0 + n_local.
-// Tokens are walked in adapter order (meta_order), so each thread loads its
-// 32-byte piece of an adapter's B rows once per 16-rank block and applies it
-// to every token of that adapter.  The two halves of the epilogue threads take
-// alternate adapters; each (token, column) has one writer.
+// Tokens are walked in adapter order (meta_order); the two halves of the
+// epilogue threads take alternate adapters, so each (token, column) has one
+// writer.  A group's (token, rank block) pairs are taken four at a time, all
+// their loads (the thread's 32-byte piece of B, the token's 16 V values)
+// issued before any is used.
+__device__ __forceinline__ void dot16_acc(const uint4 &q0, const uint4 &q1, const float4 &v0, const float4 &v1,
+                                          const float4 &v2, const float4 &v3, float &a0, float &a1, float &a2,
+                                          float &a3) {
+    float bv[16];
+    unpack_bf16x8(q0, bv);
+    unpack_bf16x8(q1, bv + 8);
+    a0 = fmaf(bv[0], v0.x, a0);
+    a1 = fmaf(bv[1], v0.y, a1);
+    a2 = fmaf(bv[2], v0.z, a2);
+    a3 = fmaf(bv[3], v0.w, a3);
+    a0 = fmaf(bv[4], v1.x, a0);
+    a1 = fmaf(bv[5], v1.y, a1);
+    a2 = fmaf(bv[6], v1.z, a2);
+    a3 = fmaf(bv[7], v1.w, a3);
+    a0 = fmaf(bv[8], v2.x, a0);
+    a1 = fmaf(bv[9], v2.y, a1);
+    a2 = fmaf(bv[10], v2.z, a2);
+    a3 = fmaf(bv[11], v2.w, a3);
+    a0 = fmaf(bv[12], v3.x, a0);
+    a1 = fmaf(bv[13], v3.y, a1);
+    a2 = fmaf(bv[14], v3.z, a2);
+    a3 = fmaf(bv[15], v3.w, a3);
+}
+
+__device__ __forceinline__ float4 add4(float4 a, const float4 &b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+    return a;
+}
+
 template <int BN>
 __device__ __forceinline__ void build_correction(const TcParams &p, int32_t n0, int32_t m0, const int32_t *meta_slot,
                                                  const int32_t *meta_rank, const float *meta_scale,
                                                  const int32_t *meta_order, float *corr) {
+    constexpr int kU = 4;  // (token, rank block) pairs in flight
     const int et = threadIdx.x - 64;
     const int n_local = et % kBM;
     const int half = et / kBM;
@@ -324,49 +358,59 @@ __device__ __forceinline__ void build_correction(const TcParams &p, int32_t n0, 
         while (b < BN && meta_slot[meta_order[b]] == slot) ++b;
         if ((g % (kEpiThreads / kBM)) == half && n_ok) {
             const int32_t r = meta_rank[e0];
+            const int32_t nblk = (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
             const float s = meta_scale[e0];
             const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;
             bool ok = true;
-            for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb)
-                ok &= (trow[jb] >= 0 && trow[jb] < p.num_blocks);
+            for (int32_t jb = 0; jb < nblk; ++jb) ok &= (trow[jb] >= 0 && trow[jb] < p.num_blocks);
             if (!ok) {
                 record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
             } else {
+                // the group's (token, rank block) pairs, kU at a time
+                const int32_t total = (b - a) * nblk;
+                int t_next = a, jb_next = 0;
 #pragma unroll 1
-                for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
-                    const uint4 *bsrc = reinterpret_cast<const uint4 *>(
-                        p.b_arena + (static_cast<size_t>(trow[jb]) * p.N + n) * LORA_BLOCK_ROWS);
-                    float bv[16];
-                    unpack_bf16x8(__ldg(bsrc), bv);
-                    unpack_bf16x8(__ldg(bsrc + 1), bv + 8);
-#pragma unroll 2
-                    for (int i = a; i < b; ++i) {
-                        const int e = meta_order[i];
-                        const float4 *vsrc = reinterpret_cast<const float4 *>(
-                            p.V + static_cast<size_t>(m0 + e) * p.ldv + jb * LORA_BLOCK_ROWS);
-                        float4 v0 = vsrc[0], v1 = vsrc[1], v2 = vsrc[2], v3 = vsrc[3];
-                        if (p.v_parts > 1) {
-                            const float4 *vs2 = vsrc + p.v_part_stride / 4;
-                            const float4 w0 = vs2[0], w1 = vs2[1], w2 = vs2[2], w3 = vs2[3];
-                            v0.x += w0.x; v0.y += w0.y; v0.z += w0.z; v0.w += w0.w;
-                            v1.x += w1.x; v1.y += w1.y; v1.z += w1.z; v1.w += w1.w;
-                            v2.x += w2.x; v2.y += w2.y; v2.z += w2.z; v2.w += w2.w;
-                            v3.x += w3.x; v3.y += w3.y; v3.z += w3.z; v3.w += w3.w;
+                for (int32_t i0 = 0; i0 < total; i0 += kU) {
+                    uint4 q[kU][2];
+                    float4 v[kU][4];
+                    int eu[kU];
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        eu[u] = -1;
+                        if (i0 + u < total) {
+                            const int e = meta_order[t_next];
+                            eu[u] = e;
+                            const uint4 *bsrc = reinterpret_cast<const uint4 *>(
+                                p.b_arena + (static_cast<size_t>(trow[jb_next]) * p.N + n) * LORA_BLOCK_ROWS);
+                            q[u][0] = __ldg(bsrc);
+                            q[u][1] = __ldg(bsrc + 1);
+                            const float4 *vsrc = reinterpret_cast<const float4 *>(
+                                p.V + static_cast<size_t>(m0 + e) * p.ldv + jb_next * LORA_BLOCK_ROWS);
+                            v[u][0] = vsrc[0];
+                            v[u][1] = vsrc[1];
+                            v[u][2] = vsrc[2];
+                            v[u][3] = vsrc[3];
+                            if (p.v_parts > 1) {
+                                const float4 *vs2 = vsrc + p.v_part_stride / 4;
+                                v[u][0] = add4(v[u][0], vs2[0]);
+                                v[u][1] = add4(v[u][1], vs2[1]);
+                                v[u][2] = add4(v[u][2], vs2[2]);
+                                v[u][3] = add4(v[u][3], vs2[3]);
+                            }
+                            if (++jb_next == nblk) {
+                                jb_next = 0;
+                                ++t_next;
+                            }
                         }
-                        float d0 = bv[0] * v0.x, d1 = bv[1] * v0.y, d2 = bv[2] * v0.z, d3 = bv[3] * v0.w;
-                        d0 = fmaf(bv[4], v1.x, d0);
-                        d1 = fmaf(bv[5], v1.y, d1);
-                        d2 = fmaf(bv[6], v1.z, d2);
-                        d3 = fmaf(bv[7], v1.w, d3);
-                        d0 = fmaf(bv[8], v2.x, d0);
-                        d1 = fmaf(bv[9], v2.y, d1);
-                        d2 = fmaf(bv[10], v2.z, d2);
-                        d3 = fmaf(bv[11], v2.w, d3);
-                        d0 = fmaf(bv[12], v3.x, d0);
-                        d1 = fmaf(bv[13], v3.y, d1);
-                        d2 = fmaf(bv[14], v3.z, d2);
-                        d3 = fmaf(bv[15], v3.w, d3);
-                        corr[e * kBM + n_local] = fmaf(s, (d0 + d1) + (d2 + d3), corr[e * kBM + n_local]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        if (eu[u] >= 0) {
+                            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+                            dot16_acc(q[u][0], q[u][1], v[u][0], v[u][1], v[u][2], v[u][3], a0, a1, a2, a3);
+                            float &c = corr[eu[u] * kBM + n_local];
+                            c = fmaf(s, (a0 + a1) + (a2 + a3), c);
+                        }
                     }
                 }
             }
