@@ -365,16 +365,16 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         if (a->proj[i].pool->d.max_slots != a->proj[0].pool->d.max_slots) return LORA_ERR_INVALID_ARG;
     // split-K scratch of the tensor-core GEMM, shared by the projections
     // (their GEMMs run one after the other on the stream)
-    size_t y32 = 0, cnt = 0;
+    size_t part = 0, cnt = 0;
     if (a->dtype == LORA_BF16 && a->M > 0) {
         for (int i = 0; i < a->n_proj; ++i) {
             const lora::TcPlan tp = lora::plan_tc(a->M, a->proj[i].pool->d.N, a->K);
-            y32 = std::max(y32, tp.y32_bytes);
+            part = std::max(part, tp.part_bytes);
             cnt = std::max(cnt, tp.counter_bytes);
         }
     }
-    ws->y32_off = off;
-    off += align_up(y32, 256);
+    ws->part_off = off;
+    off += align_up(part, 256);
     ws->counter_off = off;
     off += align_up(cnt, 256);
     ws->total = off;
@@ -399,8 +399,9 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
     unsigned char *base = static_cast<unsigned char *>(args->workspace);
     if (lora::device_status_ptr(&plan.status) != cudaSuccess) return LORA_ERR_CUDA;
     for (int i = 0; i < plan.n_proj; ++i) plan.proj[i].V = reinterpret_cast<float *>(base + ws.v_off[i]);
-    plan.y32 = reinterpret_cast<float *>(base + ws.y32_off);
+    plan.part = reinterpret_cast<float *>(base + ws.part_off);
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);
+    plan.n_counters = static_cast<int32_t>((ws.total - ws.counter_off) / sizeof(int32_t));
     cudaStream_t st = as_stream(stream);
     if (plan.stage_events &&
         cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[0]), st) != cudaSuccess)

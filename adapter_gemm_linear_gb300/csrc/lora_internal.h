@@ -67,8 +67,9 @@ struct ForwardPlan {
     ProjView proj[LORA_MAX_PROJ];
     unsigned long long *status;
     void *const *stage_events;  // NULL or 1 + 2*n_proj cudaEvent_t
-    float *y32;                 // workspace: split-K accumulator
-    int32_t *counters;          // workspace: split-K tile counters
+    float *part;                // workspace: split-K partial tiles
+    int32_t *counters;          // workspace: split-K tile counters, zeroed by the shrink
+    int32_t n_counters;         // entries of `counters`
     int v_parts;                // partial planes of V the shrink writes (1 or 2)
 };
 
@@ -79,7 +80,7 @@ void count_launches(int n);
 struct WorkspaceLayout {
     size_t row_slot_off;          // int32[M] (segment mode only)
     size_t v_off[LORA_MAX_PROJ];  // fp32[M][max_rank]
-    size_t y32_off;               // fp32[M][N] split-K accumulator (largest projection)
+    size_t part_off;              // fp32 split-K partial tiles (largest projection)
     size_t counter_off;           // int32 per output tile (split-K)
     size_t total;
 };
@@ -90,7 +91,7 @@ struct TcPlan {
     int bn;               // MMA N (tokens when swapped, output columns otherwise)
     int num_kb, kb_per_split, splits;
     int tiles_a, tiles_b, units, grid;
-    size_t y32_bytes, counter_bytes;
+    size_t part_bytes, counter_bytes;  // split-K partial tiles and tile counters
 };
 
 // Launchers (lora_kernels.cu).
@@ -105,9 +106,11 @@ cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32
                                 const void *A, const void *B, cudaStream_t stream);
 cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream);
 
+// Multiprocessors of the current device (cached per device; 148 if unknown).
+int device_sm_count();
+
 // Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K);
-cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, float *y32, int32_t *counters,
-                                cudaStream_t stream);
+cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
 
 }  // namespace lora

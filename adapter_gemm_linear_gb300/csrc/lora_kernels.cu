@@ -137,9 +137,12 @@ shrink_simt_kernel(const T *__restrict__ x, int32_t ldx, int32_t K, const int32_
                    const T *__restrict__ a_arena, const int32_t *__restrict__ table,
                    const int32_t *__restrict__ ranks, int32_t max_slots, int32_t bps,
                    int32_t num_blocks, float *__restrict__ V, int32_t ldv,
-                   unsigned long long *status) {
+                   unsigned long long *status, int32_t *__restrict__ counters, int32_t n_counters) {
     const int32_t m = blockIdx.x;
     const int32_t t = blockIdx.y;
+    // the split-K tile counters of the GEMM that follows start from zero
+    if (m == 0 && t == 0)
+        for (int32_t c = threadIdx.x; c < n_counters; c += blockDim.x) counters[c] = 0;
     int32_t r;
     float s;
     const int32_t i = resolve_slot(row_slot[m], m, ranks, nullptr, max_slots, bps, &r, &s, status,
@@ -180,6 +183,101 @@ shrink_simt_kernel(const T *__restrict__ x, int32_t ldx, int32_t K, const int32_
     if (threadIdx.x < LORA_BLOCK_ROWS) {
         const float v = red[0][threadIdx.x] + red[1][threadIdx.x] + red[2][threadIdx.x] +
                         red[3][threadIdx.x];
+        V[static_cast<size_t>(m) * ldv + t * LORA_BLOCK_ROWS + threadIdx.x] = v;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 shrink for the tensor-core path: V[m, 16t + j] = sum_k A_i[16t + j, k] x[m, k]
+// grid (M, blocks per slot), 256 threads, one row x one 16-row block per CTA.
+// Each thread takes 8 consecutive k per step and keeps kBatch steps of loads
+// (the x vector and the 16 A vectors of each step) in flight before using
+// them, so a CTA has up to 256 * kBatch * 17 * 16 bytes outstanding; with
+// K = 4096 and kBatch = 2 that is the whole 128 KiB block in one round trip.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float dot8_bf16(const uint4 &a, const float (&xv)[8], float acc) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc = fmaf(__uint_as_float(w[i] << 16), xv[2 * i], acc);
+        acc = fmaf(__uint_as_float(w[i] & 0xFFFF0000u), xv[2 * i + 1], acc);
+    }
+    return acc;
+}
+
+template <int kBatch>
+__global__ void __launch_bounds__(256)
+shrink_rows_bf16_kernel(const __nv_bfloat16 *__restrict__ x, int32_t ldx, int32_t K,
+                        const int32_t *__restrict__ row_slot, const __nv_bfloat16 *__restrict__ a_arena,
+                        const int32_t *__restrict__ table, const int32_t *__restrict__ ranks,
+                        int32_t max_slots, int32_t bps, int32_t num_blocks, float *__restrict__ V,
+                        int32_t ldv, unsigned long long *status, int32_t *__restrict__ counters,
+                        int32_t n_counters) {
+    constexpr int kThreadsS = 256;
+    const int32_t m = blockIdx.x;
+    const int32_t t = blockIdx.y;
+    // the split-K tile counters of the GEMM that follows start from zero
+    if (m == 0 && t == 0)
+        for (int32_t c = threadIdx.x; c < n_counters; c += kThreadsS) counters[c] = 0;
+    int32_t r;
+    float s;
+    const int32_t i = resolve_slot(row_slot[m], m, ranks, nullptr, max_slots, bps, &r, &s, status,
+                                   t == 0 && threadIdx.x == 0);
+    if (i < 0 || t * LORA_BLOCK_ROWS >= r) return;
+    const int32_t b = table[i * bps + t];
+    if (b < 0 || b >= num_blocks) {
+        if (threadIdx.x == 0) record_error(status, kDevBadBlock, static_cast<uint32_t>(i));
+        return;
+    }
+    const uint4 *A = reinterpret_cast<const uint4 *>(a_arena + static_cast<size_t>(b) * LORA_BLOCK_ROWS * K);
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * ldx);
+    const int32_t K8 = K / 8;  // 16-byte vectors per row
+    float acc[LORA_BLOCK_ROWS];
+#pragma unroll
+    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+    for (int32_t k0 = threadIdx.x; k0 < K8; k0 += kBatch * kThreadsS) {
+        uint4 xq[kBatch];
+        uint4 aq[kBatch][LORA_BLOCK_ROWS];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int32_t k = k0 + u * kThreadsS;
+            if (k < K8) {
+                xq[u] = __ldg(xr + k);
+#pragma unroll
+                for (int j = 0; j < LORA_BLOCK_ROWS; ++j) aq[u][j] = __ldg(A + static_cast<size_t>(j) * K8 + k);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (k0 + u * kThreadsS < K8) {
+                float xv[8];
+                const uint32_t w[4] = {xq[u].x, xq[u].y, xq[u].z, xq[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    xv[2 * q] = __uint_as_float(w[q] << 16);
+                    xv[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+                }
+#pragma unroll
+                for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = dot8_bf16(aq[u][j], xv, acc[j]);
+            }
+        }
+    }
+    __shared__ float red[kThreadsS / 32][LORA_BLOCK_ROWS];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
+        float v = acc[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[warp][j] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < LORA_BLOCK_ROWS) {
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kThreadsS / 32; ++w) v += red[w][threadIdx.x];
         V[static_cast<size_t>(m) * ldv + t * LORA_BLOCK_ROWS + threadIdx.x] = v;
     }
 }
@@ -282,7 +380,7 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
         shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
             static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
             static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
-            v.V, v.max_rank, plan.status);
+            v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (plan.stage_events) {
@@ -312,17 +410,25 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
     for (int p = 0; p < plan.n_proj; ++p) {
         const ProjView &v = plan.proj[p];
         dim3 sgrid(plan.M, v.bps);
-        shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
-            static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
-            static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
-            v.V, v.max_rank, plan.status);
+        // few (row, block) pairs: the wide kernel that keeps a whole A block
+        // in flight per CTA; many: the narrow one, several CTAs per SM
+        if (static_cast<int64_t>(plan.M) * v.bps <= 4 * static_cast<int64_t>(device_sm_count()))
+            shrink_rows_bf16_kernel<2><<<sgrid, 256, 0, stream>>>(
+                static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
+                static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
+                v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
+        else
+            shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
+                static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
+                static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
+                v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (plan.stage_events) {
             e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[1 + 2 * p]), stream);
             if (e != cudaSuccess) return e;
         }
-        e = launch_gemm_lora_tc(plan, v, plan.y32, plan.counters, stream);
+        e = launch_gemm_lora_tc(plan, v, stream);
         if (e != cudaSuccess) return e;
         count_launches(2);
         if (plan.stage_events) {

@@ -65,6 +65,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// Wait until the int at `ptr` (global memory, written by other CTAs with
+// atomics) is at least `target`, giving up after `limit_ns`.
+__device__ __forceinline__ bool wait_counter_at_least(const int32_t *ptr, int32_t target, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+        if (v >= target) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+        __nanosleep(32);
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {

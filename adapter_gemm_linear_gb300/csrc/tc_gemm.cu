@@ -17,9 +17,12 @@
 //                N = BN tokens; TMEM lane = output column, column = token.  With
 //                few tokens this puts W's rows on the 128 lanes, and split-K
 //                spreads each tile's K range over several CTAs so that ~all
-//                SMs stream W.  Partial tiles are summed with fp32 reductions
-//                into an L2-resident buffer; the CTA that finishes a tile last
-//                (per-tile counter) applies the correction and stores it.
+//                SMs stream W.  The correction of a tile is precomputed in
+//                shared memory while its MMAs run (with split-K, each split
+//                takes a share of the tile's adapters).  Each split stores its
+//                fp32 partial tile to an L2-resident slice and bumps a per-tile
+//                counter; when the count is complete every split sums the
+//                slices over its own range of tokens and stores bf16.
 // Warp roles:
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per
 //               k-block into a shared-memory ring (128-byte swizzle);
@@ -29,7 +32,7 @@
 //   warps 2-9   epilogue: each warp may read one 32-lane quarter of TMEM
 //               (two warps per quarter, alternating 32-column chunks), reads
 //               32 columns at a time with tcgen05.ld, adds the correction and
-//               stores bf16.
+//               stores bf16 (or the fp32 partial tile under split-K).
 // Every barrier wait is bounded in time; a wait that runs out records
 // kDevTimeout in the status word and the CTA unwinds without hanging.
 #include <cuda.h>
@@ -57,6 +60,7 @@ constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kRingBudget = 196 * 1024;  // shared memory for the operand ring
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kEpiBarrier = 1;         // named barrier of the epilogue warps
+constexpr int kMetaBlk = 8;            // pool block ids kept per token in shared memory (ranks <= 128)
 
 struct TcParams {
     int32_t M, N, K;
@@ -74,7 +78,7 @@ struct TcParams {
     int32_t ldv;
     int32_t v_parts;        // 1 or 2 partial planes of V, summed here
     size_t v_part_stride;   // elements between the planes
-    float *y32;         // split-K accumulator [M][N], zero on entry (splits > 1)
+    float *part;        // split-K partial tiles [splits][tiles][BN][128] fp32 (splits > 1)
     int32_t *counters;  // per tile, zero on entry (splits > 1)
     unsigned long long *status;
 };
@@ -90,9 +94,9 @@ struct Cfg {
     static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                         : 2 * BN <= 256 ? 256 : 512;
     // ring + correction tile + barriers + TMEM address + flags + per-token
-    // metadata (slot, rank, scale, order), plus alignment slack
+    // metadata (slot, rank, scale, order, first pool blocks), plus alignment slack
     static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kCorrBytes +
-                                    (2 * kStages + 4) * 8 + 16 + BN * 16;
+                                    (2 * kStages + 4) * 8 + 16 + BN * 16 + (SWAP ? BN * kMetaBlk * 4 : 0);
     static_assert(kStages >= 2, "ring too small");
 };
 
@@ -302,9 +306,11 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
 // Swapped orientation, before the tile's accumulator is ready: the LoRA
 // correction of the whole tile, corr[e][n_local] = s * sum_j B[n][j] V[m][j]
 // for the unit's tokens m = m0 + e and output columns n = n0 + n_local.
-// Tokens are walked in adapter order (meta_order); the two halves of the
-// epilogue threads take alternate adapters, so each (token, column) has one
-// writer.  A group's (token, rank block) pairs are taken four at a time, all
+// Tokens are walked in adapter order (meta_order).  Adapter groups are dealt
+// round-robin to (part, half): the n_parts splits of a split-K tile each take
+// their share (and add it to their partial tile), and within a CTA the two
+// halves of the epilogue threads alternate, so each (token, column) of `corr`
+// has one writer.  A group's (token, rank block) pairs are taken four at a time, all
 // their loads (the thread's 32-byte piece of B, the token's 16 V values)
 // issued before any is used.
 __device__ __forceinline__ void dot16_acc(const uint4 &q0, const uint4 &q1, const float4 &v0, const float4 &v1,
@@ -339,10 +345,38 @@ __device__ __forceinline__ float4 add4(float4 a, const float4 &b) {
     return a;
 }
 
+// Swapped orientation: ask L2 for the B pieces the tile's correction will
+// read (one 4 KiB piece per adapter and rank block: rows n0 .. n0+127 of the
+// block's [N][16] layout), as soon as the tile's adapters are known, so that
+// the correction's loads find them in L2 instead of waiting on DRAM.
+template <int BN>
+__device__ __forceinline__ void prefetch_b_pieces(const TcParams &p, int32_t n0, const int32_t *meta_slot,
+                                                  const int32_t *meta_rank, const int32_t *meta_order,
+                                                  const int32_t *meta_blk) {
+    constexpr int kRowsPerLine = 128 / (LORA_BLOCK_ROWS * 2);  // 4 rows of 32 bytes
+    constexpr int kLines = kBM / kRowsPerLine;
+    const int et = threadIdx.x - 64;
+    for (int idx = et; idx < BN * kLines; idx += kEpiThreads) {
+        const int i = idx / kLines;
+        const int32_t row = n0 + (idx % kLines) * kRowsPerLine;
+        const int e = meta_order[i];
+        const int32_t slot = meta_slot[e];
+        if (slot < 0 || row >= p.N) continue;
+        if (i > 0 && meta_slot[meta_order[i - 1]] == slot) continue;  // once per adapter
+        const int32_t nblk = min((meta_rank[e] + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS, kMetaBlk);
+        for (int32_t jb = 0; jb < nblk; ++jb) {
+            const __nv_bfloat16 *src =
+                p.b_arena + (static_cast<size_t>(meta_blk[e * kMetaBlk + jb]) * p.N + row) * LORA_BLOCK_ROWS;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+        }
+    }
+}
+
 template <int BN>
 __device__ __forceinline__ void build_correction(const TcParams &p, int32_t n0, int32_t m0, const int32_t *meta_slot,
                                                  const int32_t *meta_rank, const float *meta_scale,
-                                                 const int32_t *meta_order, float *corr) {
+                                                 const int32_t *meta_order, const int32_t *meta_blk, float *corr,
+                                                 int part, int n_parts) {
     constexpr int kU = 4;  // (token, rank block) pairs in flight
     const int et = threadIdx.x - 64;
     const int n_local = et % kBM;
@@ -356,16 +390,13 @@ __device__ __forceinline__ void build_correction(const TcParams &p, int32_t n0, 
         if (slot < 0) break;  // tokens without an adapter are ordered last
         int b = a + 1;
         while (b < BN && meta_slot[meta_order[b]] == slot) ++b;
-        if ((g % (kEpiThreads / kBM)) == half && n_ok) {
+        if (g % (2 * n_parts) == 2 * part + half && n_ok) {
             const int32_t r = meta_rank[e0];
             const int32_t nblk = (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
             const float s = meta_scale[e0];
-            const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;
-            bool ok = true;
-            for (int32_t jb = 0; jb < nblk; ++jb) ok &= (trow[jb] >= 0 && trow[jb] < p.num_blocks);
-            if (!ok) {
-                record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
-            } else {
+            const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;  // blocks past kMetaBlk
+            const int32_t *mblk = meta_blk + e0 * kMetaBlk;
+            {
                 // the group's (token, rank block) pairs, kU at a time
                 const int32_t total = (b - a) * nblk;
                 int t_next = a, jb_next = 0;
@@ -381,7 +412,8 @@ __device__ __forceinline__ void build_correction(const TcParams &p, int32_t n0, 
                             const int e = meta_order[t_next];
                             eu[u] = e;
                             const uint4 *bsrc = reinterpret_cast<const uint4 *>(
-                                p.b_arena + (static_cast<size_t>(trow[jb_next]) * p.N + n) * LORA_BLOCK_ROWS);
+                                p.b_arena + (static_cast<size_t>(jb_next < kMetaBlk ? mblk[jb_next] : trow[jb_next]) * p.N +
+                                             n) * LORA_BLOCK_ROWS);
                             q[u][0] = __ldg(bsrc);
                             q[u][1] = __ldg(bsrc + 1);
                             const float4 *vsrc = reinterpret_cast<const float4 *>(
@@ -428,7 +460,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                                              uint32_t tmem_base, volatile uint32_t *abort_flag,
                                              volatile uint32_t *last_flag, int32_t *meta_slot,
                                              int32_t *meta_rank, float *meta_scale, int32_t *meta_order,
-                                             float *corr) {
+                                             int32_t *meta_blk, float *corr) {
     using namespace sm100;
     constexpr int kGroups = kEpiWarps / 4;
     constexpr int kChunks = BN / 32;
@@ -452,31 +484,46 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                 if (m < p.M)
                     slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s,
                                         p.status, false);
+                if (slot >= 0) {
+                    // the adapter's pool blocks: the first kMetaBlk kept here,
+                    // every one checked (a corrupt entry drops the correction)
+                    const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;
+                    const int32_t nblk = (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
+                    bool ok = true;
+                    for (int32_t jb = 0; jb < nblk; ++jb) {
+                        const int32_t blk = trow[jb];
+                        ok &= blk >= 0 && blk < p.num_blocks;
+                        if (jb < kMetaBlk) meta_blk[e * kMetaBlk + jb] = blk;
+                    }
+                    if (!ok) {
+                        record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
+                        slot = -1;
+                    }
+                }
                 meta_slot[e] = slot;
                 meta_rank[e] = r;
                 meta_scale[e] = s;
             }
         }
-        // the split that owns the correction of a swapped tile builds it now,
-        // while the tile's MMAs run
-        const bool owns = SWAP && (p.splits == 1 || w.ks == 0);
+        // the correction of a swapped tile is built now, while the tile's MMAs
+        // run; with split-K every split builds its share of the adapters
         if (SWAP) {
             epi_sync();
-            if (owns) {
-                for (int e = et; e < BN; e += kEpiThreads) {
-                    const int32_t key = meta_slot[e] < 0 ? 0x7fffffff : meta_slot[e];
-                    int rnk = 0;
-                    for (int e2 = 0; e2 < BN; ++e2) {
-                        const int32_t k2 = meta_slot[e2] < 0 ? 0x7fffffff : meta_slot[e2];
-                        rnk += (k2 < key) || (k2 == key && e2 < e);
-                    }
-                    meta_order[rnk] = e;
+            for (int e = et; e < BN; e += kEpiThreads) {
+                const int32_t key = meta_slot[e] < 0 ? 0x7fffffff : meta_slot[e];
+                int rnk = 0;
+                for (int e2 = 0; e2 < BN; ++e2) {
+                    const int32_t k2 = meta_slot[e2] < 0 ? 0x7fffffff : meta_slot[e2];
+                    rnk += (k2 < key) || (k2 == key && e2 < e);
                 }
-                for (int i = et; i < BN * kBM; i += kEpiThreads) corr[i] = 0.0f;
-                epi_sync();
-                build_correction<BN>(p, w.ta * kBM, w.tb * BN, meta_slot, meta_rank, meta_scale, meta_order, corr);
-                epi_sync();
+                meta_order[rnk] = e;
             }
+            for (int i = et; i < BN * kBM; i += kEpiThreads) corr[i] = 0.0f;
+            epi_sync();
+            prefetch_b_pieces<BN>(p, w.ta * kBM, meta_slot, meta_rank, meta_order, meta_blk);
+            build_correction<BN>(p, w.ta * kBM, w.tb * BN, meta_slot, meta_rank, meta_scale, meta_order, meta_blk,
+                                 corr, w.ks, p.splits);
+            epi_sync();
         }
         bool ok = mbar_wait_bounded(&tmem_full[b], (t >> 1) & 1, kWaitLimitNs);
         if (!ok) {
@@ -510,21 +557,23 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tmem_empty[b]);
             } else {
-                // partial tile: reduce into the fp32 buffer
+                // partial tile, correction share included, to this split's
+                // slice; once every split of the tile has stored its slice,
+                // each sums the slices over its own range of the tile's tokens.
+                // All splits of a tile run at once: split-K is planned only
+                // when the units fit in one wave of the grid.
+                const size_t tile = static_cast<size_t>(w.ta) * p.tiles_b + w.tb;
+                const size_t tiles = static_cast<size_t>(p.tiles_a) * p.tiles_b;
+                constexpr size_t kTileElems = static_cast<size_t>(BN) * kBM;
+                float *mine = p.part + (w.ks * tiles + tile) * kTileElems + q * 32 + lane;
 #pragma unroll 1
                 for (int c = grp; c < kChunks; c += kGroups) {
                     float acc[32];
                     load_tmem_chunk(col0 + c * 32, acc);
-                    const int32_t m0 = w.tb * BN + c * 32;
-                    if (owns) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) acc[e] += corr[(c * 32 + e) * kBM + q * 32 + lane];
-                    }
-                    if (n_ok) {
+                    for (int e = 0; e < 32; ++e) acc[e] += corr[(c * 32 + e) * kBM + q * 32 + lane];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (m0 + e < p.M) atomicAdd(p.y32 + static_cast<size_t>(m0 + e) * p.N + n, acc[e]);
-                    }
+                    for (int e = 0; e < 32; ++e) __stcg(mine + (c * 32 + e) * kBM, acc[e]);
                     __syncwarp();
                 }
                 tc_fence_before_sync();
@@ -533,26 +582,40 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                 __threadfence();
                 epi_sync();
                 if (et == 0) {
-                    const int32_t old = atomicAdd(p.counters + (w.ta * p.tiles_b + w.tb), 1);
-                    *last_flag = (old == p.splits - 1) ? 1u : 0u;
+                    atomicAdd(p.counters + tile, 1);
+                    const bool all = wait_counter_at_least(p.counters + tile, p.splits, kWaitLimitNs);
+                    if (!all) record_error(p.status, kDevTimeout, 5);
+                    *last_flag = all ? 1u : 0u;
                 }
                 epi_sync();
-                const bool last = *last_flag != 0;
-                if (last) {
+                if (*last_flag) {
                     __threadfence();
+                    const int32_t per = (BN + p.splits - 1) / p.splits;
+                    const int32_t e_begin = w.ks * per;
+                    const int32_t e_end = min(BN, e_begin + per);
+                    const int n_local = et % kBM;
+                    const int32_t nn = w.ta * kBM + n_local;
+                    const float *first = p.part + tile * kTileElems + n_local;
+                    const size_t split_stride = tiles * kTileElems;
 #pragma unroll 1
-                    for (int c = grp; c < kChunks; c += kGroups) {
-                        const int32_t m0 = w.tb * BN + c * 32;
-                        float acc[32];
+                    for (int32_t e0 = e_begin + et / kBM; e0 < e_end; e0 += 4 * (kEpiThreads / kBM)) {
+                        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+                        for (int32_t ks = 0; ks < p.splits; ++ks) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            acc[e] = (n_ok && m0 + e < p.M) ? __ldcg(p.y32 + static_cast<size_t>(m0 + e) * p.N + n)
-                                                            : 0.0f;
-                        if (n_ok) {
+                            for (int v = 0; v < 4; ++v) {
+                                const int32_t e = e0 + v * (kEpiThreads / kBM);
+                                if (e < e_end) a[v] += __ldcg(first + ks * split_stride + e * kBM);
+                            }
+                        }
+                        if (nn < p.N) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (m0 + e < p.M)
-                                    p.out[static_cast<size_t>(m0 + e) * p.ldo + n] = __float2bfloat16_rn(acc[e]);
+                            for (int v = 0; v < 4; ++v) {
+                                const int32_t e = e0 + v * (kEpiThreads / kBM);
+                                const int32_t m = w.tb * BN + e;
+                                if (e < e_end && m < p.M)
+                                    p.out[static_cast<size_t>(m) * p.ldo + nn] = __float2bfloat16_rn(a[v]);
+                            }
                         }
                     }
                 }
@@ -619,6 +682,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     int32_t *meta_rank = meta_slot + BN;
     float *meta_scale = reinterpret_cast<float *>(meta_rank + BN);
     int32_t *meta_order = reinterpret_cast<int32_t *>(meta_scale + BN);
+    int32_t *meta_blk = meta_order + BN;  // [BN][kMetaBlk] (swapped orientation)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -655,7 +719,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
             run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
     } else {
         run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, meta_slot,
-                               meta_rank, meta_scale, meta_order, corr);
+                               meta_rank, meta_scale, meta_order, meta_blk, corr);
     }
 
     tc_fence_before_sync();
@@ -698,21 +762,9 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-    static int cache[128] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
-    if (!cache[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cache[dev] = n;
-    }
-    return cache[dev];
-}
 
 template <bool SWAP, int BN>
-cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, float *y32,
-                           int32_t *counters, cudaStream_t stream) {
+cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, cudaStream_t stream) {
     using C = Cfg<SWAP, BN>;
     auto kernel = tc_gemm_lora_kernel<SWAP, BN>;
     static std::mutex mu;
@@ -757,16 +809,14 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.ldv = v.max_rank;
     p.v_parts = plan.v_parts;
     p.v_part_stride = static_cast<size_t>(plan.M) * v.max_rank;
-    p.y32 = y32;
-    p.counters = counters;
+    p.part = plan.part;
+    p.counters = plan.counters;
     p.status = plan.status;
-    if (tp.splits > 1) {
-        e = cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(plan.M) * v.N, stream);
-        if (e == cudaSuccess)
-            e = cudaMemsetAsync(counters, 0, sizeof(int32_t) * static_cast<size_t>(tp.tiles_a) * tp.tiles_b,
-                                stream);
-        if (e != cudaSuccess) return e;
-    }
+    // the splits of a tile wait for one another, so they must all be resident:
+    // split-K needs every unit in the first wave of the grid
+    if (tp.splits > 1 && (!plan.part || !plan.counters || tp.units > tp.grid ||
+                          plan.n_counters < static_cast<int64_t>(tp.tiles_a) * tp.tiles_b))
+        return cudaErrorInvalidValue;
     if (SWAP) {
         kernel<<<tp.grid, kThreads, C::kSmem, stream>>>(tw, tx, p);
     } else {
@@ -777,10 +827,22 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
 
 }  // namespace
 
+int device_sm_count() {
+    static int cache[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 // Orientation, tile width and split-K factor for an M x N x K problem.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
     TcPlan t{};
-    const int sms = sm_count();
+    const int sms = device_sm_count();
     t.num_kb = (K + kBK - 1) / kBK;
     t.swap = M <= 512;
     if (t.swap) {
@@ -809,23 +871,22 @@ TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
     }
     t.units = t.tiles_a * t.tiles_b * t.splits;
     t.grid = t.units < sms ? t.units : sms;
-    t.y32_bytes = t.splits > 1 ? sizeof(float) * static_cast<size_t>(M) * N : 0;
+    t.part_bytes = t.splits > 1 ? sizeof(float) * static_cast<size_t>(t.splits) * t.tiles_a * t.tiles_b * t.bn * kBM : 0;
     t.counter_bytes = t.splits > 1 ? sizeof(int32_t) * static_cast<size_t>(t.tiles_a) * t.tiles_b : 0;
     return t;
 }
 
-cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, float *y32, int32_t *counters,
-                                cudaStream_t stream) {
+cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
     const TcPlan tp = plan_tc(plan.M, v.N, plan.K);
     if (tp.swap) {
         switch (tp.bn) {
-            case 32: return launch_variant<true, 32>(plan, v, tp, y32, counters, stream);
-            case 64: return launch_variant<true, 64>(plan, v, tp, y32, counters, stream);
-            default: return launch_variant<true, 128>(plan, v, tp, y32, counters, stream);
+            case 32: return launch_variant<true, 32>(plan, v, tp, stream);
+            case 64: return launch_variant<true, 64>(plan, v, tp, stream);
+            default: return launch_variant<true, 128>(plan, v, tp, stream);
         }
     }
-    if (tp.bn == 128) return launch_variant<false, 128>(plan, v, tp, y32, counters, stream);
-    return launch_variant<false, 256>(plan, v, tp, y32, counters, stream);
+    if (tp.bn == 128) return launch_variant<false, 128>(plan, v, tp, stream);
+    return launch_variant<false, 256>(plan, v, tp, stream);
 }
 
 }  // namespace lora
