@@ -140,6 +140,9 @@ shrink_simt_kernel(const T *__restrict__ x, int32_t ldx, int32_t K, const int32_
                    unsigned long long *status, int32_t *__restrict__ counters, int32_t n_counters) {
     const int32_t m = blockIdx.x;
     const int32_t t = blockIdx.y;
+    // the GEMM that follows may launch now: it reads V and the counters only
+    // after this grid has completed (griddepcontrol.wait)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the split-K tile counters of the GEMM that follows start from zero
     if (m == 0 && t == 0)
         for (int32_t c = threadIdx.x; c < n_counters; c += blockDim.x) counters[c] = 0;
@@ -217,6 +220,7 @@ shrink_rows_bf16_kernel(const __nv_bfloat16 *__restrict__ x, int32_t ldx, int32_
     constexpr int kThreadsS = 256;
     const int32_t m = blockIdx.x;
     const int32_t t = blockIdx.y;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in shrink_simt_kernel
     // the split-K tile counters of the GEMM that follows start from zero
     if (m == 0 && t == 0)
         for (int32_t c = threadIdx.x; c < n_counters; c += kThreadsS) counters[c] = 0;
@@ -404,7 +408,8 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
     return cudaSuccess;
 }
 
-// bf16: CUDA-core shrink, then the tensor-core GEMM with the fused expand.
+// bf16: CUDA-core shrink, then the tensor-core GEMM with the fused expand
+// (launched as a programmatic dependent of the shrink, see tc_gemm.cu).
 static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t stream) {
     using T = __nv_bfloat16;
     for (int p = 0; p < plan.n_proj; ++p) {

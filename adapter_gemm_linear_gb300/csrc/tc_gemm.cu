@@ -217,6 +217,12 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
 
 // --------------------------------------------------------------- epilogue
 
+// The kernel is launched as a programmatic dependent of the shrink kernel:
+// wait until that grid has completed and its writes are visible.  Returns at
+// once when the launch had no programmatic dependency (or after the first
+// call).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // AND of `v` over the epilogue threads, also a barrier among them.
 __device__ __forceinline__ bool epi_all(bool v) {
     uint32_t r;
@@ -521,6 +527,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
             for (int i = et; i < BN * kBM; i += kEpiThreads) corr[i] = 0.0f;
             epi_sync();
             prefetch_b_pieces<BN>(p, w.ta * kBM, meta_slot, meta_rank, meta_order, meta_blk);
+            grid_dependency_wait();  // V and the tile counters come from the shrink kernel
             build_correction<BN>(p, w.ta * kBM, w.tb * BN, meta_slot, meta_rank, meta_scale, meta_order, meta_blk,
                                  corr, w.ks, p.splits);
             epi_sync();
@@ -621,6 +628,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                 }
             }
         } else {
+            grid_dependency_wait();  // V comes from the shrink kernel
             const int32_t m = w.ta * kBM + q * 32 + lane;
             int32_t r = 0, slot = -1;
             float s = 0.0f;
@@ -817,12 +825,21 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     if (tp.splits > 1 && (!plan.part || !plan.counters || tp.units > tp.grid ||
                           plan.n_counters < static_cast<int64_t>(tp.tiles_a) * tp.tiles_b))
         return cudaErrorInvalidValue;
-    if (SWAP) {
-        kernel<<<tp.grid, kThreads, C::kSmem, stream>>>(tw, tx, p);
-    } else {
-        kernel<<<tp.grid, kThreads, C::kSmem, stream>>>(tx, tw, p);
-    }
-    return cudaGetLastError();
+    // programmatic dependent of the shrink kernel before it on the stream:
+    // the CTAs may start (and stream W and x) while the shrink finishes; the
+    // epilogue waits for the shrink's grid before it reads V or the counters
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tp.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (SWAP) return cudaLaunchKernelEx(&cfg, kernel, tw, tx, p);
+    return cudaLaunchKernelEx(&cfg, kernel, tx, tw, p);
 }
 
 }  // namespace
