@@ -57,7 +57,8 @@ constexpr int kUmmaK = 16;             // K of one tcgen05.mma for 16-bit inputs
 constexpr int kEpiWarps = 8;   // two per TMEM lane quarter
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;
-constexpr int kRingBudget = 196 * 1024;  // shared memory for the operand ring
+constexpr int kSmemLimit = 226 * 1024;   // dynamic shared memory per CTA (227 KiB opt-in maximum)
+constexpr int kVStageBytes = 16 * 1024;  // swapped orientation: staged rows of V
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kEpiBarrier = 1;         // named barrier of the epilogue warps
 constexpr int kMetaBlk = 8;            // pool block ids kept per token in shared memory (ranks <= 128)
@@ -89,14 +90,18 @@ struct Cfg {
     static constexpr uint32_t kBBytes = BN * kBK * 2;
     // swapped orientation: the LoRA correction of a tile, fp32 [BN tokens][128 columns]
     static constexpr int kCorrBytes = SWAP ? BN * kBM * 4 : 0;
-    static constexpr int kStages0 = (kRingBudget - kCorrBytes) / static_cast<int>(kABytes + kBBytes);
+    // per-token metadata: slot, rank, scale, order (+ group index, first pool
+    // blocks and the V stage when swapped)
+    static constexpr int kMetaBytes = BN * 16 + (SWAP ? BN * 4 + BN * kMetaBlk * 4 + kVStageBytes : 0);
+    // ring + correction tile + barriers + TMEM address + flags + metadata + alignment slack
+    static constexpr int kFixed = 1024 + kCorrBytes + (2 * 12 + 4) * 8 + 16 + kMetaBytes;
+    static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes);
     static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
     static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                         : 2 * BN <= 256 ? 256 : 512;
-    // ring + correction tile + barriers + TMEM address + flags + per-token
-    // metadata (slot, rank, scale, order, first pool blocks), plus alignment slack
     static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kCorrBytes +
-                                    (2 * kStages + 4) * 8 + 16 + BN * 16 + (SWAP ? BN * kMetaBlk * 4 : 0);
+                                    (2 * kStages + 4) * 8 + 16 + kMetaBytes;
+    static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kStages >= 2, "ring too small");
 };
 
@@ -309,40 +314,6 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
     for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(raw[e]);
 }
 
-// Swapped orientation, before the tile's accumulator is ready: the LoRA
-// correction of the whole tile, corr[e][n_local] = s * sum_j B[n][j] V[m][j]
-// for the unit's tokens m = m0 + e and output columns n = n0 + n_local.
-// Tokens are walked in adapter order (meta_order).  Adapter groups are dealt
-// round-robin to (part, half): the n_parts splits of a split-K tile each take
-// their share (and add it to their partial tile), and within a CTA the two
-// halves of the epilogue threads alternate, so each (token, column) of `corr`
-// has one writer.  A group's (token, rank block) pairs are taken four at a time, all
-// their loads (the thread's 32-byte piece of B, the token's 16 V values)
-// issued before any is used.
-__device__ __forceinline__ void dot16_acc(const uint4 &q0, const uint4 &q1, const float4 &v0, const float4 &v1,
-                                          const float4 &v2, const float4 &v3, float &a0, float &a1, float &a2,
-                                          float &a3) {
-    float bv[16];
-    unpack_bf16x8(q0, bv);
-    unpack_bf16x8(q1, bv + 8);
-    a0 = fmaf(bv[0], v0.x, a0);
-    a1 = fmaf(bv[1], v0.y, a1);
-    a2 = fmaf(bv[2], v0.z, a2);
-    a3 = fmaf(bv[3], v0.w, a3);
-    a0 = fmaf(bv[4], v1.x, a0);
-    a1 = fmaf(bv[5], v1.y, a1);
-    a2 = fmaf(bv[6], v1.z, a2);
-    a3 = fmaf(bv[7], v1.w, a3);
-    a0 = fmaf(bv[8], v2.x, a0);
-    a1 = fmaf(bv[9], v2.y, a1);
-    a2 = fmaf(bv[10], v2.z, a2);
-    a3 = fmaf(bv[11], v2.w, a3);
-    a0 = fmaf(bv[12], v3.x, a0);
-    a1 = fmaf(bv[13], v3.y, a1);
-    a2 = fmaf(bv[14], v3.z, a2);
-    a3 = fmaf(bv[15], v3.w, a3);
-}
-
 __device__ __forceinline__ float4 add4(float4 a, const float4 &b) {
     a.x += b.x;
     a.y += b.y;
@@ -378,83 +349,145 @@ __device__ __forceinline__ void prefetch_b_pieces(const TcParams &p, int32_t n0,
     }
 }
 
+// Next (group, rank block) pair of this thread, in sorted-position order
+// within the V chunk [c0, c1).  A group is a run of sorted positions with one
+// adapter (meta_gidx = its index in the tile); group g belongs to the thread
+// when g % (2 * n_parts) == 2 * part + half.  The cursor (a = first position of
+// the current group inside the chunk, jb = next block) advances to the next
+// owned group when the current one has no blocks left.
+struct PairCursor {
+    int a;       // first sorted position of the current group (in the chunk)
+    int b;       // one past its last position (in the chunk)
+    int jb;      // next rank block of the group
+    int nblk;    // rank blocks of the group (0: no owned group left)
+};
+
+__device__ __forceinline__ void cursor_seek(PairCursor &c, int from, int c1, const int32_t *meta_gidx,
+                                            const int32_t *meta_order, const int32_t *meta_rank, int owner,
+                                            int modulus) {
+    int a = from;
+    while (a < c1) {
+        int b = a + 1;
+        while (b < c1 && meta_gidx[b] == meta_gidx[a]) ++b;
+        if (meta_gidx[a] % modulus == owner) {
+            c.a = a;
+            c.b = b;
+            c.jb = 0;
+            c.nblk = (meta_rank[meta_order[a]] + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
+            return;
+        }
+        a = b;
+    }
+    c.a = c.b = c1;
+    c.jb = 0;
+    c.nblk = 0;
+}
+
+// Swapped orientation, before the tile's accumulator is ready: the LoRA
+// correction of the whole tile, corr[e][n_local] = s * sum_j B[n][j] V[m][j]
+// for the unit's tokens m = m0 + e and output columns n = n0 + n_local.
+// Tokens are taken in adapter order (meta_order), the adapted ones first.
+// Adapter groups are dealt round-robin to (part, half): each of the n_parts
+// splits of a split-K tile takes its share (and adds it to its partial tile);
+// within a CTA the two halves of the epilogue threads alternate, so every
+// (token, column) of `corr` has one writer.  V rows of the adapted tokens are
+// staged in shared memory (in chunks of sorted positions when they do not fit
+// at once); the thread's 32-byte pieces of B are loaded four (group, rank
+// block) pairs at a time, all four in flight before any is used, and each
+// piece serves every token of its group.
 template <int BN>
 __device__ __forceinline__ void build_correction(const TcParams &p, int32_t n0, int32_t m0, const int32_t *meta_slot,
                                                  const int32_t *meta_rank, const float *meta_scale,
-                                                 const int32_t *meta_order, const int32_t *meta_blk, float *corr,
-                                                 int part, int n_parts) {
-    constexpr int kU = 4;  // (token, rank block) pairs in flight
+                                                 const int32_t *meta_order, const int32_t *meta_gidx,
+                                                 const int32_t *meta_blk, float *vst, float *corr, int part,
+                                                 int n_parts) {
+    constexpr int kP = 4;  // (group, rank block) pairs in flight
     const int et = threadIdx.x - 64;
     const int n_local = et % kBM;
     const int half = et / kBM;
     const int32_t n = n0 + n_local;
     const bool n_ok = n < p.N;
-    int g = 0;
-    for (int a = 0; a < BN;) {
-        const int e0 = meta_order[a];
-        const int32_t slot = meta_slot[e0];
-        if (slot < 0) break;  // tokens without an adapter are ordered last
-        int b = a + 1;
-        while (b < BN && meta_slot[meta_order[b]] == slot) ++b;
-        if (g % (2 * n_parts) == 2 * part + half && n_ok) {
-            const int32_t r = meta_rank[e0];
-            const int32_t nblk = (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
-            const float s = meta_scale[e0];
-            const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;  // blocks past kMetaBlk
-            const int32_t *mblk = meta_blk + e0 * kMetaBlk;
-            {
-                // the group's (token, rank block) pairs, kU at a time
-                const int32_t total = (b - a) * nblk;
-                int t_next = a, jb_next = 0;
+    const int modulus = 2 * n_parts, owner = 2 * part + half;
+    const int32_t ldv = p.ldv;
+    // adapted tokens come first in meta_order: n_adapted = first position without one
+    int lo = 0, hi = BN;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (meta_slot[meta_order[mid]] >= 0) lo = mid + 1; else hi = mid;
+    }
+    const int n_adapted = lo;
+    const int chunk = (kVStageBytes / 4) / ldv;  // sorted positions per V stage
+    for (int c0 = 0; c0 < n_adapted; c0 += chunk) {
+        const int c1 = min(n_adapted, c0 + chunk);
+        // stage V rows (both partial planes summed) of sorted positions [c0, c1)
+        const int q4 = ldv / 4;
+        for (int i4 = et; i4 < (c1 - c0) * q4; i4 += kEpiThreads) {
+            const int row = i4 / q4;
+            const int e = meta_order[c0 + row];
+            const float4 *src = reinterpret_cast<const float4 *>(p.V + static_cast<size_t>(m0 + e) * ldv) + (i4 - row * q4);
+            float4 v = *src;
+            if (p.v_parts > 1) v = add4(v, src[p.v_part_stride / 4]);
+            reinterpret_cast<float4 *>(vst)[i4] = v;
+        }
+        epi_sync();
+        if (n_ok) {
+            PairCursor cur;
+            cursor_seek(cur, c0, c1, meta_gidx, meta_order, meta_rank, owner, modulus);
 #pragma unroll 1
-                for (int32_t i0 = 0; i0 < total; i0 += kU) {
-                    uint4 q[kU][2];
-                    float4 v[kU][4];
-                    int eu[kU];
+            while (cur.nblk > 0) {
+                uint4 q[kP][2];
+                int pa[kP], pb[kP], pj[kP];
 #pragma unroll
-                    for (int u = 0; u < kU; ++u) {
-                        eu[u] = -1;
-                        if (i0 + u < total) {
-                            const int e = meta_order[t_next];
-                            eu[u] = e;
-                            const uint4 *bsrc = reinterpret_cast<const uint4 *>(
-                                p.b_arena + (static_cast<size_t>(jb_next < kMetaBlk ? mblk[jb_next] : trow[jb_next]) * p.N +
-                                             n) * LORA_BLOCK_ROWS);
-                            q[u][0] = __ldg(bsrc);
-                            q[u][1] = __ldg(bsrc + 1);
-                            const float4 *vsrc = reinterpret_cast<const float4 *>(
-                                p.V + static_cast<size_t>(m0 + e) * p.ldv + jb_next * LORA_BLOCK_ROWS);
-                            v[u][0] = vsrc[0];
-                            v[u][1] = vsrc[1];
-                            v[u][2] = vsrc[2];
-                            v[u][3] = vsrc[3];
-                            if (p.v_parts > 1) {
-                                const float4 *vs2 = vsrc + p.v_part_stride / 4;
-                                v[u][0] = add4(v[u][0], vs2[0]);
-                                v[u][1] = add4(v[u][1], vs2[1]);
-                                v[u][2] = add4(v[u][2], vs2[2]);
-                                v[u][3] = add4(v[u][3], vs2[3]);
-                            }
-                            if (++jb_next == nblk) {
-                                jb_next = 0;
-                                ++t_next;
-                            }
-                        }
+                for (int u = 0; u < kP; ++u) {
+                    pa[u] = -1;
+                    if (cur.nblk > 0) {
+                        const int e0 = meta_order[cur.a];
+                        const int32_t blk =
+                            cur.jb < kMetaBlk
+                                ? meta_blk[e0 * kMetaBlk + cur.jb]
+                                : p.table[static_cast<size_t>(meta_slot[e0]) * p.bps + cur.jb];
+                        const uint4 *bsrc = reinterpret_cast<const uint4 *>(
+                            p.b_arena + (static_cast<size_t>(blk) * p.N + n) * LORA_BLOCK_ROWS);
+                        q[u][0] = __ldg(bsrc);
+                        q[u][1] = __ldg(bsrc + 1);
+                        pa[u] = cur.a;
+                        pb[u] = cur.b;
+                        pj[u] = cur.jb;
+                        if (++cur.jb == cur.nblk)
+                            cursor_seek(cur, cur.b, c1, meta_gidx, meta_order, meta_rank, owner, modulus);
                     }
+                }
 #pragma unroll
-                    for (int u = 0; u < kU; ++u) {
-                        if (eu[u] >= 0) {
-                            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-                            dot16_acc(q[u][0], q[u][1], v[u][0], v[u][1], v[u][2], v[u][3], a0, a1, a2, a3);
-                            float &c = corr[eu[u] * kBM + n_local];
-                            c = fmaf(s, (a0 + a1) + (a2 + a3), c);
-                        }
+                for (int u = 0; u < kP; ++u) {
+                    if (pa[u] < 0) continue;
+                    float bv[16];
+                    unpack_bf16x8(q[u][0], bv);
+                    unpack_bf16x8(q[u][1], bv + 8);
+                    const float sc = meta_scale[meta_order[pa[u]]];
+#pragma unroll 1
+                    for (int i = pa[u]; i < pb[u]; ++i) {
+                        const float4 *vr = reinterpret_cast<const float4 *>(vst + (i - c0) * ldv + pj[u] * LORA_BLOCK_ROWS);
+                        const float4 v0 = vr[0], v1 = vr[1], v2 = vr[2], v3 = vr[3];
+                        float a0 = bv[0] * v0.x, a1 = bv[1] * v0.y, a2 = bv[2] * v0.z, a3 = bv[3] * v0.w;
+                        a0 = fmaf(bv[4], v1.x, a0);
+                        a1 = fmaf(bv[5], v1.y, a1);
+                        a2 = fmaf(bv[6], v1.z, a2);
+                        a3 = fmaf(bv[7], v1.w, a3);
+                        a0 = fmaf(bv[8], v2.x, a0);
+                        a1 = fmaf(bv[9], v2.y, a1);
+                        a2 = fmaf(bv[10], v2.z, a2);
+                        a3 = fmaf(bv[11], v2.w, a3);
+                        a0 = fmaf(bv[12], v3.x, a0);
+                        a1 = fmaf(bv[13], v3.y, a1);
+                        a2 = fmaf(bv[14], v3.z, a2);
+                        a3 = fmaf(bv[15], v3.w, a3);
+                        float &c = corr[meta_order[i] * kBM + n_local];
+                        c = fmaf(sc, (a0 + a1) + (a2 + a3), c);
                     }
                 }
             }
         }
-        ++g;
-        a = b;
+        epi_sync();  // the stage is rewritten by the next chunk
     }
 }
 
@@ -466,7 +499,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                                              uint32_t tmem_base, volatile uint32_t *abort_flag,
                                              volatile uint32_t *last_flag, int32_t *meta_slot,
                                              int32_t *meta_rank, float *meta_scale, int32_t *meta_order,
-                                             int32_t *meta_blk, float *corr) {
+                                             int32_t *meta_gidx, int32_t *meta_blk, float *vst, float *corr) {
     using namespace sm100;
     constexpr int kGroups = kEpiWarps / 4;
     constexpr int kChunks = BN / 32;
@@ -526,10 +559,17 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
             }
             for (int i = et; i < BN * kBM; i += kEpiThreads) corr[i] = 0.0f;
             epi_sync();
+            // group index of every sorted position (a new group starts where the slot changes)
+            for (int i = et; i < BN; i += kEpiThreads) {
+                int gi = 0;
+                for (int j = 1; j <= i; ++j) gi += meta_slot[meta_order[j]] != meta_slot[meta_order[j - 1]];
+                meta_gidx[i] = gi;
+            }
             prefetch_b_pieces<BN>(p, w.ta * kBM, meta_slot, meta_rank, meta_order, meta_blk);
             grid_dependency_wait();  // V and the tile counters come from the shrink kernel
-            build_correction<BN>(p, w.ta * kBM, w.tb * BN, meta_slot, meta_rank, meta_scale, meta_order, meta_blk,
-                                 corr, w.ks, p.splits);
+            epi_sync();
+            build_correction<BN>(p, w.ta * kBM, w.tb * BN, meta_slot, meta_rank, meta_scale, meta_order, meta_gidx,
+                                 meta_blk, vst, corr, w.ks, p.splits);
             epi_sync();
         }
         bool ok = mbar_wait_bounded(&tmem_full[b], (t >> 1) & 1, kWaitLimitNs);
@@ -690,7 +730,9 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     int32_t *meta_rank = meta_slot + BN;
     float *meta_scale = reinterpret_cast<float *>(meta_rank + BN);
     int32_t *meta_order = reinterpret_cast<int32_t *>(meta_scale + BN);
-    int32_t *meta_blk = meta_order + BN;  // [BN][kMetaBlk] (swapped orientation)
+    int32_t *meta_gidx = meta_order + BN;  // [BN] group index by sorted position (swapped orientation)
+    int32_t *meta_blk = meta_gidx + BN;    // [BN][kMetaBlk] (swapped orientation)
+    float *vst = reinterpret_cast<float *>(meta_blk + BN * kMetaBlk);  // kVStageBytes (swapped orientation)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -727,7 +769,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
             run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
     } else {
         run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, meta_slot,
-                               meta_rank, meta_scale, meta_order, meta_blk, corr);
+                               meta_rank, meta_scale, meta_order, meta_gidx, meta_blk, vst, corr);
     }
 
     tc_fence_before_sync();
