@@ -321,7 +321,10 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     if (a->num_stage_events == 0 && a->stage_events) return LORA_ERR_INVALID_ARG;
     plan->stage_events = a->stage_events;
     plan->dtype = a->dtype;
-    plan->v_parts = 1;
+    // the small-M orientation's grouped shrink writes one V plane per K slice
+    plan->v_parts = (a->dtype == LORA_BF16 && a->M > 0 && lora::plan_tc(a->M, 128, a->K).swap)
+                        ? lora::grouped_v_planes(a->K)
+                        : 1;
     plan->M = a->M;
     plan->K = a->K;
     plan->ldx = a->ldx;
@@ -363,19 +366,25 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     // slot ids of every pool must mean the same adapters
     for (int i = 1; i < a->n_proj; ++i)
         if (a->proj[i].pool->d.max_slots != a->proj[0].pool->d.max_slots) return LORA_ERR_INVALID_ARG;
-    // split-K scratch of the tensor-core GEMM, shared by the projections
-    // (their GEMMs run one after the other on the stream)
-    size_t part = 0, cnt = 0;
+    // split-K scratch and the small-M orientation's correction array of the
+    // tensor-core GEMM, shared by the projections (their kernels run one
+    // after the other on the stream)
+    size_t part = 0, cnt = 0, ycorr = 0;
     if (a->dtype == LORA_BF16 && a->M > 0) {
         for (int i = 0; i < a->n_proj; ++i) {
             const lora::TcPlan tp = lora::plan_tc(a->M, a->proj[i].pool->d.N, a->K);
             part = std::max(part, tp.part_bytes);
             cnt = std::max(cnt, tp.counter_bytes);
+            if (tp.swap) ycorr = std::max(ycorr, sizeof(float) * static_cast<size_t>(a->M) * a->proj[i].pool->d.N);
         }
     }
     ws->part_off = off;
     off += align_up(part, 256);
-    ws->counter_off = off;
+    ws->ycorr_off = off;
+    off += align_up(ycorr, 256);
+    ws->group_off = off;
+    if (ycorr) off += align_up(sizeof(int32_t) * lora::group_table_ints(a->M), 256);
+    ws->counter_off = off;  // last: the counters run to the end of the workspace
     off += align_up(cnt, 256);
     ws->total = off;
     return LORA_OK;
@@ -400,6 +409,8 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
     if (lora::device_status_ptr(&plan.status) != cudaSuccess) return LORA_ERR_CUDA;
     for (int i = 0; i < plan.n_proj; ++i) plan.proj[i].V = reinterpret_cast<float *>(base + ws.v_off[i]);
     plan.part = reinterpret_cast<float *>(base + ws.part_off);
+    plan.ycorr = reinterpret_cast<float *>(base + ws.ycorr_off);
+    plan.group_table = reinterpret_cast<int32_t *>(base + ws.group_off);
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);
     plan.n_counters = static_cast<int32_t>((ws.total - ws.counter_off) / sizeof(int32_t));
     cudaStream_t st = as_stream(stream);

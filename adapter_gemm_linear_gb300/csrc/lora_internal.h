@@ -58,6 +58,26 @@ struct ProjView {
     float *V;              // workspace: [v_parts][M][max_rank] fp32
 };
 
+// Rows grouped by adapter slot (device int32 arrays in the workspace):
+// count[0] = G groups; group g holds the sorted positions [start[g],
+// start[g+1]) and slot[g]; perm[i] = the row at sorted position i; positions
+// start[G] .. M-1 are the rows without an adapter.  The groups are cut into
+// chunks of at most kGroupChunkRows positions (the grouped kernels' work
+// items): chunk c covers positions [chunk_begin[c], chunk_begin[c+1]) of group
+// chunk_group[c]; count[1] chunks belong to groups, count[2] >= count[1] also
+// cover the rows without an adapter (chunk_group = G).
+struct GroupTable {
+    int32_t *count;        // [3]
+    int32_t *start;        // [M + 1]
+    int32_t *slot;         // [M]
+    int32_t *perm;         // [M]
+    int32_t *chunk_group;  // [M + 1]
+    int32_t *chunk_begin;  // [M + 2]
+};
+constexpr int kGroupChunkRows = 8;
+constexpr int kGroupedMaxRows = 2048;  // rows the group table is built for (shared memory of its kernel)
+constexpr int kMaxVPlanes = 4;         // K slices of the grouped shrink
+
 struct ForwardPlan {
     lora_dtype_t dtype;
     int32_t M, K, ldx;
@@ -68,6 +88,8 @@ struct ForwardPlan {
     unsigned long long *status;
     void *const *stage_events;  // NULL or 1 + 2*n_proj cudaEvent_t
     float *part;                // workspace: split-K partial tiles
+    float *ycorr;               // workspace: fp32 [M][N] LoRA correction (small-M orientation)
+    int32_t *group_table;       // workspace: GroupTable storage (small-M orientation)
     int32_t *counters;          // workspace: split-K tile counters, zeroed by the shrink
     int32_t n_counters;         // entries of `counters`
     int v_parts;                // partial planes of V the shrink writes (1 or 2)
@@ -81,6 +103,8 @@ struct WorkspaceLayout {
     size_t row_slot_off;          // int32[M] (segment mode only)
     size_t v_off[LORA_MAX_PROJ];  // fp32[M][max_rank]
     size_t part_off;              // fp32 split-K partial tiles (largest projection)
+    size_t ycorr_off;             // fp32 [M][N] correction of the small-M orientation (largest projection)
+    size_t group_off;             // int32 group table (small-M orientation)
     size_t counter_off;           // int32 per output tile (split-K)
     size_t total;
 };
@@ -108,6 +132,23 @@ cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream);
 
 // Multiprocessors of the current device (cached per device; 148 if unknown).
 int device_sm_count();
+
+// The small-M LoRA path by adapter group (lora_grouped.cu): the rows' group
+// table (rows sorted by slot), then per projection the grouped shrink into
+// plan.v_parts K-slice planes of V and the grouped expand into plan.ycorr
+// ([M][N] fp32, zero for rows without an adapter).
+int grouped_v_planes(int32_t K);
+// Rows few and ranks small enough for the per-row LoRA kernel (one kernel:
+// v = A_i x[m] in shared memory, then ycorr[m, :]); otherwise the grouped path.
+bool row_lora_preferred(int32_t M, int32_t K, int32_t N, int32_t max_rank);
+cudaError_t launch_lora_rows(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+size_t group_table_ints(int32_t M);
+GroupTable group_table_at(int32_t *base, int32_t M);
+cudaError_t launch_group_rows(const ForwardPlan &plan, const GroupTable &gt, int32_t max_slots, cudaStream_t stream);
+cudaError_t launch_shrink_grouped(const ForwardPlan &plan, const ProjView &v, const GroupTable &gt,
+                                  cudaStream_t stream);
+cudaError_t launch_expand_grouped(const ForwardPlan &plan, const ProjView &v, const GroupTable &gt,
+                                  cudaStream_t stream);
 
 // Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K);

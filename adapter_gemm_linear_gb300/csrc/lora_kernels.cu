@@ -408,34 +408,60 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
     return cudaSuccess;
 }
 
-// bf16: CUDA-core shrink, then the tensor-core GEMM with the fused expand
-// (launched as a programmatic dependent of the shrink, see tc_gemm.cu).
+// bf16.  Small M (the GEMM's swapped orientation): per projection the LoRA
+// term into plan.ycorr (lora_grouped.cu) -- by one per-row kernel when each
+// row's A and B are cheap to read, else by the rows' group table and the
+// grouped shrink and expand -- then the GEMM, which adds it.  Large M: the
+// per-row shrink, then the GEMM, whose epilogue applies the expand.  The GEMM
+// is launched as a programmatic dependent of the kernel before it (see
+// tc_gemm.cu).
 static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t stream) {
     using T = __nv_bfloat16;
+    const bool swapped = plan_tc(plan.M, plan.proj[0].N, plan.K).swap;
+    bool by_row = swapped;
+    for (int p = 0; p < plan.n_proj; ++p)
+        by_row = by_row && row_lora_preferred(plan.M, plan.K, plan.proj[p].N, plan.proj[p].max_rank);
+    GroupTable gt{};
+    cudaError_t e = cudaSuccess;
+    if (swapped && !by_row) {
+        gt = group_table_at(plan.group_table, plan.M);
+        e = launch_group_rows(plan, gt, plan.proj[0].max_slots, stream);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+    }
     for (int p = 0; p < plan.n_proj; ++p) {
         const ProjView &v = plan.proj[p];
-        dim3 sgrid(plan.M, v.bps);
-        // few (row, block) pairs: the wide kernel that keeps a whole A block
-        // in flight per CTA; many: the narrow one, several CTAs per SM
-        if (static_cast<int64_t>(plan.M) * v.bps <= 4 * static_cast<int64_t>(device_sm_count()))
-            shrink_rows_bf16_kernel<2><<<sgrid, 256, 0, stream>>>(
-                static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
-                static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
-                v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
-        else
-            shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
-                static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
-                static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
-                v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if (by_row) {
+            e = launch_lora_rows(plan, v, stream);
+            if (e != cudaSuccess) return e;
+        } else if (swapped) {
+            e = launch_shrink_grouped(plan, v, gt, stream);
+            if (e == cudaSuccess) e = launch_expand_grouped(plan, v, gt, stream);
+            if (e != cudaSuccess) return e;
+        } else {
+            dim3 sgrid(plan.M, v.bps);
+            // few (row, block) pairs: the wide kernel that keeps a whole A
+            // block in flight per CTA; many: the narrow one, several CTAs per SM
+            if (static_cast<int64_t>(plan.M) * v.bps <= 4 * static_cast<int64_t>(device_sm_count()))
+                shrink_rows_bf16_kernel<2><<<sgrid, 256, 0, stream>>>(
+                    static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
+                    static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
+                    v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
+            else
+                shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
+                    static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
+                    static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
+                    v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
         if (plan.stage_events) {
             e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[1 + 2 * p]), stream);
             if (e != cudaSuccess) return e;
         }
         e = launch_gemm_lora_tc(plan, v, stream);
         if (e != cudaSuccess) return e;
-        count_launches(2);
+        count_launches(swapped && !by_row ? 3 : 2);
         if (plan.stage_events) {
             e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[2 + 2 * p]), stream);
             if (e != cudaSuccess) return e;

@@ -1,5 +1,5 @@
 // Base GEMM on the 5th-generation tensor cores (tcgen05, fp32 accumulators in
-// TMEM, operands staged by TMA) with the LoRA expand fused into the epilogue:
+// TMEM, operands staged by TMA) with the LoRA term added in the epilogue:
 //
 //   out[m, n] = round( sum_k x[m,k] W[n,k]  +  s_i * sum_j B_i[n,j] V[m,j] )
 //
@@ -17,12 +17,12 @@
 //                N = BN tokens; TMEM lane = output column, column = token.  With
 //                few tokens this puts W's rows on the 128 lanes, and split-K
 //                spreads each tile's K range over several CTAs so that ~all
-//                SMs stream W.  The correction of a tile is precomputed in
-//                shared memory while its MMAs run (with split-K, each split
-//                takes a share of the tile's adapters).  Each split stores its
+//                SMs stream W.  The correction comes precomputed from the
+//                grouped expand kernel as an fp32 [M][N] array (ycorr) and is
+//                added before the rounding.  Under split-K each split stores its
 //                fp32 partial tile to an L2-resident slice and bumps a per-tile
 //                counter; when the count is complete every split sums the
-//                slices over its own range of tokens and stores bf16.
+//                slices and ycorr over its own range of tokens and stores bf16.
 // Warp roles:
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per
 //               k-block into a shared-memory ring (128-byte swizzle);
@@ -58,10 +58,8 @@ constexpr int kEpiWarps = 8;   // two per TMEM lane quarter
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kSmemLimit = 226 * 1024;   // dynamic shared memory per CTA (227 KiB opt-in maximum)
-constexpr int kVStageBytes = 16 * 1024;  // swapped orientation: staged rows of V
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kEpiBarrier = 1;         // named barrier of the epilogue warps
-constexpr int kMetaBlk = 8;            // pool block ids kept per token in shared memory (ranks <= 128)
 
 struct TcParams {
     int32_t M, N, K;
@@ -80,6 +78,7 @@ struct TcParams {
     int32_t v_parts;        // 1 or 2 partial planes of V, summed here
     size_t v_part_stride;   // elements between the planes
     float *part;        // split-K partial tiles [splits][tiles][BN][128] fp32 (splits > 1)
+    const float *ycorr; // swapped orientation: fp32 [M][N] LoRA correction from the expand kernel
     int32_t *counters;  // per tile, zero on entry (splits > 1)
     unsigned long long *status;
 };
@@ -88,19 +87,14 @@ template <bool SWAP, int BN>
 struct Cfg {
     static constexpr uint32_t kABytes = kBM * kBK * 2;
     static constexpr uint32_t kBBytes = BN * kBK * 2;
-    // swapped orientation: the LoRA correction of a tile, fp32 [BN tokens][128 columns]
-    static constexpr int kCorrBytes = SWAP ? BN * kBM * 4 : 0;
-    // per-token metadata: slot, rank, scale, order (+ group index, first pool
-    // blocks and the V stage when swapped)
-    static constexpr int kMetaBytes = BN * 16 + (SWAP ? BN * 4 + BN * kMetaBlk * 4 + kVStageBytes : 0);
-    // ring + correction tile + barriers + TMEM address + flags + metadata + alignment slack
-    static constexpr int kFixed = 1024 + kCorrBytes + (2 * 12 + 4) * 8 + 16 + kMetaBytes;
+    // ring + barriers + TMEM address + flags + alignment slack
+    static constexpr int kFixed = 1024 + (2 * 12 + 4) * 8 + 16;
     static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes);
     static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
     static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                         : 2 * BN <= 256 ? 256 : 512;
-    static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + kCorrBytes +
-                                    (2 * kStages + 4) * 8 + 16 + kMetaBytes;
+    static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) +
+                                    (2 * kStages + 4) * 8 + 16;
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kStages >= 2, "ring too small");
 };
@@ -125,15 +119,6 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
         w.tb = r / p.tiles_a;
     }
     return w;
-}
-
-__device__ __forceinline__ void unpack_bf16x8(const uint4 &q, float *v) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -314,192 +299,13 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
     for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(raw[e]);
 }
 
-__device__ __forceinline__ float4 add4(float4 a, const float4 &b) {
-    a.x += b.x;
-    a.y += b.y;
-    a.z += b.z;
-    a.w += b.w;
-    return a;
-}
-
-// Swapped orientation: ask L2 for the B pieces the tile's correction will
-// read (one 4 KiB piece per adapter and rank block: rows n0 .. n0+127 of the
-// block's [N][16] layout), as soon as the tile's adapters are known, so that
-// the correction's loads find them in L2 instead of waiting on DRAM.
-template <int BN>
-__device__ __forceinline__ void prefetch_b_pieces(const TcParams &p, int32_t n0, const int32_t *meta_slot,
-                                                  const int32_t *meta_rank, const int32_t *meta_order,
-                                                  const int32_t *meta_blk) {
-    constexpr int kRowsPerLine = 128 / (LORA_BLOCK_ROWS * 2);  // 4 rows of 32 bytes
-    constexpr int kLines = kBM / kRowsPerLine;
-    const int et = threadIdx.x - 64;
-    for (int idx = et; idx < BN * kLines; idx += kEpiThreads) {
-        const int i = idx / kLines;
-        const int32_t row = n0 + (idx % kLines) * kRowsPerLine;
-        const int e = meta_order[i];
-        const int32_t slot = meta_slot[e];
-        if (slot < 0 || row >= p.N) continue;
-        if (i > 0 && meta_slot[meta_order[i - 1]] == slot) continue;  // once per adapter
-        const int32_t nblk = min((meta_rank[e] + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS, kMetaBlk);
-        for (int32_t jb = 0; jb < nblk; ++jb) {
-            const __nv_bfloat16 *src =
-                p.b_arena + (static_cast<size_t>(meta_blk[e * kMetaBlk + jb]) * p.N + row) * LORA_BLOCK_ROWS;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
-        }
-    }
-}
-
-// Next (group, rank block) pair of this thread, in sorted-position order
-// within the V chunk [c0, c1).  A group is a run of sorted positions with one
-// adapter (meta_gidx = its index in the tile); group g belongs to the thread
-// when g % (2 * n_parts) == 2 * part + half.  The cursor (a = first position of
-// the current group inside the chunk, jb = next block) advances to the next
-// owned group when the current one has no blocks left.
-struct PairCursor {
-    int a;       // first sorted position of the current group (in the chunk)
-    int b;       // one past its last position (in the chunk)
-    int jb;      // next rank block of the group
-    int nblk;    // rank blocks of the group (0: no owned group left)
-};
-
-__device__ __forceinline__ void cursor_seek(PairCursor &c, int from, int c1, const int32_t *meta_gidx,
-                                            const int32_t *meta_order, const int32_t *meta_rank, int owner,
-                                            int modulus) {
-    int a = from;
-    while (a < c1) {
-        int b = a + 1;
-        while (b < c1 && meta_gidx[b] == meta_gidx[a]) ++b;
-        if (meta_gidx[a] % modulus == owner) {
-            c.a = a;
-            c.b = b;
-            c.jb = 0;
-            c.nblk = (meta_rank[meta_order[a]] + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
-            return;
-        }
-        a = b;
-    }
-    c.a = c.b = c1;
-    c.jb = 0;
-    c.nblk = 0;
-}
-
-// Swapped orientation, before the tile's accumulator is ready: the LoRA
-// correction of the whole tile, corr[e][n_local] = s * sum_j B[n][j] V[m][j]
-// for the unit's tokens m = m0 + e and output columns n = n0 + n_local.
-// Tokens are taken in adapter order (meta_order), the adapted ones first.
-// Adapter groups are dealt round-robin to (part, half): each of the n_parts
-// splits of a split-K tile takes its share (and adds it to its partial tile);
-// within a CTA the two halves of the epilogue threads alternate, so every
-// (token, column) of `corr` has one writer.  V rows of the adapted tokens are
-// staged in shared memory (in chunks of sorted positions when they do not fit
-// at once); the thread's 32-byte pieces of B are loaded four (group, rank
-// block) pairs at a time, all four in flight before any is used, and each
-// piece serves every token of its group.
-template <int BN>
-__device__ __forceinline__ void build_correction(const TcParams &p, int32_t n0, int32_t m0, const int32_t *meta_slot,
-                                                 const int32_t *meta_rank, const float *meta_scale,
-                                                 const int32_t *meta_order, const int32_t *meta_gidx,
-                                                 const int32_t *meta_blk, float *vst, float *corr, int part,
-                                                 int n_parts) {
-    constexpr int kP = 4;  // (group, rank block) pairs in flight
-    const int et = threadIdx.x - 64;
-    const int n_local = et % kBM;
-    const int half = et / kBM;
-    const int32_t n = n0 + n_local;
-    const bool n_ok = n < p.N;
-    const int modulus = 2 * n_parts, owner = 2 * part + half;
-    const int32_t ldv = p.ldv;
-    // adapted tokens come first in meta_order: n_adapted = first position without one
-    int lo = 0, hi = BN;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (meta_slot[meta_order[mid]] >= 0) lo = mid + 1; else hi = mid;
-    }
-    const int n_adapted = lo;
-    const int chunk = (kVStageBytes / 4) / ldv;  // sorted positions per V stage
-    for (int c0 = 0; c0 < n_adapted; c0 += chunk) {
-        const int c1 = min(n_adapted, c0 + chunk);
-        // stage V rows (both partial planes summed) of sorted positions [c0, c1)
-        const int q4 = ldv / 4;
-        for (int i4 = et; i4 < (c1 - c0) * q4; i4 += kEpiThreads) {
-            const int row = i4 / q4;
-            const int e = meta_order[c0 + row];
-            const float4 *src = reinterpret_cast<const float4 *>(p.V + static_cast<size_t>(m0 + e) * ldv) + (i4 - row * q4);
-            float4 v = *src;
-            if (p.v_parts > 1) v = add4(v, src[p.v_part_stride / 4]);
-            reinterpret_cast<float4 *>(vst)[i4] = v;
-        }
-        epi_sync();
-        if (n_ok) {
-            PairCursor cur;
-            cursor_seek(cur, c0, c1, meta_gidx, meta_order, meta_rank, owner, modulus);
-#pragma unroll 1
-            while (cur.nblk > 0) {
-                uint4 q[kP][2];
-                int pa[kP], pb[kP], pj[kP];
-#pragma unroll
-                for (int u = 0; u < kP; ++u) {
-                    pa[u] = -1;
-                    if (cur.nblk > 0) {
-                        const int e0 = meta_order[cur.a];
-                        const int32_t blk =
-                            cur.jb < kMetaBlk
-                                ? meta_blk[e0 * kMetaBlk + cur.jb]
-                                : p.table[static_cast<size_t>(meta_slot[e0]) * p.bps + cur.jb];
-                        const uint4 *bsrc = reinterpret_cast<const uint4 *>(
-                            p.b_arena + (static_cast<size_t>(blk) * p.N + n) * LORA_BLOCK_ROWS);
-                        q[u][0] = __ldg(bsrc);
-                        q[u][1] = __ldg(bsrc + 1);
-                        pa[u] = cur.a;
-                        pb[u] = cur.b;
-                        pj[u] = cur.jb;
-                        if (++cur.jb == cur.nblk)
-                            cursor_seek(cur, cur.b, c1, meta_gidx, meta_order, meta_rank, owner, modulus);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kP; ++u) {
-                    if (pa[u] < 0) continue;
-                    float bv[16];
-                    unpack_bf16x8(q[u][0], bv);
-                    unpack_bf16x8(q[u][1], bv + 8);
-                    const float sc = meta_scale[meta_order[pa[u]]];
-#pragma unroll 1
-                    for (int i = pa[u]; i < pb[u]; ++i) {
-                        const float4 *vr = reinterpret_cast<const float4 *>(vst + (i - c0) * ldv + pj[u] * LORA_BLOCK_ROWS);
-                        const float4 v0 = vr[0], v1 = vr[1], v2 = vr[2], v3 = vr[3];
-                        float a0 = bv[0] * v0.x, a1 = bv[1] * v0.y, a2 = bv[2] * v0.z, a3 = bv[3] * v0.w;
-                        a0 = fmaf(bv[4], v1.x, a0);
-                        a1 = fmaf(bv[5], v1.y, a1);
-                        a2 = fmaf(bv[6], v1.z, a2);
-                        a3 = fmaf(bv[7], v1.w, a3);
-                        a0 = fmaf(bv[8], v2.x, a0);
-                        a1 = fmaf(bv[9], v2.y, a1);
-                        a2 = fmaf(bv[10], v2.z, a2);
-                        a3 = fmaf(bv[11], v2.w, a3);
-                        a0 = fmaf(bv[12], v3.x, a0);
-                        a1 = fmaf(bv[13], v3.y, a1);
-                        a2 = fmaf(bv[14], v3.z, a2);
-                        a3 = fmaf(bv[15], v3.w, a3);
-                        float &c = corr[meta_order[i] * kBM + n_local];
-                        c = fmaf(sc, (a0 + a1) + (a2 + a3), c);
-                    }
-                }
-            }
-        }
-        epi_sync();  // the stage is rewritten by the next chunk
-    }
-}
-
 // Epilogue warps: warp w (2..2+kEpiWarps-1) may access TMEM lane quarter
 // w % 4; the kEpiWarps / 4 warps sharing a quarter take turns over the
 // 32-column chunks.
 template <bool SWAP, int BN>
 __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_full, uint64_t *tmem_empty,
                                              uint32_t tmem_base, volatile uint32_t *abort_flag,
-                                             volatile uint32_t *last_flag, int32_t *meta_slot,
-                                             int32_t *meta_rank, float *meta_scale, int32_t *meta_order,
-                                             int32_t *meta_gidx, int32_t *meta_blk, float *vst, float *corr) {
+                                             volatile uint32_t *last_flag) {
     using namespace sm100;
     constexpr int kGroups = kEpiWarps / 4;
     constexpr int kChunks = BN / 32;
@@ -513,64 +319,22 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
     for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
         const Unit w = decode_unit<SWAP>(u, p);
         const int b = t & 1;
-        if (SWAP) {
-            // slot, rank and scale of this unit's tokens (the previous unit is
-            // done with the arrays: every unit ends with a barrier)
-            for (int e = et; e < BN; e += kEpiThreads) {
-                const int32_t m = w.tb * BN + e;
-                int32_t r = 0, slot = -1;
-                float s = 0.0f;
-                if (m < p.M)
-                    slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s,
-                                        p.status, false);
-                if (slot >= 0) {
-                    // the adapter's pool blocks: the first kMetaBlk kept here,
-                    // every one checked (a corrupt entry drops the correction)
-                    const int32_t *trow = p.table + static_cast<size_t>(slot) * p.bps;
-                    const int32_t nblk = (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
-                    bool ok = true;
-                    for (int32_t jb = 0; jb < nblk; ++jb) {
-                        const int32_t blk = trow[jb];
-                        ok &= blk >= 0 && blk < p.num_blocks;
-                        if (jb < kMetaBlk) meta_blk[e * kMetaBlk + jb] = blk;
-                    }
-                    if (!ok) {
-                        record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
-                        slot = -1;
-                    }
-                }
-                meta_slot[e] = slot;
-                meta_rank[e] = r;
-                meta_scale[e] = s;
+        // swapped, one split: this thread's correction values (rows of its
+        // 32-token chunks, its column) are fetched while the MMAs finish
+        constexpr int kMyChunks = (kChunks + kGroups - 1) / kGroups;
+        float yc[SWAP ? kMyChunks : 1][32];
+        const int32_t n_sw = w.ta * kBM + q * 32 + lane;
+        if (SWAP && p.splits == 1) {
+            grid_dependency_wait();  // ycorr comes from the expand kernel
+#pragma unroll
+            for (int ci = 0; ci < kMyChunks; ++ci) {
+                const int32_t m0 = w.tb * BN + (grp + ci * kGroups) * 32;
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    yc[ci][e] = (n_sw < p.N && m0 + e < p.M && grp + ci * kGroups < kChunks)
+                                    ? __ldcg(p.ycorr + static_cast<size_t>(m0 + e) * p.N + n_sw)
+                                    : 0.0f;
             }
-        }
-        // the correction of a swapped tile is built now, while the tile's MMAs
-        // run; with split-K every split builds its share of the adapters
-        if (SWAP) {
-            epi_sync();
-            for (int e = et; e < BN; e += kEpiThreads) {
-                const int32_t key = meta_slot[e] < 0 ? 0x7fffffff : meta_slot[e];
-                int rnk = 0;
-                for (int e2 = 0; e2 < BN; ++e2) {
-                    const int32_t k2 = meta_slot[e2] < 0 ? 0x7fffffff : meta_slot[e2];
-                    rnk += (k2 < key) || (k2 == key && e2 < e);
-                }
-                meta_order[rnk] = e;
-            }
-            for (int i = et; i < BN * kBM; i += kEpiThreads) corr[i] = 0.0f;
-            epi_sync();
-            // group index of every sorted position (a new group starts where the slot changes)
-            for (int i = et; i < BN; i += kEpiThreads) {
-                int gi = 0;
-                for (int j = 1; j <= i; ++j) gi += meta_slot[meta_order[j]] != meta_slot[meta_order[j - 1]];
-                meta_gidx[i] = gi;
-            }
-            prefetch_b_pieces<BN>(p, w.ta * kBM, meta_slot, meta_rank, meta_order, meta_blk);
-            grid_dependency_wait();  // V and the tile counters come from the shrink kernel
-            epi_sync();
-            build_correction<BN>(p, w.ta * kBM, w.tb * BN, meta_slot, meta_rank, meta_scale, meta_order, meta_gidx,
-                                 meta_blk, vst, corr, w.ks, p.splits);
-            epi_sync();
         }
         bool ok = mbar_wait_bounded(&tmem_full[b], (t >> 1) & 1, kWaitLimitNs);
         if (!ok) {
@@ -585,13 +349,15 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
             const int32_t n = w.ta * kBM + q * 32 + lane;
             const bool n_ok = n < p.N;
             if (p.splits == 1) {
-#pragma unroll 1
-                for (int c = grp; c < kChunks; c += kGroups) {
+#pragma unroll
+                for (int ci = 0; ci < kMyChunks; ++ci) {
+                    const int c = grp + ci * kGroups;
+                    if (c >= kChunks) break;
                     float acc[32];
                     load_tmem_chunk(col0 + c * 32, acc);
                     const int32_t m0 = w.tb * BN + c * 32;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[e] += corr[(c * 32 + e) * kBM + q * 32 + lane];
+                    for (int e = 0; e < 32; ++e) acc[e] += yc[ci][e];
                     if (n_ok) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
@@ -604,11 +370,11 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tmem_empty[b]);
             } else {
-                // partial tile, correction share included, to this split's
-                // slice; once every split of the tile has stored its slice,
-                // each sums the slices over its own range of the tile's tokens.
-                // All splits of a tile run at once: split-K is planned only
-                // when the units fit in one wave of the grid.
+                // partial tile to this split's slice; once every split of the
+                // tile has stored its slice, each sums the slices and the
+                // correction over its own range of the tile's tokens.  All
+                // splits of a tile run at once: split-K is planned only when
+                // the units fit in one wave of the grid.
                 const size_t tile = static_cast<size_t>(w.ta) * p.tiles_b + w.tb;
                 const size_t tiles = static_cast<size_t>(p.tiles_a) * p.tiles_b;
                 constexpr size_t kTileElems = static_cast<size_t>(BN) * kBM;
@@ -618,14 +384,13 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                     float acc[32];
                     load_tmem_chunk(col0 + c * 32, acc);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[e] += corr[(c * 32 + e) * kBM + q * 32 + lane];
-#pragma unroll
                     for (int e = 0; e < 32; ++e) __stcg(mine + (c * 32 + e) * kBM, acc[e]);
                     __syncwarp();
                 }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tmem_empty[b]);
+                grid_dependency_wait();  // the counters' zeroing and ycorr precede this kernel
                 __threadfence();
                 epi_sync();
                 if (et == 0) {
@@ -646,7 +411,15 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                     const size_t split_stride = tiles * kTileElems;
 #pragma unroll 1
                     for (int32_t e0 = e_begin + et / kBM; e0 < e_end; e0 += 4 * (kEpiThreads / kBM)) {
-                        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        float a[4];
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int32_t e = e0 + v * (kEpiThreads / kBM);
+                            const int32_t m = w.tb * BN + e;
+                            a[v] = (e < e_end && m < p.M && nn < p.N)
+                                       ? __ldcg(p.ycorr + static_cast<size_t>(m) * p.N + nn)
+                                       : 0.0f;
+                        }
 #pragma unroll 4
                         for (int32_t ks = 0; ks < p.splits; ++ks) {
 #pragma unroll
@@ -718,21 +491,13 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::kStages * C::kABytes;
-    float *corr = reinterpret_cast<float *>(sB + C::kStages * C::kBBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes + C::kCorrBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes);
     uint64_t *empty = full + C::kStages;
     uint64_t *tmem_full = empty + C::kStages;   // [2]
     uint64_t *tmem_empty = tmem_full + 2;       // [2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
     volatile uint32_t *last_flag = tmem_slot + 2;
-    int32_t *meta_slot = reinterpret_cast<int32_t *>(tmem_slot + 4);
-    int32_t *meta_rank = meta_slot + BN;
-    float *meta_scale = reinterpret_cast<float *>(meta_rank + BN);
-    int32_t *meta_order = reinterpret_cast<int32_t *>(meta_scale + BN);
-    int32_t *meta_gidx = meta_order + BN;  // [BN] group index by sorted position (swapped orientation)
-    int32_t *meta_blk = meta_gidx + BN;    // [BN][kMetaBlk] (swapped orientation)
-    float *vst = reinterpret_cast<float *>(meta_blk + BN * kMetaBlk);  // kVStageBytes (swapped orientation)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -768,8 +533,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
         if (lane == 0)
             run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
     } else {
-        run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, meta_slot,
-                               meta_rank, meta_scale, meta_order, meta_gidx, meta_blk, vst, corr);
+        run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag);
     }
 
     tc_fence_before_sync();
@@ -860,6 +624,7 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.v_parts = plan.v_parts;
     p.v_part_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.part = plan.part;
+    p.ycorr = plan.ycorr;
     p.counters = plan.counters;
     p.status = plan.status;
     // the splits of a tile wait for one another, so they must all be resident:
