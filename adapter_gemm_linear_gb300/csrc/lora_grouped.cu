@@ -648,9 +648,10 @@ cudaError_t launch_lora_rows(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.counters = plan.counters;
     p.n_counters = plan.n_counters;
     p.status = plan.status;
-    // column splits: about two CTAs per SM, at least kRowThreads columns each
+    // column splits: one wave (the kernel holds one CTA per SM), at least
+    // kRowThreads columns per CTA
     const int sms = device_sm_count();
-    int splits = (2 * sms + plan.M - 1) / plan.M;
+    int splits = sms / plan.M;
     const int max_splits = (v.N + kRowThreads - 1) / kRowThreads;
     splits = splits < 1 ? 1 : splits > max_splits ? max_splits : splits;
     p.cols_per_cta = ((v.N + splits - 1) / splits + kRowThreads - 1) / kRowThreads * kRowThreads;

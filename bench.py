@@ -1,11 +1,14 @@
 #!/usr/bin/env python
 """Benchmark of the multi-adapter LoRA linear layer (lora_linear_forward) on GB300.
 
-One step = one lora_linear_forward call over one batch: the shrink kernel
-(V = A_i x per row), the tensor-core base GEMM with the expand fused in its
-epilogue, for every projection of the workload.  Prints ONE JSON line per
-workload (default: the decode BGMV workload, 64 rows of q_proj 4096->4096
-with 32 rank-16 adapters).
+One step = one lora_linear_forward call over one batch, for every projection
+of the workload: the LoRA kernels, then the tensor-core base GEMM that adds
+the LoRA term before rounding.  For M <= 512 (the GEMM's swapped
+orientation) the LoRA kernels write the whole correction s_i B_i A_i x as an
+fp32 [M][N] array (per-row kernel, or the adapter-grouped shrink and
+expand); for larger M the per-row shrink writes V and the GEMM's epilogue
+applies the expand.  Prints ONE JSON line per workload (default: the decode
+BGMV workload, 64 rows of q_proj 4096->4096 with 32 rank-16 adapters).
 
 Timing: W warm-up steps, then K steps; L2 is flushed (a 2 x L2 write)
 before every step, outside the timed intervals.  The timed steps replay one
@@ -155,29 +158,45 @@ def workload_stats(wl):
     }
 
 
-def algorithmic(wl):
-    """Per-call algorithmic bytes and flops of each kernel stage.
+SWAPPED_MAX_M = 512  # the library's GEMM takes the swapped orientation up to this many rows
 
-    GEMM (per projection): W, x and out once, plus the fused expand's
-    adapter B rows (each distinct adapter once) and V reads; flops 2MNK
-    plus the expand's 2 r N per adapted row.  Shrink: each distinct
-    adapter's A rows once, x rows of adapted rows, V writes.
+
+def algorithmic(wl):
+    """Per-call algorithmic bytes and flops of the two stages of a projection.
+
+    Small M (bf16, M <= 512): the LoRA stage reads each distinct adapter's A
+    and B once and the adapted rows of x, and writes the fp32 correction
+    [M][N]; the GEMM reads W, x and the correction and writes out.  Large M:
+    the LoRA stage (shrink) reads the distinct adapters' A and the adapted
+    rows of x and writes V; the GEMM reads W, x, the distinct adapters' B
+    and V and writes out.  FLOPs: 2MNK for the GEMM, 2 r (K + N) per adapted
+    row for the LoRA term (counted where it is computed).
     """
     eb = 2 if wl.dtype == "bf16" else 4
     st = workload_stats(wl)
     M, K = wl.M, wl.K
-    out = {"gemm_bytes": 0, "gemm_flops": 0, "shrink_bytes": 0, "shrink_flops": 0, "per_proj": []}
+    swapped = wl.dtype == "bf16" and M <= SWAPPED_MAX_M
+    out = {"gemm_bytes": 0, "gemm_flops": 0, "lora_bytes": 0, "lora_flops": 0, "per_proj": [],
+           "orientation": "swapped" if swapped else "rows"}
     for p in wl.projections:
         N = p.N
-        gb = (N * K + M * K + M * N) * eb + st["sum_r_distinct"] * N * eb + st["sum_r_rows"] * 4
-        gf = 2 * M * N * K + 2 * st["sum_r_rows"] * N
-        sb = st["sum_r_distinct"] * K * eb + st["adapted_rows"] * K * eb + st["sum_r_rows"] * 4
-        sf = 2 * st["sum_r_rows"] * K
+        a_bytes = st["sum_r_distinct"] * K * eb + st["adapted_rows"] * K * eb
+        b_bytes = st["sum_r_distinct"] * N * eb
+        if swapped:
+            gb = (N * K + M * K + M * N) * eb + M * N * 4
+            gf = 2 * M * N * K
+            lb = a_bytes + b_bytes + M * N * 4
+            lf = 2 * st["sum_r_rows"] * (K + N)
+        else:
+            gb = (N * K + M * K + M * N) * eb + b_bytes + st["sum_r_rows"] * 4
+            gf = 2 * M * N * K + 2 * st["sum_r_rows"] * N
+            lb = a_bytes + st["sum_r_rows"] * 4
+            lf = 2 * st["sum_r_rows"] * K
         out["gemm_bytes"] += gb
         out["gemm_flops"] += gf
-        out["shrink_bytes"] += sb
-        out["shrink_flops"] += sf
-        out["per_proj"].append({"N": N, "gemm_bytes": gb, "gemm_flops": gf})
+        out["lora_bytes"] += lb
+        out["lora_flops"] += lf
+        out["per_proj"].append({"N": N, "gemm_bytes": gb, "gemm_flops": gf, "lora_bytes": lb})
     out.update(st)
     return out
 
@@ -393,25 +412,31 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     alg = algorithmic(wl)
     tokens = wl.M * steps * world
     value = tokens / (total_ms / 1e3)
-    # dominant kernel: the GEMM (compare stage time shares)
+    # dominant stage: the GEMM or the LoRA kernels, by their share of the
+    # eager stage time
     gemm_avg_s = gemm_ms / steps / 1e3
-    shrink_avg_s = shrink_ms / steps / 1e3
-    ai = alg["gemm_flops"] / alg["gemm_bytes"]
+    lora_avg_s = shrink_ms / steps / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if ai > ridge:
-        achieved = alg["gemm_flops"] / gemm_avg_s / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+    gemm_dominant = gemm_ms >= shrink_ms
+    if gemm_dominant:
+        b, f, t = alg["gemm_bytes"], alg["gemm_flops"], gemm_avg_s
+        kernel = "tc_gemm_lora_kernel"
+    else:
+        b, f, t = alg["lora_bytes"], alg["lora_flops"], lora_avg_s
+        kernel = ("lora_rows_kernel or group_rows_kernel + shrink_grouped_kernel + expand_grouped_kernel"
+                  if alg["orientation"] == "swapped" else "shrink kernel")
+    if f / b > ridge:
+        roof = {"bound": "tensor", "achieved": round(f / t / 1e12, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     else:
-        achieved = alg["gemm_bytes"] / gemm_avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": round(b / t / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ncu_traffic(wl.name)
-    roof["kernel"] = "tc_gemm_lora_kernel"
+    roof["traffic"] = ncu_traffic(wl.name) if gemm_dominant else None
+    roof["kernel"] = kernel
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
-    roof["algorithmic_bytes_per_call"] = alg["gemm_bytes"]
-    roof["algorithmic_flops_per_call"] = alg["gemm_flops"]
-    roof["time_share"] = round(gemm_ms / total_ms, 3) if total_ms else None
+    roof["algorithmic_bytes_per_call"] = b
+    roof["algorithmic_flops_per_call"] = f
+    roof["time_share"] = round((gemm_ms if gemm_dominant else shrink_ms) / total_ms, 3) if total_ms else None
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -434,11 +459,12 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
             "parallelism": f"replicas x{world}",
         },
         "roofline": roof,
-        "lora_path": {
-            "shrink_us": round(shrink_avg_s * 1e6, 3),
-            "shrink_gbs": round(alg["shrink_bytes"] / shrink_avg_s / 1e9, 1) if shrink_avg_s > 0 else None,
-            "shrink_frac_hbm": round(alg["shrink_bytes"] / shrink_avg_s / 1e9 / peaks["hbm_gbs"], 4)
-            if shrink_avg_s > 0 else None,
+        "stages": {
+            "orientation": alg["orientation"],
+            "lora_us": round(lora_avg_s * 1e6, 3),
+            "lora_gbs": round(alg["lora_bytes"] / lora_avg_s / 1e9, 1) if lora_avg_s > 0 else None,
+            "lora_frac_hbm": round(alg["lora_bytes"] / lora_avg_s / 1e9 / peaks["hbm_gbs"], 4)
+            if lora_avg_s > 0 else None,
             "gemm_us": round(gemm_avg_s * 1e6, 3),
             "gemm_tc_frac": round(alg["gemm_flops"] / gemm_avg_s / 1e12 / peaks["bf16_tflops"], 4),
             "gemm_hbm_frac": round(alg["gemm_bytes"] / gemm_avg_s / 1e9 / peaks["hbm_gbs"], 4),
