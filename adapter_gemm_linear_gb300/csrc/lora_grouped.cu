@@ -35,12 +35,12 @@ namespace {
 constexpr int kSegThreads = 1024;
 constexpr int kShrThreads = 256;
 constexpr int kShrStep = kShrThreads * 8;   // k covered by one pass of the CTA (8 bf16 per thread)
-constexpr int kShrRows = 4;                 // rows of a group per pass
+constexpr int kShrRows = 2;                 // rows of a group per pass
 constexpr int kExpThreads = 256;
 constexpr int kExpColsPerThread = 4;
 constexpr int kExpCols = kExpThreads * kExpColsPerThread;  // output columns per expand item
 constexpr int kExpRows = 8;                 // rows of a group per pass
-constexpr int kExpBlkChunk = 2;             // rank blocks whose B pieces are in flight together
+constexpr int kExpBlkChunk = 1;             // rank blocks whose B pieces are in flight together
 static_assert(kExpRows * kMaxRankLimit * 4 <= 48 * 1024, "expand stage within the default shared memory");
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &q, float *v) {
@@ -85,7 +85,7 @@ __device__ __forceinline__ int32_t cta_exclusive_scan(int32_t v, int32_t *warp_t
 __global__ void __launch_bounds__(kSegThreads)
 group_rows_kernel(int32_t M, const int32_t *__restrict__ row_slot, int32_t max_slots, GroupTable gt,
                   unsigned long long *status) {
-    extern __shared__ int32_t seg_smem[];
+    extern __shared__ __align__(16) int32_t seg_smem[];
     int32_t *key = seg_smem;              // [M]
     int32_t *pos_row = key + M;           // [M] sorted position -> row
     int32_t *gs = pos_row + M;            // [M + 1] group -> first sorted position
@@ -94,25 +94,36 @@ group_rows_kernel(int32_t M, const int32_t *__restrict__ row_slot, int32_t max_s
     const int tid = threadIdx.x;
     if (tid == 0) n_adapted = 0;
     __syncthreads();
-    for (int32_t m = tid; m < M; m += kSegThreads) {
-        const int32_t id = row_slot[m];
-        int32_t k = 0x7fffffff;
-        if (id >= 0 && id < max_slots) {
-            k = id;
-            atomicAdd(&n_adapted, 1);
-        } else if (id != -1) {
-            record_error(status, kDevBadAdapter, static_cast<uint32_t>(m));
+    for (int32_t base = 0; base < M; base += kSegThreads) {
+        const int32_t m = base + tid;
+        bool adapted = false;
+        if (m < M) {
+            const int32_t id = row_slot[m];
+            int32_t k = 0x7fffffff;
+            if (id >= 0 && id < max_slots) {
+                k = id;
+                adapted = true;
+            } else if (id != -1) {
+                record_error(status, kDevBadAdapter, static_cast<uint32_t>(m));
+            }
+            key[m] = k;
         }
-        key[m] = k;
+        const unsigned ballot = __ballot_sync(0xffffffffu, adapted);  // one shared atomic per warp
+        if ((tid & 31) == 0 && ballot) atomicAdd(&n_adapted, __popc(ballot));
     }
     __syncthreads();
     for (int32_t m = tid; m < M; m += kSegThreads) {
         const int32_t k = key[m];
         int32_t rnk = 0;
-        for (int32_t m2 = 0; m2 < M; ++m2) {
-            const int32_t k2 = key[m2];
-            rnk += (k2 < k) || (k2 == k && m2 < m);
+        int32_t m2 = 0;
+        for (; m2 + 4 <= M; m2 += 4) {
+            const int4 k4 = *reinterpret_cast<const int4 *>(key + m2);
+            rnk += (k4.x < k) || (k4.x == k && m2 < m);
+            rnk += (k4.y < k) || (k4.y == k && m2 + 1 < m);
+            rnk += (k4.z < k) || (k4.z == k && m2 + 2 < m);
+            rnk += (k4.w < k) || (k4.w == k && m2 + 3 < m);
         }
+        for (; m2 < M; ++m2) rnk += (key[m2] < k) || (key[m2] == k && m2 < m);
         pos_row[rnk] = m;
     }
     __syncthreads();
@@ -138,27 +149,31 @@ group_rows_kernel(int32_t M, const int32_t *__restrict__ row_slot, int32_t max_s
         gt.start[G] = na;  // end of the last group; rows without an adapter follow
     }
     __syncthreads();
-    // chunks of at most kGroupChunkRows positions: the groups', then the rows
-    // without an adapter
-    int32_t C = 0;
-    for (int32_t base = 0; base <= G; base += kSegThreads) {
-        const int32_t g = base + tid;
-        int32_t rows = 0;
-        if (g < G) rows = gs[g + 1] - gs[g];
-        else if (g == G) rows = M - na;
-        const int32_t nch = (rows + kGroupChunkRows - 1) / kGroupChunkRows;
-        int32_t tot;
-        const int32_t c0 = C + cta_exclusive_scan(nch, warp_tot, &tot);
-        for (int32_t c = 0; c < nch; ++c) {
-            gt.chunk_group[c0 + c] = g;
-            gt.chunk_begin[c0 + c] = (g < G ? gs[g] : na) + c * kGroupChunkRows;
+    // chunk lists (see GroupTable): the groups' chunks, then the rows without
+    // an adapter
+#pragma unroll 1
+    for (int L = 0; L < 2; ++L) {
+        const int32_t R = L == 0 ? kGroupChunkRowsShrink : kGroupChunkRowsExpand;
+        int32_t C = 0;
+        for (int32_t base = 0; base <= G; base += kSegThreads) {
+            const int32_t g = base + tid;
+            int32_t rows = 0;
+            if (g < G) rows = gs[g + 1] - gs[g];
+            else if (g == G) rows = M - na;
+            const int32_t nch = (rows + R - 1) / R;
+            int32_t tot;
+            const int32_t c0 = C + cta_exclusive_scan(nch, warp_tot, &tot);
+            for (int32_t c = 0; c < nch; ++c) {
+                gt.chunk_group[L][c0 + c] = g;
+                gt.chunk_begin[L][c0 + c] = (g < G ? gs[g] : na) + c * R;
+            }
+            if (g == G) {
+                gt.count[1 + 2 * L] = c0;  // chunks of the groups
+                gt.count[2 + 2 * L] = c0 + nch;
+                gt.chunk_begin[L][c0 + nch] = M;
+            }
+            C += tot;
         }
-        if (g == G) {
-            gt.count[1] = c0;  // chunks of the groups
-            gt.count[2] = c0 + nch;
-            gt.chunk_begin[c0 + nch] = M;
-        }
-        C += tot;
     }
     if (tid == 0) gt.count[0] = G;
 }
@@ -191,13 +206,13 @@ struct GroupedShrinkParams {
 // of the slice per step, keeps the 16 A values of each of those k in
 // registers and applies them to the pass's rows; the CTA then sums the
 // per-thread partial dot products.
-__global__ void __launch_bounds__(kShrThreads)
+__global__ void __launch_bounds__(kShrThreads, 2)
 shrink_grouped_kernel(const GroupedShrinkParams p) {
     __shared__ float red[kShrThreads / 32][kShrRows * LORA_BLOCK_ROWS];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (blockIdx.x == 0)
         for (int32_t c = tid; c < p.n_counters; c += kShrThreads) p.counters[c] = 0;
-    const int32_t chunks = p.gt.count[1];
+    const int32_t chunks = p.gt.count[1];  // list 0
     const int32_t items = chunks * p.bps * p.ksplit;
     const int32_t K8 = p.K / 8;
     for (int32_t u = blockIdx.x; u < items; u += gridDim.x) {
@@ -205,14 +220,14 @@ shrink_grouped_kernel(const GroupedShrinkParams p) {
         const int32_t t = u / p.ksplit;
         const int32_t jb = t % p.bps;
         const int32_t ch = t / p.bps;
-        const int32_t g = p.gt.chunk_group[ch];
+        const int32_t g = p.gt.chunk_group[0][ch];
         const int32_t slot = p.gt.slot[g];
         const int32_t r = p.ranks[slot];
         if (r <= 0 || r > p.bps * LORA_BLOCK_ROWS) continue;  // reported by the expand
         if (jb * LORA_BLOCK_ROWS >= r) continue;
         const int32_t blk = p.table[static_cast<size_t>(slot) * p.bps + jb];
         if (blk < 0 || blk >= p.num_blocks) continue;        // reported by the expand
-        const int32_t p0 = p.gt.chunk_begin[ch], p1 = p.gt.chunk_begin[ch + 1];
+        const int32_t p0 = p.gt.chunk_begin[0][ch], p1 = p.gt.chunk_begin[0][ch + 1];
         const int32_t k8_0 = kc * (p.kc_len / 8);
         const int32_t k8_1 = min(K8, k8_0 + p.kc_len / 8);
         const uint4 *A = reinterpret_cast<const uint4 *>(p.a_arena + static_cast<size_t>(blk) * LORA_BLOCK_ROWS * p.K);
@@ -303,7 +318,7 @@ struct GroupedExpandParams {
 // of the group the rows' V (planes summed) are staged in shared memory while
 // the first kExpBlkChunk blocks' B pieces are in flight; every B piece then
 // serves all rows of the pass.
-__global__ void __launch_bounds__(kExpThreads)
+__global__ void __launch_bounds__(kExpThreads, 2)
 expand_grouped_kernel(const GroupedExpandParams p) {
     extern __shared__ __align__(16) float vs[];  // [kExpRows][ldv]
     // the GEMM that follows may launch now; it reads ycorr only after this
@@ -312,13 +327,13 @@ expand_grouped_kernel(const GroupedExpandParams p) {
     const int tid = threadIdx.x;
     const int32_t G = p.gt.count[0];
     const int32_t n_ranges = (p.N + kExpCols - 1) / kExpCols;
-    const int32_t items = p.gt.count[2] * n_ranges;
+    const int32_t items = p.gt.count[4] * n_ranges;  // list 1
     for (int32_t u = blockIdx.x; u < items; u += gridDim.x) {
         const int32_t ch = u / n_ranges;
         const int32_t nr = u % n_ranges;
-        const int32_t g = p.gt.chunk_group[ch];
-        const int32_t p0 = p.gt.chunk_begin[ch];
-        const int32_t p1 = p.gt.chunk_begin[ch + 1];
+        const int32_t g = p.gt.chunk_group[1][ch];
+        const int32_t p0 = p.gt.chunk_begin[1][ch];
+        const int32_t p1 = p.gt.chunk_begin[1][ch + 1];
         int32_t nblk = 0, slot = -1;
         float sc = 0.0f;
         if (g < G) {
@@ -660,16 +675,18 @@ cudaError_t launch_lora_rows(const ForwardPlan &plan, const ProjView &v, cudaStr
     return cudaGetLastError();
 }
 
-size_t group_table_ints(int32_t M) { return 5 * static_cast<size_t>(M) + 8; }
+size_t group_table_ints(int32_t M) { return 7 * static_cast<size_t>(M) + 16; }
 
 GroupTable group_table_at(int32_t *base, int32_t M) {
     GroupTable gt;
-    gt.count = base;                          // [3]
-    gt.start = base + 3;                      // [M + 1]
-    gt.slot = gt.start + (M + 1);             // [M]
-    gt.perm = gt.slot + M;                    // [M]
-    gt.chunk_group = gt.perm + M;             // [M + 1]
-    gt.chunk_begin = gt.chunk_group + M + 1;  // [M + 2]
+    gt.count = base;                                // [5]
+    gt.start = base + 5;                            // [M + 1]
+    gt.slot = gt.start + (M + 1);                   // [M]
+    gt.perm = gt.slot + M;                          // [M]
+    gt.chunk_group[0] = gt.perm + M;                // [M + 1]
+    gt.chunk_begin[0] = gt.chunk_group[0] + M + 1;  // [M + 2]
+    gt.chunk_group[1] = gt.chunk_begin[0] + M + 2;  // [M + 1]
+    gt.chunk_begin[1] = gt.chunk_group[1] + M + 1;  // [M + 2]
     return gt;
 }
 
@@ -704,10 +721,10 @@ cudaError_t launch_shrink_grouped(const ForwardPlan &plan, const ProjView &v, co
     p.counters = plan.counters;
     p.n_counters = plan.n_counters;
     p.status = plan.status;
-    // upper bound of the items: chunks <= groups + rows / kGroupChunkRows
+    // upper bound of the items: chunks <= groups + rows / chunk rows
     const long groups = plan.M < v.max_slots ? plan.M : v.max_slots;
-    const long items = (groups + plan.M / kGroupChunkRows + 1) * v.bps * p.ksplit;
-    const long cap = 2L * device_sm_count();
+    const long items = (groups + plan.M / kGroupChunkRowsShrink + 1) * v.bps * p.ksplit;
+    const long cap = 4L * device_sm_count();  // two CTAs per SM, two waves of items
     const int grid = static_cast<int>(items < cap ? items : cap);
     shrink_grouped_kernel<<<grid > 0 ? grid : 1, kShrThreads, 0, stream>>>(p);
     return cudaGetLastError();
@@ -736,8 +753,8 @@ cudaError_t launch_expand_grouped(const ForwardPlan &plan, const ProjView &v, co
     // at most kExpRows * 1024 fp32 = 32 KiB: within the default dynamic shared memory
     const size_t smem = sizeof(float) * kExpRows * static_cast<size_t>(v.max_rank);
     const long groups = plan.M < v.max_slots ? plan.M : v.max_slots;
-    const long items = (groups + plan.M / kGroupChunkRows + 2) * ((v.N + kExpCols - 1) / kExpCols);
-    const long cap = 4L * device_sm_count();
+    const long items = (groups + plan.M / kGroupChunkRowsExpand + 2) * ((v.N + kExpCols - 1) / kExpCols);
+    const long cap = 8L * device_sm_count();
     const int grid = static_cast<int>(items < cap ? items : cap);
     expand_grouped_kernel<<<grid > 0 ? grid : 1, kExpThreads, smem, stream>>>(p);
     return cudaGetLastError();

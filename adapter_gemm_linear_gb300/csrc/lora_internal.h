@@ -62,19 +62,24 @@ struct ProjView {
 // count[0] = G groups; group g holds the sorted positions [start[g],
 // start[g+1]) and slot[g]; perm[i] = the row at sorted position i; positions
 // start[G] .. M-1 are the rows without an adapter.  The groups are cut into
-// chunks of at most kGroupChunkRows positions (the grouped kernels' work
-// items): chunk c covers positions [chunk_begin[c], chunk_begin[c+1]) of group
-// chunk_group[c]; count[1] chunks belong to groups, count[2] >= count[1] also
-// cover the rows without an adapter (chunk_group = G).
+// two lists of chunks, the grouped kernels' work items: list L cuts every
+// group into chunks of at most kGroupChunkRowsShrink (L = 0) or
+// kGroupChunkRowsExpand (L = 1) positions; chunk c covers
+// positions [chunk_begin[L][c], chunk_begin[L][c+1]) of group chunk_group[L][c].
+// count[1 + 2L] chunks belong to groups, count[2 + 2L] >= count[1 + 2L] also
+// cover the rows without an adapter (chunk_group = G).  List 0 feeds the
+// shrink (short chunks: many items), list 1 the expand (long chunks: each B
+// piece serves more rows).
+constexpr int kGroupChunkRowsShrink = 8;   // list 0
+constexpr int kGroupChunkRowsExpand = 32;  // list 1
 struct GroupTable {
-    int32_t *count;        // [3]
-    int32_t *start;        // [M + 1]
-    int32_t *slot;         // [M]
-    int32_t *perm;         // [M]
-    int32_t *chunk_group;  // [M + 1]
-    int32_t *chunk_begin;  // [M + 2]
+    int32_t *count;           // [5]
+    int32_t *start;           // [M + 1]
+    int32_t *slot;            // [M]
+    int32_t *perm;            // [M]
+    int32_t *chunk_group[2];  // [M + 1] each
+    int32_t *chunk_begin[2];  // [M + 2] each
 };
-constexpr int kGroupChunkRows = 8;
 constexpr int kGroupedMaxRows = 2048;  // rows the group table is built for (shared memory of its kernel)
 constexpr int kMaxVPlanes = 4;         // K slices of the grouped shrink
 
