@@ -97,7 +97,7 @@ struct ForwardPlan {
     int32_t *group_table;       // workspace: GroupTable storage (small-M orientation)
     int32_t *counters;          // workspace: split-K tile counters, zeroed by the shrink
     int32_t n_counters;         // entries of `counters`
-    int v_parts;                // partial planes of V the shrink writes (1 or 2)
+    int v_parts;                // K-slice planes of V the shrink writes
 };
 
 // Count of kernels launched by the library (lora_kernel_launches).

@@ -75,7 +75,7 @@ struct TcParams {
     int32_t max_slots, bps, num_blocks;
     const float *V;
     int32_t ldv;
-    int32_t v_parts;        // 1 or 2 partial planes of V, summed here
+    int32_t v_parts;        // K-slice planes of V, summed here
     size_t v_part_stride;   // elements between the planes
     float *part;        // split-K partial tiles [splits][tiles][BN][128] fp32 (splits > 1)
     const float *ycorr; // swapped orientation: fp32 [M][N] LoRA correction from the expand kernel
@@ -250,8 +250,8 @@ __device__ __forceinline__ void rows_finish_chunk(const TcParams &p, int32_t slo
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             float4 q = vsrc[g];
-            if (p.v_parts > 1) {
-                const float4 w2 = vsrc[g + p.v_part_stride / 4];
+            for (int32_t pl = 1; pl < p.v_parts; ++pl) {  // K-slice planes of the shrink
+                const float4 w2 = vsrc[g + pl * (p.v_part_stride / 4)];
                 q.x += w2.x; q.y += w2.y; q.z += w2.z; q.w += w2.w;
             }
             v[4 * g] = q.x;
