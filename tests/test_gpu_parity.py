@@ -83,6 +83,32 @@ def test_integer_exact_split_k_and_orientations(shape):
         assert np.array_equal(got, want), f"{shape} projection {p}: {np.sum(got != want)} outputs differ"
 
 
+@pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
+@pytest.mark.parametrize("shape", [(500, 1032, 392), (480, 1032, 136)])
+def test_grouped_path_small(shape, mode):
+    """Rows few enough for the swapped GEMM but ranks large enough that the
+    library groups rows by adapter (device group table, grouped shrink and
+    expand) instead of reading each row's A and B per row; a popular adapter
+    spans several row chunks, the column tail is ragged."""
+    M, K, N = shape
+    wl = synth(M=M, K=K, Ns=[N], num_slots=9, rank_choices=(1, 40, 129, 256), seed=M + N,
+               zipf_s=1.5, mode=mode)
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, mode)[0]
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0), f"grouped {shape} {mode}")
+
+
+def test_grouped_path_integer_exact():
+    wl = synth(M=450, K=1024, Ns=[264, 72], num_slots=7, rank_choices=(3, 64, 200, 256), integer=True,
+               seed=33, none_frac=0.2, zipf_s=1.3)
+    pools = H.make_pools(wl, DEV)
+    outs = H.forward(wl, pools, "bgmv")
+    for p in range(2):
+        want = H.oracle_bf16_bits(H.oracle_rows(wl, p))
+        got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), f"projection {p}: {np.sum(got != want)} outputs differ"
+
+
 def test_tiny_fp32_full():
     wl = make_config("tiny_fp32")
     pools = H.make_pools(wl, DEV)
