@@ -360,8 +360,18 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         v.num_blocks = d.num_blocks;
         v.max_rank = d.max_rank;
         v.V = nullptr;
+        // large M in bf16 with few slot columns: the LoRA term joins the
+        // GEMM's K on the tensor cores (Vm, Bm; no fp32 V)
+        const int64_t cols = (static_cast<int64_t>(d.max_slots) * d.max_rank + 63) / 64 * 64;
+        v.ext_cols = (a->dtype == LORA_BF16 && a->M > 0 && !lora::plan_tc(a->M, d.N, a->K).swap &&
+                      cols <= lora::kExtMaxCols)
+                         ? static_cast<int32_t>(cols)
+                         : 0;
+        v.vm = v.bm = nullptr;
+        v.tile_range = nullptr;
         ws->v_off[i] = off;
-        off += align_up(sizeof(float) * static_cast<size_t>(a->M) * d.max_rank * plan->v_parts, 256);
+        if (v.ext_cols == 0)
+            off += align_up(sizeof(float) * static_cast<size_t>(a->M) * d.max_rank * plan->v_parts, 256);
     }
     // slot ids of every pool must mean the same adapters
     for (int i = 1; i < a->n_proj; ++i)
@@ -384,6 +394,21 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     off += align_up(ycorr, 256);
     ws->group_off = off;
     if (ycorr) off += align_up(sizeof(int32_t) * lora::group_table_ints(a->M), 256);
+    // the tensor-core LoRA term of large M: Vm, Bm and the token tiles' slot
+    // ranges, shared by the projections
+    size_t vm = 0, bm = 0;
+    for (int i = 0; i < a->n_proj; ++i) {
+        const lora::ProjView &v = plan->proj[i];
+        if (v.ext_cols == 0) continue;
+        vm = std::max(vm, sizeof(uint16_t) * static_cast<size_t>(a->M) * 2 * v.ext_cols);
+        bm = std::max(bm, sizeof(uint16_t) * static_cast<size_t>(v.N) * v.ext_cols);
+    }
+    ws->vm_off = off;
+    off += align_up(vm, 256);
+    ws->bm_off = off;
+    off += align_up(bm, 256);
+    ws->range_off = off;
+    if (vm) off += align_up(sizeof(int32_t) * 2 * static_cast<size_t>((a->M + 127) / 128), 256);
     ws->counter_off = off;  // last: the counters run to the end of the workspace
     off += align_up(cnt, 256);
     ws->total = off;
@@ -411,6 +436,12 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
     plan.part = reinterpret_cast<float *>(base + ws.part_off);
     plan.ycorr = reinterpret_cast<float *>(base + ws.ycorr_off);
     plan.group_table = reinterpret_cast<int32_t *>(base + ws.group_off);
+    for (int i = 0; i < plan.n_proj; ++i) {
+        if (plan.proj[i].ext_cols == 0) continue;
+        plan.proj[i].vm = base + ws.vm_off;
+        plan.proj[i].bm = base + ws.bm_off;
+        plan.proj[i].tile_range = reinterpret_cast<int32_t *>(base + ws.range_off);
+    }
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);
     plan.n_counters = static_cast<int32_t>((ws.total - ws.counter_off) / sizeof(int32_t));
     cudaStream_t st = as_stream(stream);

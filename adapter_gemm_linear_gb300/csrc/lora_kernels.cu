@@ -287,6 +287,175 @@ shrink_rows_bf16_kernel(const __nv_bfloat16 *__restrict__ x, int32_t ldx, int32_
 }
 
 // ---------------------------------------------------------------------------
+// Large M, LoRA term on the tensor cores: the GEMM's K extends over
+//   [Vm_hi | Vm_lo] (beside x) and [Bm | Bm] (beside W),
+// Bm[n][s*R + j] = B_s[n][j] (zero for j >= r_s and for empty slots or
+// corrupt block entries), Vm[m][s*R + j] = hi / lo bf16 parts of s_i V[m][j]
+// for the row's own slot s (zero elsewhere), R = the pool's max rank.  The
+// two bf16 parts carry about 16 significant bits of s_i V, so Vm Bm^T adds the
+// correction to the fp32 accumulator with the precision of an fp32 V.
+// ---------------------------------------------------------------------------
+
+// One thread per (output row n, slot): the slot's R columns of Bm row n, 32
+// bytes (16 ranks of one pool block) at a time; the last "slot" index writes
+// the zero padding past max_slots * R.  The first threads also reset the
+// token tiles' slot ranges for the shrink that follows.
+__global__ void ext_prepare_kernel(int32_t N, int32_t max_slots, int32_t R, int32_t ext_cols,
+                                   const __nv_bfloat16 *__restrict__ b_arena,
+                                   const int32_t *__restrict__ table, const int32_t *__restrict__ ranks,
+                                   int32_t bps, int32_t num_blocks, __nv_bfloat16 *__restrict__ bm,
+                                   int32_t *__restrict__ tile_range, int32_t n_tiles) {
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (gid < n_tiles) {
+        tile_range[2 * gid] = 0x7fffffff;
+        tile_range[2 * gid + 1] = -1;
+    }
+    const int64_t total = static_cast<int64_t>(N) * (max_slots + 1);
+    if (gid >= total) return;
+    const int32_t slot = static_cast<int32_t>(gid % (max_slots + 1));
+    const int32_t n = static_cast<int32_t>(gid / (max_slots + 1));
+    uint4 *dst_row = reinterpret_cast<uint4 *>(bm + static_cast<size_t>(n) * ext_cols);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    if (slot == max_slots) {  // padding columns
+        for (int32_t c = max_slots * R; c < ext_cols; c += LORA_BLOCK_ROWS) {
+            dst_row[c / 8] = zero;
+            dst_row[c / 8 + 1] = zero;
+        }
+        return;
+    }
+    const int32_t r = ranks[slot];
+    const int32_t nblk = (r > 0 && r <= bps * LORA_BLOCK_ROWS) ? (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS : 0;
+    bool ok = true;
+    for (int32_t jb = 0; jb < nblk; ++jb) {
+        const int32_t blk = table[static_cast<size_t>(slot) * bps + jb];
+        ok &= blk >= 0 && blk < num_blocks;
+    }
+    for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < R; ++jb) {
+        uint4 q0 = zero, q1 = zero;
+        if (ok && jb < nblk) {
+            const int32_t blk = table[static_cast<size_t>(slot) * bps + jb];
+            const uint4 *src = reinterpret_cast<const uint4 *>(b_arena + (static_cast<size_t>(blk) * N + n) * LORA_BLOCK_ROWS);
+            q0 = __ldg(src);
+            q1 = __ldg(src + 1);
+        }
+        const int32_t c = slot * R + jb * LORA_BLOCK_ROWS;
+        dst_row[c / 8] = q0;
+        dst_row[c / 8 + 1] = q1;
+    }
+}
+
+cudaError_t launch_ext_prepare(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
+    const int32_t n_tiles = (plan.M + 127) / 128;
+    const int64_t total = static_cast<int64_t>(v.N) * (v.max_slots + 1);
+    const int64_t threads = total > n_tiles ? total : n_tiles;
+    const int block = 256;
+    const int64_t grid = (threads + block - 1) / block;
+    ext_prepare_kernel<<<static_cast<unsigned>(grid), block, 0, stream>>>(
+        v.N, v.max_slots, v.max_rank, v.ext_cols, static_cast<const __nv_bfloat16 *>(v.b_arena), v.table,
+        v.ranks, v.bps, v.num_blocks, static_cast<__nv_bfloat16 *>(v.bm), v.tile_range, n_tiles);
+    return cudaGetLastError();
+}
+
+// grid (M, blocks per slot), 128 threads: the 16 ranks of block t of row m's
+// adapter, v[j] = A_i[16t + j, :] . x[m, :], written to Vm as the hi and lo
+// bf16 parts of s_i v[j]; the CTA of block 0 also zero-fills the rest of the
+// row of Vm and widens its token tile's slot range.  A corrupt block entry of
+// the slot drops the row's correction (reported), like a row without adapter.
+__global__ void __launch_bounds__(128)
+shrink_vm_kernel(const __nv_bfloat16 *__restrict__ x, int32_t ldx, int32_t K, const int32_t *__restrict__ row_slot,
+                 const __nv_bfloat16 *__restrict__ a_arena, const int32_t *__restrict__ table,
+                 const int32_t *__restrict__ ranks, const float *__restrict__ scales, int32_t max_slots, int32_t bps,
+                 int32_t num_blocks, int32_t R, int32_t ext_cols, __nv_bfloat16 *__restrict__ vm,
+                 int32_t *__restrict__ tile_range, unsigned long long *status, int32_t *__restrict__ counters,
+                 int32_t n_counters) {
+    const int32_t m = blockIdx.x;
+    const int32_t t = blockIdx.y;
+    // the GEMM that follows may launch now; it reads Vm and the tile ranges
+    // only after this grid has completed (griddepcontrol.wait)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (m == 0 && t == 0)
+        for (int32_t c = threadIdx.x; c < n_counters; c += blockDim.x) counters[c] = 0;
+    int32_t r;
+    float s;
+    int32_t i = resolve_slot(row_slot[m], m, ranks, scales, max_slots, bps, &r, &s, status,
+                             t == 0 && threadIdx.x == 0);
+    const int32_t nblk = i >= 0 ? (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS : 0;
+    if (i >= 0) {
+        bool ok = true;
+        for (int32_t jb = 0; jb < nblk; ++jb) {
+            const int32_t blk = table[static_cast<size_t>(i) * bps + jb];
+            ok &= blk >= 0 && blk < num_blocks;
+        }
+        if (!ok) {
+            if (t == 0 && threadIdx.x == 0) record_error(status, kDevBadBlock, static_cast<uint32_t>(i));
+            i = -1;
+        }
+    }
+    __nv_bfloat16 *row_hi = vm + static_cast<size_t>(m) * 2 * ext_cols;
+    __nv_bfloat16 *row_lo = row_hi + ext_cols;
+    if (t == 0) {
+        // zeros outside the slot's own blocks (everything for a row without adapter)
+        const int32_t own0 = i >= 0 ? i * R : 0, own1 = i >= 0 ? i * R + nblk * LORA_BLOCK_ROWS : 0;
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        for (int32_t c = threadIdx.x * 8; c < ext_cols; c += blockDim.x * 8) {
+            if (c >= own0 && c < own1) continue;
+            *reinterpret_cast<uint4 *>(row_hi + c) = zero;
+            *reinterpret_cast<uint4 *>(row_lo + c) = zero;
+        }
+        if (i >= 0 && threadIdx.x == 0) {
+            atomicMin(tile_range + 2 * (m / 128), i);
+            atomicMax(tile_range + 2 * (m / 128) + 1, i);
+        }
+    }
+    if (i < 0 || t >= nblk) return;
+    const int32_t b = table[static_cast<size_t>(i) * bps + t];
+    const __nv_bfloat16 *A = a_arena + static_cast<size_t>(b) * LORA_BLOCK_ROWS * K;
+    const __nv_bfloat16 *xr = x + static_cast<size_t>(m) * ldx;
+    float acc[LORA_BLOCK_ROWS];
+#pragma unroll
+    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = 0.0f;
+    for (int32_t k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+        float xv[8];
+        VecTraits<__nv_bfloat16>::load(xr + k, xv);
+#pragma unroll
+        for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
+            float av[8];
+            VecTraits<__nv_bfloat16>::load(A + static_cast<size_t>(j) * K + k, av);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j] = fmaf(av[e], xv[e], acc[j]);
+        }
+    }
+    __shared__ float red[4][LORA_BLOCK_ROWS];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
+        float v = acc[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[warp][j] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < LORA_BLOCK_ROWS) {
+        const float v = s * (red[0][threadIdx.x] + red[1][threadIdx.x] + red[2][threadIdx.x] + red[3][threadIdx.x]);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        const int32_t c = i * R + t * LORA_BLOCK_ROWS + threadIdx.x;
+        row_hi[c] = hi;
+        row_lo[c] = lo;
+    }
+}
+
+cudaError_t launch_shrink_vm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
+    dim3 grid(plan.M, v.bps);
+    shrink_vm_kernel<<<grid, 128, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(plan.x), plan.ldx, plan.K, plan.row_slot,
+        static_cast<const __nv_bfloat16 *>(v.a_arena), v.table, v.ranks, v.scales, v.max_slots, v.bps,
+        v.num_blocks, v.max_rank, v.ext_cols, static_cast<__nv_bfloat16 *>(v.vm), v.tile_range, plan.status,
+        plan.counters, plan.n_counters);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // SIMT GEMM with the expand fused into the epilogue:
 // out[m, n] = sum_k x[m,k] W[n,k] + s_i * sum_j B_i[n, j] V[m, j]
 // 64x64 tile, 256 threads, 4x4 outputs per thread (rows ty+16a, cols tx+16b)
@@ -438,6 +607,10 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
             e = launch_shrink_grouped(plan, v, gt, stream);
             if (e == cudaSuccess) e = launch_expand_grouped(plan, v, gt, stream);
             if (e != cudaSuccess) return e;
+        } else if (v.ext_cols > 0) {
+            e = launch_ext_prepare(plan, v, stream);
+            if (e == cudaSuccess) e = launch_shrink_vm(plan, v, stream);
+            if (e != cudaSuccess) return e;
         } else {
             dim3 sgrid(plan.M, v.bps);
             // few (row, block) pairs: the wide kernel that keeps a whole A
@@ -461,7 +634,7 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
         }
         e = launch_gemm_lora_tc(plan, v, stream);
         if (e != cudaSuccess) return e;
-        count_launches(swapped && !by_row ? 3 : 2);
+        count_launches((swapped && !by_row) || (!swapped && v.ext_cols > 0) ? 3 : 2);
         if (plan.stage_events) {
             e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[2 + 2 * p]), stream);
             if (e != cudaSuccess) return e;

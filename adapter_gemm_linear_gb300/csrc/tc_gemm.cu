@@ -79,6 +79,13 @@ struct TcParams {
     size_t v_part_stride;   // elements between the planes
     float *part;        // split-K partial tiles [splits][tiles][BN][128] fp32 (splits > 1)
     const float *ycorr; // swapped orientation: fp32 [M][N] LoRA correction from the expand kernel
+    // non-swapped orientation, LoRA term on the tensor cores: extra k-blocks
+    // over [Vm_hi | Vm_lo] (A side) and [Bm | Bm] (B side); Vm is [M][2 ext_cols],
+    // Bm [N][ext_cols], slot s owning columns [s*ext_rank, (s+1)*ext_rank)
+    int32_t ext;             // 0: the epilogue applies the expand instead
+    int32_t ext_cols;        // columns per half of Vm (a multiple of kBK)
+    int32_t ext_rank;        // columns per slot (the pool's max rank)
+    const int32_t *tile_range;  // [token tiles][2]: lowest and highest slot of the tile's rows
     int32_t *counters;  // per tile, zero on entry (splits > 1)
     unsigned long long *status;
 };
@@ -132,8 +139,29 @@ __device__ __forceinline__ void epi_sync() {
 
 // --------------------------------------------------------------- producer
 
+// Extension k-blocks of token tile ta: the columns of the slots its rows use,
+// [lo, hi), in k-blocks [kb0, kb0 + n); every k-block runs twice (Vm_hi, Vm_lo).
+__device__ __forceinline__ void ext_kblocks(const TcParams &p, int32_t ta, int32_t *kb0, int32_t *n) {
+    const int32_t smin = p.tile_range[2 * ta], smax = p.tile_range[2 * ta + 1];
+    if (smax < smin) {
+        *kb0 = 0;
+        *n = 0;
+        return;
+    }
+    const int32_t lo = smin * p.ext_rank, hi = (smax + 1) * p.ext_rank;
+    *kb0 = lo / kBK;
+    *n = (hi + kBK - 1) / kBK - *kb0;
+}
+
+// The kernel is launched as a programmatic dependent of the LoRA kernel before it:
+// wait until that grid has completed and its writes are visible.  Returns at
+// once when the launch had no programmatic dependency (or after the first
+// call).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <bool SWAP, int BN>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUtensorMap *tma_b,
+                                             const CUtensorMap *tma_va, const CUtensorMap *tma_vb,
                                              const TcParams &p, uint8_t *sA, uint8_t *sB,
                                              uint64_t *full, uint64_t *empty,
                                              volatile uint32_t *abort_flag) {
@@ -144,7 +172,16 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
         const Unit w = decode_unit<SWAP>(u, p);
         const int32_t kb0 = w.ks * p.kb_per_split;
         const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
-        for (int32_t kb = kb0; kb < kb1; ++kb, ++it) {
+        const int32_t nmain = kb1 - kb0;
+        int32_t ekb0 = 0, ekn = 0, total = nmain;
+        for (int32_t i = 0; i < total; ++i, ++it) {
+            if (!SWAP && p.ext && i == nmain - 1) {
+                // with the unit's last main k-block next: Vm and the tile
+                // ranges come from the shrink kernel
+                grid_dependency_wait();
+                ext_kblocks(p, w.ta, &ekb0, &ekn);
+                total = nmain + 2 * ekn;
+            }
             const int s = it % C::kStages;
             const uint32_t ph = (it / C::kStages) & 1;
             if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimitNs)) {
@@ -153,8 +190,17 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
             }
             if (*abort_flag) return;
             mbar_arrive_expect_tx(&full[s], C::kABytes + C::kBBytes);
-            tma_load_2d(sA + s * C::kABytes, tma_a, kb * kBK, w.ta * kBM, &full[s]);
-            tma_load_2d(sB + s * C::kBBytes, tma_b, kb * kBK, w.tb * BN, &full[s]);
+            if (i < nmain) {
+                const int32_t kb = kb0 + i;
+                tma_load_2d(sA + s * C::kABytes, tma_a, kb * kBK, w.ta * kBM, &full[s]);
+                tma_load_2d(sB + s * C::kBBytes, tma_b, kb * kBK, w.tb * BN, &full[s]);
+            } else {
+                // LoRA extension: k-block e of the slot columns, hi half then lo half of Vm
+                const int32_t e = i - nmain;
+                const int32_t half = e / ekn, kb = ekb0 + e % ekn;
+                tma_load_2d(sA + s * C::kABytes, tma_va, half * p.ext_cols + kb * kBK, w.ta * kBM, &full[s]);
+                tma_load_2d(sB + s * C::kBBytes, tma_vb, kb * kBK, w.tb * BN, &full[s]);
+            }
         }
     }
 }
@@ -172,13 +218,22 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
     for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
         const Unit w = decode_unit<SWAP>(u, p);
         const int32_t kb0 = w.ks * p.kb_per_split;
-        const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+        const int32_t kb_main = min(kb0 + p.kb_per_split, p.num_kb);
+        int32_t kb1 = kb_main;
         const int b = t & 1;
         bool ok = mbar_wait_bounded(&tmem_empty[b], ((t >> 1) & 1) ^ 1, kWaitLimitNs);
         if (!ok) record_error(p.status, kDevTimeout, 2);
         tc_fence_after_sync();
         const uint32_t d = tmem_base + b * BN;
         for (int32_t kb = kb0; kb < kb1 && ok; ++kb, ++it) {
+            if (!SWAP && p.ext && kb == kb_main - 1) {
+                // the LoRA extension k-blocks follow the main ones in the ring
+                // (the tile ranges come from the shrink kernel)
+                grid_dependency_wait();
+                int32_t ekb0, ekn;
+                ext_kblocks(p, w.ta, &ekb0, &ekn);
+                kb1 = kb_main + 2 * ekn;
+            }
             const int s = it % C::kStages;
             const uint32_t ph = (it / C::kStages) & 1;
             if (!mbar_wait_bounded(&full[s], ph, kWaitLimitNs)) {
@@ -206,12 +261,6 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
 }
 
 // --------------------------------------------------------------- epilogue
-
-// The kernel is launched as a programmatic dependent of the shrink kernel:
-// wait until that grid has completed and its writes are visible.  Returns at
-// once when the launch had no programmatic dependency (or after the first
-// call).
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // AND of `v` over the epilogue threads, also a barrier among them.
 __device__ __forceinline__ bool epi_all(bool v) {
@@ -453,7 +502,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                 float acc[32];
                 load_tmem_chunk(col0 + c * 32, acc);
                 const int32_t n0 = w.tb * BN + c * 32;
-                rows_finish_chunk(p, slot, r, s, m, n0, acc);
+                if (!p.ext) rows_finish_chunk(p, slot, r, s, m, n0, acc);
                 if (m < p.M) {
                     __nv_bfloat16 *dst = p.out + static_cast<size_t>(m) * p.ldo + n0;
 #pragma unroll
@@ -483,6 +532,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
 template <bool SWAP, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                    const __grid_constant__ CUtensorMap tma_va, const __grid_constant__ CUtensorMap tma_vb,
                     const TcParams p) {
     using namespace sm100;
     using C = Cfg<SWAP, BN>;
@@ -517,6 +567,10 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tma_a);
         prefetch_tensormap(&tma_b);
+        if (!SWAP && p.ext) {
+            prefetch_tensormap(&tma_va);
+            prefetch_tensormap(&tma_vb);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::kTmemCols);
@@ -528,7 +582,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) run_producer<SWAP, BN>(&tma_a, &tma_b, p, sA, sB, full, empty, abort_flag);
+        if (lane == 0) run_producer<SWAP, BN>(&tma_a, &tma_b, &tma_va, &tma_vb, p, sA, sB, full, empty, abort_flag);
     } else if (warp == 1) {
         if (lane == 0)
             run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
@@ -599,6 +653,15 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     CUtensorMap tx, tw;
     if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, SWAP ? BN : kBM)) return cudaErrorInvalidValue;
     if (!make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, SWAP ? kBM : BN)) return cudaErrorInvalidValue;
+    // LoRA extension operands (non-swapped orientation): [Vm_hi | Vm_lo] beside
+    // x, Bm beside W; unused maps are copies of the main ones
+    CUtensorMap tva = tx, tvb = tw;
+    const bool ext = !SWAP && v.ext_cols > 0;
+    if (ext) {
+        if (!make_tmap_bf16(&tva, v.vm, plan.M, 2 * static_cast<uint64_t>(v.ext_cols), 2 * static_cast<uint64_t>(v.ext_cols), kBM) ||
+            !make_tmap_bf16(&tvb, v.bm, v.N, v.ext_cols, v.ext_cols, BN))
+            return cudaErrorInvalidValue;
+    }
     TcParams p;
     p.M = plan.M;
     p.N = v.N;
@@ -625,6 +688,10 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.v_part_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.part = plan.part;
     p.ycorr = plan.ycorr;
+    p.ext = ext ? 1 : 0;
+    p.ext_cols = v.ext_cols;
+    p.ext_rank = v.max_rank;
+    p.tile_range = v.tile_range;
     p.counters = plan.counters;
     p.status = plan.status;
     // the splits of a tile wait for one another, so they must all be resident:
@@ -645,8 +712,8 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (SWAP) return cudaLaunchKernelEx(&cfg, kernel, tw, tx, p);
-    return cudaLaunchKernelEx(&cfg, kernel, tx, tw, p);
+    if (SWAP) return cudaLaunchKernelEx(&cfg, kernel, tw, tx, tva, tvb, p);
+    return cudaLaunchKernelEx(&cfg, kernel, tx, tw, tva, tvb, p);
 }
 
 }  // namespace
