@@ -367,7 +367,7 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
                       cols <= lora::kExtMaxCols)
                          ? static_cast<int32_t>(cols)
                          : 0;
-        v.vm = v.bm = nullptr;
+        v.vm = v.bm = v.adense = nullptr;
         v.tile_range = nullptr;
         ws->v_off[i] = off;
         if (v.ext_cols == 0)
@@ -396,17 +396,20 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     if (ycorr) off += align_up(sizeof(int32_t) * lora::group_table_ints(a->M), 256);
     // the tensor-core LoRA term of large M: Vm, Bm and the token tiles' slot
     // ranges, shared by the projections
-    size_t vm = 0, bm = 0;
+    size_t vm = 0, bm = 0, ad = 0;
     for (int i = 0; i < a->n_proj; ++i) {
         const lora::ProjView &v = plan->proj[i];
         if (v.ext_cols == 0) continue;
         vm = std::max(vm, sizeof(uint16_t) * static_cast<size_t>(a->M) * 2 * v.ext_cols);
         bm = std::max(bm, sizeof(uint16_t) * static_cast<size_t>(v.N) * v.ext_cols);
+        ad = std::max(ad, sizeof(uint16_t) * static_cast<size_t>(v.ext_cols) * a->K);
     }
     ws->vm_off = off;
     off += align_up(vm, 256);
     ws->bm_off = off;
     off += align_up(bm, 256);
+    ws->adense_off = off;
+    off += align_up(ad, 256);
     ws->range_off = off;
     if (vm) off += align_up(sizeof(int32_t) * 2 * static_cast<size_t>((a->M + 127) / 128), 256);
     ws->counter_off = off;  // last: the counters run to the end of the workspace
@@ -440,6 +443,7 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
         if (plan.proj[i].ext_cols == 0) continue;
         plan.proj[i].vm = base + ws.vm_off;
         plan.proj[i].bm = base + ws.bm_off;
+        plan.proj[i].adense = base + ws.adense_off;
         plan.proj[i].tile_range = reinterpret_cast<int32_t *>(base + ws.range_off);
     }
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);

@@ -61,6 +61,7 @@ struct ProjView {
     int32_t ext_cols;      // columns of Bm = of each half of Vm (a multiple of 64), 0: not used
     void *vm;              // workspace: bf16 [M][2 ext_cols]: s_i V of the row's slot, hi and lo parts
     void *bm;              // workspace: bf16 [N][ext_cols]: every slot's B, zero past its rank
+    void *adense;          // workspace: bf16 [ext_cols][K]: every slot's A rows, zero past its rank
     int32_t *tile_range;   // workspace: [ceil(M/128)][2] lowest and highest slot of each token tile
 };
 constexpr int kExtMaxCols = 2048;  // largest max_slots * max_rank (rounded to 64) for the extension
@@ -117,7 +118,7 @@ struct WorkspaceLayout {
     size_t part_off;              // fp32 split-K partial tiles (largest projection)
     size_t ycorr_off;             // fp32 [M][N] correction of the small-M orientation (largest projection)
     size_t group_off;             // int32 group table (small-M orientation)
-    size_t vm_off, bm_off, range_off;  // large-M tensor-core LoRA term: Vm, Bm, tile slot ranges
+    size_t vm_off, bm_off, adense_off, range_off;  // large-M tensor-core LoRA term: Vm, Bm, A_dense, tile slot ranges
     size_t counter_off;           // int32 per output tile (split-K)
     size_t total;
 };
@@ -146,11 +147,13 @@ cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream);
 // Multiprocessors of the current device (cached per device; 148 if unknown).
 int device_sm_count();
 
-// Large M with the LoRA term on the tensor cores (lora_kernels.cu): Bm from
-// the pool's B blocks and the tile ranges reset (ext_prepare), then the hi
-// and lo bf16 parts of s_i V in Vm (shrink_vm); the GEMM adds [Vm] x [Bm]^T.
+// Large M with the LoRA term on the tensor cores (lora_kernels.cu): Bm and
+// A_dense from the pool's blocks and the token tiles' slot ranges
+// (ext_prepare), then Vm by a GEMM x A_dense^T (launch_gemm_vm); the main
+// GEMM adds [Vm] x [Bm]^T.
 cudaError_t launch_ext_prepare(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
-cudaError_t launch_shrink_vm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+// V of the large-M tensor-core path as a GEMM x A_dense^T into Vm (tc_gemm.cu).
+cudaError_t launch_gemm_vm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
 
 // The small-M LoRA path by adapter group (lora_grouped.cu): the rows' group
 // table (rows sorted by slot), then per projection the grouped shrink into

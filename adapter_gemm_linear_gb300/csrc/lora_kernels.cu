@@ -293,165 +293,137 @@ shrink_rows_bf16_kernel(const __nv_bfloat16 *__restrict__ x, int32_t ldx, int32_
 // corrupt block entries), Vm[m][s*R + j] = hi / lo bf16 parts of s_i V[m][j]
 // for the row's own slot s (zero elsewhere), R = the pool's max rank.  The
 // two bf16 parts carry about 16 significant bits of s_i V, so Vm Bm^T adds the
-// correction to the fp32 accumulator with the precision of an fp32 V.
+// correction to the fp32 accumulator with the precision of an fp32 V.  V itself
+// is a GEMM x A_dense^T (tc_gemm.cu, vm mode) with A_dense[s*R + j] = A_s[j].
 // ---------------------------------------------------------------------------
 
-// One thread per (output row n, slot): the slot's R columns of Bm row n, 32
-// bytes (16 ranks of one pool block) at a time; the last "slot" index writes
-// the zero padding past max_slots * R.  The first threads also reset the
-// token tiles' slot ranges for the shrink that follows.
-__global__ void ext_prepare_kernel(int32_t N, int32_t max_slots, int32_t R, int32_t ext_cols,
-                                   const __nv_bfloat16 *__restrict__ b_arena,
-                                   const int32_t *__restrict__ table, const int32_t *__restrict__ ranks,
-                                   int32_t bps, int32_t num_blocks, __nv_bfloat16 *__restrict__ bm,
-                                   int32_t *__restrict__ tile_range, int32_t n_tiles) {
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (gid < n_tiles) {
-        tile_range[2 * gid] = 0x7fffffff;
-        tile_range[2 * gid + 1] = -1;
-    }
-    const int64_t total = static_cast<int64_t>(N) * (max_slots + 1);
-    if (gid >= total) return;
-    const int32_t slot = static_cast<int32_t>(gid % (max_slots + 1));
-    const int32_t n = static_cast<int32_t>(gid / (max_slots + 1));
-    uint4 *dst_row = reinterpret_cast<uint4 *>(bm + static_cast<size_t>(n) * ext_cols);
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    if (slot == max_slots) {  // padding columns
-        for (int32_t c = max_slots * R; c < ext_cols; c += LORA_BLOCK_ROWS) {
-            dst_row[c / 8] = zero;
-            dst_row[c / 8 + 1] = zero;
-        }
-        return;
-    }
+// Per-slot validity of the dense copies: the slot's rank blocks, or 0 when
+// the slot is empty or one of its block entries is corrupt (its rows then get
+// no correction, as on every other path).
+__device__ __forceinline__ int32_t dense_blocks(int32_t slot, const int32_t *table, const int32_t *ranks,
+                                                int32_t bps, int32_t num_blocks) {
     const int32_t r = ranks[slot];
-    const int32_t nblk = (r > 0 && r <= bps * LORA_BLOCK_ROWS) ? (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS : 0;
-    bool ok = true;
+    if (r <= 0 || r > bps * LORA_BLOCK_ROWS) return 0;
+    const int32_t nblk = (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
     for (int32_t jb = 0; jb < nblk; ++jb) {
         const int32_t blk = table[static_cast<size_t>(slot) * bps + jb];
-        ok &= blk >= 0 && blk < num_blocks;
+        if (blk < 0 || blk >= num_blocks) return 0;
     }
-    for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < R; ++jb) {
-        uint4 q0 = zero, q1 = zero;
-        if (ok && jb < nblk) {
-            const int32_t blk = table[static_cast<size_t>(slot) * bps + jb];
-            const uint4 *src = reinterpret_cast<const uint4 *>(b_arena + (static_cast<size_t>(blk) * N + n) * LORA_BLOCK_ROWS);
-            q0 = __ldg(src);
-            q1 = __ldg(src + 1);
+    return nblk;
+}
+
+struct ExtPrepareParams {
+    int32_t M, N, K, max_slots, R, ext_cols, bps, num_blocks;
+    const __nv_bfloat16 *a_arena, *b_arena;
+    const int32_t *table, *ranks, *row_slot;
+    __nv_bfloat16 *bm, *adense;
+    int32_t *tile_range;
+};
+
+// blockIdx.y selects the job, blockIdx.x walks it:
+//   0: Bm row n, slot s: the slot's R columns, 32 bytes (16 ranks of one pool
+//      block) at a time; slot index max_slots writes the zero padding;
+//   1: A_dense row c (slot c / R, rank c % R), 8 columns per thread;
+//   2: one warp per token tile: the lowest and highest slot its rows name.
+__global__ void __launch_bounds__(256) ext_prepare_kernel(const ExtPrepareParams p) {
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    if (blockIdx.y == 0) {
+        if (gid >= static_cast<int64_t>(p.N) * (p.max_slots + 1)) return;
+        const int32_t slot = static_cast<int32_t>(gid % (p.max_slots + 1));
+        const int32_t n = static_cast<int32_t>(gid / (p.max_slots + 1));
+        uint4 *dst_row = reinterpret_cast<uint4 *>(p.bm + static_cast<size_t>(n) * p.ext_cols);
+        if (slot == p.max_slots) {  // padding columns
+            for (int32_t c = p.max_slots * p.R; c < p.ext_cols; c += LORA_BLOCK_ROWS) {
+                dst_row[c / 8] = zero;
+                dst_row[c / 8 + 1] = zero;
+            }
+            return;
         }
-        const int32_t c = slot * R + jb * LORA_BLOCK_ROWS;
-        dst_row[c / 8] = q0;
-        dst_row[c / 8 + 1] = q1;
+        const int32_t nblk = dense_blocks(slot, p.table, p.ranks, p.bps, p.num_blocks);
+        for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < p.R; ++jb) {
+            uint4 q0 = zero, q1 = zero;
+            if (jb < nblk) {
+                const int32_t blk = p.table[static_cast<size_t>(slot) * p.bps + jb];
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(p.b_arena + (static_cast<size_t>(blk) * p.N + n) * LORA_BLOCK_ROWS);
+                q0 = __ldg(src);
+                q1 = __ldg(src + 1);
+            }
+            const int32_t c = slot * p.R + jb * LORA_BLOCK_ROWS;
+            dst_row[c / 8] = q0;
+            dst_row[c / 8 + 1] = q1;
+        }
+    } else if (blockIdx.y == 1) {
+        const int32_t K8 = p.K / 8;
+        if (gid >= static_cast<int64_t>(p.ext_cols) * K8) return;
+        const int32_t c = static_cast<int32_t>(gid / K8);
+        const int32_t k8 = static_cast<int32_t>(gid % K8);
+        uint4 q = zero;
+        const int32_t slot = c / p.R, j = c % p.R;
+        if (slot < p.max_slots) {
+            const int32_t nblk = dense_blocks(slot, p.table, p.ranks, p.bps, p.num_blocks);
+            const int32_t jb = j / LORA_BLOCK_ROWS;
+            if (jb < nblk) {
+                const int32_t blk = p.table[static_cast<size_t>(slot) * p.bps + jb];
+                q = __ldg(reinterpret_cast<const uint4 *>(
+                          p.a_arena + (static_cast<size_t>(blk) * LORA_BLOCK_ROWS + j % LORA_BLOCK_ROWS) * p.K) +
+                      k8);
+            }
+        }
+        reinterpret_cast<uint4 *>(p.adense + static_cast<size_t>(c) * p.K)[k8] = q;
+    } else {
+        const int64_t tile = gid / 32;
+        const int lane = threadIdx.x & 31;
+        if (tile >= (p.M + 127) / 128) return;  // whole warps: 128 rows per tile
+        int32_t lo = 0x7fffffff, hi = -1;
+        for (int32_t i = lane; i < 128; i += 32) {
+            const int32_t m = static_cast<int32_t>(tile) * 128 + i;
+            if (m >= p.M) break;
+            const int32_t id = p.row_slot[m];
+            if (id >= 0 && id < p.max_slots) {
+                lo = min(lo, id);
+                hi = max(hi, id);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        if (lane == 0) {
+            p.tile_range[2 * tile] = lo;
+            p.tile_range[2 * tile + 1] = hi;
+        }
     }
 }
 
 cudaError_t launch_ext_prepare(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
-    const int32_t n_tiles = (plan.M + 127) / 128;
-    const int64_t total = static_cast<int64_t>(v.N) * (v.max_slots + 1);
-    const int64_t threads = total > n_tiles ? total : n_tiles;
+    ExtPrepareParams p;
+    p.M = plan.M;
+    p.N = v.N;
+    p.K = plan.K;
+    p.max_slots = v.max_slots;
+    p.R = v.max_rank;
+    p.ext_cols = v.ext_cols;
+    p.bps = v.bps;
+    p.num_blocks = v.num_blocks;
+    p.a_arena = static_cast<const __nv_bfloat16 *>(v.a_arena);
+    p.b_arena = static_cast<const __nv_bfloat16 *>(v.b_arena);
+    p.table = v.table;
+    p.ranks = v.ranks;
+    p.row_slot = plan.row_slot;
+    p.bm = static_cast<__nv_bfloat16 *>(v.bm);
+    p.adense = static_cast<__nv_bfloat16 *>(v.adense);
+    p.tile_range = v.tile_range;
     const int block = 256;
-    const int64_t grid = (threads + block - 1) / block;
-    ext_prepare_kernel<<<static_cast<unsigned>(grid), block, 0, stream>>>(
-        v.N, v.max_slots, v.max_rank, v.ext_cols, static_cast<const __nv_bfloat16 *>(v.b_arena), v.table,
-        v.ranks, v.bps, v.num_blocks, static_cast<__nv_bfloat16 *>(v.bm), v.tile_range, n_tiles);
-    return cudaGetLastError();
-}
-
-// grid (M, blocks per slot), 128 threads: the 16 ranks of block t of row m's
-// adapter, v[j] = A_i[16t + j, :] . x[m, :], written to Vm as the hi and lo
-// bf16 parts of s_i v[j]; the CTA of block 0 also zero-fills the rest of the
-// row of Vm and widens its token tile's slot range.  A corrupt block entry of
-// the slot drops the row's correction (reported), like a row without adapter.
-__global__ void __launch_bounds__(128)
-shrink_vm_kernel(const __nv_bfloat16 *__restrict__ x, int32_t ldx, int32_t K, const int32_t *__restrict__ row_slot,
-                 const __nv_bfloat16 *__restrict__ a_arena, const int32_t *__restrict__ table,
-                 const int32_t *__restrict__ ranks, const float *__restrict__ scales, int32_t max_slots, int32_t bps,
-                 int32_t num_blocks, int32_t R, int32_t ext_cols, __nv_bfloat16 *__restrict__ vm,
-                 int32_t *__restrict__ tile_range, unsigned long long *status, int32_t *__restrict__ counters,
-                 int32_t n_counters) {
-    const int32_t m = blockIdx.x;
-    const int32_t t = blockIdx.y;
-    // the GEMM that follows may launch now; it reads Vm and the tile ranges
-    // only after this grid has completed (griddepcontrol.wait)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (m == 0 && t == 0)
-        for (int32_t c = threadIdx.x; c < n_counters; c += blockDim.x) counters[c] = 0;
-    int32_t r;
-    float s;
-    int32_t i = resolve_slot(row_slot[m], m, ranks, scales, max_slots, bps, &r, &s, status,
-                             t == 0 && threadIdx.x == 0);
-    const int32_t nblk = i >= 0 ? (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS : 0;
-    if (i >= 0) {
-        bool ok = true;
-        for (int32_t jb = 0; jb < nblk; ++jb) {
-            const int32_t blk = table[static_cast<size_t>(i) * bps + jb];
-            ok &= blk >= 0 && blk < num_blocks;
-        }
-        if (!ok) {
-            if (t == 0 && threadIdx.x == 0) record_error(status, kDevBadBlock, static_cast<uint32_t>(i));
-            i = -1;
-        }
-    }
-    __nv_bfloat16 *row_hi = vm + static_cast<size_t>(m) * 2 * ext_cols;
-    __nv_bfloat16 *row_lo = row_hi + ext_cols;
-    if (t == 0) {
-        // zeros outside the slot's own blocks (everything for a row without adapter)
-        const int32_t own0 = i >= 0 ? i * R : 0, own1 = i >= 0 ? i * R + nblk * LORA_BLOCK_ROWS : 0;
-        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-        for (int32_t c = threadIdx.x * 8; c < ext_cols; c += blockDim.x * 8) {
-            if (c >= own0 && c < own1) continue;
-            *reinterpret_cast<uint4 *>(row_hi + c) = zero;
-            *reinterpret_cast<uint4 *>(row_lo + c) = zero;
-        }
-        if (i >= 0 && threadIdx.x == 0) {
-            atomicMin(tile_range + 2 * (m / 128), i);
-            atomicMax(tile_range + 2 * (m / 128) + 1, i);
-        }
-    }
-    if (i < 0 || t >= nblk) return;
-    const int32_t b = table[static_cast<size_t>(i) * bps + t];
-    const __nv_bfloat16 *A = a_arena + static_cast<size_t>(b) * LORA_BLOCK_ROWS * K;
-    const __nv_bfloat16 *xr = x + static_cast<size_t>(m) * ldx;
-    float acc[LORA_BLOCK_ROWS];
-#pragma unroll
-    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = 0.0f;
-    for (int32_t k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
-        float xv[8];
-        VecTraits<__nv_bfloat16>::load(xr + k, xv);
-#pragma unroll
-        for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
-            float av[8];
-            VecTraits<__nv_bfloat16>::load(A + static_cast<size_t>(j) * K + k, av);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[j] = fmaf(av[e], xv[e], acc[j]);
-        }
-    }
-    __shared__ float red[4][LORA_BLOCK_ROWS];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
-        float v = acc[j];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[warp][j] = v;
-    }
-    __syncthreads();
-    if (threadIdx.x < LORA_BLOCK_ROWS) {
-        const float v = s * (red[0][threadIdx.x] + red[1][threadIdx.x] + red[2][threadIdx.x] + red[3][threadIdx.x]);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-        const int32_t c = i * R + t * LORA_BLOCK_ROWS + threadIdx.x;
-        row_hi[c] = hi;
-        row_lo[c] = lo;
-    }
-}
-
-cudaError_t launch_shrink_vm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
-    dim3 grid(plan.M, v.bps);
-    shrink_vm_kernel<<<grid, 128, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(plan.x), plan.ldx, plan.K, plan.row_slot,
-        static_cast<const __nv_bfloat16 *>(v.a_arena), v.table, v.ranks, v.scales, v.max_slots, v.bps,
-        v.num_blocks, v.max_rank, v.ext_cols, static_cast<__nv_bfloat16 *>(v.vm), v.tile_range, plan.status,
-        plan.counters, plan.n_counters);
+    const int64_t jobs[3] = {static_cast<int64_t>(v.N) * (v.max_slots + 1),
+                             static_cast<int64_t>(v.ext_cols) * (plan.K / 8),
+                             32 * static_cast<int64_t>((plan.M + 127) / 128)};
+    int64_t most = 0;
+    for (int64_t j : jobs) most = j > most ? j : most;
+    const int64_t gx = (most + block - 1) / block;
+    ext_prepare_kernel<<<dim3(static_cast<unsigned>(gx), 3), block, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -609,7 +581,7 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
             if (e != cudaSuccess) return e;
         } else if (v.ext_cols > 0) {
             e = launch_ext_prepare(plan, v, stream);
-            if (e == cudaSuccess) e = launch_shrink_vm(plan, v, stream);
+            if (e == cudaSuccess) e = launch_gemm_vm(plan, v, stream);
             if (e != cudaSuccess) return e;
         } else {
             dim3 sgrid(plan.M, v.bps);

@@ -86,6 +86,12 @@ struct TcParams {
     int32_t ext_cols;        // columns per half of Vm (a multiple of kBK)
     int32_t ext_rank;        // columns per slot (the pool's max rank)
     const int32_t *tile_range;  // [token tiles][2]: lowest and highest slot of the tile's rows
+    // shrink mode (non-swapped, W = A_dense [ext_cols][K]): the tile's fp32
+    // result x A_dense^T becomes the hi and lo bf16 parts of s_i V in vm_out
+    // ([M][2 ext_cols]), masked to the row's own slot columns; units whose
+    // columns lie outside their token tile's slot range are skipped
+    int32_t vm_mode;
+    __nv_bfloat16 *vm_out;
     int32_t *counters;  // per tile, zero on entry (splits > 1)
     unsigned long long *status;
 };
@@ -153,6 +159,16 @@ __device__ __forceinline__ void ext_kblocks(const TcParams &p, int32_t ta, int32
     *n = (hi + kBK - 1) / kBK - *kb0;
 }
 
+// Shrink mode: does unit w's column tile meet its token tile's slot columns?
+template <int BN>
+__device__ __forceinline__ bool unit_active(const TcParams &p, const Unit &w) {
+    if (!p.vm_mode) return true;
+    const int32_t smin = p.tile_range[2 * w.ta], smax = p.tile_range[2 * w.ta + 1];
+    if (smax < smin) return false;
+    const int32_t lo = smin * p.ext_rank, hi = (smax + 1) * p.ext_rank;
+    return w.tb * BN < hi && (w.tb + 1) * BN > lo;
+}
+
 // The kernel is launched as a programmatic dependent of the LoRA kernel before it:
 // wait until that grid has completed and its writes are visible.  Returns at
 // once when the launch had no programmatic dependency (or after the first
@@ -168,8 +184,10 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
     using namespace sm100;
     using C = Cfg<SWAP, BN>;
     int32_t it = 0;
+    if (p.vm_mode) grid_dependency_wait();  // the tile ranges come from the kernel before
     for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         const Unit w = decode_unit<SWAP>(u, p);
+        if (!unit_active<BN>(p, w)) continue;
         const int32_t kb0 = w.ks * p.kb_per_split;
         const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
         const int32_t nmain = kb1 - kb0;
@@ -215,8 +233,10 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
     using C = Cfg<SWAP, BN>;
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
     int32_t it = 0, t = 0;
-    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
+    if (p.vm_mode) grid_dependency_wait();
+    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         const Unit w = decode_unit<SWAP>(u, p);
+        if (!unit_active<BN>(p, w)) continue;
         const int32_t kb0 = w.ks * p.kb_per_split;
         const int32_t kb_main = min(kb0 + p.kb_per_split, p.num_kb);
         int32_t kb1 = kb_main;
@@ -257,6 +277,7 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
             return;
         }
         mma_commit(&tmem_full[b]);
+        ++t;
     }
 }
 
@@ -365,8 +386,10 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
     const int lane = threadIdx.x & 31;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int32_t t = 0;
-    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
+    if (p.vm_mode) grid_dependency_wait();
+    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         const Unit w = decode_unit<SWAP>(u, p);
+        if (!unit_active<BN>(p, w)) continue;
         const int b = t & 1;
         // swapped, one split: this thread's correction values (rows of its
         // 32-token chunks, its column) are fetched while the MMAs finish
@@ -497,11 +520,52 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
             if (m < p.M)
                 slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s, p.status,
                                     false);
+            if (p.vm_mode && slot >= 0) {
+                // a corrupt block entry drops the row's correction
+                bool okb = true;
+                for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
+                    const int32_t blk = p.table[static_cast<size_t>(slot) * p.bps + jb];
+                    okb &= blk >= 0 && blk < p.num_blocks;
+                }
+                if (!okb) slot = -1;
+            }
 #pragma unroll 1
             for (int c = grp; c < kChunks; c += kGroups) {
                 float acc[32];
                 load_tmem_chunk(col0 + c * 32, acc);
                 const int32_t n0 = w.tb * BN + c * 32;
+                if (p.vm_mode) {
+                    // columns n0 .. n0+31 of Vm: s_i V for the row's own slot, else 0
+                    if (m < p.M && n0 < p.N) {
+                        __nv_bfloat16 *hi_dst = p.vm_out + static_cast<size_t>(m) * 2 * p.ext_cols + n0;
+                        __nv_bfloat16 *lo_dst = hi_dst + p.ext_cols;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            float hv[8], lv[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int32_t col = n0 + g * 8 + e;
+                                const float val = (slot >= 0 && col / p.ext_rank == slot) ? s * acc[g * 8 + e] : 0.0f;
+                                const __nv_bfloat16 h = __float2bfloat16_rn(val);
+                                hv[e] = __bfloat162float(h);
+                                lv[e] = val - hv[e];
+                            }
+                            uint4 qh, ql;
+                            qh.x = pack_bf16x2(hv[0], hv[1]);
+                            qh.y = pack_bf16x2(hv[2], hv[3]);
+                            qh.z = pack_bf16x2(hv[4], hv[5]);
+                            qh.w = pack_bf16x2(hv[6], hv[7]);
+                            ql.x = pack_bf16x2(lv[0], lv[1]);
+                            ql.y = pack_bf16x2(lv[2], lv[3]);
+                            ql.z = pack_bf16x2(lv[4], lv[5]);
+                            ql.w = pack_bf16x2(lv[6], lv[7]);
+                            *reinterpret_cast<uint4 *>(hi_dst + g * 8) = qh;
+                            *reinterpret_cast<uint4 *>(lo_dst + g * 8) = ql;
+                        }
+                    }
+                    __syncwarp();
+                    continue;
+                }
                 if (!p.ext) rows_finish_chunk(p, slot, r, s, m, n0, acc);
                 if (m < p.M) {
                     __nv_bfloat16 *dst = p.out + static_cast<size_t>(m) * p.ldo + n0;
@@ -523,7 +587,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
             __syncwarp();
             if (lane == 0) mbar_arrive(&tmem_empty[b]);
         }
-        epi_sync();  // metadata and last_flag are rewritten by the next unit
+        epi_sync();  // last_flag is rewritten by the next unit
+        ++t;
     }
 }
 
@@ -632,7 +697,8 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
 
 
 template <bool SWAP, int BN>
-cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, cudaStream_t stream) {
+cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, cudaStream_t stream,
+                           bool vm_mode = false) {
     using C = Cfg<SWAP, BN>;
     auto kernel = tc_gemm_lora_kernel<SWAP, BN>;
     static std::mutex mu;
@@ -656,7 +722,7 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     // LoRA extension operands (non-swapped orientation): [Vm_hi | Vm_lo] beside
     // x, Bm beside W; unused maps are copies of the main ones
     CUtensorMap tva = tx, tvb = tw;
-    const bool ext = !SWAP && v.ext_cols > 0;
+    const bool ext = !SWAP && !vm_mode && v.ext_cols > 0;
     if (ext) {
         if (!make_tmap_bf16(&tva, v.vm, plan.M, 2 * static_cast<uint64_t>(v.ext_cols), 2 * static_cast<uint64_t>(v.ext_cols), kBM) ||
             !make_tmap_bf16(&tvb, v.bm, v.N, v.ext_cols, v.ext_cols, BN))
@@ -692,6 +758,8 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.ext_cols = v.ext_cols;
     p.ext_rank = v.max_rank;
     p.tile_range = v.tile_range;
+    p.vm_mode = vm_mode ? 1 : 0;
+    p.vm_out = vm_mode ? static_cast<__nv_bfloat16 *>(v.vm) : nullptr;
     p.counters = plan.counters;
     p.status = plan.status;
     // the splits of a tile wait for one another, so they must all be resident:
@@ -765,6 +833,28 @@ TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
     t.part_bytes = t.splits > 1 ? sizeof(float) * static_cast<size_t>(t.splits) * t.tiles_a * t.tiles_b * t.bn * kBM : 0;
     t.counter_bytes = t.splits > 1 ? sizeof(int32_t) * static_cast<size_t>(t.tiles_a) * t.tiles_b : 0;
     return t;
+}
+
+// The shrink of the large-M tensor-core path as a GEMM: x A_dense^T over the
+// slot columns of each token tile (other column tiles are skipped), written
+// to Vm as the hi and lo bf16 parts of s_i V (see TcParams::vm_mode).
+cudaError_t launch_gemm_vm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
+    if (v.ext_cols <= 0 || !v.adense || !v.vm || !v.tile_range) return cudaErrorInvalidValue;
+    TcPlan tp = plan_tc(plan.M, v.ext_cols, plan.K);
+    if (tp.swap) return cudaErrorInvalidValue;
+    tp.bn = 128;
+    tp.tiles_b = (v.ext_cols + 127) / 128;
+    tp.splits = 1;
+    tp.kb_per_split = tp.num_kb;
+    tp.units = tp.tiles_a * tp.tiles_b;
+    const int sms = device_sm_count();
+    tp.grid = tp.units < sms ? tp.units : sms;
+    ProjView vv = v;
+    vv.W = v.adense;
+    vv.N = v.ext_cols;
+    vv.out = nullptr;
+    vv.ldo = v.ext_cols;
+    return launch_variant<false, 128>(plan, vv, tp, stream, true);
 }
 
 cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
