@@ -60,6 +60,7 @@ constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kSmemLimit = 226 * 1024;   // dynamic shared memory per CTA (227 KiB opt-in maximum)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kEpiBarrier = 1;         // named barrier of the epilogue warps
+constexpr int kMaxUnitList = 256;      // shrink mode: active units one CTA can take
 
 struct TcParams {
     int32_t M, N, K;
@@ -100,14 +101,14 @@ template <bool SWAP, int BN>
 struct Cfg {
     static constexpr uint32_t kABytes = kBM * kBK * 2;
     static constexpr uint32_t kBBytes = BN * kBK * 2;
-    // ring + barriers + TMEM address + flags + alignment slack
-    static constexpr int kFixed = 1024 + (2 * 12 + 4) * 8 + 16;
+    // ring + barriers + TMEM address + flags + unit list + alignment slack
+    static constexpr int kFixed = 1024 + (2 * 12 + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
     static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes);
     static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
     static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                         : 2 * BN <= 256 ? 256 : 512;
     static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) +
-                                    (2 * kStages + 4) * 8 + 16;
+                                    (2 * kStages + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kStages >= 2, "ring too small");
 };
@@ -159,14 +160,12 @@ __device__ __forceinline__ void ext_kblocks(const TcParams &p, int32_t ta, int32
     *n = (hi + kBK - 1) / kBK - *kb0;
 }
 
-// Shrink mode: does unit w's column tile meet its token tile's slot columns?
-template <int BN>
-__device__ __forceinline__ bool unit_active(const TcParams &p, const Unit &w) {
-    if (!p.vm_mode) return true;
-    const int32_t smin = p.tile_range[2 * w.ta], smax = p.tile_range[2 * w.ta + 1];
-    if (smax < smin) return false;
-    const int32_t lo = smin * p.ext_rank, hi = (smax + 1) * p.ext_rank;
-    return w.tb * BN < hi && (w.tb + 1) * BN > lo;
+// The idx-th work unit of this CTA, or -1: every gridDim.x-th unit, or in
+// shrink mode the CTA's share of the active units (built in the prologue).
+__device__ __forceinline__ int32_t next_unit(const TcParams &p, const int32_t *unit_list, int32_t idx) {
+    if (p.vm_mode) return idx < unit_list[-1] ? unit_list[idx] : -1;
+    const int32_t u = blockIdx.x + idx * static_cast<int32_t>(gridDim.x);
+    return u < p.num_units ? u : -1;
 }
 
 // The kernel is launched as a programmatic dependent of the LoRA kernel before it:
@@ -180,14 +179,15 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                                              const CUtensorMap *tma_va, const CUtensorMap *tma_vb,
                                              const TcParams &p, uint8_t *sA, uint8_t *sB,
                                              uint64_t *full, uint64_t *empty,
-                                             volatile uint32_t *abort_flag) {
+                                             volatile uint32_t *abort_flag, const int32_t *unit_list) {
     using namespace sm100;
     using C = Cfg<SWAP, BN>;
     int32_t it = 0;
-    if (p.vm_mode) grid_dependency_wait();  // the tile ranges come from the kernel before
-    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    if (p.vm_mode) grid_dependency_wait();  // A_dense comes from the kernel before
+    for (int32_t idx = 0;; ++idx) {
+        const int32_t u = next_unit(p, unit_list, idx);
+        if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
-        if (!unit_active<BN>(p, w)) continue;
         const int32_t kb0 = w.ks * p.kb_per_split;
         const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
         const int32_t nmain = kb1 - kb0;
@@ -228,15 +228,16 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
 template <bool SWAP, int BN>
 __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
                                         uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
-                                        uint32_t tmem_base, volatile uint32_t *abort_flag) {
+                                        uint32_t tmem_base, volatile uint32_t *abort_flag,
+                                        const int32_t *unit_list) {
     using namespace sm100;
     using C = Cfg<SWAP, BN>;
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
     int32_t it = 0, t = 0;
-    if (p.vm_mode) grid_dependency_wait();
-    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    for (int32_t idx = 0;; ++idx) {
+        const int32_t u = next_unit(p, unit_list, idx);
+        if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
-        if (!unit_active<BN>(p, w)) continue;
         const int32_t kb0 = w.ks * p.kb_per_split;
         const int32_t kb_main = min(kb0 + p.kb_per_split, p.num_kb);
         int32_t kb1 = kb_main;
@@ -375,7 +376,7 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
 template <bool SWAP, int BN>
 __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_full, uint64_t *tmem_empty,
                                              uint32_t tmem_base, volatile uint32_t *abort_flag,
-                                             volatile uint32_t *last_flag) {
+                                             volatile uint32_t *last_flag, const int32_t *unit_list) {
     using namespace sm100;
     constexpr int kGroups = kEpiWarps / 4;
     constexpr int kChunks = BN / 32;
@@ -386,10 +387,10 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
     const int lane = threadIdx.x & 31;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int32_t t = 0;
-    if (p.vm_mode) grid_dependency_wait();
-    for (int32_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    for (int32_t idx = 0;; ++idx) {
+        const int32_t u = next_unit(p, unit_list, idx);
+        if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
-        if (!unit_active<BN>(p, w)) continue;
         const int b = t & 1;
         // swapped, one split: this thread's correction values (rows of its
         // 32-token chunks, its column) are fetched while the MMAs finish
@@ -613,6 +614,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
     volatile uint32_t *last_flag = tmem_slot + 2;
+    int32_t *unit_list = reinterpret_cast<int32_t *>(tmem_slot + 4) + 1;  // unit_list[-1] = its length
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -641,18 +643,56 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
         tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
+    if (p.vm_mode && warp == 2) {
+        // shrink mode: the active units (column tiles inside their token
+        // tile's slot range) in unit order; the j-th goes to CTA j % gridDim.x
+        grid_dependency_wait();  // the tile ranges come from the kernel before
+        int32_t base = 0;
+        for (int32_t t0 = 0; t0 < p.tiles_a; t0 += 32) {
+            const int32_t ta = t0 + lane;
+            int32_t cnt = 0, tb0 = 0;
+            if (ta < p.tiles_a) {
+                const int32_t smin = p.tile_range[2 * ta], smax = p.tile_range[2 * ta + 1];
+                if (smax >= smin) {
+                    tb0 = smin * p.ext_rank / BN;
+                    cnt = ((smax + 1) * p.ext_rank - 1) / BN - tb0 + 1;
+                }
+            }
+            int32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            for (int32_t k = 0; k < cnt; ++k) {
+                const int32_t j = base + incl - cnt + k;
+                if (j % static_cast<int32_t>(gridDim.x) == static_cast<int32_t>(blockIdx.x)) {
+                    const int32_t pos = j / static_cast<int32_t>(gridDim.x);
+                    if (pos < kMaxUnitList) unit_list[pos] = (tb0 + k) * p.tiles_a + ta;  // see decode_unit
+                }
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            const int32_t g = static_cast<int32_t>(gridDim.x), bid = static_cast<int32_t>(blockIdx.x);
+            const int32_t mine = base > bid ? (base - bid + g - 1) / g : 0;
+            if (mine > kMaxUnitList) record_error(p.status, kDevTimeout, 9);
+            unit_list[-1] = mine < kMaxUnitList ? mine : kMaxUnitList;
+        }
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) run_producer<SWAP, BN>(&tma_a, &tma_b, &tma_va, &tma_vb, p, sA, sB, full, empty, abort_flag);
+        if (lane == 0)
+            run_producer<SWAP, BN>(&tma_a, &tma_b, &tma_va, &tma_vb, p, sA, sB, full, empty, abort_flag, unit_list);
     } else if (warp == 1) {
         if (lane == 0)
-            run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
+            run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag, unit_list);
     } else {
-        run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag);
+        run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, unit_list);
     }
 
     tc_fence_before_sync();
@@ -842,8 +882,8 @@ cudaError_t launch_gemm_vm(const ForwardPlan &plan, const ProjView &v, cudaStrea
     if (v.ext_cols <= 0 || !v.adense || !v.vm || !v.tile_range) return cudaErrorInvalidValue;
     TcPlan tp = plan_tc(plan.M, v.ext_cols, plan.K);
     if (tp.swap) return cudaErrorInvalidValue;
-    tp.bn = 128;
-    tp.tiles_b = (v.ext_cols + 127) / 128;
+    tp.bn = 64;  // one slot of a rank-64 pool per column tile
+    tp.tiles_b = (v.ext_cols + 63) / 64;
     tp.splits = 1;
     tp.kb_per_split = tp.num_kb;
     tp.units = tp.tiles_a * tp.tiles_b;
@@ -854,7 +894,7 @@ cudaError_t launch_gemm_vm(const ForwardPlan &plan, const ProjView &v, cudaStrea
     vv.N = v.ext_cols;
     vv.out = nullptr;
     vv.ldo = v.ext_cols;
-    return launch_variant<false, 128>(plan, vv, tp, stream, true);
+    return launch_variant<false, 64>(plan, vv, tp, stream, true);
 }
 
 cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
