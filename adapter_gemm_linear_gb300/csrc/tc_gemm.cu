@@ -61,6 +61,7 @@ constexpr int kSmemLimit = 226 * 1024;   // dynamic shared memory per CTA (227 K
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kEpiBarrier = 1;         // named barrier of the epilogue warps
 constexpr int kMaxUnitList = 256;      // shrink mode: active units one CTA can take
+constexpr int kTaBand = 8;             // non-swapped unit order: token tiles per band
 
 struct TcParams {
     int32_t M, N, K;
@@ -119,7 +120,8 @@ struct Unit {
 
 // Units are numbered with the split fastest; for the swapped orientation the
 // token tiles of one W tile come next (so they run at the same time and share
-// the W tile through L2), for the non-swapped one the x tiles of one W tile.
+// the W tile through L2), for the non-swapped one the x tiles of one W tile
+// within a band of kTaBand token tiles.
 template <bool SWAP>
 __device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
     Unit w;
@@ -128,6 +130,15 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
     if (SWAP) {
         w.tb = r % p.tiles_b;
         w.ta = r / p.tiles_b;
+    } else if (!p.vm_mode && p.tiles_a > kTaBand) {
+        // bands of kTaBand token tiles, each over all W tiles: a wave of CTAs
+        // then streams a few MB of x (read from DRAM about once) while the W
+        // tiles it shares stay in L2
+        const int32_t per = kTaBand * p.tiles_b;
+        const int32_t band = r / per, q = r % per;
+        const int32_t rows = min(kTaBand, p.tiles_a - band * kTaBand);
+        w.ta = band * kTaBand + q % rows;
+        w.tb = q / rows;
     } else {
         w.ta = r % p.tiles_a;
         w.tb = r / p.tiles_a;
