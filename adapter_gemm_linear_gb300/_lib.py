@@ -110,6 +110,8 @@ SIGNATURES = [
     ("lora_linear_forward_noalloc", ctypes.c_int, [ctypes.POINTER(ForwardArgs), ctypes.c_void_p]),
     ("lora_get_device_status", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("lora_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("lora_last_cuda_error", ctypes.c_int32, []),
+    ("lora_cuda_error_name", ctypes.c_char_p, [ctypes.c_int32]),
     ("lora_abi_version", ctypes.c_int32, []),
     ("lora_kernel_launches", ctypes.c_uint64, []),
 ]

@@ -27,6 +27,11 @@ class LoraError(RuntimeError):
         self.status = int(status)
         self.name = STATUS_NAMES.get(self.status, str(status))
         msg = _lib.lib().lora_status_string(self.status).decode()
+        self.cuda_error = 0
+        if self.name == "LORA_ERR_CUDA":
+            self.cuda_error = int(_lib.lib().lora_last_cuda_error())
+            if self.cuda_error:
+                msg += ": " + _lib.lib().lora_cuda_error_name(self.cuda_error).decode()
         super().__init__(f"{what}: {self.name} ({msg})")
 
 

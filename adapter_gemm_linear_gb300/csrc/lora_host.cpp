@@ -13,6 +13,7 @@
 #include "lora_internal.h"
 
 static std::atomic<uint64_t> g_kernel_launches{0};
+static thread_local int32_t g_last_cuda_error = 0;  // behind this thread's last forward LORA_ERR_CUDA
 
 void lora::count_launches(int n) { g_kernel_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
@@ -56,6 +57,10 @@ lora_status_t push_slot(lora_pool *p, int32_t slot, cudaStream_t st) {
 extern "C" {
 
 int32_t lora_abi_version(void) { return LORA_ABI_VERSION; }
+
+int32_t lora_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *lora_cuda_error_name(int32_t code) { return cudaGetErrorName(static_cast<cudaError_t>(code)); }
 
 uint64_t lora_kernel_launches(void) { return g_kernel_launches.load(std::memory_order_relaxed); }
 
@@ -425,7 +430,16 @@ size_t lora_forward_workspace_bytes(const lora_forward_args_t *args) {
     return ws.total > 0 ? ws.total : 256;
 }
 
+static lora_status_t linear_forward(const lora_forward_args_t *args, void *stream);
+
 lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream) {
+    g_last_cuda_error = 0;
+    const lora_status_t s = linear_forward(args, stream);
+    if (s == LORA_ERR_CUDA && g_last_cuda_error == 0) g_last_cuda_error = static_cast<int32_t>(cudaGetLastError());
+    return s;
+}
+
+static lora_status_t linear_forward(const lora_forward_args_t *args, void *stream) {
     lora::ForwardPlan plan;
     lora::WorkspaceLayout ws;
     lora_status_t s = plan_forward(args, &plan, &ws);
@@ -467,7 +481,9 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
         }
         plan.row_slot = row_slot;
     }
-    return lora::launch_forward(plan, st) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    const cudaError_t e = lora::launch_forward(plan, st);
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 lora_status_t lora_get_device_status(void *stream, int32_t *detail) {

@@ -90,6 +90,8 @@ struct GroupTable {
 };
 constexpr int kGroupedMaxRows = 2048;  // rows the group table is built for (shared memory of its kernel)
 constexpr int kMaxVPlanes = 4;         // K slices of the grouped shrink
+constexpr int kPipeMaxRows = 512;      // rows the pipelined grouped kernels sort in shared memory
+constexpr int kPipeMaxRank = 128;      // pool max_rank of the pipelined grouped kernels
 
 struct ForwardPlan {
     lora_dtype_t dtype;
@@ -171,6 +173,13 @@ cudaError_t launch_shrink_grouped(const ForwardPlan &plan, const ProjView &v, co
                                   cudaStream_t stream);
 cudaError_t launch_expand_grouped(const ForwardPlan &plan, const ProjView &v, const GroupTable &gt,
                                   cudaStream_t stream);
+// The same path as two pipelined persistent kernels (lora_pipe.cu), each of
+// which groups the rows itself: the shrink writes plan.v_parts K-slice planes
+// of V with rows in sorted order, the expand plan.ycorr.  For M <=
+// kPipeMaxRows and pools of max_rank <= kPipeMaxRank.
+bool pipe_grouped_supported(int32_t M, int32_t max_rank);
+cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
 
 // Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K);

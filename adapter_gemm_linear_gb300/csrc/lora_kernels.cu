@@ -551,8 +551,9 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
 
 // bf16.  Small M (the GEMM's swapped orientation): per projection the LoRA
 // term into plan.ycorr (lora_grouped.cu) -- by one per-row kernel when each
-// row's A and B are cheap to read, else by the rows' group table and the
-// grouped shrink and expand -- then the GEMM, which adds it.  Large M: the
+// row's A and B are cheap to read, else by the pipelined grouped shrink and
+// expand (lora_pipe.cu; for larger pools, the rows' group table and the
+// grouped kernels of lora_grouped.cu) -- then the GEMM, which adds it.  Large M: the
 // per-row shrink, then the GEMM, whose epilogue applies the expand.  The GEMM
 // is launched as a programmatic dependent of the kernel before it (see
 // tc_gemm.cu).
@@ -562,9 +563,12 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
     bool by_row = swapped;
     for (int p = 0; p < plan.n_proj; ++p)
         by_row = by_row && row_lora_preferred(plan.M, plan.K, plan.proj[p].N, plan.proj[p].max_rank);
+    // the pipelined grouped kernels group the rows themselves
+    bool piped = swapped && !by_row;
+    for (int p = 0; p < plan.n_proj; ++p) piped = piped && pipe_grouped_supported(plan.M, plan.proj[p].max_rank);
     GroupTable gt{};
     cudaError_t e = cudaSuccess;
-    if (swapped && !by_row) {
+    if (swapped && !by_row && !piped) {
         gt = group_table_at(plan.group_table, plan.M);
         e = launch_group_rows(plan, gt, plan.proj[0].max_slots, stream);
         if (e != cudaSuccess) return e;
@@ -574,6 +578,10 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
         const ProjView &v = plan.proj[p];
         if (by_row) {
             e = launch_lora_rows(plan, v, stream);
+            if (e != cudaSuccess) return e;
+        } else if (piped) {
+            e = launch_pipe_shrink(plan, v, stream);
+            if (e == cudaSuccess) e = launch_pipe_expand(plan, v, stream);
             if (e != cudaSuccess) return e;
         } else if (swapped) {
             e = launch_shrink_grouped(plan, v, gt, stream);

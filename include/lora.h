@@ -298,6 +298,12 @@ lora_status_t lora_get_device_status(void *stream, int32_t *detail);
 /* Static, human-readable name of a status code. */
 const char *lora_status_string(lora_status_t status);
 
+/* The CUDA runtime error behind the calling thread's most recent
+ * LORA_ERR_CUDA from lora_linear_forward (a cudaError_t value; 0 when that
+ * call saw none), and the runtime's static name for such a code. */
+int32_t lora_last_cuda_error(void);
+const char *lora_cuda_error_name(int32_t code);
+
 /* LORA_ABI_VERSION of the library. */
 int32_t lora_abi_version(void);
 

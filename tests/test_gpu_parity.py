@@ -109,6 +109,37 @@ def test_grouped_path_integer_exact():
         assert np.array_equal(got, want), f"projection {p}: {np.sum(got != want)} outputs differ"
 
 
+@pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
+@pytest.mark.parametrize("shape", [(500, 2056, 1032), (480, 4104, 264), (200, 8200, 3080)])
+def test_pipelined_grouped_path(shape, mode):
+    """Pools of max_rank <= 128 take the pipelined grouped kernels (rows
+    sorted in every CTA, adapter pieces streamed by bulk copies, 16 x 16 x 16
+    warp MMAs).  K is ragged against the 512-wide stages and the K slices, N
+    against the 1024-column ranges; a popular adapter spans several 16-row
+    chunks; ranks 1 and 100 leave partial rank blocks."""
+    M, K, N = shape
+    wl = synth(M=M, K=K, Ns=[N], num_slots=9, rank_choices=(1, 40, 100, 128), seed=M + K + N,
+               zipf_s=1.5, mode=mode, none_frac=0.12)
+    assert H.pool_max_rank(wl) <= 128
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, mode)[0]
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0), f"pipelined {shape} {mode}")
+
+
+def test_pipelined_grouped_integer_exact():
+    """Integer inputs through the pipelined grouped kernels: V's bf16 hi/lo
+    parts carry the integer partial sums exactly, so the output bits must
+    equal the oracle's."""
+    wl = synth(M=450, K=2048, Ns=[1032, 264], num_slots=13, rank_choices=(3, 16, 64, 120, 128), integer=True,
+               seed=35, none_frac=0.2, zipf_s=1.3)
+    pools = H.make_pools(wl, DEV, extra_blocks=5)
+    outs = H.forward(wl, pools, "bgmv")
+    for p in range(2):
+        want = H.oracle_bf16_bits(H.oracle_rows(wl, p))
+        got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), f"projection {p}: {np.sum(got != want)} outputs differ"
+
+
 def test_tiny_fp32_full():
     wl = make_config("tiny_fp32")
     pools = H.make_pools(wl, DEV)
