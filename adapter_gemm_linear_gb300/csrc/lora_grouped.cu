@@ -25,8 +25,11 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "lora_device.cuh"
 #include "lora_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace lora {
 
@@ -479,8 +482,13 @@ struct RowLoraParams {
     unsigned long long *status;
 };
 
-constexpr int kRowThreads = 256;
-constexpr int kRowBatch = 2;  // k steps of A loads in flight per thread
+// Four warps of at most 152 registers: a CTA fits on an SM beside a CTA of
+// the swapped GEMM (ten warps, allocated as twelve, of 120 registers), so the
+// GEMM that follows as a programmatic dependent streams W while this kernel
+// runs.
+constexpr int kRowThreads = 128;
+constexpr int kRowMaxRegs = 152;
+constexpr int kRowBatch = 1;  // k steps of A loads in flight per thread
 constexpr int kRowCols = 8;   // output columns per thread whose B pieces are in flight together
 
 // grid (M, column splits).  The CTA resolves its row's adapter, computes
@@ -488,10 +496,9 @@ constexpr int kRowCols = 8;   // output columns per thread whose B pieces are in
 // per step and the CTA sums the partial dot products) into shared memory, then
 // writes ycorr[m, n] = s_i <B_i[n, :], v> for its columns (zeros for a row
 // without an adapter).
-__global__ void __launch_bounds__(kRowThreads)
-lora_rows_kernel(const RowLoraParams p) {
+__global__ void __maxnreg__(kRowMaxRegs) lora_rows_kernel(const RowLoraParams p) {
     __shared__ float red[kRowThreads / 32][LORA_BLOCK_ROWS];
-    __shared__ __align__(16) float v[kMaxRankLimit];
+    extern __shared__ __align__(16) float v[];  // [max_rank]
     // the GEMM that follows may launch now; it reads ycorr only after this
     // grid has completed (griddepcontrol.wait)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -514,6 +521,20 @@ lora_rows_kernel(const RowLoraParams p) {
             if (blockIdx.y == 0 && tid == 0) record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
             slot = -1;
         }
+    }
+    if (slot >= 0 && tid == 0) {
+        // the row's A blocks (16 rows x K, contiguous) and this CTA's columns
+        // of its B blocks head for L2 now, so that the loads below, issued a
+        // few at a time, mostly hit it
+        for (int32_t jb = 0; jb < nblk; ++jb) {
+            sm100::bulk_prefetch_l2(p.a_arena + static_cast<size_t>(trow[jb]) * LORA_BLOCK_ROWS * p.K,
+                                    static_cast<uint32_t>(LORA_BLOCK_ROWS) * p.K * 2u);
+            if (n_end > n_begin)
+                sm100::bulk_prefetch_l2(
+                    p.b_arena + (static_cast<size_t>(trow[jb]) * p.N + n_begin) * LORA_BLOCK_ROWS,
+                    static_cast<uint32_t>(n_end - n_begin) * LORA_BLOCK_ROWS * 2u);
+        }
+        sm100::bulk_prefetch_l2(p.x + static_cast<size_t>(m) * p.ldx, static_cast<uint32_t>(p.K) * 2u);
     }
     float *dst = p.ycorr + static_cast<size_t>(m) * p.N;
     if (slot < 0) {
@@ -663,15 +684,32 @@ cudaError_t launch_lora_rows(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.counters = plan.counters;
     p.n_counters = plan.n_counters;
     p.status = plan.status;
-    // column splits: one wave (the kernel holds one CTA per SM), at least
-    // kRowThreads columns per CTA
+    // column splits: about one CTA per SM (each fits beside a GEMM CTA), at
+    // least kRowThreads columns per CTA
     const int sms = device_sm_count();
     int splits = sms / plan.M;
     const int max_splits = (v.N + kRowThreads - 1) / kRowThreads;
     splits = splits < 1 ? 1 : splits > max_splits ? max_splits : splits;
     p.cols_per_cta = ((v.N + splits - 1) / splits + kRowThreads - 1) / kRowThreads * kRowThreads;
     splits = (v.N + p.cols_per_cta - 1) / p.cols_per_cta;
-    lora_rows_kernel<<<dim3(plan.M, splits), kRowThreads, 0, stream>>>(p);
+    {
+        // run with the shared-memory carveout the GEMM needs, so that its CTAs
+        // can be placed beside this kernel's (an SM changes its carveout only
+        // when idle)
+        static std::mutex mu;
+        static bool done[128] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 128) {
+            std::lock_guard<std::mutex> lock(mu);
+            if (!done[dev]) {
+                const cudaError_t e = cudaFuncSetAttribute(lora_rows_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                           static_cast<int>(cudaSharedmemCarveoutMaxShared));
+                if (e != cudaSuccess) return e;
+                done[dev] = true;
+            }
+        }
+    }
+    lora_rows_kernel<<<dim3(plan.M, splits), kRowThreads, sizeof(float) * v.max_rank, stream>>>(p);
     return cudaGetLastError();
 }
 

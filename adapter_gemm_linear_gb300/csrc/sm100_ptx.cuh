@@ -112,6 +112,14 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
         : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global
+// memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gmem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gmem_src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- warp-level MMA
 
 // Four 8x8 b16 matrices from shared memory; lane l supplies the row address

@@ -10,11 +10,16 @@ expand); for larger M the per-row shrink writes V and the GEMM's epilogue
 applies the expand.  Prints ONE JSON line per workload (default: the decode
 BGMV workload, 64 rows of q_proj 4096->4096 with 32 rank-16 adapters).
 
-Timing: W warm-up steps, then K steps; L2 is flushed (a 2 x L2 write)
-before every step, outside the timed intervals.  The timed steps replay one
-forward call captured in a CUDA graph (the launch mode of a decode server),
-each replay bracketed by CUDA events on the launching stream; step times are
-summed.  The dominant kernel's roofline uses stage events the library
+Timing: W warm-up steps, then K steps; L2 is flushed before every step,
+outside the timed intervals: a 2 x L2 write, then a 2 x L2 read of another
+buffer (so that no dirty lines of the flush are written back inside the
+next step).  The timed steps replay one
+forward call captured in a CUDA graph (the launch mode of a decode server);
+a step's time is the interval between two CUDA events recorded as nodes of
+that graph, right before the forward's first kernel and after its last, so
+it excludes the latency of launching the graph (reported beside it as
+`replay_ms_per_step`, from events recorded around each replay); step times
+are summed.  The dominant kernel's roofline uses stage events the library
 records around each kernel in an eager pass over the same K steps; the eager
 step rate is reported beside the graph one.  `e2e` repeats the measurement through the C ABI
 with pinned host buffers: the host->device copy of x and the row ids and the
@@ -242,11 +247,70 @@ def build_case(wl, device):
     return {"pools": pools, "x": x, "Ws": Ws, "outs": outs, "ids": ids, "call": call}
 
 
+class L2Flush:
+    """Evicts the workload from L2 before a step: a write of 2 x L2 bytes,
+    then a read of another 2 x L2 bytes, so that L2 holds none of the
+    workload's data and no dirty lines whose write-back would fall into the
+    next timed interval."""
+
+    def __init__(self, l2, device):
+        import torch
+
+        self.w = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+        self.r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def zero_(self):
+        import torch
+
+        self.w.zero_()
+        self.sink.copy_(self.r.sum())
+
+
+def graph_event_pair():
+    """Two timing events that a CUDA graph records as nodes of its own, and
+    the function that records one on the capturing stream."""
+    import torch
+
+    try:
+        a = torch.cuda.Event(enable_timing=True, external=True)
+        b = torch.cuda.Event(enable_timing=True, external=True)
+        return a, b, lambda ev: ev.record()
+    except TypeError:  # a torch without external events: the runtime's own call
+        import ctypes
+
+        lib = None
+        for name in ("libcudart.so.13", "libcudart.so", "/usr/local/cuda/lib64/libcudart.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise RuntimeError("no CUDA runtime library for in-graph timing events")
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        for ev in (a, b):  # create the raw events
+            ev.record()
+        torch.cuda.synchronize()
+
+        def record(ev):
+            stream = torch.cuda.current_stream()
+            rc = lib.cudaEventRecordWithFlags(ctypes.c_void_p(ev.cuda_event), ctypes.c_void_p(stream.cuda_stream),
+                                              ctypes.c_uint(1))  # cudaEventRecordExternal
+            if rc != 0:
+                raise RuntimeError(f"cudaEventRecordWithFlags failed ({rc})")
+
+        return a, b, record
+
+
 def time_device(case, wl, steps, warmup, flush, clocks_index):
     """Eager pass with per-stage events (kernel durations for the roofline),
     then the timed pass: one forward captured in a CUDA graph and replayed
-    once per step, an L2 flush before each replay, events around each replay
-    on the launching stream."""
+    once per step, an L2 flush before each replay.  A step's time is the
+    interval between two events recorded inside the graph around the
+    forward; the interval between events recorded around each replay (which
+    adds the graph's launch latency) is reported beside it."""
     import torch
     from adapter_gemm_linear_gb300 import kernel_launches
 
@@ -284,9 +348,15 @@ def time_device(case, wl, steps, warmup, flush, clocks_index):
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
+    g_start, g_end, record_in_graph = graph_event_pair()
     n_cap = kernel_launches()
     with torch.cuda.graph(graph):
+        # timing events as nodes of the graph itself, right around the
+        # forward's kernels: they measure the forward's device time without
+        # the latency of launching the graph
+        record_in_graph(g_start)
         call()
+        record_in_graph(g_end)
     kernels_per_call = kernel_launches() - n_cap
     for _ in range(warmup):
         flush.zero_()
@@ -296,16 +366,20 @@ def time_device(case, wl, steps, warmup, flush, clocks_index):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     sampler = ClockSampler(clocks_index)
     time.sleep(0.3)
+    step_ms = []
     for i in range(steps):
         flush.zero_()
         starts[i].record()
         graph.replay()
         ends[i].record()
+        ends[i].synchronize()  # the in-graph events are recorded again by the next replay
+        step_ms.append(g_start.elapsed_time(g_end))
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    replay_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     del graph
-    return {"step_ms": step_ms, "eager_ms": eager_ms, "shrink_ms": shrink_ms, "gemm_ms": gemm_ms,
+    return {"step_ms": step_ms, "replay_ms": replay_ms, "eager_ms": eager_ms, "shrink_ms": shrink_ms,
+            "gemm_ms": gemm_ms,
             "launches": kernels_per_call * steps, "kernels_per_call": kernels_per_call, "clocks": clocks}
 
 
@@ -370,7 +444,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     case = build_case(wl, device)
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    flush = L2Flush(l2, device)
     if args.steps is None:
         # about 1.5 s of forwards plus flushes
         case["call"]()
@@ -423,7 +497,8 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         kernel = "tc_gemm_lora_kernel"
     else:
         b, f, t = alg["lora_bytes"], alg["lora_flops"], lora_avg_s
-        kernel = ("lora_rows_kernel or group_rows_kernel + shrink_grouped_kernel + expand_grouped_kernel"
+        kernel = ("lora_rows_kernel, or pipe_shrink_kernel + pipe_expand_kernel (max_rank <= 128), or "
+                  "group_rows_kernel + shrink_grouped_kernel + expand_grouped_kernel"
                   if alg["orientation"] == "swapped" else "shrink kernel")
     if f / b > ridge:
         roof = {"bound": "tensor", "achieved": round(f / t / 1e12, 2), "peak": peaks["bf16_tflops"],
@@ -445,6 +520,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         "steps": steps,
         "warmup": warmup,
         "ms_per_step": round(total_ms / steps, 5),
+        "replay_ms_per_step": round(sum(res["replay_ms"]) / steps, 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -454,8 +530,10 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
             "workload": wl.name, "M": wl.M, "K": wl.K, "N": [p.N for p in wl.projections],
             "slots": wl.num_slots, "ranks": sorted(set(int(r) for r in wl.ranks)),
             "mode": wl.mode, "distinct_adapters": alg["distinct"], "adapted_rows": alg["adapted_rows"],
-            "l2": "flushed before every step (2 x L2 write, outside the timed intervals)",
-            "launch": "CUDA graph of one lora_linear_forward call, replayed per step; events around each replay",
+            "l2": "flushed before every step (2 x L2 write, then 2 x L2 read of another buffer; outside the "
+                  "timed intervals)",
+            "launch": "CUDA graph of one lora_linear_forward call, replayed per step; step = events recorded "
+                      "inside the graph around the forward",
             "parallelism": f"replicas x{world}",
         },
         "roofline": roof,
