@@ -961,8 +961,10 @@ cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView &v, cudaS
     p.num_blocks = v.num_blocks;
     p.V = v.V;
     p.ldv = v.max_rank;
-    p.ksplit = plan.v_parts;
-    p.kc_len = pipe_kc_len(plan.K, plan.v_parts);
+    // one item covers all of K (in kShrStageK stages), so V is one plane:
+    // the expand then fetches one V piece per item instead of one per slice
+    p.ksplit = 1;
+    p.kc_len = pipe_kc_len(plan.K, 1);
     p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.counters = plan.counters;
     p.n_counters = plan.n_counters;
@@ -987,9 +989,9 @@ cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaS
     p.num_blocks = v.num_blocks;
     p.V = v.V;
     p.ldv = v.max_rank;
-    p.ksplit = plan.v_parts;
+    p.ksplit = 1;  // as the shrink writes it
     p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
-    p.vslot_floats = plan.v_parts * kChunkRows * v.max_rank;
+    p.vslot_floats = kChunkRows * v.max_rank;
     p.ycorr = plan.ycorr;
     p.status = plan.status;
     const size_t vbytes = sizeof(float) * static_cast<size_t>(p.vslot_floats);

@@ -404,14 +404,17 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
         const Unit w = decode_unit<SWAP>(u, p);
         const int b = t & 1;
         // swapped, one split: this thread's correction values (rows of its
-        // 32-token chunks, its column) are fetched while the MMAs finish
+        // 32-token chunks, its column) are fetched while the MMAs finish --
+        // the first kPre chunks; each later chunk's into the slot its
+        // predecessor kPre back has just used
         constexpr int kMyChunks = (kChunks + kGroups - 1) / kGroups;
-        float yc[SWAP ? kMyChunks : 1][32];
+        constexpr int kPre = kMyChunks <= 2 ? kMyChunks : 1;  // four chunks: one slot (registers)
+        float yc[SWAP ? kPre : 1][32];
         const int32_t n_sw = w.ta * kBM + q * 32 + lane;
         if (SWAP && p.splits == 1) {
             grid_dependency_wait();  // ycorr comes from the expand kernel
 #pragma unroll
-            for (int ci = 0; ci < kMyChunks; ++ci) {
+            for (int ci = 0; ci < kPre; ++ci) {
                 const int32_t m0 = w.tb * BN + (grp + ci * kGroups) * 32;
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
@@ -441,7 +444,16 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                     load_tmem_chunk(col0 + c * 32, acc);
                     const int32_t m0 = w.tb * BN + c * 32;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[e] += yc[ci][e];
+                    for (int e = 0; e < 32; ++e) acc[e] += yc[ci % kPre][e];
+                    if (ci + kPre < kMyChunks) {
+                        const int c2 = grp + (ci + kPre) * kGroups;
+                        const int32_t m2 = w.tb * BN + c2 * 32;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            yc[ci % kPre][e] = (n_sw < p.N && m2 + e < p.M && c2 < kChunks)
+                                                   ? __ldcg(p.ycorr + static_cast<size_t>(m2 + e) * p.N + n_sw)
+                                                   : 0.0f;
+                    }
                     if (n_ok) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
@@ -856,8 +868,11 @@ TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
     t.num_kb = (K + kBK - 1) / kBK;
     t.swap = M <= 512;
     if (t.swap) {
-        // tokens per tile at most 128, so an x tile is never larger than a W tile
-        t.bn = M <= 32 ? 32 : M <= 64 ? 64 : 128;
+        // tokens per tile: 256 above 256 tokens (an MMA of 128 W rows x 256
+        // tokens needs less shared-memory operand bandwidth per flop than 128
+        // x 128; measured 78 -> 75 us on 512 x 5120 -> 13824, while 256 tokens
+        // in one tile lost to two of 128 on 8192 -> 8192)
+        t.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 256 ? 128 : 256;
         t.tiles_a = (N + kBM - 1) / kBM;
         t.tiles_b = (M + t.bn - 1) / t.bn;
         const int tiles = t.tiles_a * t.tiles_b;
@@ -914,7 +929,8 @@ cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cuda
         switch (tp.bn) {
             case 32: return launch_variant<true, 32>(plan, v, tp, stream);
             case 64: return launch_variant<true, 64>(plan, v, tp, stream);
-            default: return launch_variant<true, 128>(plan, v, tp, stream);
+            case 128: return launch_variant<true, 128>(plan, v, tp, stream);
+            default: return launch_variant<true, 256>(plan, v, tp, stream);
         }
     }
     if (tp.bn == 128) return launch_variant<false, 128>(plan, v, tp, stream);

@@ -140,6 +140,20 @@ def test_pipelined_grouped_integer_exact():
         assert np.array_equal(got, want), f"projection {p}: {np.sum(got != want)} outputs differ"
 
 
+@pytest.mark.parametrize("shape", [(300, 1024, 9856), (400, 2056, 9992)])
+def test_integer_exact_many_tiles(shape):
+    """Swapped GEMM with 256-token tiles and more tiles than SMs (a short last
+    wave).  Integer inputs: bit-exact."""
+    M, K, N = shape
+    wl = synth(M=M, K=K, Ns=[N], num_slots=5, rank_choices=(8, 16, 32), integer=True, seed=M + N,
+               none_frac=0.1)
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, "bgmv")[0]
+    want = H.oracle_bf16_bits(H.oracle_rows(wl, 0))
+    got = torch.from_numpy(out).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want), f"{shape}: {np.sum(got != want)} outputs differ"
+
+
 def test_tiny_fp32_full():
     wl = make_config("tiny_fp32")
     pools = H.make_pools(wl, DEV)
