@@ -70,11 +70,11 @@ constexpr size_t kShrSmem = static_cast<size_t>(kShrStages) * kShrStageBytes + k
 // expand stages: one rank block's B for 1024 output columns
 constexpr int kExpCols = 1024;
 constexpr int kExpStageBytes = kExpCols * LORA_BLOCK_ROWS * 2;
-constexpr int kExpStages = 3;
+constexpr int kExpStages = 4;
 constexpr int kExpWarps = 16;                   // consumer warps of the expand
 constexpr int kExpThreads = (kExpWarps + 1) * 32;
 constexpr int kExpGroups = kExpCols / 16 / kExpWarps;  // 16-column groups a consumer warp owns per range
-constexpr int kExpMaxVSlots = 4;  // V slots (an item's V stays until its last stage): the producer's lookahead in items
+constexpr int kExpMaxVSlots = 6;  // V slots (an item's V stays until its last stage): the producer's lookahead in items
 constexpr int kEpiPitch = 20;  // floats a row of the epilogue's 16 x 16 tile: fragment writes free of bank conflicts
 
 static_assert(kShrStageBytes % 16 == 0 && kShrPitch % 16 == 0, "bulk copy destinations 16-byte aligned");
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_shrink_kernel(const Pipe
 // expand
 // ---------------------------------------------------------------------------
 
-constexpr int kExpVSlotFloatsMax = kMaxVPlanes * kChunkRows * kPipeMaxRank;
+constexpr int kExpVSlotFloatsMax = kChunkRows * kPipeMaxRank;  // one V plane
 // dynamic shared memory of the expand: the B stages and as many V slots (2 to
 // kExpMaxVSlots) as fit beside them and the static arrays
 constexpr size_t kExpSmemMax = 180 * 1024;
