@@ -93,6 +93,12 @@ SIGNATURES = [
      [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
       ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     ("lora_pool_unload_slot", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    ("lora_pool_touch", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("lora_pool_pin", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("lora_pool_unpin", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("lora_pool_evict_lru", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    ("lora_pool_slot_use", ctypes.c_int,
+     [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)]),
     ("lora_pool_slot_info", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
       ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]),

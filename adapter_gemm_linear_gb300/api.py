@@ -110,25 +110,70 @@ class LoraPool:
         return self._handle.value
 
     def load(self, slot: int, A: torch.Tensor, B: torch.Tensor, alpha: float,
-             stream: Optional[torch.cuda.Stream] = None) -> None:
-        """lora_pool_load_slot: A [r, K], B [N, r] in the pool dtype, on the
-        host or on this pool's device."""
+             stream: Optional[torch.cuda.Stream] = None, src: str = "auto") -> None:
+        """lora_pool_load_slot: A [r, K], B [N, r] in the pool dtype.
+
+        src "auto": this pool's device if A is on the GPU, else "host".
+        "host": staged copies, synchronous.  "device": a kernel on `stream`.
+        "mapped": A and B are page-locked host tensors (pin_memory=True) read
+        by that kernel over the host link, asynchronously on `stream`; this
+        object keeps them alive until the stream has passed the load.  (The C
+        ABI also takes pageable memory where the GPU can address it.)"""
         r = int(A.shape[0])
         if A.shape != (r, self.K) or B.shape != (self.N, r):
             raise ValueError(f"A {tuple(A.shape)} / B {tuple(B.shape)} do not match K={self.K}, N={self.N}")
-        A = A.to(self.dtype).contiguous()
-        B = B.to(self.dtype).contiguous()
-        on_dev = A.is_cuda
-        if on_dev != B.is_cuda:
-            raise ValueError("A and B must both be on the host or both on the device")
+        if src == "auto":
+            src = "device" if A.is_cuda else "host"
+        mode = {"host": 0, "device": 1, "mapped": 2}.get(src)
+        if mode is None:
+            raise ValueError(f"unknown src {src!r}")
+        if (mode == 1) != A.is_cuda or A.is_cuda != B.is_cuda:
+            raise ValueError("A and B must both be on this pool's device for src='device', else on the host")
+        if mode == 2:
+            if not (A.dtype == self.dtype and B.dtype == self.dtype and A.is_contiguous() and B.is_contiguous()
+                    and A.is_pinned() and B.is_pinned()):
+                raise ValueError("src='mapped' needs contiguous page-locked tensors in the pool dtype")
+        else:
+            A = A.to(self.dtype).contiguous()
+            B = B.to(self.dtype).contiguous()
         with torch.cuda.device(self.device):
             st = stream if stream is not None else torch.cuda.current_stream()
             _check(_lib.lib().lora_pool_load_slot(self.handle, int(slot), r, float(alpha), _ptr(A), _ptr(B),
-                                                  1 if on_dev else 0, int(st.cuda_stream)),
+                                                  mode, int(st.cuda_stream)),
                    f"lora_pool_load_slot(slot={slot}, rank={r})")
-            if on_dev:
+            if mode == 1:
                 A.record_stream(st)
                 B.record_stream(st)
+            elif mode == 2:
+                done = torch.cuda.Event()
+                done.record(st)
+                self._inflight = [(e, a, b) for e, a, b in getattr(self, "_inflight", []) if not e.query()]
+                self._inflight.append((done, A, B))
+
+    # residency bookkeeping (host side): LRU with in-flight pins
+    def touch(self, slot: int) -> None:
+        _check(_lib.lib().lora_pool_touch(self.handle, int(slot)), f"lora_pool_touch(slot={slot})")
+
+    def pin(self, slot: int) -> None:
+        _check(_lib.lib().lora_pool_pin(self.handle, int(slot)), f"lora_pool_pin(slot={slot})")
+
+    def unpin(self, slot: int) -> None:
+        _check(_lib.lib().lora_pool_unpin(self.handle, int(slot)), f"lora_pool_unpin(slot={slot})")
+
+    def evict_lru(self, stream: Optional[torch.cuda.Stream] = None) -> int:
+        """Unloads the least recently used unpinned slot; returns it."""
+        out = ctypes.c_int32(-1)
+        with torch.cuda.device(self.device):
+            _check(_lib.lib().lora_pool_evict_lru(self.handle, _stream_handle(stream), ctypes.byref(out)),
+                   "lora_pool_evict_lru")
+        return int(out.value)
+
+    def slot_use(self, slot: int) -> Tuple[int, int]:
+        """(last use on the pool's use clock, 0 if empty; in-flight pins)."""
+        last, pins = ctypes.c_int64(0), ctypes.c_int32(0)
+        _check(_lib.lib().lora_pool_slot_use(self.handle, int(slot), ctypes.byref(last), ctypes.byref(pins)),
+               f"lora_pool_slot_use(slot={slot})")
+        return int(last.value), int(pins.value)
 
     def unload(self, slot: int, stream: Optional[torch.cuda.Stream] = None) -> None:
         with torch.cuda.device(self.device):

@@ -119,6 +119,8 @@ lora_status_t lora_pool_create(const lora_pool_desc_t *desc, void *stream, lora_
         p->rank.assign(d.max_slots, 0);
         p->scale.assign(d.max_slots, 0.0f);
         p->table.assign(static_cast<size_t>(d.max_slots) * p->bps, -1);
+        p->last_use.assign(d.max_slots, 0);
+        p->pins.assign(d.max_slots, 0);
         // free list as a stack: back() is handed out first
         p->free_list.resize(d.num_blocks);
         for (int32_t b = 0; b < d.num_blocks; ++b) p->free_list[b] = d.num_blocks - 1 - b;
@@ -191,7 +193,20 @@ lora_status_t lora_pool_load_slot(lora_pool_t *pool, int32_t slot, int32_t rank,
     if (rank <= 0 || rank > p->d.max_rank) return LORA_ERR_RANK;
     const int nb = (rank + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
     if (static_cast<int>(p->free_list.size()) < nb) return LORA_ERR_OUT_OF_BLOCKS;
-    if (src_on_device && (!aligned16(A) || !aligned16(B))) return LORA_ERR_ALIGNMENT;
+    if (src_on_device < LORA_SRC_HOST || src_on_device > LORA_SRC_MAPPED_HOST) return LORA_ERR_INVALID_ARG;
+    if (src_on_device != LORA_SRC_HOST && (!aligned16(A) || !aligned16(B))) return LORA_ERR_ALIGNMENT;
+    if (src_on_device == LORA_SRC_MAPPED_HOST) {
+        // the device's view of page-locked host memory; anything else is refused
+        void *dA = nullptr, *dB = nullptr;
+        if (cudaHostGetDevicePointer(&dA, const_cast<void *>(A), 0) != cudaSuccess ||
+            cudaHostGetDevicePointer(&dB, const_cast<void *>(B), 0) != cudaSuccess || !dA || !dB) {
+            (void)cudaGetLastError();  // not a sticky error: leave no trace for later calls
+            return LORA_ERR_INVALID_ARG;
+        }
+        if (!aligned16(dA) || !aligned16(dB)) return LORA_ERR_ALIGNMENT;
+        A = dA;
+        B = dB;
+    }
 
     std::vector<int32_t> blocks(nb);
     for (int t = 0; t < nb; ++t) blocks[t] = p->free_list[p->free_list.size() - 1 - t];
@@ -200,7 +215,23 @@ lora_status_t lora_pool_load_slot(lora_pool_t *pool, int32_t slot, int32_t rank,
     const size_t eb = dtype_bytes(p->d.dtype);
     const size_t K = static_cast<size_t>(p->d.K), N = static_cast<size_t>(p->d.N);
     cudaError_t e = cudaSuccess;
-    if (src_on_device) {
+    bool direct = src_on_device != LORA_SRC_HOST;
+    if (!direct) {
+        // host memory the device can address (page-locked, or any memory where
+        // the GPU translates host addresses, as over NVLink-C2C on Grace): the
+        // scatter kernel reads it directly, and the call waits for it below
+        void *dA = nullptr, *dB = nullptr;
+        if (cudaHostGetDevicePointer(&dA, const_cast<void *>(A), 0) == cudaSuccess &&
+            cudaHostGetDevicePointer(&dB, const_cast<void *>(B), 0) == cudaSuccess && dA && dB && aligned16(dA) &&
+            aligned16(dB)) {
+            A = dA;
+            B = dB;
+            direct = true;
+        } else {
+            (void)cudaGetLastError();  // not a sticky error: the staged copies follow
+        }
+    }
+    if (direct) {
         e = lora::launch_pool_scatter(p, rank, blocks.data(), A, B, st);
     } else {
         // per block t: A rows 16t.. (contiguous) and B columns 16t..16t+15
@@ -243,8 +274,11 @@ lora_status_t lora_pool_load_slot(lora_pool_t *pool, int32_t slot, int32_t rank,
     for (int t = 0; t < nb; ++t) p->table[static_cast<size_t>(slot) * p->bps + t] = blocks[t];
     p->rank[slot] = rank;
     p->scale[slot] = alpha / static_cast<float>(rank);
+    p->last_use[slot] = ++p->use_clock;
+    p->pins[slot] = 0;
     lora_status_t s = push_slot(p, slot, st);
-    if (s == LORA_OK && !src_on_device && cudaStreamSynchronize(st) != cudaSuccess) s = LORA_ERR_CUDA;
+    if (s == LORA_OK && src_on_device == LORA_SRC_HOST && cudaStreamSynchronize(st) != cudaSuccess)
+        s = LORA_ERR_CUDA;
     return s;
 }
 
@@ -253,6 +287,7 @@ lora_status_t lora_pool_unload_slot(lora_pool_t *pool, int32_t slot, void *strea
     lora_pool *p = pool;
     if (slot < 0 || slot >= p->d.max_slots) return LORA_ERR_SLOT;
     if (p->rank[slot] == 0) return LORA_ERR_SLOT;
+    if (p->pins[slot] > 0) return LORA_ERR_SLOT;  // in use by in-flight work
     const int nb = (p->rank[slot] + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
     int32_t *row = p->table.data() + static_cast<size_t>(slot) * p->bps;
     // blocks go back so that the most recently freed is handed out last
@@ -262,7 +297,52 @@ lora_status_t lora_pool_unload_slot(lora_pool_t *pool, int32_t slot, void *strea
     }
     p->rank[slot] = 0;
     p->scale[slot] = 0.0f;
+    p->last_use[slot] = 0;
     return push_slot(p, slot, as_stream(stream));
+}
+
+lora_status_t lora_pool_touch(lora_pool_t *pool, int32_t slot) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    if (slot < 0 || slot >= pool->d.max_slots || pool->rank[slot] == 0) return LORA_ERR_SLOT;
+    pool->last_use[slot] = ++pool->use_clock;
+    return LORA_OK;
+}
+
+lora_status_t lora_pool_pin(lora_pool_t *pool, int32_t slot) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    if (slot < 0 || slot >= pool->d.max_slots || pool->rank[slot] == 0) return LORA_ERR_SLOT;
+    ++pool->pins[slot];
+    pool->last_use[slot] = ++pool->use_clock;
+    return LORA_OK;
+}
+
+lora_status_t lora_pool_unpin(lora_pool_t *pool, int32_t slot) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    if (slot < 0 || slot >= pool->d.max_slots || pool->rank[slot] == 0 || pool->pins[slot] <= 0)
+        return LORA_ERR_SLOT;
+    --pool->pins[slot];
+    return LORA_OK;
+}
+
+lora_status_t lora_pool_evict_lru(lora_pool_t *pool, void *stream, int32_t *slot) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    int32_t victim = -1;
+    for (int32_t s = 0; s < pool->d.max_slots; ++s)
+        if (pool->rank[s] != 0 && pool->pins[s] == 0 &&
+            (victim < 0 || pool->last_use[s] < pool->last_use[victim]))
+            victim = s;
+    if (victim < 0) return LORA_ERR_SLOT;
+    const lora_status_t st = lora_pool_unload_slot(pool, victim, stream);
+    if (st == LORA_OK && slot) *slot = victim;
+    return st;
+}
+
+lora_status_t lora_pool_slot_use(const lora_pool_t *pool, int32_t slot, int64_t *last_use, int32_t *pins) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    if (slot < 0 || slot >= pool->d.max_slots) return LORA_ERR_SLOT;
+    if (last_use) *last_use = pool->last_use[slot];
+    if (pins) *pins = pool->pins[slot];
+    return LORA_OK;
 }
 
 lora_status_t lora_segment_rows(const int32_t *ids, int32_t M, int32_t num_slots, int32_t *perm,

@@ -19,6 +19,9 @@ struct lora_pool {
     std::vector<int32_t> rank;       // [max_slots], 0 = empty
     std::vector<float> scale;        // [max_slots]
     std::vector<int32_t> table;      // [max_slots * bps], -1 = unused
+    std::vector<int64_t> last_use;   // [max_slots] use clock at the last load or touch, 0 = empty
+    std::vector<int32_t> pins;       // [max_slots] in-flight uses (never evicted while > 0)
+    int64_t use_clock = 0;
 };
 
 namespace lora {

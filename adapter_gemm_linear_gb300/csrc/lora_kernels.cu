@@ -106,12 +106,66 @@ __global__ void pool_scatter_kernel(const T *__restrict__ A, const T *__restrict
             j < rank ? B[static_cast<size_t>(n) * rank + j] : from_float<T>(0.0f);
 }
 
+// The same scatter in 16-byte vectors, for ranks whose B rows are whole
+// vectors (rank * element size a multiple of 16): A's rows straight into the
+// blocks (zero rows past the rank), and B read a row at a time -- consecutive
+// threads take consecutive vectors of a row, so reads are coalesced (also
+// over the host link, for page-locked host sources) -- each vector written to
+// its block's [N][16] layout; the last block's columns past the rank zeroed.
+template <typename T>
+__global__ void __launch_bounds__(256)
+pool_scatter_vec_kernel(const T *__restrict__ A, const T *__restrict__ B, int32_t rank, int32_t K, int32_t N,
+                        T *__restrict__ a_arena, T *__restrict__ b_arena, ScatterBlocks blocks) {
+    constexpr int kVec = 16 / sizeof(T);                   // elements per vector
+    constexpr int kRowVecs = LORA_BLOCK_ROWS / kVec;       // vectors of a block row of B
+    const int32_t nb = (rank + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
+    const int64_t kv = K / kVec;                           // vectors of an A row
+    const int64_t a_work = static_cast<int64_t>(nb) * LORA_BLOCK_ROWS * kv;
+    const int64_t b_row = static_cast<int64_t>(nb) * kRowVecs;  // destination vectors per B row
+    const int64_t b_work = static_cast<int64_t>(N) * b_row;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < a_work + b_work; i += stride) {
+        if (i < a_work) {
+            const int64_t jrow = i / kv, v = i - jrow * kv;  // block row jrow of the slot (j = jrow)
+            const int32_t t = static_cast<int32_t>(jrow / LORA_BLOCK_ROWS), r = static_cast<int32_t>(jrow % LORA_BLOCK_ROWS);
+            uint4 *dst = reinterpret_cast<uint4 *>(a_arena + (static_cast<size_t>(blocks.b[t]) * LORA_BLOCK_ROWS + r) * K) + v;
+            *dst = jrow < rank ? reinterpret_cast<const uint4 *>(A + jrow * K)[v] : zero;
+        } else {
+            const int64_t w = i - a_work;
+            const int64_t n = w / b_row, c = w - n * b_row;  // c: vector of the slot's (padded) rank
+            const int32_t j0 = static_cast<int32_t>(c) * kVec;
+            const int32_t t = j0 / LORA_BLOCK_ROWS, jj = j0 % LORA_BLOCK_ROWS;
+            uint4 *dst = reinterpret_cast<uint4 *>(b_arena + (static_cast<size_t>(blocks.b[t]) * N + n) * LORA_BLOCK_ROWS + jj);
+            *dst = j0 < rank ? *reinterpret_cast<const uint4 *>(B + n * rank + j0) : zero;
+        }
+    }
+}
+
 cudaError_t launch_pool_scatter(const lora_pool *pool, int32_t rank, const int32_t *blocks,
                                 const void *A, const void *B, cudaStream_t stream) {
     const int nb = (rank + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
     ScatterBlocks sb;
     for (int t = 0; t < kMaxBlocksPerSlot; ++t) sb.b[t] = t < nb ? blocks[t] : 0;
     count_launches(1);
+    const lora_pool_desc_t &dd = pool->d;
+    const size_t eb = dd.dtype == LORA_FP32 ? 4 : 2;
+    if ((static_cast<size_t>(rank) * eb) % 16 == 0 && (static_cast<size_t>(dd.K) * eb) % 16 == 0) {
+        const int64_t work = static_cast<int64_t>(nb) * LORA_BLOCK_ROWS * (dd.K * static_cast<int64_t>(eb) / 16) +
+                             static_cast<int64_t>(dd.N) * nb * (LORA_BLOCK_ROWS * static_cast<int64_t>(eb) / 16);
+        int64_t grid = (work + 255) / 256;
+        const int64_t cap = 4L * device_sm_count();
+        grid = grid < 1 ? 1 : grid > cap ? cap : grid;
+        if (dd.dtype == LORA_FP32)
+            pool_scatter_vec_kernel<float><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+                static_cast<const float *>(A), static_cast<const float *>(B), rank, dd.K, dd.N,
+                static_cast<float *>(dd.a_arena), static_cast<float *>(dd.b_arena), sb);
+        else
+            pool_scatter_vec_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+                static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), rank, dd.K, dd.N,
+                static_cast<__nv_bfloat16 *>(dd.a_arena), static_cast<__nv_bfloat16 *>(dd.b_arena), sb);
+        return cudaGetLastError();
+    }
     dim3 grid(8, nb, LORA_BLOCK_ROWS);
     const lora_pool_desc_t &d = pool->d;
     if (d.dtype == LORA_FP32)

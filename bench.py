@@ -383,6 +383,43 @@ def time_device(case, wl, steps, warmup, flush, clocks_index):
             "launches": kernels_per_call * steps, "kernels_per_call": kernels_per_call, "clocks": clocks}
 
 
+def time_adapter_loads(wl, device, reps=8):
+    """Pool residency: time to load one adapter of the workload's largest
+    rank into a slot of its first projection's pool shape, by source --
+    staged pageable host memory (synchronous), page-locked host memory read
+    by the scatter kernel over the host link (asynchronous), and device
+    memory.  Each load is followed by an unload; times are medians."""
+    import torch
+    from adapter_gemm_linear_gb300 import LoraPool
+
+    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    K, N = wl.K, wl.projections[0].N
+    r = max(16, -(-int(wl.ranks.max()) // 16) * 16)
+    nbytes = r * (K + N) * (2 if wl.dtype == "bf16" else 4)
+    pool = LoraPool(K, N, 2, r, r // 16, dtype=td, device=device)
+    gen = torch.Generator().manual_seed(7)
+    A = (torch.randn(r, K, generator=gen) * 0.02).to(td)
+    B = (torch.randn(N, r, generator=gen) * 0.02).to(td)
+    srcs = {"host": (A, B), "mapped_host": (A.pin_memory(), B.pin_memory()),
+            "device": (A.to(device), B.to(device))}
+    out = {"rank": r, "bytes": nbytes}
+    stream = torch.cuda.current_stream()
+    for name, (a, b) in srcs.items():
+        ms = []
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            pool.load(0, a, b, float(2 * r), stream=stream, src=name.replace("_host", ""))
+            torch.cuda.synchronize()
+            ms.append((time.perf_counter() - t0) * 1e3)
+            pool.unload(0, stream=stream)
+        med = statistics.median(ms[1:])
+        out[name] = {"ms": round(med, 4), "gbs": round(nbytes / (med / 1e3) / 1e9, 2)}
+    torch.cuda.synchronize()
+    pool.close()
+    return out
+
+
 def time_e2e(case, wl, steps, flush, device):
     """Through the C ABI with pinned host buffers; copies inside each step."""
     import torch
@@ -473,6 +510,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     shrink_ms = sum(res["shrink_ms"])
     e2e_steps = max(3, min(steps, 200))
     e2e = time_e2e(case, wl, e2e_steps, flush, device)
+    loads = time_adapter_loads(wl, device) if world == 1 else None
     if world > 1:
         t = torch.tensor([total_ms, e2e["ms"]], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -549,6 +587,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         },
         "e2e": {"value": round(wl.M * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "adapter_load": loads,
         "gpu_launches": int(res["launches"]),
         "kernels_per_step": int(res["kernels_per_call"]),
         "eager": {"value": round(tokens / (sum(res["eager_ms"]) / 1e3), 1), "unit": "tokens/s",

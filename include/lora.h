@@ -124,16 +124,39 @@ lora_status_t lora_pool_destroy(lora_pool_t *pool);
  * last block, and writes the slot's table row, rank and scale.  The pages call
  * this activating an adapter into a GPU slot ("LoRA Adapters: Many Models
  * in One", §"Three tiers of storage"; "S-LoRA…", §"Unified paging").
- * src_on_device = 0: A and B are host memory; the call returns once the
- *   copies are done (A/B may be freed after it returns).
- * src_on_device = 1: A and B are device memory; the copy is a kernel on
- *   `stream`, so A/B must stay valid until `stream` reaches that point.
+ * src_on_device = LORA_SRC_HOST (0): A and B are host memory; the call
+ *   returns once the copies are done (A/B may be freed after it returns).
+ *   Where the device can address them (page-locked memory, or any memory on
+ *   a Grace system), the scatter kernel below reads them directly; else they
+ *   are staged block by block.
+ * src_on_device = LORA_SRC_DEVICE (1): A and B are device memory; the copy
+ *   is a kernel on `stream`, so A/B must stay valid until `stream` reaches
+ *   that point.
+ * src_on_device = LORA_SRC_MAPPED_HOST (2): A and B are page-locked host
+ *   memory mapped into the device address space (cudaHostAlloc, or
+ *   cudaHostRegister with cudaHostRegisterMapped; on a 64-bit system every
+ *   page-locked allocation is mapped).  The same kernel reads them straight
+ *   over the host link (NVLink-C2C on Grace systems), asynchronously on
+ *   `stream`: A/B must stay valid and unchanged until `stream` reaches it.
+ *   This is the application of adapter weights from host memory of "Adapter
+ *   Residency When One Replica Serves Many Fine-Tunes" (§"Residency: which
+ *   adapters stay loaded"), into the pool without a staging copy.  Host
+ *   memory the device cannot address is refused (INVALID_ARG) before any
+ *   access: page-locked memory always qualifies; where the GPU can address
+ *   pageable memory (address translation over NVLink-C2C on Grace), any
+ *   host memory does.
+ * A load counts as a use of the slot for lora_pool_evict_lru.
  * Errors: SLOT (out of range or already loaded), RANK, OUT_OF_BLOCKS,
- * INVALID_ARG, ALIGNMENT (device sources must be 16-byte aligned), CUDA.
+ * INVALID_ARG, ALIGNMENT (device and mapped sources must be 16-byte
+ * aligned), CUDA.
  */
 lora_status_t lora_pool_load_slot(lora_pool_t *pool, int32_t slot, int32_t rank,
                                   float alpha, const void *A, const void *B,
                                   int32_t src_on_device, void *stream);
+
+#define LORA_SRC_HOST 0
+#define LORA_SRC_DEVICE 1
+#define LORA_SRC_MAPPED_HOST 2
 
 /*
  * Empty slot `slot` and return its blocks to the free list.  The device
@@ -142,6 +165,33 @@ lora_status_t lora_pool_load_slot(lora_pool_t *pool, int32_t slot, int32_t rank,
  * is never torn out from under it.  Errors: SLOT (out of range or empty).
  */
 lora_status_t lora_pool_unload_slot(lora_pool_t *pool, int32_t slot, void *stream);
+
+/*
+ * Residency bookkeeping for a slot cache: LRU eviction ("Your LoRA Adapters
+ * Are Thrashing Your GPUs", §"Eviction: LRU by default, but routing makes it
+ * rare") that never evicts an adapter in use by in-flight requests ("Multi-
+ * LoRA Adapter Caching in Production…", §"Data Plane: Managing 'Where the
+ * Adapter Currently Is'").  All host-side:
+ * the library cannot see which slots a queued forward's row ids name, so the
+ * caller pins the slots of a batch before launching its forward and unpins
+ * them once the stream has passed it.
+ * lora_pool_touch: marks a loaded slot as used now (recency for LRU).
+ * lora_pool_pin / lora_pool_unpin: count in-flight uses of a loaded slot.
+ *   A pinned slot is never evicted, and lora_pool_unload_slot refuses it
+ *   (SLOT).  Unpinning a slot with no pins is an error (SLOT).
+ * lora_pool_evict_lru: unloads (as lora_pool_unload_slot, ordered on
+ *   `stream`) the loaded, unpinned slot used least recently, and returns it
+ *   in *slot (may be NULL).  SLOT if every loaded slot is pinned or none is
+ *   loaded.
+ * lora_pool_slot_use: *last_use (a pool-wide use counter, 0 if empty) and
+ *   *pins of a slot (either may be NULL).
+ */
+lora_status_t lora_pool_touch(lora_pool_t *pool, int32_t slot);
+lora_status_t lora_pool_pin(lora_pool_t *pool, int32_t slot);
+lora_status_t lora_pool_unpin(lora_pool_t *pool, int32_t slot);
+lora_status_t lora_pool_evict_lru(lora_pool_t *pool, void *stream, int32_t *slot);
+lora_status_t lora_pool_slot_use(const lora_pool_t *pool, int32_t slot, int64_t *last_use,
+                                 int32_t *pins);
 
 /* Host view of a slot: rank (0 if empty), scale, and its block ids
  * (`blocks` receives max_rank/16 entries, -1 where unused; may be NULL). */
