@@ -154,6 +154,47 @@ def test_integer_exact_many_tiles(shape):
     assert np.array_equal(got, want), f"{shape}: {np.sum(got != want)} outputs differ"
 
 
+@pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
+@pytest.mark.parametrize("shape", [
+    (64, 2048, (2048, 256, 256)),         # q, k, v with grouped-query k/v, sharing x
+    (200, 1024, (2752, 2752)),            # gate and up sharing x
+    (96, 5504, (1024,)),                  # down: K > N
+    (520, 2752, (1024, 1032, 264, 8)),    # four projections, large M (the other GEMM orientation)
+    (300, 8192, (1024, 8192)),            # 70B-shaped k/v and o widths at a prefill-ish M
+])
+def test_more_target_modules(shape, mode):
+    """Several target modules of one layer in one call (shared x and row ids,
+    one pool per projection), including K > N and widths down to 8."""
+    M, K, Ns = shape
+    wl = synth(M=M, K=K, Ns=list(Ns), num_slots=9, rank_choices=(8, 16, 64), seed=M + K + len(Ns), mode=mode)
+    pools = H.make_pools(wl, DEV)
+    outs = H.forward(wl, pools, mode)
+    rows = _sample_rows(wl, n=64) if M * K > 2_000_000 else np.arange(M)
+    for p in range(len(Ns)):
+        H.assert_close("bf16", outs[p][rows], H.oracle_rows(wl, p, rows), f"{shape} {mode} projection {p}")
+
+
+@pytest.mark.parametrize("case", ["all_base", "one_adapter", "all_max_rank"])
+def test_pipelined_grouped_edges(case):
+    """Edges of the pipelined grouped path (pools of max_rank <= 128, rows
+    too many for the per-row kernel): every row without an adapter (only
+    zero items); one adapter owning all 512 rows (32 chunks of one group);
+    every slot at rank 128 (eight rank blocks per item)."""
+    M, K, N = 512, 2056, 1032
+    if case == "all_base":
+        wl = synth(M=M, K=K, Ns=[N], num_slots=4, rank_choices=(128,), seed=71, none_frac=1.0)
+    elif case == "one_adapter":
+        wl = synth(M=M, K=K, Ns=[N], num_slots=1, rank_choices=(128,), seed=72, none_frac=0.0)
+    else:
+        wl = synth(M=M, K=K, Ns=[N], num_slots=12, rank_choices=(128,), seed=73, none_frac=0.05, zipf_s=1.2)
+    assert H.pool_max_rank(wl) == 128
+    pools = H.make_pools(wl, DEV, slots=list(range(wl.num_slots)))
+    out = H.forward(wl, pools, "bgmv")[0]
+    rows = _sample_rows(wl, n=96)
+    H.assert_close("bf16", out[rows], H.oracle_rows(wl, 0, rows), f"pipelined edge {case}")
+    assert not np.isnan(out).any()
+
+
 def test_tiny_fp32_full():
     wl = make_config("tiny_fp32")
     pools = H.make_pools(wl, DEV)
