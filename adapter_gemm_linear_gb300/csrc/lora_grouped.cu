@@ -465,10 +465,9 @@ expand_grouped_kernel(const GroupedExpandParams p) {
 //    A and B per row is cheap)
 // ---------------------------------------------------------------------------
 
-struct RowLoraParams {
-    int32_t M, N, K, ldx;
-    const __nv_bfloat16 *x;
-    const int32_t *row_slot;
+// One projection (its pool and correction array) of the per-row kernel.
+struct RowProj {
+    int32_t N;
     const __nv_bfloat16 *a_arena;
     const __nv_bfloat16 *b_arena;
     const int32_t *table;
@@ -476,10 +475,18 @@ struct RowLoraParams {
     const float *scales;
     int32_t max_slots, bps, num_blocks;
     int32_t cols_per_cta;  // output columns per CTA (a multiple of kRowThreads)
+    int32_t splits;        // column ranges: CTAs of blockIdx.y >= splits have no work
     float *ycorr;          // [M][N]
-    int32_t *counters;     // split-K tile counters of the GEMM that follows, zeroed here
+};
+
+struct RowLoraParams {
+    int32_t M, K, ldx;
+    const __nv_bfloat16 *x;
+    const int32_t *row_slot;
+    int32_t *counters;     // split-K tile counters of the GEMMs that follow, zeroed here
     int32_t n_counters;
     unsigned long long *status;
+    RowProj proj[LORA_MAX_PROJ];  // blockIdx.z selects one
 };
 
 // Four warps of at most 152 registers: a CTA fits on an SM beside a CTA of
@@ -496,7 +503,7 @@ constexpr int kRowCols = 8;   // output columns per thread whose B pieces are in
 // per step and the CTA sums the partial dot products) into shared memory, then
 // writes ycorr[m, n] = s_i <B_i[n, :], v> for its columns (zeros for a row
 // without an adapter).
-__global__ void __maxnreg__(kRowMaxRegs) lora_rows_kernel(const RowLoraParams p) {
+__global__ void __maxnreg__(kRowMaxRegs) lora_rows_kernel(const __grid_constant__ RowLoraParams p) {
     __shared__ float red[kRowThreads / 32][LORA_BLOCK_ROWS];
     extern __shared__ __align__(16) float v[];  // [max_rank]
     // the GEMM that follows may launch now; it reads ycorr only after this
@@ -504,19 +511,21 @@ __global__ void __maxnreg__(kRowMaxRegs) lora_rows_kernel(const RowLoraParams p)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t m = blockIdx.x;
-    if (m == 0 && blockIdx.y == 0)
+    if (m == 0 && blockIdx.y == 0 && blockIdx.z == 0)
         for (int32_t c = tid; c < p.n_counters; c += kRowThreads) p.counters[c] = 0;
-    const int32_t n_begin = blockIdx.y * p.cols_per_cta;
-    const int32_t n_end = min(p.N, n_begin + p.cols_per_cta);
+    const RowProj &q = p.proj[blockIdx.z];
+    if (static_cast<int32_t>(blockIdx.y) >= q.splits) return;
+    const int32_t n_begin = blockIdx.y * q.cols_per_cta;
+    const int32_t n_end = min(q.N, n_begin + q.cols_per_cta);
     int32_t r = 0;
     float sc = 0.0f;
-    int32_t slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &sc, p.status,
+    int32_t slot = resolve_slot(p.row_slot[m], m, q.ranks, q.scales, q.max_slots, q.bps, &r, &sc, p.status,
                                 blockIdx.y == 0 && tid == 0);
     const int32_t nblk = (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
-    const int32_t *trow = p.table + static_cast<size_t>(slot < 0 ? 0 : slot) * p.bps;
+    const int32_t *trow = q.table + static_cast<size_t>(slot < 0 ? 0 : slot) * q.bps;
     if (slot >= 0) {
         bool ok = true;
-        for (int32_t jb = 0; jb < nblk; ++jb) ok &= trow[jb] >= 0 && trow[jb] < p.num_blocks;
+        for (int32_t jb = 0; jb < nblk; ++jb) ok &= trow[jb] >= 0 && trow[jb] < q.num_blocks;
         if (!ok) {
             if (blockIdx.y == 0 && tid == 0) record_error(p.status, kDevBadBlock, static_cast<uint32_t>(slot));
             slot = -1;
@@ -527,16 +536,16 @@ __global__ void __maxnreg__(kRowMaxRegs) lora_rows_kernel(const RowLoraParams p)
         // of its B blocks head for L2 now, so that the loads below, issued a
         // few at a time, mostly hit it
         for (int32_t jb = 0; jb < nblk; ++jb) {
-            sm100::bulk_prefetch_l2(p.a_arena + static_cast<size_t>(trow[jb]) * LORA_BLOCK_ROWS * p.K,
+            sm100::bulk_prefetch_l2(q.a_arena + static_cast<size_t>(trow[jb]) * LORA_BLOCK_ROWS * p.K,
                                     static_cast<uint32_t>(LORA_BLOCK_ROWS) * p.K * 2u);
             if (n_end > n_begin)
                 sm100::bulk_prefetch_l2(
-                    p.b_arena + (static_cast<size_t>(trow[jb]) * p.N + n_begin) * LORA_BLOCK_ROWS,
+                    q.b_arena + (static_cast<size_t>(trow[jb]) * q.N + n_begin) * LORA_BLOCK_ROWS,
                     static_cast<uint32_t>(n_end - n_begin) * LORA_BLOCK_ROWS * 2u);
         }
         sm100::bulk_prefetch_l2(p.x + static_cast<size_t>(m) * p.ldx, static_cast<uint32_t>(p.K) * 2u);
     }
-    float *dst = p.ycorr + static_cast<size_t>(m) * p.N;
+    float *dst = q.ycorr + static_cast<size_t>(m) * q.N;
     if (slot < 0) {
         for (int32_t n = n_begin + tid; n < n_end; n += kRowThreads) dst[n] = 0.0f;
         return;
@@ -546,7 +555,7 @@ __global__ void __maxnreg__(kRowMaxRegs) lora_rows_kernel(const RowLoraParams p)
     const int32_t K8 = p.K / 8;
 #pragma unroll 1
     for (int32_t jb = 0; jb < nblk; ++jb) {
-        const uint4 *A = reinterpret_cast<const uint4 *>(p.a_arena + static_cast<size_t>(trow[jb]) * LORA_BLOCK_ROWS * p.K);
+        const uint4 *A = reinterpret_cast<const uint4 *>(q.a_arena + static_cast<size_t>(trow[jb]) * LORA_BLOCK_ROWS * p.K);
         float acc[LORA_BLOCK_ROWS];
 #pragma unroll
         for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = 0.0f;
@@ -605,7 +614,7 @@ __global__ void __maxnreg__(kRowMaxRegs) lora_rows_kernel(const RowLoraParams p)
         for (int c = 0; c < kRowCols; ++c) acc[c] = 0.0f;
 #pragma unroll 1
         for (int32_t jb = 0; jb < nblk; ++jb) {
-            const __nv_bfloat16 *bb = p.b_arena + static_cast<size_t>(trow[jb]) * p.N * LORA_BLOCK_ROWS;
+            const __nv_bfloat16 *bb = q.b_arena + static_cast<size_t>(trow[jb]) * q.N * LORA_BLOCK_ROWS;
             uint4 q[kRowCols][2];
 #pragma unroll
             for (int c = 0; c < kRowCols; ++c) {
@@ -663,35 +672,52 @@ bool row_lora_preferred(int32_t M, int32_t K, int32_t N, int32_t max_rank) {
     return bytes <= 256.0 * 1024 * 1024;
 }
 
-cudaError_t launch_lora_rows(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
+bool fuse_row_projections(int32_t M, int32_t K, int n, const int32_t *N, const int32_t *max_rank) {
+    // the paired GEMM launches take token tiles of 128 or 256 (M > 64)
+    if (n < 2 || M <= 64 || !plan_tc(M, N[0], K).swap) return false;
+    for (int i = 0; i < n; ++i)
+        if (!row_lora_preferred(M, K, N[i], max_rank[i])) return false;
+    return true;
+}
+
+// The per-row kernel over projections vs[0..n): grid (M, column splits, n).
+static cudaError_t launch_rows(const ForwardPlan &plan, const ProjView *const *vs, int n, cudaStream_t stream) {
     if (plan.M <= 0) return cudaSuccess;
-    RowLoraParams p;
+    if (n < 1 || n > LORA_MAX_PROJ) return cudaErrorInvalidValue;
+    RowLoraParams p = {};
     p.M = plan.M;
-    p.N = v.N;
     p.K = plan.K;
     p.ldx = plan.ldx;
     p.x = static_cast<const __nv_bfloat16 *>(plan.x);
     p.row_slot = plan.row_slot;
-    p.a_arena = static_cast<const __nv_bfloat16 *>(v.a_arena);
-    p.b_arena = static_cast<const __nv_bfloat16 *>(v.b_arena);
-    p.table = v.table;
-    p.ranks = v.ranks;
-    p.scales = v.scales;
-    p.max_slots = v.max_slots;
-    p.bps = v.bps;
-    p.num_blocks = v.num_blocks;
-    p.ycorr = plan.ycorr;
     p.counters = plan.counters;
     p.n_counters = plan.n_counters;
     p.status = plan.status;
-    // column splits: about one CTA per SM (each fits beside a GEMM CTA), at
-    // least kRowThreads columns per CTA
     const int sms = device_sm_count();
-    int splits = sms / plan.M;
-    const int max_splits = (v.N + kRowThreads - 1) / kRowThreads;
-    splits = splits < 1 ? 1 : splits > max_splits ? max_splits : splits;
-    p.cols_per_cta = ((v.N + splits - 1) / splits + kRowThreads - 1) / kRowThreads * kRowThreads;
-    splits = (v.N + p.cols_per_cta - 1) / p.cols_per_cta;
+    int max_splits = 1, max_rank = 0;
+    for (int i = 0; i < n; ++i) {
+        const ProjView &v = *vs[i];
+        RowProj &q = p.proj[i];
+        q.N = v.N;
+        q.a_arena = static_cast<const __nv_bfloat16 *>(v.a_arena);
+        q.b_arena = static_cast<const __nv_bfloat16 *>(v.b_arena);
+        q.table = v.table;
+        q.ranks = v.ranks;
+        q.scales = v.scales;
+        q.max_slots = v.max_slots;
+        q.bps = v.bps;
+        q.num_blocks = v.num_blocks;
+        q.ycorr = v.ycorr;
+        // column splits: about one CTA per SM (each fits beside a GEMM CTA),
+        // at least kRowThreads columns per CTA
+        int splits = sms / plan.M;
+        const int most = (v.N + kRowThreads - 1) / kRowThreads;
+        splits = splits < 1 ? 1 : splits > most ? most : splits;
+        q.cols_per_cta = ((v.N + splits - 1) / splits + kRowThreads - 1) / kRowThreads * kRowThreads;
+        q.splits = (v.N + q.cols_per_cta - 1) / q.cols_per_cta;
+        max_splits = q.splits > max_splits ? q.splits : max_splits;
+        max_rank = v.max_rank > max_rank ? v.max_rank : max_rank;
+    }
     {
         // run with the shared-memory carveout the GEMM needs, so that its CTAs
         // can be placed beside this kernel's (an SM changes its carveout only
@@ -709,8 +735,19 @@ cudaError_t launch_lora_rows(const ForwardPlan &plan, const ProjView &v, cudaStr
             }
         }
     }
-    lora_rows_kernel<<<dim3(plan.M, splits), kRowThreads, sizeof(float) * v.max_rank, stream>>>(p);
+    lora_rows_kernel<<<dim3(plan.M, max_splits, n), kRowThreads, sizeof(float) * max_rank, stream>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_lora_rows(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
+    const ProjView *vs[1] = {&v};
+    return launch_rows(plan, vs, 1, stream);
+}
+
+cudaError_t launch_lora_rows_all(const ForwardPlan &plan, cudaStream_t stream) {
+    const ProjView *vs[LORA_MAX_PROJ];
+    for (int i = 0; i < plan.n_proj && i < LORA_MAX_PROJ; ++i) vs[i] = &plan.proj[i];
+    return launch_rows(plan, vs, plan.n_proj, stream);
 }
 
 size_t group_table_ints(int32_t M) { return 7 * static_cast<size_t>(M) + 16; }
@@ -786,7 +823,7 @@ cudaError_t launch_expand_grouped(const ForwardPlan &plan, const ProjView &v, co
     p.ldv = v.max_rank;
     p.ksplit = plan.v_parts;
     p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
-    p.ycorr = plan.ycorr;
+    p.ycorr = v.ycorr;
     p.status = plan.status;
     // at most kExpRows * 1024 fp32 = 32 KiB: within the default dynamic shared memory
     const size_t smem = sizeof(float) * kExpRows * static_cast<size_t>(v.max_rank);

@@ -464,13 +464,33 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     // split-K scratch and the small-M orientation's correction array of the
     // tensor-core GEMM, shared by the projections (their kernels run one
     // after the other on the stream)
+    // With the fused per-row path every projection keeps its own correction
+    // array and each GEMM launch (two projections) its own tile counters.
     size_t part = 0, cnt = 0, ycorr = 0;
+    plan->fused_rows = false;
     if (a->dtype == LORA_BF16 && a->M > 0) {
+        int32_t Ns[LORA_MAX_PROJ], ranks[LORA_MAX_PROJ];
         for (int i = 0; i < a->n_proj; ++i) {
-            const lora::TcPlan tp = lora::plan_tc(a->M, a->proj[i].pool->d.N, a->K);
-            part = std::max(part, tp.part_bytes);
-            cnt = std::max(cnt, tp.counter_bytes);
-            if (tp.swap) ycorr = std::max(ycorr, sizeof(float) * static_cast<size_t>(a->M) * a->proj[i].pool->d.N);
+            Ns[i] = a->proj[i].pool->d.N;
+            ranks[i] = a->proj[i].pool->d.max_rank;
+        }
+        plan->fused_rows = lora::fuse_row_projections(a->M, a->K, a->n_proj, Ns, ranks);
+        if (plan->fused_rows) {
+            for (int i = 0; i < a->n_proj; i += 2) {
+                const lora::TcPlan tp = i + 1 < a->n_proj ? lora::plan_tc_pair(a->M, Ns[i], Ns[i + 1], a->K)
+                                                          : lora::plan_tc(a->M, Ns[i], a->K);
+                part = std::max(part, tp.part_bytes);
+                cnt += tp.counter_bytes;
+            }
+            for (int i = 0; i < a->n_proj; ++i)
+                ycorr += align_up(sizeof(float) * static_cast<size_t>(a->M) * Ns[i], 256);
+        } else {
+            for (int i = 0; i < a->n_proj; ++i) {
+                const lora::TcPlan tp = lora::plan_tc(a->M, Ns[i], a->K);
+                part = std::max(part, tp.part_bytes);
+                cnt = std::max(cnt, tp.counter_bytes);
+                if (tp.swap) ycorr = std::max(ycorr, sizeof(float) * static_cast<size_t>(a->M) * Ns[i]);
+            }
         }
     }
     ws->part_off = off;
@@ -532,6 +552,13 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
     for (int i = 0; i < plan.n_proj; ++i) plan.proj[i].V = reinterpret_cast<float *>(base + ws.v_off[i]);
     plan.part = reinterpret_cast<float *>(base + ws.part_off);
     plan.ycorr = reinterpret_cast<float *>(base + ws.ycorr_off);
+    {
+        size_t yoff = ws.ycorr_off;
+        for (int i = 0; i < plan.n_proj; ++i) {
+            plan.proj[i].ycorr = reinterpret_cast<float *>(base + (plan.fused_rows ? yoff : ws.ycorr_off));
+            yoff += align_up(sizeof(float) * static_cast<size_t>(plan.M) * plan.proj[i].N, 256);
+        }
+    }
     plan.group_table = reinterpret_cast<int32_t *>(base + ws.group_off);
     for (int i = 0; i < plan.n_proj; ++i) {
         if (plan.proj[i].ext_cols == 0) continue;

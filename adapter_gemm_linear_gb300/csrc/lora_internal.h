@@ -59,6 +59,7 @@ struct ProjView {
     const float *scales;
     int32_t max_slots, bps, num_blocks, max_rank;
     float *V;              // workspace: [v_parts][M][max_rank] fp32
+    float *ycorr;          // workspace: fp32 [M][N] LoRA correction of the small-M orientation
     // large M, LoRA term on the tensor cores (ext_cols > 0): the GEMM's K runs
     // on over [Vm_hi | Vm_lo] x [Bm | Bm]; slot s owns columns [s*max_rank, (s+1)*max_rank)
     int32_t ext_cols;      // columns of Bm = of each half of Vm (a multiple of 64), 0: not used
@@ -111,6 +112,10 @@ struct ForwardPlan {
     int32_t *counters;          // workspace: split-K tile counters, zeroed by the shrink
     int32_t n_counters;         // entries of `counters`
     int v_parts;                // K-slice planes of V the shrink writes
+    // small M, every projection's LoRA term by the per-row kernel: one launch
+    // of it for all projections (each its own ycorr), then the GEMMs two
+    // projections per launch (each launch its own split-K counters)
+    bool fused_rows;
 };
 
 // Count of kernels launched by the library (lora_kernel_launches).
@@ -169,6 +174,11 @@ int grouped_v_planes(int32_t K);
 // v = A_i x[m] in shared memory, then ycorr[m, :]); otherwise the grouped path.
 bool row_lora_preferred(int32_t M, int32_t K, int32_t N, int32_t max_rank);
 cudaError_t launch_lora_rows(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+// Whether a call of n projections (widths N, pool max ranks max_rank) takes
+// the fused per-row path (ForwardPlan::fused_rows).
+bool fuse_row_projections(int32_t M, int32_t K, int n, const int32_t *N, const int32_t *max_rank);
+// The per-row kernel over every projection of the plan in one launch.
+cudaError_t launch_lora_rows_all(const ForwardPlan &plan, cudaStream_t stream);
 size_t group_table_ints(int32_t M);
 GroupTable group_table_at(int32_t *base, int32_t M);
 cudaError_t launch_group_rows(const ForwardPlan &plan, const GroupTable &gt, int32_t max_slots, cudaStream_t stream);
@@ -187,5 +197,10 @@ cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaS
 // Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K);
 cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+// Swapped orientation: projections v0 and (if not NULL) v1 of the same x in
+// one launch, with its own split-K tile counters.
+TcPlan plan_tc_pair(int32_t M, int32_t N0, int32_t N1, int32_t K);
+cudaError_t launch_gemm_lora_tc_pair(const ForwardPlan &plan, const ProjView &v0, const ProjView *v1,
+                                     int32_t *counters, int64_t n_counters, cudaStream_t stream);
 
 }  // namespace lora

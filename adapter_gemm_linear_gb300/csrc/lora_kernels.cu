@@ -611,9 +611,44 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
 // per-row shrink, then the GEMM, whose epilogue applies the expand.  The GEMM
 // is launched as a programmatic dependent of the kernel before it (see
 // tc_gemm.cu).
+// Several projections, each's LoRA term by the per-row kernel: one launch of
+// it for all of them, then the GEMMs, two projections per launch, each launch
+// a programmatic dependent of the kernel before it and with its own split-K
+// tile counters (all zeroed by the per-row kernel).  Stage events: the LoRA
+// stage of projection 0 covers the per-row kernel, the GEMM stage of the
+// first of a pair covers the pair's launch; the other stages are empty.
+static cudaError_t launch_forward_fused_rows(const ForwardPlan &plan, cudaStream_t stream) {
+    auto record = [&](int i) -> cudaError_t {
+        return plan.stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[i]), stream)
+                                 : cudaSuccess;
+    };
+    cudaError_t e = launch_lora_rows_all(plan, stream);
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    if ((e = record(1)) != cudaSuccess) return e;
+    int64_t coff = 0;
+    for (int i = 0; i < plan.n_proj; i += 2) {
+        const bool pair = i + 1 < plan.n_proj;
+        if (i > 0 && (e = record(1 + 2 * i)) != cudaSuccess) return e;
+        const TcPlan tp = pair ? plan_tc_pair(plan.M, plan.proj[i].N, plan.proj[i + 1].N, plan.K)
+                               : plan_tc(plan.M, plan.proj[i].N, plan.K);
+        const int64_t ntiles = tp.splits > 1 ? static_cast<int64_t>(tp.tiles_a) * tp.tiles_b : 0;
+        if (coff + ntiles > plan.n_counters) return cudaErrorInvalidValue;
+        e = launch_gemm_lora_tc_pair(plan, plan.proj[i], pair ? &plan.proj[i + 1] : nullptr, plan.counters + coff,
+                                     plan.n_counters - coff, stream);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        coff += ntiles;
+        if ((e = record(2 + 2 * i)) != cudaSuccess) return e;
+        if (pair && ((e = record(3 + 2 * i)) != cudaSuccess || (e = record(4 + 2 * i)) != cudaSuccess)) return e;
+    }
+    return cudaSuccess;
+}
+
 static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t stream) {
     using T = __nv_bfloat16;
     const bool swapped = plan_tc(plan.M, plan.proj[0].N, plan.K).swap;
+    if (plan.fused_rows) return launch_forward_fused_rows(plan, stream);
     bool by_row = swapped;
     for (int p = 0; p < plan.n_proj; ++p)
         by_row = by_row && row_lora_preferred(plan.M, plan.K, plan.proj[p].N, plan.proj[p].max_rank);

@@ -992,7 +992,7 @@ cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaS
     p.ksplit = 1;  // as the shrink writes it
     p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.vslot_floats = kChunkRows * v.max_rank;
-    p.ycorr = plan.ycorr;
+    p.ycorr = v.ycorr;
     p.status = plan.status;
     const size_t vbytes = sizeof(float) * static_cast<size_t>(p.vslot_floats);
     const size_t room = kExpSmemMax - static_cast<size_t>(kExpStages) * kExpStageBytes;

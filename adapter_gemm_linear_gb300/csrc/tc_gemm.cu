@@ -96,6 +96,30 @@ struct TcParams {
     __nv_bfloat16 *vm_out;
     int32_t *counters;  // per tile, zero on entry (splits > 1)
     unsigned long long *status;
+    // swapped orientation, two projections of the same x in one launch: W
+    // tiles [0, tiles_a0) are the first projection's (tma_a; N, out, ldo,
+    // ycorr above), the rest the second's (tma_va; the fields below).  With
+    // one projection tiles_a0 = tiles_a.
+    int32_t tiles_a0;
+    int32_t N1, ldo1;
+    __nv_bfloat16 *out1;
+    const float *ycorr1;
+};
+
+// The projection of a swapped W tile (second: the launch's second
+// projection) and its fields; with one projection per launch (PAIR false)
+// these are the parameters themselves.
+template <bool PAIR>
+struct ProjTile {
+    const TcParams &p;
+    bool second;
+    int32_t ta;  // the tile's index within its projection
+    __device__ __forceinline__ ProjTile(const TcParams &p_, int32_t ta_)
+        : p(p_), second(PAIR && ta_ >= p_.tiles_a0), ta(PAIR && ta_ >= p_.tiles_a0 ? ta_ - p_.tiles_a0 : ta_) {}
+    __device__ __forceinline__ int32_t N() const { return PAIR && second ? p.N1 : p.N; }
+    __device__ __forceinline__ int32_t ldo() const { return PAIR && second ? p.ldo1 : p.ldo; }
+    __device__ __forceinline__ __nv_bfloat16 *out() const { return PAIR && second ? p.out1 : p.out; }
+    __device__ __forceinline__ const float *ycorr() const { return PAIR && second ? p.ycorr1 : p.ycorr; }
 };
 
 template <bool SWAP, int BN>
@@ -185,7 +209,7 @@ __device__ __forceinline__ int32_t next_unit(const TcParams &p, const int32_t *u
 // call).
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <bool SWAP, int BN>
+template <bool SWAP, int BN, bool PAIR = false>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUtensorMap *tma_b,
                                              const CUtensorMap *tma_va, const CUtensorMap *tma_vb,
                                              const TcParams &p, uint8_t *sA, uint8_t *sB,
@@ -203,6 +227,10 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
         const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
         const int32_t nmain = kb1 - kb0;
         int32_t ekb0 = 0, ekn = 0, total = nmain;
+        // swapped: the W tile's projection (its tensor map) and row
+        const bool second = SWAP && PAIR && w.ta >= p.tiles_a0;
+        const CUtensorMap *map_a = second ? tma_va : tma_a;
+        const int32_t row_a = (second ? w.ta - p.tiles_a0 : w.ta) * kBM;
         for (int32_t i = 0; i < total; ++i, ++it) {
             if (!SWAP && p.ext && i == nmain - 1) {
                 // with the unit's last main k-block next: Vm and the tile
@@ -221,7 +249,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
             mbar_arrive_expect_tx(&full[s], C::kABytes + C::kBBytes);
             if (i < nmain) {
                 const int32_t kb = kb0 + i;
-                tma_load_2d(sA + s * C::kABytes, tma_a, kb * kBK, w.ta * kBM, &full[s]);
+                tma_load_2d(sA + s * C::kABytes, map_a, kb * kBK, row_a, &full[s]);
                 tma_load_2d(sB + s * C::kBBytes, tma_b, kb * kBK, w.tb * BN, &full[s]);
             } else {
                 // LoRA extension: k-block e of the slot columns, hi half then lo half of Vm
@@ -384,7 +412,7 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
 // Epilogue warps: warp w (2..2+kEpiWarps-1) may access TMEM lane quarter
 // w % 4; the kEpiWarps / 4 warps sharing a quarter take turns over the
 // 32-column chunks.
-template <bool SWAP, int BN>
+template <bool SWAP, int BN, bool PAIR = false>
 __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_full, uint64_t *tmem_empty,
                                              uint32_t tmem_base, volatile uint32_t *abort_flag,
                                              volatile uint32_t *last_flag, const int32_t *unit_list) {
@@ -410,7 +438,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
         constexpr int kMyChunks = (kChunks + kGroups - 1) / kGroups;
         constexpr int kPre = kMyChunks <= 2 ? kMyChunks : 1;  // four chunks: one slot (registers)
         float yc[SWAP ? kPre : 1][32];
-        const int32_t n_sw = w.ta * kBM + q * 32 + lane;
+        const ProjTile<PAIR> pt(p, w.ta);
+        const int32_t n_sw = pt.ta * kBM + q * 32 + lane;
         if (SWAP && p.splits == 1) {
             grid_dependency_wait();  // ycorr comes from the expand kernel
 #pragma unroll
@@ -418,8 +447,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                 const int32_t m0 = w.tb * BN + (grp + ci * kGroups) * 32;
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                    yc[ci][e] = (n_sw < p.N && m0 + e < p.M && grp + ci * kGroups < kChunks)
-                                    ? __ldcg(p.ycorr + static_cast<size_t>(m0 + e) * p.N + n_sw)
+                    yc[ci][e] = (n_sw < pt.N() && m0 + e < p.M && grp + ci * kGroups < kChunks)
+                                    ? __ldcg(pt.ycorr() + static_cast<size_t>(m0 + e) * pt.N() + n_sw)
                                     : 0.0f;
             }
         }
@@ -433,8 +462,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
         const uint32_t col0 = lane_addr + b * BN;
 
         if (SWAP) {
-            const int32_t n = w.ta * kBM + q * 32 + lane;
-            const bool n_ok = n < p.N;
+            const int32_t n = pt.ta * kBM + q * 32 + lane;
+            const bool n_ok = n < pt.N();
             if (p.splits == 1) {
 #pragma unroll
                 for (int ci = 0; ci < kMyChunks; ++ci) {
@@ -450,15 +479,15 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                         const int32_t m2 = w.tb * BN + c2 * 32;
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            yc[ci % kPre][e] = (n_sw < p.N && m2 + e < p.M && c2 < kChunks)
-                                                   ? __ldcg(p.ycorr + static_cast<size_t>(m2 + e) * p.N + n_sw)
+                            yc[ci % kPre][e] = (n_sw < pt.N() && m2 + e < p.M && c2 < kChunks)
+                                                   ? __ldcg(pt.ycorr() + static_cast<size_t>(m2 + e) * pt.N() + n_sw)
                                                    : 0.0f;
                     }
                     if (n_ok) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             if (m0 + e < p.M)
-                                p.out[static_cast<size_t>(m0 + e) * p.ldo + n] = __float2bfloat16_rn(acc[e]);
+                                pt.out()[static_cast<size_t>(m0 + e) * pt.ldo() + n] = __float2bfloat16_rn(acc[e]);
                     }
                     __syncwarp();
                 }
@@ -502,7 +531,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                     const int32_t e_begin = w.ks * per;
                     const int32_t e_end = min(BN, e_begin + per);
                     const int n_local = et % kBM;
-                    const int32_t nn = w.ta * kBM + n_local;
+                    const int32_t nn = pt.ta * kBM + n_local;
                     const float *first = p.part + tile * kTileElems + n_local;
                     const size_t split_stride = tiles * kTileElems;
 #pragma unroll 1
@@ -512,8 +541,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                         for (int v = 0; v < 4; ++v) {
                             const int32_t e = e0 + v * (kEpiThreads / kBM);
                             const int32_t m = w.tb * BN + e;
-                            a[v] = (e < e_end && m < p.M && nn < p.N)
-                                       ? __ldcg(p.ycorr + static_cast<size_t>(m) * p.N + nn)
+                            a[v] = (e < e_end && m < p.M && nn < pt.N())
+                                       ? __ldcg(pt.ycorr() + static_cast<size_t>(m) * pt.N() + nn)
                                        : 0.0f;
                         }
 #pragma unroll 4
@@ -524,13 +553,13 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                                 if (e < e_end) a[v] += __ldcg(first + ks * split_stride + e * kBM);
                             }
                         }
-                        if (nn < p.N) {
+                        if (nn < pt.N()) {
 #pragma unroll
                             for (int v = 0; v < 4; ++v) {
                                 const int32_t e = e0 + v * (kEpiThreads / kBM);
                                 const int32_t m = w.tb * BN + e;
                                 if (e < e_end && m < p.M)
-                                    p.out[static_cast<size_t>(m) * p.ldo + nn] = __float2bfloat16_rn(a[v]);
+                                    pt.out()[static_cast<size_t>(m) * pt.ldo() + nn] = __float2bfloat16_rn(a[v]);
                             }
                         }
                     }
@@ -618,7 +647,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
 
 // --------------------------------------------------------------- kernel
 
-template <bool SWAP, int BN>
+template <bool SWAP, int BN, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                     const __grid_constant__ CUtensorMap tma_va, const __grid_constant__ CUtensorMap tma_vb,
@@ -710,12 +739,12 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
 
     if (warp == 0) {
         if (lane == 0)
-            run_producer<SWAP, BN>(&tma_a, &tma_b, &tma_va, &tma_vb, p, sA, sB, full, empty, abort_flag, unit_list);
+            run_producer<SWAP, BN, PAIR>(&tma_a, &tma_b, &tma_va, &tma_vb, p, sA, sB, full, empty, abort_flag, unit_list);
     } else if (warp == 1) {
         if (lane == 0)
             run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag, unit_list);
     } else {
-        run_epilogue<SWAP, BN>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, unit_list);
+        run_epilogue<SWAP, BN, PAIR>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, unit_list);
     }
 
     tc_fence_before_sync();
@@ -759,11 +788,15 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
 }
 
 
-template <bool SWAP, int BN>
+// v1: a second projection of the same x in the same launch (swapped
+// orientation only; tp plans both).  counters: the split-K tile counters of
+// this launch (NULL: the plan's).
+template <bool SWAP, int BN, bool PAIR = false>
 cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, cudaStream_t stream,
-                           bool vm_mode = false) {
+                           bool vm_mode = false, const ProjView *v1 = nullptr, int32_t *counters = nullptr,
+                           int64_t n_counters = 0) {
     using C = Cfg<SWAP, BN>;
-    auto kernel = tc_gemm_lora_kernel<SWAP, BN>;
+    auto kernel = tc_gemm_lora_kernel<SWAP, BN, PAIR>;
     static std::mutex mu;
     static bool done[128] = {};
     int dev = 0;
@@ -786,6 +819,10 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     // x, Bm beside W; unused maps are copies of the main ones
     CUtensorMap tva = tx, tvb = tw;
     const bool ext = !SWAP && !vm_mode && v.ext_cols > 0;
+    if (PAIR != (v1 != nullptr)) return cudaErrorInvalidValue;
+    if (v1) {  // the second projection's W in the slot of the extension's A-side map
+        if (!SWAP || vm_mode || !make_tmap_bf16(&tva, v1->W, v1->N, plan.K, plan.K, kBM)) return cudaErrorInvalidValue;
+    }
     if (ext) {
         if (!make_tmap_bf16(&tva, v.vm, plan.M, 2 * static_cast<uint64_t>(v.ext_cols), 2 * static_cast<uint64_t>(v.ext_cols), kBM) ||
             !make_tmap_bf16(&tvb, v.bm, v.N, v.ext_cols, v.ext_cols, BN))
@@ -816,19 +853,33 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.v_parts = plan.v_parts;
     p.v_part_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.part = plan.part;
-    p.ycorr = plan.ycorr;
+    p.ycorr = v.ycorr;
     p.ext = ext ? 1 : 0;
     p.ext_cols = v.ext_cols;
     p.ext_rank = v.max_rank;
     p.tile_range = v.tile_range;
     p.vm_mode = vm_mode ? 1 : 0;
     p.vm_out = vm_mode ? static_cast<__nv_bfloat16 *>(v.vm) : nullptr;
-    p.counters = plan.counters;
+    p.counters = counters ? counters : plan.counters;
+    if (!counters) n_counters = plan.n_counters;
     p.status = plan.status;
+    p.tiles_a0 = tp.tiles_a;
+    p.N1 = 0;
+    p.ldo1 = 0;
+    p.out1 = nullptr;
+    p.ycorr1 = nullptr;
+    if (v1) {
+        p.tiles_a0 = (v.N + kBM - 1) / kBM;
+        if (p.tiles_a0 + (v1->N + kBM - 1) / kBM != tp.tiles_a) return cudaErrorInvalidValue;
+        p.N1 = v1->N;
+        p.ldo1 = v1->ldo;
+        p.out1 = static_cast<__nv_bfloat16 *>(v1->out);
+        p.ycorr1 = v1->ycorr;
+    }
     // the splits of a tile wait for one another, so they must all be resident:
     // split-K needs every unit in the first wave of the grid
-    if (tp.splits > 1 && (!plan.part || !plan.counters || tp.units > tp.grid ||
-                          plan.n_counters < static_cast<int64_t>(tp.tiles_a) * tp.tiles_b))
+    if (tp.splits > 1 && (!plan.part || !p.counters || tp.units > tp.grid ||
+                          n_counters < static_cast<int64_t>(tp.tiles_a) * tp.tiles_b))
         return cudaErrorInvalidValue;
     // programmatic dependent of the shrink kernel before it on the stream:
     // the CTAs may start (and stream W and x) while the shrink finishes; the
@@ -861,6 +912,26 @@ int device_sm_count() {
     return cache[dev];
 }
 
+// Split-K of the swapped orientation: enough splits to give every SM a unit,
+// each at least four k-blocks long, at most 16.
+static void swapped_splits(TcPlan *t, int sms) {
+    const int tiles = t->tiles_a * t->tiles_b;
+    int s = tiles >= sms ? 1 : sms / tiles;
+    s = s < 1 ? 1 : s;
+    const int max_s = t->num_kb / 4 > 0 ? t->num_kb / 4 : 1;
+    if (s > max_s) s = max_s;
+    if (s > 16) s = 16;
+    t->kb_per_split = (t->num_kb + s - 1) / s;
+    t->splits = (t->num_kb + t->kb_per_split - 1) / t->kb_per_split;
+}
+
+static void finish_plan(TcPlan *t, int sms) {
+    t->units = t->tiles_a * t->tiles_b * t->splits;
+    t->grid = t->units < sms ? t->units : sms;
+    t->part_bytes = t->splits > 1 ? sizeof(float) * static_cast<size_t>(t->splits) * t->tiles_a * t->tiles_b * t->bn * kBM : 0;
+    t->counter_bytes = t->splits > 1 ? sizeof(int32_t) * static_cast<size_t>(t->tiles_a) * t->tiles_b : 0;
+}
+
 // Orientation, tile width and split-K factor for an M x N x K problem.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
     TcPlan t{};
@@ -875,14 +946,7 @@ TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
         t.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 256 ? 128 : 256;
         t.tiles_a = (N + kBM - 1) / kBM;
         t.tiles_b = (M + t.bn - 1) / t.bn;
-        const int tiles = t.tiles_a * t.tiles_b;
-        int s = tiles >= sms ? 1 : sms / tiles;
-        s = s < 1 ? 1 : s;
-        const int max_s = t.num_kb / 4 > 0 ? t.num_kb / 4 : 1;
-        if (s > max_s) s = max_s;
-        if (s > 16) s = 16;
-        t.kb_per_split = (t.num_kb + s - 1) / s;
-        t.splits = (t.num_kb + t.kb_per_split - 1) / t.kb_per_split;
+        swapped_splits(&t, sms);
     } else {
         t.tiles_a = (M + kBM - 1) / kBM;
         const long u256 = static_cast<long>(t.tiles_a) * ((N + 255) / 256);
@@ -894,10 +958,19 @@ TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
         t.splits = 1;
         t.kb_per_split = t.num_kb;
     }
-    t.units = t.tiles_a * t.tiles_b * t.splits;
-    t.grid = t.units < sms ? t.units : sms;
-    t.part_bytes = t.splits > 1 ? sizeof(float) * static_cast<size_t>(t.splits) * t.tiles_a * t.tiles_b * t.bn * kBM : 0;
-    t.counter_bytes = t.splits > 1 ? sizeof(int32_t) * static_cast<size_t>(t.tiles_a) * t.tiles_b : 0;
+    finish_plan(&t, sms);
+    return t;
+}
+
+// Two projections of one x in one swapped launch: their W tiles side by
+// side (M <= 512 only; swap is false otherwise).
+TcPlan plan_tc_pair(int32_t M, int32_t N0, int32_t N1, int32_t K) {
+    TcPlan t = plan_tc(M, N0, K);
+    if (!t.swap) return t;
+    const int sms = device_sm_count();
+    t.tiles_a = (N0 + kBM - 1) / kBM + (N1 + kBM - 1) / kBM;
+    swapped_splits(&t, sms);
+    finish_plan(&t, sms);
     return t;
 }
 
@@ -921,6 +994,25 @@ cudaError_t launch_gemm_vm(const ForwardPlan &plan, const ProjView &v, cudaStrea
     vv.out = nullptr;
     vv.ldo = v.ext_cols;
     return launch_variant<false, 64>(plan, vv, tp, stream, true);
+}
+
+cudaError_t launch_gemm_lora_tc_pair(const ForwardPlan &plan, const ProjView &v0, const ProjView *v1,
+                                     int32_t *counters, int64_t n_counters, cudaStream_t stream) {
+    const TcPlan tp = v1 ? plan_tc_pair(plan.M, v0.N, v1->N, plan.K) : plan_tc(plan.M, v0.N, plan.K);
+    if (!tp.swap) return cudaErrorInvalidValue;
+    // pairs: tiles of at least 128 tokens (the narrower variants keep their
+    // register count low enough to share an SM with the per-row kernel)
+    if (v1) {
+        if (tp.bn == 128) return launch_variant<true, 128, true>(plan, v0, tp, stream, false, v1, counters, n_counters);
+        if (tp.bn == 256) return launch_variant<true, 256, true>(plan, v0, tp, stream, false, v1, counters, n_counters);
+        return cudaErrorInvalidValue;
+    }
+    switch (tp.bn) {
+        case 32: return launch_variant<true, 32>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+        case 64: return launch_variant<true, 64>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+        case 128: return launch_variant<true, 128>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+        default: return launch_variant<true, 256>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+    }
 }
 
 cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
