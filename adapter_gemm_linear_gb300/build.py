@@ -65,8 +65,21 @@ def _compile(src: str, obj: str, extra_flags, verbose: bool) -> None:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if sources changed) and return the path of liblora.so."""
+    """Compile (if sources changed) and return the path of liblora.so.
+
+    Processes that build at once (the ranks of one job) take turns through a
+    lock file, so that none reads an object file another is writing."""
+    import fcntl
     os.makedirs(BUILD_DIR, exist_ok=True)
+    with open(os.path.join(BUILD_DIR, "build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(force, verbose, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(force: bool, verbose: bool, extra_flags) -> str:
     stamp = os.path.join(BUILD_DIR, "liblora.stamp")
     fp = _fingerprint(extra_flags)
     if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp):

@@ -23,7 +23,10 @@ are summed.  The dominant kernel's roofline uses stage events the library
 records around each kernel in an eager pass over the same K steps; the eager
 step rate is reported beside the graph one.  `e2e` repeats the measurement through the C ABI
 with pinned host buffers: the host->device copy of x and the row ids and the
-device->host copy of the outputs are inside each timed step.
+device->host copy of the outputs are inside each timed step, all on one
+stream of the caller's (not the legacy default stream).  The step is captured
+in a CUDA graph and replayed (`e2e.value`); issued from the host call by call
+it gives `e2e.eager_value`.
 
 --impl reference times the float64 CPU oracle on the host cores on a bounded
 row sample of the same workload (the reference arm of this comparison).
@@ -65,6 +68,8 @@ def parse_args():
                     help="workload name, or 'all' for one line per workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the oracle baseline")
+    ap.add_argument("--reference-seconds", type=float, default=90.0,
+                    help="oracle work of the whole --impl reference run")
     return ap.parse_args()
 
 
@@ -430,21 +435,50 @@ def time_e2e(case, wl, steps, flush, device):
     outs_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in case["outs"]]
     h2d = x_host.numel() * x_host.element_size() + (0 if ids_host is None else ids_host.numel() * 4)
     d2h = sum(o.numel() * o.element_size() for o in outs_host)
-    total_ms = 0.0
-    for i in range(steps):
-        flush.zero_()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
+
+    def step():
         case["x"].copy_(x_host, non_blocking=True)
         if ids_host is not None:
             case["ids"].copy_(ids_host, non_blocking=True)
         call()
         for o, oh in zip(case["outs"], outs_host):
             oh.copy_(o, non_blocking=True)
-        e.record()
-        e.synchronize()
-        total_ms += s.elapsed_time(e)
-    return {"ms": total_ms, "h2d": h2d, "d2h": d2h}
+
+    # a stream of the caller's own, as a serving loop would use (on the legacy
+    # default stream the GEMM could not start beside the LoRA kernel)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    eager_ms, graph_ms = 0.0, 0.0
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+        side.synchronize()
+        # eager: the copies and the forward call issued from the host every step
+        for i in range(steps):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(side)
+            step()
+            e.record(side)
+            e.synchronize()
+            eager_ms += s.elapsed_time(e)
+        # graph: the same step (both copies and the forward) captured once and
+        # replayed, as a decode loop replays its step
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            step()
+        g.replay()
+        side.synchronize()
+        for i in range(steps):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(side)
+            g.replay()
+            e.record(side)
+            e.synchronize()
+            graph_ms += s.elapsed_time(e)
+    torch.cuda.current_stream().wait_stream(side)
+    return {"ms": graph_ms, "eager_ms": eager_ms, "h2d": h2d, "d2h": d2h}
 
 
 def cpu_baseline(wl, seconds):
@@ -466,6 +500,35 @@ def cpu_baseline(wl, seconds):
     return {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} pass(es) of all {wl.M} rows x {len(wl.projections)} projection(s), "
                       f"float64 oracle, {cores} threads, {dt:.1f} s"}
+
+
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the default process group (a
+    job's time is its slowest rank's); the values themselves without one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def rank0_value(value, device):
+    """Rank 0's value on every rank (so that all ranks time the same number
+    of steps); the value itself without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.broadcast(t, src=0)
+    return type(value)(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units processed by all ranks per second, over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
 
 
 def run_gpu(cfg_name, args, rank, world, local_rank):
@@ -495,6 +558,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         steps = int(min(20000, max(50, 1.5 / max(per, 1e-6))))
     else:
         steps = args.steps
+    steps = rank0_value(steps, device)
     warmup = max(3, args.warmup)
     if world > 1:
         dist.barrier()
@@ -511,19 +575,13 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     e2e_steps = max(3, min(steps, 200))
     e2e = time_e2e(case, wl, e2e_steps, flush, device)
     loads = time_adapter_loads(wl, device) if world == 1 else None
-    if world > 1:
-        t = torch.tensor([total_ms, e2e["ms"]], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
-    else:
-        e2e_ms = e2e["ms"]
+    total_ms, e2e_ms, e2e_eager_ms = max_over_ranks([total_ms, e2e["ms"], e2e["eager_ms"]], device)
     if rank != 0:
         return None
 
     peaks, peak_src = load_peaks()
     alg = algorithmic(wl)
-    tokens = wl.M * steps * world
-    value = tokens / (total_ms / 1e3)
+    value = whole_job_rate(wl.M * steps, world, total_ms)
     # dominant stage: the GEMM or the LoRA kernels, by their share of the
     # eager stage time
     gemm_avg_s = gemm_ms / steps / 1e3
@@ -585,12 +643,14 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
             "gemm_tc_frac": round(alg["gemm_flops"] / gemm_avg_s / 1e12 / peaks["bf16_tflops"], 4),
             "gemm_hbm_frac": round(alg["gemm_bytes"] / gemm_avg_s / 1e9 / peaks["hbm_gbs"], 4),
         },
-        "e2e": {"value": round(wl.M * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "e2e": {"value": round(whole_job_rate(wl.M * e2e_steps, world, e2e_ms), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "launch": "CUDA graph of the step (copies and forward) replayed per step",
+                "eager_value": round(whole_job_rate(wl.M * e2e_steps, world, e2e_eager_ms), 1)},
         "adapter_load": loads,
         "gpu_launches": int(res["launches"]),
         "kernels_per_step": int(res["kernels_per_call"]),
-        "eager": {"value": round(tokens / (sum(res["eager_ms"]) / 1e3), 1), "unit": "tokens/s",
+        "eager": {"value": round(whole_job_rate(wl.M * steps, world, sum(res["eager_ms"])), 1), "unit": "tokens/s",
                   "ms_per_step": round(sum(res["eager_ms"]) / steps, 5)},
         "clocks": res["clocks"],
     }
@@ -617,7 +677,7 @@ def run_reference(cfg_name, args):
     for p in range(len(wl.projections)):
         oracle.workload_forward(wl, p, rows=[0], threads=1)
     row_s = max(time.perf_counter() - t, 1e-4)
-    budget = 90.0  # seconds of oracle work for the whole run
+    budget = args.reference_seconds  # seconds of oracle work for the whole run
     rows_per_step = int(max(1, min(wl.M, budget * cores / (steps + warmup) / row_s)))
     rng = np.random.default_rng(0)
 

@@ -1,0 +1,79 @@
+"""Host logic of bench.py's multi-process path, on CPU: two gloo ranks time
+rank 0's number of steps, a job's time is its slowest rank's, the whole-job
+rate counts every rank's units; under torchrun the reference arm prints one
+line from rank 0 and every rank exits 0."""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        steps = bench.rank0_value(100 + 7 * rank, "cpu")
+        times = bench.max_over_ranks([1.0 + rank, 5.0 - rank, 3.0], "cpu")
+        q.put((rank, steps, times))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_rank_reductions_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, steps, times in got:
+        assert steps == 100, (rank, steps)            # rank 0's step count everywhere
+        assert times == [2.0, 5.0, 3.0], (rank, times)  # each time's maximum over the ranks
+
+
+def test_whole_job_rate_counts_every_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    # 64 rows x 10 steps on each of 2 ranks in 1000 ms
+    assert bench.whole_job_rate(64 * 10, 2, 1000.0) == pytest.approx(1280.0)
+    assert bench.whole_job_rate(64 * 10, 1, 500.0) == pytest.approx(1280.0)
+    # no process group: the values come back unchanged
+    assert bench.max_over_ranks([1.5, 2.5], "cpu") == [1.5, 2.5]
+    assert bench.rank0_value(17, "cpu") == 17
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--reference-seconds", "2"]
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}

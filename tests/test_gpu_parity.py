@@ -154,25 +154,27 @@ def test_integer_exact_many_tiles(shape):
     assert np.array_equal(got, want), f"{shape}: {np.sum(got != want)} outputs differ"
 
 
+@pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
 @pytest.mark.parametrize("shape, launches", [
     ((128, 1024, (256, 512, 264)), 3),         # a pair and a single GEMM launch, both split-K (own tile counters)
     ((256, 2048, (1024, 1040, 512, 520)), 3),  # two pairs
     ((448, 512, (4096, 1024)), 2),             # a pair with 256-token tiles
 ])
-def test_fused_projection_launches(shape, launches):
+def test_fused_projection_launches(shape, launches, mode):
     """Several projections whose LoRA terms go through the per-row kernel:
     one launch of it for all of them, then the GEMMs two projections per
-    launch.  Integer inputs: every projection bit-exact."""
+    launch (SGMV adds the segments-to-rows kernel).  Integer inputs: every
+    projection bit-exact."""
     from adapter_gemm_linear_gb300 import kernel_launches
     M, K, Ns = shape
     wl = synth(M=M, K=K, Ns=list(Ns), num_slots=7, rank_choices=(8, 16), integer=True, seed=M + K + len(Ns),
                none_frac=0.1)
     pools = H.make_pools(wl, DEV)
-    H.forward(wl, pools, "bgmv")
+    H.forward(wl, pools, mode)
     torch.cuda.synchronize()
     before = kernel_launches()
-    outs = H.forward(wl, pools, "bgmv")
-    assert kernel_launches() - before == launches
+    outs = H.forward(wl, pools, mode)
+    assert kernel_launches() - before == launches + (1 if mode == "sgmv" else 0)
     for p in range(len(Ns)):
         want = H.oracle_bf16_bits(H.oracle_rows(wl, p))
         got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
