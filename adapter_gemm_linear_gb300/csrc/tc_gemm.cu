@@ -136,6 +136,9 @@ struct Cfg {
                                     (2 * kStages + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kStages >= 2, "ring too small");
+    // swapped with a deep ring (narrow token tiles): k-blocks whose loads are
+    // issued together
+    static constexpr int kLoadGroup = SWAP && kStages >= 8 ? 2 : 1;
 };
 
 struct Unit {
@@ -238,6 +241,18 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                 grid_dependency_wait();
                 ext_kblocks(p, w.ta, &ekb0, &ekn);
                 total = nmain + 2 * ekn;
+            }
+            if (C::kLoadGroup > 1 && i % C::kLoadGroup == 0) {
+                // wait until the next kLoadGroup stages are all free,
+                // so that their W boxes (adjacent 128-byte pieces of the same
+                // 128 rows) reach memory together
+                for (int32_t j = 1; j < C::kLoadGroup && i + j < total; ++j) {
+                    const int s2 = (it + j) % C::kStages;
+                    if (!mbar_wait_bounded(&empty[s2], (((it + j) / C::kStages) & 1) ^ 1, kWaitLimitNs)) {
+                        record_error(p.status, kDevTimeout, 1);
+                        *abort_flag = 1;
+                    }
+                }
             }
             const int s = it % C::kStages;
             const uint32_t ph = (it / C::kStages) & 1;
