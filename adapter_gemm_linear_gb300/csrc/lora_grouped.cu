@@ -498,7 +498,8 @@ constexpr int kRowMaxRegs = 152;
 constexpr int kRowBatch = 1;  // k steps of A loads in flight per thread
 constexpr int kRowCols = 8;   // output columns per thread whose B pieces are in flight together
 
-// grid (M, column splits).  The CTA resolves its row's adapter, computes
+// grid (M, column splits, projections).  The CTA resolves its row's adapter
+// in the pool of projection blockIdx.z, computes
 // v = A_i x[m] (all rank blocks; per block every thread takes 8 consecutive k
 // per step and the CTA sums the partial dot products) into shared memory, then
 // writes ycorr[m, n] = s_i <B_i[n, :], v> for its columns (zeros for a row
