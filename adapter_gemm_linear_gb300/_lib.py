@@ -35,6 +35,7 @@ STATUS = {v: k for k, v in STATUS_NAMES.items()}
 
 LORA_BF16 = 0
 LORA_FP32 = 1
+ABI_VERSION = 3  # include/lora.h LORA_ABI_VERSION
 
 
 class PoolDesc(ctypes.Structure):
@@ -60,6 +61,7 @@ class Proj(ctypes.Structure):
         ("pool", ctypes.c_void_p),
         ("out", ctypes.c_void_p),
         ("ldo", ctypes.c_int32),
+        ("w_scale", ctypes.c_void_p),
     ]
 
 
@@ -145,5 +147,7 @@ def lib():
                 fn = getattr(L, name)
                 fn.restype = res
                 fn.argtypes = args
+            if L.lora_abi_version() != ABI_VERSION:  # the structs below follow this version's layout
+                raise RuntimeError(f"{path} has ABI {L.lora_abi_version()}, this binding {ABI_VERSION}; rebuild it")
             _lib = L
     return _lib

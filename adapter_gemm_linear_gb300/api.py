@@ -219,6 +219,28 @@ def segment_rows(ids, num_slots: int) -> Tuple[np.ndarray, np.ndarray, np.ndarra
     return perm[:M].copy(), offs[:S + 1].copy(), adp[:S].copy()
 
 
+class Int8Weight:
+    """A quantized base weight: W[n][k] = q[n][k] * scale[n] (int8 q [N][K]
+    row-major, fp32 scale [N]), dequantized inside the GEMM; the adapters
+    stay 16-bit ("Your LoRA Adapters Are Thrashing Your GPUs", §02
+    "Numerical precision: FP16 adapters on INT4 base models")."""
+
+    def __init__(self, q: torch.Tensor, scale: torch.Tensor):
+        if q.dtype != torch.int8 or q.dim() != 2 or not q.is_contiguous():
+            raise ValueError("q must be a contiguous int8 [N][K] tensor")
+        if scale.dtype != torch.float32 or scale.shape != (q.shape[0],) or not scale.is_contiguous():
+            raise ValueError("scale must be a contiguous float32 [N] tensor")
+        self.q, self.scale = q, scale
+
+    @staticmethod
+    def quantize(W: torch.Tensor) -> "Int8Weight":
+        """Symmetric per-row int8 of a float weight: scale = max|W[n]| / 127."""
+        Wf = W.float()
+        scale = (Wf.abs().amax(dim=1) / 127.0).clamp_min(torch.finfo(torch.float32).tiny)
+        q = torch.round(Wf / scale[:, None]).clamp_(-127, 127).to(torch.int8)
+        return Int8Weight(q.contiguous(), scale.contiguous())
+
+
 class LinearCall:
     """Prepared arguments of one lora_linear_forward call.
 
@@ -243,8 +265,12 @@ class LinearCall:
             if out.dim() != 2 or (out.numel() > 0 and out.stride(1) != 1):
                 raise ValueError("out must be a row-major 2-D tensor")
             ldo = int(out.stride(0)) if out.numel() > 0 else int(out.shape[1])
-            projs[i] = _lib.Proj(_ptr(W), pool.handle, _ptr(out), ldo)
-            self._keep += [W, pool, out]
+            if isinstance(W, Int8Weight):
+                projs[i] = _lib.Proj(_ptr(W.q), pool.handle, _ptr(out), ldo, _ptr(W.scale))
+                self._keep += [W.q, W.scale, pool, out]
+            else:
+                projs[i] = _lib.Proj(_ptr(W), pool.handle, _ptr(out), ldo, None)
+                self._keep += [W, pool, out]
         self._projs = projs
         for t in (row_adapter, seg_offsets, seg_adapter, perm):
             if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):

@@ -430,8 +430,14 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
             if (!pj.W || !pj.out) return LORA_ERR_INVALID_ARG;
             if (!aligned16(pj.W) || !aligned16(pj.out)) return LORA_ERR_ALIGNMENT;
         }
+        if (pj.w_scale) {  // int8 base weights: bf16 x, the decode orientation
+            if (a->dtype != LORA_BF16 || a->M > lora::kQuantMaxRows) return LORA_ERR_UNSUPPORTED;
+            if (a->K % 16) return LORA_ERR_ALIGNMENT;
+            if (!aligned16(pj.w_scale)) return LORA_ERR_ALIGNMENT;
+        }
         lora::ProjView &v = plan->proj[i];
         v.W = pj.W;
+        v.w_scale = pj.w_scale;
         v.out = pj.out;
         v.N = d.N;
         v.ldo = pj.ldo;

@@ -51,6 +51,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Per-projection view handed to the kernel launchers.
 struct ProjView {
     const void *W;
+    const float *w_scale;  // NULL, or W is int8 with these per-row scales
     void *out;
     int32_t N, ldo;
     const void *a_arena, *b_arena;
@@ -96,6 +97,7 @@ constexpr int kGroupedMaxRows = 2048;  // rows the group table is built for (sha
 constexpr int kMaxVPlanes = 4;         // K slices of the grouped shrink
 constexpr int kPipeMaxRows = 512;      // rows the pipelined grouped kernels sort in shared memory
 constexpr int kPipeMaxRank = 128;      // pool max_rank of the pipelined grouped kernels
+constexpr int kQuantMaxRows = 64;      // int8 base weights: rows of x (token tiles of 32 or 64)
 
 struct ForwardPlan {
     lora_dtype_t dtype;

@@ -104,6 +104,8 @@ struct TcParams {
     int32_t N1, ldo1;
     __nv_bfloat16 *out1;
     const float *ycorr1;
+    // int8 base weights (QUANT variants): W[n][k] = q[n][k] * w_scale[n]
+    const float *w_scale;
 };
 
 // The projection of a swapped W tile (second: the launch's second
@@ -122,18 +124,21 @@ struct ProjTile {
     __device__ __forceinline__ const float *ycorr() const { return PAIR && second ? p.ycorr1 : p.ycorr; }
 };
 
-template <bool SWAP, int BN>
+// QUANT (swapped only): W arrives as int8 in a staging tile of its own and
+// is converted to the bf16 A tile in shared memory before the MMAs read it.
+template <bool SWAP, int BN, bool QUANT = false>
 struct Cfg {
     static constexpr uint32_t kABytes = kBM * kBK * 2;
     static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr uint32_t kQBytes = QUANT ? kBM * kBK : 0;  // int8 W staging
     // ring + barriers + TMEM address + flags + unit list + alignment slack
-    static constexpr int kFixed = 1024 + (2 * 12 + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
-    static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes);
+    static constexpr int kFixed = 1024 + (3 * 12 + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
+    static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes + kQBytes);
     static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
     static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                         : 2 * BN <= 256 ? 256 : 512;
-    static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) +
-                                    (2 * kStages + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
+    static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + kQBytes) +
+                                    ((QUANT ? 3 : 2) * kStages + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kStages >= 2, "ring too small");
     // swapped with a deep ring (narrow token tiles): k-blocks whose loads are
@@ -171,6 +176,15 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
         w.tb = r / p.tiles_a;
     }
     return w;
+}
+
+// Bytes `sh` and `sh` + 1 of w as signed int8, converted exactly to a bf16
+// pair (the low half takes byte sh): |v| <= 128 fits bf16's 8-bit mantissa,
+// so the upper half of the float is the value.
+__device__ __forceinline__ uint32_t int8x2_to_bf16x2(uint32_t w, int sh) {
+    const int lo = static_cast<int8_t>(static_cast<uint8_t>(w >> (8 * sh)));
+    const int hi = static_cast<int8_t>(static_cast<uint8_t>(w >> (8 * sh + 8)));
+    return (__float_as_uint(static_cast<float>(lo)) >> 16) | (__float_as_uint(static_cast<float>(hi)) & 0xFFFF0000u);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -212,14 +226,14 @@ __device__ __forceinline__ int32_t next_unit(const TcParams &p, const int32_t *u
 // call).
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <bool SWAP, int BN, bool PAIR = false>
+template <bool SWAP, int BN, bool PAIR = false, bool QUANT = false>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUtensorMap *tma_b,
                                              const CUtensorMap *tma_va, const CUtensorMap *tma_vb,
-                                             const TcParams &p, uint8_t *sA, uint8_t *sB,
+                                             const TcParams &p, uint8_t *sA, uint8_t *sB, uint8_t *sQ,
                                              uint64_t *full, uint64_t *empty,
                                              volatile uint32_t *abort_flag, const int32_t *unit_list) {
     using namespace sm100;
-    using C = Cfg<SWAP, BN>;
+    using C = Cfg<SWAP, BN, QUANT>;
     int32_t it = 0;
     if (p.vm_mode) grid_dependency_wait();  // A_dense comes from the kernel before
     for (int32_t idx = 0;; ++idx) {
@@ -261,10 +275,13 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                 *abort_flag = 1;
             }
             if (*abort_flag) return;
-            mbar_arrive_expect_tx(&full[s], C::kABytes + C::kBBytes);
+            mbar_arrive_expect_tx(&full[s], (QUANT ? C::kQBytes : C::kABytes) + C::kBBytes);
             if (i < nmain) {
                 const int32_t kb = kb0 + i;
-                tma_load_2d(sA + s * C::kABytes, map_a, kb * kBK, row_a, &full[s]);
+                if (QUANT)  // int8 W into the staging tile; the epilogue warps convert it
+                    tma_load_2d(sQ + s * C::kQBytes, map_a, kb * kBK, row_a, &full[s]);
+                else
+                    tma_load_2d(sA + s * C::kABytes, map_a, kb * kBK, row_a, &full[s]);
                 tma_load_2d(sB + s * C::kBBytes, tma_b, kb * kBK, w.tb * BN, &full[s]);
             } else {
                 // LoRA extension: k-block e of the slot columns, hi half then lo half of Vm
@@ -279,13 +296,13 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
 
 // --------------------------------------------------------------- MMA issuer
 
-template <bool SWAP, int BN>
+template <bool SWAP, int BN, bool QUANT = false>
 __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
                                         uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
                                         uint32_t tmem_base, volatile uint32_t *abort_flag,
                                         const int32_t *unit_list) {
     using namespace sm100;
-    using C = Cfg<SWAP, BN>;
+    using C = Cfg<SWAP, BN, QUANT>;
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
     int32_t it = 0, t = 0;
     for (int32_t idx = 0;; ++idx) {
@@ -427,11 +444,13 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
 // Epilogue warps: warp w (2..2+kEpiWarps-1) may access TMEM lane quarter
 // w % 4; the kEpiWarps / 4 warps sharing a quarter take turns over the
 // 32-column chunks.
-template <bool SWAP, int BN, bool PAIR = false>
-__device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_full, uint64_t *tmem_empty,
+template <bool SWAP, int BN, bool PAIR = false, bool QUANT = false>
+__device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, const uint8_t *sQ, uint64_t *full,
+                                             uint64_t *conv, uint64_t *tmem_full, uint64_t *tmem_empty,
                                              uint32_t tmem_base, volatile uint32_t *abort_flag,
                                              volatile uint32_t *last_flag, const int32_t *unit_list) {
     using namespace sm100;
+    using C = Cfg<SWAP, BN, QUANT>;
     constexpr int kGroups = kEpiWarps / 4;
     constexpr int kChunks = BN / 32;
     const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
@@ -440,11 +459,44 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
     const int grp = (warp - 2) >> 2;  // which of the warps sharing the quarter
     const int lane = threadIdx.x & 31;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    int32_t t = 0;
+    int32_t t = 0, cit = 0;
     for (int32_t idx = 0;; ++idx) {
         const int32_t u = next_unit(p, unit_list, idx);
         if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
+        if (QUANT) {
+            // the unit's k-blocks as they land: the int8 W staging tile into
+            // the bf16 A tile, laid out as a TMA load with the 128-byte
+            // swizzle leaves it (16-byte chunk c of row r at chunk c ^ (r % 8)).
+            // Thread et converts half hh of row r's 64 values.
+            const int32_t kb0 = w.ks * p.kb_per_split;
+            const int32_t nk = min(kb0 + p.kb_per_split, p.num_kb) - kb0;
+            const int r = et >> 1, hh = et & 1;
+            for (int32_t i = 0; i < nk; ++i, ++cit) {
+                const int s = cit % C::kStages;
+                if (!mbar_wait_bounded(&full[s], (cit / C::kStages) & 1, kWaitLimitNs)) {
+                    record_error(p.status, kDevTimeout, 6);
+                    *abort_flag = 1;
+                    break;  // without arriving: the MMA gives up too
+                }
+                const uint4 *src = reinterpret_cast<const uint4 *>(sQ + s * C::kQBytes + r * kBK + hh * 32);
+                const uint4 q0 = src[0], q1 = src[1];
+                const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                uint8_t *row = sA + s * C::kABytes + r * (kBK * 2);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 o;
+                    o.x = int8x2_to_bf16x2(wd[2 * c], 0);
+                    o.y = int8x2_to_bf16x2(wd[2 * c], 2);
+                    o.z = int8x2_to_bf16x2(wd[2 * c + 1], 0);
+                    o.w = int8x2_to_bf16x2(wd[2 * c + 1], 2);
+                    *reinterpret_cast<uint4 *>(row + (((4 * hh + c) ^ (r & 7)) << 4)) = o;
+                }
+                fence_proxy_async_shared();  // the MMAs read the tile through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&conv[s]);
+            }
+        }
         const int b = t & 1;
         // swapped, one split: this thread's correction values (rows of its
         // 32-token chunks, its column) are fetched while the MMAs finish --
@@ -487,8 +539,14 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                     float acc[32];
                     load_tmem_chunk(col0 + c * 32, acc);
                     const int32_t m0 = w.tb * BN + c * 32;
+                    if (QUANT) {  // the int8 W row's scale
+                        const float wsc = n_ok ? __ldg(p.w_scale + n) : 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[e] += yc[ci % kPre][e];
+                        for (int e = 0; e < 32; ++e) acc[e] = fmaf(acc[e], wsc, yc[ci % kPre][e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[e] += yc[ci % kPre][e];
+                    }
                     if (ci + kPre < kMyChunks) {
                         const int c2 = grp + (ci + kPre) * kGroups;
                         const int32_t m2 = w.tb * BN + c2 * 32;
@@ -560,14 +618,19 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
                                        ? __ldcg(pt.ycorr() + static_cast<size_t>(m) * pt.N() + nn)
                                        : 0.0f;
                         }
+                        float sp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
                         for (int32_t ks = 0; ks < p.splits; ++ks) {
 #pragma unroll
                             for (int v = 0; v < 4; ++v) {
                                 const int32_t e = e0 + v * (kEpiThreads / kBM);
-                                if (e < e_end) a[v] += __ldcg(first + ks * split_stride + e * kBM);
+                                if (e < e_end) sp[v] += __ldcg(first + ks * split_stride + e * kBM);
                             }
                         }
+                        // the int8 W row's scale multiplies the base sum only
+                        const float wsc = QUANT ? (nn < pt.N() ? __ldg(p.w_scale + nn) : 0.0f) : 1.0f;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) a[v] = QUANT ? fmaf(sp[v], wsc, a[v]) : a[v] + sp[v];
                         if (nn < pt.N()) {
 #pragma unroll
                             for (int v = 0; v < 4; ++v) {
@@ -662,21 +725,23 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint64_t *tmem_f
 
 // --------------------------------------------------------------- kernel
 
-template <bool SWAP, int BN, bool PAIR = false>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool SWAP, int BN, bool PAIR = false, bool QUANT = false>
+__global__ void __maxnreg__(SWAP && BN <= 64 ? 120 : 168)
 tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                     const __grid_constant__ CUtensorMap tma_va, const __grid_constant__ CUtensorMap tma_vb,
                     const TcParams p) {
     using namespace sm100;
-    using C = Cfg<SWAP, BN>;
+    using C = Cfg<SWAP, BN, QUANT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::kStages * C::kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes);
+    uint8_t *sQ = sB + C::kStages * C::kBBytes;  // QUANT: int8 W staging
+    uint64_t *full = reinterpret_cast<uint64_t *>(sQ + C::kStages * C::kQBytes);
     uint64_t *empty = full + C::kStages;
-    uint64_t *tmem_full = empty + C::kStages;   // [2]
+    uint64_t *conv = empty + C::kStages;        // QUANT: the A tile is converted
+    uint64_t *tmem_full = conv + (QUANT ? C::kStages : 0);   // [2]
     uint64_t *tmem_empty = tmem_full + 2;       // [2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
@@ -689,6 +754,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            if (QUANT) mbar_init(&conv[s], kEpiWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tmem_full[b], 1);
@@ -754,12 +820,16 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
 
     if (warp == 0) {
         if (lane == 0)
-            run_producer<SWAP, BN, PAIR>(&tma_a, &tma_b, &tma_va, &tma_vb, p, sA, sB, full, empty, abort_flag, unit_list);
+            run_producer<SWAP, BN, PAIR, QUANT>(&tma_a, &tma_b, &tma_va, &tma_vb, p, sA, sB, sQ, full, empty,
+                                                abort_flag, unit_list);
     } else if (warp == 1) {
         if (lane == 0)
-            run_mma<SWAP, BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag, unit_list);
+            // with int8 W the MMAs wait for the converted tile, not the load
+            run_mma<SWAP, BN, QUANT>(p, sA, sB, QUANT ? conv : full, empty, tmem_full, tmem_empty, tmem_base,
+                                     abort_flag, unit_list);
     } else {
-        run_epilogue<SWAP, BN, PAIR>(p, tmem_full, tmem_empty, tmem_base, abort_flag, last_flag, unit_list);
+        run_epilogue<SWAP, BN, PAIR, QUANT>(p, sA, sQ, full, conv, tmem_full, tmem_empty, tmem_base, abort_flag,
+                                            last_flag, unit_list);
     }
 
     tc_fence_before_sync();
@@ -803,15 +873,30 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
 }
 
 
+// Row-major int8 matrix [rows][cols] (row stride `cols` bytes, a multiple of
+// 16) in boxes of box_rows x 64 without swizzle; out-of-range elements read
+// as zero.
+bool make_tmap_i8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // v1: a second projection of the same x in the same launch (swapped
 // orientation only; tp plans both).  counters: the split-K tile counters of
 // this launch (NULL: the plan's).
-template <bool SWAP, int BN, bool PAIR = false>
+template <bool SWAP, int BN, bool PAIR = false, bool QUANT = false>
 cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, cudaStream_t stream,
                            bool vm_mode = false, const ProjView *v1 = nullptr, int32_t *counters = nullptr,
                            int64_t n_counters = 0) {
-    using C = Cfg<SWAP, BN>;
-    auto kernel = tc_gemm_lora_kernel<SWAP, BN, PAIR>;
+    using C = Cfg<SWAP, BN, QUANT>;
+    auto kernel = tc_gemm_lora_kernel<SWAP, BN, PAIR, QUANT>;
     static std::mutex mu;
     static bool done[128] = {};
     int dev = 0;
@@ -829,7 +914,12 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     }
     CUtensorMap tx, tw;
     if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, SWAP ? BN : kBM)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, SWAP ? kBM : BN)) return cudaErrorInvalidValue;
+    if (QUANT != (v.w_scale != nullptr) || (QUANT && (!SWAP || PAIR || vm_mode))) return cudaErrorInvalidValue;
+    if (QUANT) {
+        if (!make_tmap_i8(&tw, v.W, v.N, plan.K, kBM)) return cudaErrorInvalidValue;
+    } else if (!make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, SWAP ? kBM : BN)) {
+        return cudaErrorInvalidValue;
+    }
     // LoRA extension operands (non-swapped orientation): [Vm_hi | Vm_lo] beside
     // x, Bm beside W; unused maps are copies of the main ones
     CUtensorMap tva = tx, tvb = tw;
@@ -878,6 +968,7 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.counters = counters ? counters : plan.counters;
     if (!counters) n_counters = plan.n_counters;
     p.status = plan.status;
+    p.w_scale = v.w_scale;
     p.tiles_a0 = tp.tiles_a;
     p.N1 = 0;
     p.ldo1 = 0;
@@ -1005,6 +1096,7 @@ cudaError_t launch_gemm_vm(const ForwardPlan &plan, const ProjView &v, cudaStrea
     tp.grid = tp.units < sms ? tp.units : sms;
     ProjView vv = v;
     vv.W = v.adense;
+    vv.w_scale = nullptr;
     vv.N = v.ext_cols;
     vv.out = nullptr;
     vv.ldo = v.ext_cols;
@@ -1015,6 +1107,14 @@ cudaError_t launch_gemm_lora_tc_pair(const ForwardPlan &plan, const ProjView &v0
                                      int32_t *counters, int64_t n_counters, cudaStream_t stream) {
     const TcPlan tp = v1 ? plan_tc_pair(plan.M, v0.N, v1->N, plan.K) : plan_tc(plan.M, v0.N, plan.K);
     if (!tp.swap) return cudaErrorInvalidValue;
+    if (v0.w_scale || (v1 && v1->w_scale)) {  // int8 W: one projection, token tiles of 32 or 64
+        if (v1) return cudaErrorInvalidValue;
+        if (tp.bn == 32)
+            return launch_variant<true, 32, false, true>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+        if (tp.bn == 64)
+            return launch_variant<true, 64, false, true>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+        return cudaErrorInvalidValue;
+    }
     // pairs: tiles of at least 128 tokens (the narrower variants keep their
     // register count low enough to share an SM with the per-row kernel)
     if (v1) {
@@ -1031,6 +1131,7 @@ cudaError_t launch_gemm_lora_tc_pair(const ForwardPlan &plan, const ProjView &v0
 }
 
 cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
+    if (v.w_scale) return launch_gemm_lora_tc_pair(plan, v, nullptr, nullptr, 0, stream);
     const TcPlan tp = plan_tc(plan.M, v.N, plan.K);
     if (tp.swap) {
         switch (tp.bn) {

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.lora_abi_version() == 2
+    assert L.lora_abi_version() == 3
     from adapter_gemm_linear_gb300._lib import STATUS_NAMES
     texts = {L.lora_status_string(c).decode() for c in STATUS_NAMES}
     assert len(texts) == len(STATUS_NAMES) and all(texts)
