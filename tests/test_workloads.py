@@ -85,3 +85,4 @@ def test_synth_integer_and_sgmv():
 
 def test_config_names():
     assert len(CONFIG_NAMES) == 5
+
