@@ -7,6 +7,7 @@ package only binds it to PyTorch tensors and streams.
 """
 
 from .api import (  # noqa: F401
+    Int4Weight,
     Int8Weight,
     LinearCall,
     LoraError,

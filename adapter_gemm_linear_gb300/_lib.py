@@ -35,7 +35,7 @@ STATUS = {v: k for k, v in STATUS_NAMES.items()}
 
 LORA_BF16 = 0
 LORA_FP32 = 1
-ABI_VERSION = 3  # include/lora.h LORA_ABI_VERSION
+ABI_VERSION = 4  # include/lora.h LORA_ABI_VERSION
 
 
 class PoolDesc(ctypes.Structure):
@@ -62,6 +62,7 @@ class Proj(ctypes.Structure):
         ("out", ctypes.c_void_p),
         ("ldo", ctypes.c_int32),
         ("w_scale", ctypes.c_void_p),
+        ("w_bits", ctypes.c_int32),
     ]
 
 

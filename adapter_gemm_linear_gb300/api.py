@@ -241,6 +241,35 @@ class Int8Weight:
         return Int8Weight(q.contiguous(), scale.contiguous())
 
 
+class Int4Weight:
+    """A 4-bit quantized base weight: W[n][k] = q[n][k] * scale[n] with q in
+    [-8, 7] packed two per byte (uint8 [N][K/2], element 2j in the low nibble
+    of byte j), fp32 scale [N]; dequantized inside the GEMM like Int8Weight."""
+
+    def __init__(self, packed: torch.Tensor, scale: torch.Tensor):
+        if packed.dtype != torch.uint8 or packed.dim() != 2 or not packed.is_contiguous():
+            raise ValueError("packed must be a contiguous uint8 [N][K/2] tensor")
+        if scale.dtype != torch.float32 or scale.shape != (packed.shape[0],) or not scale.is_contiguous():
+            raise ValueError("scale must be a contiguous float32 [N] tensor")
+        self.q, self.scale = packed, scale
+
+    @staticmethod
+    def pack(q: torch.Tensor) -> torch.Tensor:
+        """int [N][K] values in [-8, 7] (K even) to the packed uint8 [N][K/2]."""
+        if q.shape[1] % 2 or int(q.min()) < -8 or int(q.max()) > 7:
+            raise ValueError("need an even K and values in [-8, 7]")
+        u = (q.to(torch.int16) & 0xF).to(torch.uint8)
+        return (u[:, 0::2] | (u[:, 1::2] << 4)).contiguous()
+
+    @staticmethod
+    def quantize(W: torch.Tensor) -> "Int4Weight":
+        """Symmetric per-row int4 of a float weight: scale = max|W[n]| / 7."""
+        Wf = W.float()
+        scale = (Wf.abs().amax(dim=1) / 7.0).clamp_min(torch.finfo(torch.float32).tiny)
+        q = torch.round(Wf / scale[:, None]).clamp_(-7, 7).to(torch.int8)
+        return Int4Weight(Int4Weight.pack(q), scale.contiguous())
+
+
 class LinearCall:
     """Prepared arguments of one lora_linear_forward call.
 
@@ -265,11 +294,12 @@ class LinearCall:
             if out.dim() != 2 or (out.numel() > 0 and out.stride(1) != 1):
                 raise ValueError("out must be a row-major 2-D tensor")
             ldo = int(out.stride(0)) if out.numel() > 0 else int(out.shape[1])
-            if isinstance(W, Int8Weight):
-                projs[i] = _lib.Proj(_ptr(W.q), pool.handle, _ptr(out), ldo, _ptr(W.scale))
+            if isinstance(W, (Int8Weight, Int4Weight)):
+                bits = 4 if isinstance(W, Int4Weight) else 8
+                projs[i] = _lib.Proj(_ptr(W.q), pool.handle, _ptr(out), ldo, _ptr(W.scale), bits)
                 self._keep += [W.q, W.scale, pool, out]
             else:
-                projs[i] = _lib.Proj(_ptr(W), pool.handle, _ptr(out), ldo, None)
+                projs[i] = _lib.Proj(_ptr(W), pool.handle, _ptr(out), ldo, None, 0)
                 self._keep += [W, pool, out]
         self._projs = projs
         for t in (row_adapter, seg_offsets, seg_adapter, perm):

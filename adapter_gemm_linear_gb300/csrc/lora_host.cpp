@@ -430,14 +430,16 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
             if (!pj.W || !pj.out) return LORA_ERR_INVALID_ARG;
             if (!aligned16(pj.W) || !aligned16(pj.out)) return LORA_ERR_ALIGNMENT;
         }
-        if (pj.w_scale) {  // int8 base weights: bf16 x, the decode orientation
+        if (pj.w_scale) {  // quantized base weights: bf16 x, the decode orientation
+            if (pj.w_bits != 0 && pj.w_bits != 8 && pj.w_bits != 4) return LORA_ERR_INVALID_ARG;
             if (a->dtype != LORA_BF16 || a->M > lora::kQuantMaxRows) return LORA_ERR_UNSUPPORTED;
-            if (a->K % 16) return LORA_ERR_ALIGNMENT;
+            if (a->K % (pj.w_bits == 4 ? 32 : 16)) return LORA_ERR_ALIGNMENT;  // 16-byte rows
             if (!aligned16(pj.w_scale)) return LORA_ERR_ALIGNMENT;
         }
         lora::ProjView &v = plan->proj[i];
         v.W = pj.W;
         v.w_scale = pj.w_scale;
+        v.w_bits = pj.w_scale ? (pj.w_bits == 4 ? 4 : 8) : 0;
         v.out = pj.out;
         v.N = d.N;
         v.ldo = pj.ldo;

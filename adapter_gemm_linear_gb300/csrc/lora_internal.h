@@ -51,7 +51,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Per-projection view handed to the kernel launchers.
 struct ProjView {
     const void *W;
-    const float *w_scale;  // NULL, or W is int8 with these per-row scales
+    const float *w_scale;  // NULL, or W is quantized with these per-row scales
+    int32_t w_bits;        // with w_scale: 8 (int8) or 4 (packed int4)
     void *out;
     int32_t N, ldo;
     const void *a_arena, *b_arena;

@@ -104,8 +104,10 @@ struct TcParams {
     int32_t N1, ldo1;
     __nv_bfloat16 *out1;
     const float *ycorr1;
-    // int8 base weights (QUANT variants): W[n][k] = q[n][k] * w_scale[n]
+    // quantized base weights (QUANT variants): W[n][k] = q[n][k] * w_scale[n],
+    // q int8 (w_bits 8) or packed int4, two per byte, low nibble first (4)
     const float *w_scale;
+    int32_t w_bits;
 };
 
 // The projection of a swapped W tile (second: the launch's second
@@ -176,6 +178,15 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
         w.tb = r / p.tiles_a;
     }
     return w;
+}
+
+// Byte `j` of w as two signed int4 (low nibble first), converted exactly to
+// a bf16 pair.
+__device__ __forceinline__ uint32_t int4x2_to_bf16x2(uint32_t w, int j) {
+    const uint32_t b = (w >> (8 * j)) & 0xFFu;
+    const int lo = static_cast<int>((b & 0xFu) ^ 8u) - 8;
+    const int hi = static_cast<int>((b >> 4) ^ 8u) - 8;
+    return (__float_as_uint(static_cast<float>(lo)) >> 16) | (__float_as_uint(static_cast<float>(hi)) & 0xFFFF0000u);
 }
 
 // Bytes `sh` and `sh` + 1 of w as signed int8, converted exactly to a bf16
@@ -275,11 +286,13 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                 *abort_flag = 1;
             }
             if (*abort_flag) return;
-            mbar_arrive_expect_tx(&full[s], (QUANT ? C::kQBytes : C::kABytes) + C::kBBytes);
+            mbar_arrive_expect_tx(&full[s], (QUANT ? (p.w_bits == 4 ? C::kQBytes / 2 : C::kQBytes) : C::kABytes) +
+                                                C::kBBytes);
             if (i < nmain) {
                 const int32_t kb = kb0 + i;
-                if (QUANT)  // int8 W into the staging tile; the epilogue warps convert it
-                    tma_load_2d(sQ + s * C::kQBytes, map_a, kb * kBK, row_a, &full[s]);
+                if (QUANT)  // int8 (or packed int4) W into the staging tile; the epilogue warps convert it
+                    tma_load_2d(sQ + s * C::kQBytes, map_a, p.w_bits == 4 ? kb * (kBK / 2) : kb * kBK, row_a,
+                                &full[s]);
                 else
                     tma_load_2d(sA + s * C::kABytes, map_a, kb * kBK, row_a, &full[s]);
                 tma_load_2d(sB + s * C::kBBytes, tma_b, kb * kBK, w.tb * BN, &full[s]);
@@ -479,18 +492,32 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
                     *abort_flag = 1;
                     break;  // without arriving: the MMA gives up too
                 }
-                const uint4 *src = reinterpret_cast<const uint4 *>(sQ + s * C::kQBytes + r * kBK + hh * 32);
-                const uint4 q0 = src[0], q1 = src[1];
-                const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                 uint8_t *row = sA + s * C::kABytes + r * (kBK * 2);
+                if (p.w_bits == 4) {  // the row's 32 bytes staged; this half's 16 hold 32 values
+                    const uint4 qv = *reinterpret_cast<const uint4 *>(sQ + s * C::kQBytes + r * (kBK / 2) + hh * 16);
+                    const uint32_t wd[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint4 o;
-                    o.x = int8x2_to_bf16x2(wd[2 * c], 0);
-                    o.y = int8x2_to_bf16x2(wd[2 * c], 2);
-                    o.z = int8x2_to_bf16x2(wd[2 * c + 1], 0);
-                    o.w = int8x2_to_bf16x2(wd[2 * c + 1], 2);
-                    *reinterpret_cast<uint4 *>(row + (((4 * hh + c) ^ (r & 7)) << 4)) = o;
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 o;
+                        o.x = int4x2_to_bf16x2(wd[c], 0);
+                        o.y = int4x2_to_bf16x2(wd[c], 1);
+                        o.z = int4x2_to_bf16x2(wd[c], 2);
+                        o.w = int4x2_to_bf16x2(wd[c], 3);
+                        *reinterpret_cast<uint4 *>(row + (((4 * hh + c) ^ (r & 7)) << 4)) = o;
+                    }
+                } else {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(sQ + s * C::kQBytes + r * kBK + hh * 32);
+                    const uint4 q0 = src[0], q1 = src[1];
+                    const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 o;
+                        o.x = int8x2_to_bf16x2(wd[2 * c], 0);
+                        o.y = int8x2_to_bf16x2(wd[2 * c], 2);
+                        o.z = int8x2_to_bf16x2(wd[2 * c + 1], 0);
+                        o.w = int8x2_to_bf16x2(wd[2 * c + 1], 2);
+                        *reinterpret_cast<uint4 *>(row + (((4 * hh + c) ^ (r & 7)) << 4)) = o;
+                    }
                 }
                 fence_proxy_async_shared();  // the MMAs read the tile through the async proxy
                 __syncwarp();
@@ -873,15 +900,16 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
 }
 
 
-// Row-major int8 matrix [rows][cols] (row stride `cols` bytes, a multiple of
-// 16) in boxes of box_rows x 64 without swizzle; out-of-range elements read
-// as zero.
-bool make_tmap_i8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// Row-major byte matrix [rows][cols] (row stride `cols` bytes, a multiple of
+// 16) in boxes of box_rows x box_cols bytes without swizzle; out-of-range
+// elements read as zero.
+bool make_tmap_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                  uint32_t box_cols) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -915,8 +943,10 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     CUtensorMap tx, tw;
     if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, SWAP ? BN : kBM)) return cudaErrorInvalidValue;
     if (QUANT != (v.w_scale != nullptr) || (QUANT && (!SWAP || PAIR || vm_mode))) return cudaErrorInvalidValue;
-    if (QUANT) {
-        if (!make_tmap_i8(&tw, v.W, v.N, plan.K, kBM)) return cudaErrorInvalidValue;
+    if (QUANT) {  // int8 [N][K] bytes, or packed int4 [N][K/2]: 64 values of a row per box
+        const bool i4 = v.w_bits == 4;
+        if (!make_tmap_u8(&tw, v.W, v.N, i4 ? plan.K / 2 : plan.K, kBM, i4 ? kBK / 2 : kBK))
+            return cudaErrorInvalidValue;
     } else if (!make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, SWAP ? kBM : BN)) {
         return cudaErrorInvalidValue;
     }
@@ -969,6 +999,7 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     if (!counters) n_counters = plan.n_counters;
     p.status = plan.status;
     p.w_scale = v.w_scale;
+    p.w_bits = v.w_scale ? (v.w_bits == 4 ? 4 : 8) : 0;
     p.tiles_a0 = tp.tiles_a;
     p.N1 = 0;
     p.ldo1 = 0;

@@ -70,6 +70,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the oracle baseline")
     ap.add_argument("--w-int8", action="store_true",
                     help="base weights as int8 with per-row scales (decode shapes, M <= 64)")
+    ap.add_argument("--w-int4", action="store_true",
+                    help="base weights as packed int4 with per-row scales (decode shapes, M <= 64)")
     ap.add_argument("--reference-seconds", type=float, default=90.0,
                     help="oracle work of the whole --impl reference run")
     return ap.parse_args()
@@ -173,7 +175,7 @@ def workload_stats(wl):
 SWAPPED_MAX_M = 512  # the library's GEMM takes the swapped orientation up to this many rows
 
 
-def algorithmic(wl, w_int8=False):
+def algorithmic(wl, w_bits=0):
     """Per-call algorithmic bytes and flops of the two stages of a projection.
 
     Small M (bf16, M <= 512): the LoRA stage reads each distinct adapter's A
@@ -186,7 +188,7 @@ def algorithmic(wl, w_int8=False):
     """
     eb = 2 if wl.dtype == "bf16" else 4
     st = workload_stats(wl)
-    wb = 1 if w_int8 else eb  # bytes per base weight (int8 W adds a float scale per row)
+    wb = {8: 1, 4: 0.5}.get(w_bits, eb)  # bytes per base weight (quantized W adds a float scale per row)
     M, K = wl.M, wl.K
     swapped = wl.dtype == "bf16" and M <= SWAPPED_MAX_M
     out = {"gemm_bytes": 0, "gemm_flops": 0, "lora_bytes": 0, "lora_flops": 0, "per_proj": [],
@@ -196,7 +198,7 @@ def algorithmic(wl, w_int8=False):
         a_bytes = st["sum_r_distinct"] * K * eb + st["adapted_rows"] * K * eb
         b_bytes = st["sum_r_distinct"] * N * eb
         if swapped:
-            gb = N * K * wb + (N * 4 if w_int8 else 0) + (M * K + M * N) * eb + M * N * 4
+            gb = int(N * K * wb) + (N * 4 if w_bits else 0) + (M * K + M * N) * eb + M * N * 4
             gf = 2 * M * N * K
             lb = a_bytes + b_bytes + M * N * 4
             lf = 2 * st["sum_r_rows"] * (K + N)
@@ -216,9 +218,9 @@ def algorithmic(wl, w_int8=False):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def build_case(wl, device, w_int8=False):
+def build_case(wl, device, w_bits=0):
     import torch
-    from adapter_gemm_linear_gb300 import Int8Weight, LinearCall, LoraPool
+    from adapter_gemm_linear_gb300 import Int4Weight, Int8Weight, LinearCall, LoraPool
 
     td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     max_rank = max(16, -(-int(wl.ranks.max()) // 16) * 16)
@@ -242,8 +244,8 @@ def build_case(wl, device, w_int8=False):
         pools.append(pool)
     x = torch.from_numpy(wl.x).to(td).to(device)
     Ws = [torch.from_numpy(p.W).to(td).to(device) for p in wl.projections]
-    if w_int8:  # symmetric per-row int8 of the same weights
-        Ws = [Int8Weight.quantize(W) for W in Ws]
+    if w_bits:  # symmetric per-row int8 / int4 of the same weights
+        Ws = [(Int8Weight if w_bits == 8 else Int4Weight).quantize(W) for W in Ws]
     outs = [torch.empty((wl.M, p.N), dtype=td, device=device) for p in wl.projections]
     if wl.mode == "sgmv":
         offs = torch.from_numpy(wl.seg_offsets).to(device)
@@ -546,7 +548,8 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     import __graft_entry__
     __graft_entry__.build()
     wl = make_config(cfg_name)
-    case = build_case(wl, device, args.w_int8)
+    w_bits = 8 if args.w_int8 else 4 if args.w_int4 else 0
+    case = build_case(wl, device, w_bits)
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
     flush = L2Flush(l2, device)
@@ -585,7 +588,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         return None
 
     peaks, peak_src = load_peaks()
-    alg = algorithmic(wl, args.w_int8)
+    alg = algorithmic(wl, w_bits)
     value = whole_job_rate(wl.M * steps, world, total_ms)
     # dominant stage: the GEMM or the LoRA kernels, by their share of the
     # eager stage time
@@ -607,7 +610,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     else:
         roof = {"bound": "hbm", "achieved": round(b / t / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ncu_traffic(wl.name + ("+int8w" if args.w_int8 else "")) if gemm_dominant else None
+    roof["traffic"] = ncu_traffic(wl.name + (f"+int{w_bits}w" if w_bits else "")) if gemm_dominant else None
     roof["kernel"] = kernel
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
     roof["algorithmic_bytes_per_call"] = b
@@ -636,7 +639,8 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
             "launch": "CUDA graph of one lora_linear_forward call, replayed per step; step = events recorded "
                       "inside the graph around the forward",
             "parallelism": f"replicas x{world}",
-            "base_weights": "int8, one fp32 scale per row" if args.w_int8 else wl.dtype,
+            "base_weights": {8: "int8, one fp32 scale per row", 4: "int4 packed, one fp32 scale per row"}.get(
+                w_bits, wl.dtype),
         },
         "roofline": roof,
         "stages": {

@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define LORA_ABI_VERSION 3  /* 3: lora_proj_t.w_scale (int8 base weights) */
+#define LORA_ABI_VERSION 4  /* 3: lora_proj_t.w_scale (int8 base weights); 4: w_bits (int4) */
 #define LORA_BLOCK_ROWS 16
 #define LORA_MAX_PROJ 4
 
@@ -244,19 +244,26 @@ lora_status_t lora_segment_rows(const int32_t *ids, int32_t M, int32_t num_slots
  * Quantized base ("Your LoRA Adapters Are Thrashing Your GPUs", §02
  * "Numerical precision: FP16 adapters on INT4 base models": the base weights
  * are stored quantized and dequantized on the fly inside the matrix
- * multiply, the adapters stay 16-bit).  With w_scale non-NULL, W is int8
- * [N][K] row-major and the base weight is W[n][k] * w_scale[n] (symmetric,
- * one fp32 scale per output channel); the adapters keep the pool's dtype.
- * Supported for bf16 x with M <= 64 (the decode orientation of the GEMM)
- * and K a multiple of 16; other shapes return LORA_ERR_UNSUPPORTED.
- * w_scale: device fp32 [N], 16-byte aligned.  NULL: W has the pool dtype.
+ * multiply, the adapters stay 16-bit).  With w_scale non-NULL the base
+ * weight is q[n][k] * w_scale[n] (symmetric, one fp32 scale per output
+ * channel) and W holds q:
+ *  - w_bits 8 (or 0): int8 [N][K] row-major, K a multiple of 16;
+ *  - w_bits 4: int4 in [-8, 7] packed two per byte, [N][K/2] bytes row-major,
+ *    element 2j in the low nibble of byte j, 2j+1 in the high nibble; K a
+ *    multiple of 32.
+ * The adapters keep the pool's dtype.  Supported for bf16 x with M <= 64
+ * (the decode orientation of the GEMM); other shapes return
+ * LORA_ERR_UNSUPPORTED, a misaligned K LORA_ERR_ALIGNMENT, another w_bits
+ * LORA_ERR_INVALID_ARG.  w_scale: device fp32 [N], 16-byte aligned.  NULL:
+ * W has the pool dtype and w_bits is ignored.
  */
 typedef struct lora_proj {
     const void *W;            /* device [N][K] row-major, pool dtype (int8 with w_scale) */
     const lora_pool_t *pool;  /* adapters of this projection (N, K from it) */
     void *out;                /* device [M][ldo], overwritten (not accumulated) */
     int32_t ldo;              /* row stride of out in elements, >= N */
-    const float *w_scale;     /* NULL, or the int8 W's per-row scales (see above) */
+    const float *w_scale;     /* NULL, or the quantized W's per-row scales (see above) */
+    int32_t w_bits;           /* with w_scale: 8 (0 means 8) or 4 */
 } lora_proj_t;
 
 /*

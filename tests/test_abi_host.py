@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.lora_abi_version() == 3
+    assert L.lora_abi_version() == 4
     from adapter_gemm_linear_gb300._lib import STATUS_NAMES
     texts = {L.lora_status_string(c).decode() for c in STATUS_NAMES}
     assert len(texts) == len(STATUS_NAMES) and all(texts)
@@ -96,7 +96,7 @@ def test_pool_create_validation_without_device(L):
 
 def test_forward_validation_without_device(L):
     from adapter_gemm_linear_gb300._lib import ForwardArgs, Proj
-    projs = (Proj * 1)(Proj(0x1000, None, 0x2000, 64))
+    projs = (Proj * 1)(Proj(0x1000, None, 0x2000, 64, None, 0))
 
     def args(**kw):
         d = dict(dtype=0, M=4, K=64, x=0x3000, ldx=64, n_proj=1,
