@@ -1,5 +1,5 @@
 """Shared helpers for the GPU tests: pools from workloads, the forward call
-through the C ABI, and the tolerance of the spec contract.
+through the C ABI, and the parity tolerance.
 
 Tolerances (per output row m, over its N columns):
   bf16 inputs, fp32 accumulation:  max |y - y_ref| <= 2e-2 * (max |y_ref| + 1)
