@@ -77,3 +77,20 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_algorithmic_bytes_of_quantized_base():
+    """The GEMM's algorithmic bytes count 1 byte (int8) or half a byte (int4)
+    per base weight plus one fp32 scale per row; the rest is unchanged."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from workloads import make_config
+    wl = make_config("decode_bgmv")
+    N, K = wl.projections[0].N, wl.K
+    bf16 = bench.algorithmic(wl)
+    i8 = bench.algorithmic(wl, 8)
+    i4 = bench.algorithmic(wl, 4)
+    assert bf16["gemm_bytes"] - i8["gemm_bytes"] == N * K - N * 4
+    assert bf16["gemm_bytes"] - i4["gemm_bytes"] == N * K * 3 // 2 - N * 4
+    assert bf16["gemm_flops"] == i8["gemm_flops"] == i4["gemm_flops"] == 2 * wl.M * N * K
+    assert bf16["lora_bytes"] == i8["lora_bytes"] == i4["lora_bytes"]
