@@ -20,5 +20,6 @@ from .api import (  # noqa: F401
     pool_slot_bytes,
     segment_rows,
     status_string,
+    arm_test_wait_timeout,
 )
 from .build import build  # noqa: F401

@@ -35,7 +35,7 @@ STATUS = {v: k for k, v in STATUS_NAMES.items()}
 
 LORA_BF16 = 0
 LORA_FP32 = 1
-ABI_VERSION = 4  # include/lora.h LORA_ABI_VERSION
+ABI_VERSION = 5  # include/lora.h LORA_ABI_VERSION
 
 
 class PoolDesc(ctypes.Structure):
@@ -84,6 +84,7 @@ class ForwardArgs(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("stage_events", ctypes.POINTER(ctypes.c_void_p)),
         ("num_stage_events", ctypes.c_int32),
+        ("scales", ctypes.c_void_p),
     ]
 
 
@@ -118,6 +119,7 @@ SIGNATURES = [
     ("lora_linear_forward", ctypes.c_int, [ctypes.POINTER(ForwardArgs), ctypes.c_void_p]),
     ("lora_linear_forward_noalloc", ctypes.c_int, [ctypes.POINTER(ForwardArgs), ctypes.c_void_p]),
     ("lora_get_device_status", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    ("lora_test_arm_wait_timeout", ctypes.c_int, [ctypes.c_uint64]),
     ("lora_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("lora_last_cuda_error", ctypes.c_int32, []),
     ("lora_cuda_error_name", ctypes.c_char_p, [ctypes.c_int32]),

@@ -281,14 +281,17 @@ class LinearCall:
     def __init__(self, x: torch.Tensor, projections: Sequence[Tuple[torch.Tensor, LoraPool, torch.Tensor]],
                  row_adapter: Optional[torch.Tensor] = None,
                  seg_offsets: Optional[torch.Tensor] = None, seg_adapter: Optional[torch.Tensor] = None,
-                 perm: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+                 perm: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 scales: Optional[torch.Tensor] = None):
         if x.dim() != 2 or (x.numel() > 0 and x.stride(1) != 1):
             raise ValueError("x must be a row-major 2-D tensor")
         if (row_adapter is None) == (seg_offsets is None and seg_adapter is None):
             if row_adapter is not None or x.shape[0] > 0:
                 raise ValueError("give either row_adapter or (seg_offsets, seg_adapter)")
         dt = lora_dtype(x.dtype)
-        self._keep = [x, row_adapter, seg_offsets, seg_adapter, perm]
+        if scales is not None and (scales.dtype != torch.float32 or not scales.is_contiguous()):
+            raise ValueError("scales must be a contiguous float32 [max_slots] tensor")
+        self._keep = [x, row_adapter, seg_offsets, seg_adapter, perm, scales]
         projs = (_lib.Proj * len(projections))()
         for i, (W, pool, out) in enumerate(projections):
             if out.dim() != 2 or (out.numel() > 0 and out.stride(1) != 1):
@@ -310,7 +313,7 @@ class LinearCall:
         self.args = _lib.ForwardArgs(
             dt, int(x.shape[0]), int(x.shape[1]), _ptr(x), ldx, len(projections),
             ctypes.cast(projs, ctypes.POINTER(_lib.Proj)), _ptr(row_adapter), _ptr(seg_offsets),
-            _ptr(seg_adapter), _ptr(perm), num_segs, None, 0, None, 0)
+            _ptr(seg_adapter), _ptr(perm), num_segs, None, 0, None, 0, _ptr(scales))
         self.n_proj = len(projections)
         need = int(_lib.lib().lora_forward_workspace_bytes(ctypes.byref(self.args)))
         if need == 0:
@@ -362,15 +365,22 @@ def kernel_launches() -> int:
 
 def linear_forward(x: torch.Tensor, projections, row_adapter=None, seg_offsets=None,
                    seg_adapter=None, perm=None, workspace=None,
-                   stream: Optional[torch.cuda.Stream] = None) -> None:
+                   stream: Optional[torch.cuda.Stream] = None, scales=None) -> None:
     """lora_linear_forward: out_p = x W_p^T + per-row (alpha_i/r_i) B_i (A_i x).
 
     ``projections`` is a sequence of (W [N, K], LoraPool, out [M, >=N]).
     Rows reach adapters through ``row_adapter`` (device int32 [M], -1 = none)
     or through sorted segments (``seg_offsets``, ``seg_adapter``, optional
-    ``perm``; device int32).
+    ``perm``; device int32).  ``scales`` (device float32 [max_slots]) replaces
+    the pools' own alpha/r for this call.
     """
-    LinearCall(x, projections, row_adapter, seg_offsets, seg_adapter, perm, workspace)(stream)
+    LinearCall(x, projections, row_adapter, seg_offsets, seg_adapter, perm, workspace, scales)(stream)
+
+
+def arm_test_wait_timeout(limit_ns: int) -> None:
+    """lora_test_arm_wait_timeout: the next forward's split-K counter waits
+    expect an arrival that never comes and give up after ``limit_ns``."""
+    _check(_lib.lib().lora_test_arm_wait_timeout(int(limit_ns)), "lora_test_arm_wait_timeout")
 
 
 def device_status(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:

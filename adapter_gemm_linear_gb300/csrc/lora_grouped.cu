@@ -724,15 +724,16 @@ static cudaError_t launch_rows(const ForwardPlan &plan, const ProjView *const *v
         // can be placed beside this kernel's (an SM changes its carveout only
         // when idle)
         static std::mutex mu;
-        static bool done[128] = {};
+        static uint64_t done_ctx[128] = {};  // per device: the context the attribute was set in
         int dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 128) {
             std::lock_guard<std::mutex> lock(mu);
-            if (!done[dev]) {
+            uint64_t ctx = done_ctx[dev];
+            if (first_use_in_context(&ctx)) {
                 const cudaError_t e = cudaFuncSetAttribute(lora_rows_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                                            static_cast<int>(cudaSharedmemCarveoutMaxShared));
                 if (e != cudaSuccess) return e;
-                done[dev] = true;
+                done_ctx[dev] = current_context_id();
             }
         }
     }

@@ -13,6 +13,7 @@
 #include "lora_internal.h"
 
 static std::atomic<uint64_t> g_kernel_launches{0};
+static std::atomic<uint64_t> g_test_wait_limit_ns{0};  // lora_test_arm_wait_timeout: armed limit, 0 = off
 static thread_local int32_t g_last_cuda_error = 0;  // behind this thread's last forward LORA_ERR_CUDA
 
 void lora::count_launches(int n) { g_kernel_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
@@ -404,6 +405,8 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         (a->num_stage_events != 1 + 2 * a->n_proj || !a->stage_events))
         return LORA_ERR_INVALID_ARG;
     if (a->num_stage_events == 0 && a->stage_events) return LORA_ERR_INVALID_ARG;
+    if (a->scales && !aligned16(a->scales)) return LORA_ERR_ALIGNMENT;
+    plan->test_wait_limit_ns = 0;
     plan->stage_events = a->stage_events;
     plan->dtype = a->dtype;
     // the small-M orientation's grouped shrink writes one V plane per K slice
@@ -447,7 +450,7 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         v.b_arena = d.b_arena;
         v.table = d.block_table;
         v.ranks = d.ranks;
-        v.scales = d.scales;
+        v.scales = a->scales ? a->scales : d.scales;  // the call's own scales, if given
         v.max_slots = d.max_slots;
         v.bps = pj.pool->bps;
         v.num_blocks = d.num_blocks;
@@ -578,6 +581,7 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);
     plan.n_counters = static_cast<int32_t>((ws.total - ws.counter_off) / sizeof(int32_t));
     cudaStream_t st = as_stream(stream);
+    plan.test_wait_limit_ns = g_test_wait_limit_ns.exchange(0);
     if (plan.stage_events &&
         cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[0]), st) != cudaSuccess)
         return LORA_ERR_CUDA;
@@ -599,6 +603,12 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
     const cudaError_t e = lora::launch_forward(plan, st);
     g_last_cuda_error = static_cast<int32_t>(e);
     return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+lora_status_t lora_test_arm_wait_timeout(uint64_t limit_ns) {
+    if (limit_ns != 0 && (limit_ns < 1000000ull || limit_ns > 2000000000ull)) return LORA_ERR_INVALID_ARG;
+    g_test_wait_limit_ns.store(limit_ns);
+    return LORA_OK;
 }
 
 lora_status_t lora_get_device_status(void *stream, int32_t *detail) {

@@ -40,8 +40,20 @@ enum DeviceError : uint32_t {
 };
 
 // Device address of this device's status word (a 64-bit word holding
-// code << 32 | detail).  Looked up once per device.
+// code << 32 | detail).  Looked up once per CUDA context of each device.
 cudaError_t device_status_ptr(unsigned long long **out);
+
+// Process-unique id of the calling thread's current CUDA context (the
+// driver's cuCtxGetId), or 0 when there is none or the driver cannot say.
+// Per-device caches of device addresses and function attributes key on it,
+// so that a device reset (a new primary context) invalidates them.
+uint64_t current_context_id();
+
+// Whether the per-device entry *slot records a context other than the
+// current one (or none); if so it records the current one.  For one-time
+// set-up per context (a function attribute, a symbol address).  A zero
+// context id (unknown) always counts as new.
+bool first_use_in_context(uint64_t *slot);
 
 // Element size of a dtype.
 inline size_t dtype_bytes(lora_dtype_t t) { return t == LORA_FP32 ? 4 : 2; }
@@ -119,6 +131,9 @@ struct ForwardPlan {
     // of it for all projections (each its own ycorr), then the GEMMs two
     // projections per launch (each launch its own split-K counters)
     bool fused_rows;
+    // lora_test_arm_wait_timeout: 0, or the time limit of this call's split-K
+    // counter waits, which then wait for one arrival more than any launch makes
+    uint64_t test_wait_limit_ns;
 };
 
 // Count of kernels launched by the library (lora_kernel_launches).

@@ -1,5 +1,6 @@
 // Device status word, row-map and pool-copy kernels, and the SIMT
 // (CUDA-core) forward path used for fp32 inputs.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -17,19 +18,61 @@ namespace lora {
 
 __device__ unsigned long long g_lora_status;
 
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <typename F>
+F driver_entry(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(p);
+}
+}  // namespace
+
+uint64_t current_context_id() {
+    static std::once_flag once;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        get_current = driver_entry<CtxGetCurrentFn>("cuCtxGetCurrent");
+        get_id = driver_entry<CtxGetIdFn>("cuCtxGetId");
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return static_cast<uint64_t>(id) + 1;  // 0 stays "unknown"
+}
+
+bool first_use_in_context(uint64_t *slot) {
+    const uint64_t id = current_context_id();
+    if (id != 0 && *slot == id) return false;
+    *slot = id;
+    return true;
+}
+
 cudaError_t device_status_ptr(unsigned long long **out) {
     static std::mutex mu;
     static unsigned long long *cache[128] = {};
+    static uint64_t cache_ctx[128] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
+    const uint64_t ctx = current_context_id();
+    if (!cache[dev] || ctx == 0 || cache_ctx[dev] != ctx) {
+        // first use on this device, or its context was replaced (a device
+        // reset): the symbol's address is the new context's
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_lora_status);
         if (e != cudaSuccess) return e;
         cache[dev] = static_cast<unsigned long long *>(p);
+        cache_ctx[dev] = current_context_id();  // the lookup made the context current
     }
     *out = cache[dev];
     return cudaSuccess;

@@ -906,7 +906,7 @@ template <typename Params>
 cudaError_t launch_pipe(void (*kernel)(Params), const Params &p, int threads, size_t smem, size_t smem_max,
                         cudaStream_t stream) {
     static std::mutex mu;
-    static bool done[2][128] = {};
+    static uint64_t done_ctx[2][128] = {};  // per kernel and device: the context the opt-in was set in
     const int which = reinterpret_cast<const void *>(kernel) == reinterpret_cast<const void *>(&pipe_shrink_kernel) ? 0 : 1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -914,10 +914,11 @@ cudaError_t launch_pipe(void (*kernel)(Params), const Params &p, int threads, si
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!done[which][dev]) {  // the opt-in is per device; the largest size any call needs
+        uint64_t ctx = done_ctx[which][dev];
+        if (first_use_in_context(&ctx)) {  // the opt-in is per device; the largest size any call needs
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
             if (e != cudaSuccess) return e;
-            done[which][dev] = true;
+            done_ctx[which][dev] = current_context_id();
         }
     }
     cudaLaunchConfig_t cfg = {};

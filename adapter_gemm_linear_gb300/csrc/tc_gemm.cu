@@ -108,6 +108,10 @@ struct TcParams {
     // q int8 (w_bits 8) or packed int4, two per byte, low nibble first (4)
     const float *w_scale;
     int32_t w_bits;
+    // split-K tile-counter waits: the arrivals expected beyond `splits` (1
+    // only when armed for a test, so that the waits run out) and their limit
+    int32_t counter_extra;
+    uint64_t counter_wait_ns;
 };
 
 // The projection of a swapped W tile (second: the launch's second
@@ -620,7 +624,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
                 epi_sync();
                 if (et == 0) {
                     atomicAdd(p.counters + tile, 1);
-                    const bool all = wait_counter_at_least(p.counters + tile, p.splits, kWaitLimitNs);
+                    const bool all =
+                        wait_counter_at_least(p.counters + tile, p.splits + p.counter_extra, p.counter_wait_ns);
                     if (!all) record_error(p.status, kDevTimeout, 5);
                     *last_flag = all ? 1u : 0u;
                 }
@@ -926,18 +931,19 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     using C = Cfg<SWAP, BN, QUANT>;
     auto kernel = tc_gemm_lora_kernel<SWAP, BN, PAIR, QUANT>;
     static std::mutex mu;
-    static bool done[128] = {};
+    static uint64_t done_ctx[128] = {};  // per device: the context the opt-in was set in
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!done[dev]) {  // the shared-memory opt-in is a per-device function attribute
+        uint64_t ctx = done_ctx[dev];
+        if (first_use_in_context(&ctx)) {  // the shared-memory opt-in is a per-device function attribute
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(C::kSmem));
             if (e != cudaSuccess) return e;
-            done[dev] = true;
+            done_ctx[dev] = current_context_id();
         }
     }
     CUtensorMap tx, tw;
@@ -1000,6 +1006,8 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.status = plan.status;
     p.w_scale = v.w_scale;
     p.w_bits = v.w_scale ? (v.w_bits == 4 ? 4 : 8) : 0;
+    p.counter_extra = plan.test_wait_limit_ns ? 1 : 0;
+    p.counter_wait_ns = plan.test_wait_limit_ns ? plan.test_wait_limit_ns : kWaitLimitNs;
     p.tiles_a0 = tp.tiles_a;
     p.N1 = 0;
     p.ldo1 = 0;

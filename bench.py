@@ -7,8 +7,10 @@ the LoRA term before rounding.  For M <= 512 (the GEMM's swapped
 orientation) the LoRA kernels write the whole correction s_i B_i A_i x as an
 fp32 [M][N] array (per-row kernel, or the adapter-grouped shrink and
 expand); for larger M the per-row shrink writes V and the GEMM's epilogue
-applies the expand.  Prints ONE JSON line per workload (default: the decode
-BGMV workload, 64 rows of q_proj 4096->4096 with 32 rank-16 adapters).
+applies the expand.  Prints ONE JSON line per workload (default: the
+prefill SGMV workload, 8192 tokens of a 4096->4096 projection in 16 sorted
+segments over adapters of ranks {8, 16, 32, 64}: the largest workload, and
+the one whose base GEMM is bound by the tensor cores).
 
 Timing: W warm-up steps, then K steps; L2 is flushed before every step,
 outside the timed intervals: a 2 x L2 write, then a 2 x L2 read of another
@@ -51,7 +53,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "adapted tokens/s per LoRA linear; TC util (base GEMM) and HBM GB/s (LoRA path)"
-DEFAULT_CONFIG = "decode_bgmv"
+DEFAULT_CONFIG = "prefill_sgmv"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -176,44 +178,61 @@ SWAPPED_MAX_M = 512  # the library's GEMM takes the swapped orientation up to th
 
 
 def algorithmic(wl, w_bits=0):
-    """Per-call algorithmic bytes and flops of the two stages of a projection.
+    """Per-call algorithmic bytes and flops, as the method defines them.
 
-    Small M (bf16, M <= 512): the LoRA stage reads each distinct adapter's A
-    and B once and the adapted rows of x, and writes the fp32 correction
-    [M][N]; the GEMM reads W, x and the correction and writes out.  Large M:
-    the LoRA stage (shrink) reads the distinct adapters' A and the adapted
-    rows of x and writes V; the GEMM reads W, x, the distinct adapters' B
-    and V and writes out.  FLOPs: 2MNK for the GEMM, 2 r (K + N) per adapted
-    row for the LoRA term (counted where it is computed).
+    Base GEMM (every projection): flops 2MNK, bytes (NK + MK + MN) * eb (a
+    quantized W counts its packed bytes and one fp32 scale per row).
+    LoRA term, standalone kernels (small M: the LoRA kernels read x and the
+    distinct adapters and produce the correction the GEMM adds):
+        sum_distinct r (K + N) eb + M_a (K + 2N) eb + 2 M_a r 4
+    (adapters once each, the adapted rows of x read and of y read and
+    written, the rank-r intermediate written and read).  Large M (the shrink
+    is its own kernel, the expand runs inside the GEMM): the shrink's share,
+        sum_distinct r K eb + M_a K eb + M_a r 4,
+    and the GEMM's share, sum_distinct r N eb + M_a r 4, beside the base
+    bytes.  The fused form of the LoRA bytes (x and y shared with the base
+    GEMM), sum_distinct r (K + N) eb + 2 M_a r 4, is reported beside them.
+    LoRA flops: 2 r (K + N) per adapted row.
+    The implementation's own intermediates (the fp32 correction array of the
+    small-M path, the bf16 hi/lo V operand of the large-M path) are not
+    algorithmic: they are reported separately as ``intermediate_bytes``
+    (written once and read once).
     """
     eb = 2 if wl.dtype == "bf16" else 4
     st = workload_stats(wl)
-    wb = {8: 1, 4: 0.5}.get(w_bits, eb)  # bytes per base weight (quantized W adds a float scale per row)
+    wb = {8: 1, 4: 0.5}.get(w_bits, eb)  # bytes per base weight
     M, K = wl.M, wl.K
     swapped = wl.dtype == "bf16" and M <= SWAPPED_MAX_M
-    out = {"gemm_bytes": 0, "gemm_flops": 0, "lora_bytes": 0, "lora_flops": 0, "per_proj": [],
-           "orientation": "swapped" if swapped else "rows"}
+    out = {"gemm_bytes": 0, "gemm_flops": 0, "lora_bytes": 0, "lora_flops": 0, "lora_bytes_fused": 0,
+           "intermediate_bytes": 0, "per_proj": [], "orientation": "swapped" if swapped else "rows"}
+    Ma, rd, rr = st["adapted_rows"], st["sum_r_distinct"], st["sum_r_rows"]
     for p in wl.projections:
         N = p.N
-        a_bytes = st["sum_r_distinct"] * K * eb + st["adapted_rows"] * K * eb
-        b_bytes = st["sum_r_distinct"] * N * eb
+        base = int(N * K * wb) + (N * 4 if w_bits else 0) + (M * K + M * N) * eb
+        fused = rd * (K + N) * eb + 2 * rr * 4
         if swapped:
-            gb = int(N * K * wb) + (N * 4 if w_bits else 0) + (M * K + M * N) * eb + M * N * 4
-            gf = 2 * M * N * K
-            lb = a_bytes + b_bytes + M * N * 4
-            lf = 2 * st["sum_r_rows"] * (K + N)
+            gb, lb = base, rd * (K + N) * eb + Ma * (K + 2 * N) * eb + 2 * rr * 4
+            inter = 2 * M * N * 4  # the fp32 correction array
         else:
-            gb = (N * K + M * K + M * N) * eb + b_bytes + st["sum_r_rows"] * 4
-            gf = 2 * M * N * K + 2 * st["sum_r_rows"] * N
-            lb = a_bytes + st["sum_r_rows"] * 4
-            lf = 2 * st["sum_r_rows"] * K
+            gb = base + rd * N * eb + rr * 4
+            lb = rd * K * eb + Ma * K * eb + rr * 4
+            inter = 0
         out["gemm_bytes"] += gb
-        out["gemm_flops"] += gf
+        out["gemm_flops"] += 2 * M * N * K
         out["lora_bytes"] += lb
-        out["lora_flops"] += lf
-        out["per_proj"].append({"N": N, "gemm_bytes": gb, "gemm_flops": gf, "lora_bytes": lb})
+        out["lora_bytes_fused"] += fused
+        out["lora_flops"] += 2 * rr * (K + N)
+        out["intermediate_bytes"] += inter
+        out["per_proj"].append({"N": N, "gemm_bytes": gb, "gemm_flops": 2 * M * N * K, "lora_bytes": lb})
     out.update(st)
     return out
+
+
+def percentiles(values):
+    """Median, 10th and 90th percentile of a list of step times."""
+    a = np.asarray(values, dtype=np.float64)
+    return {"p10": float(np.percentile(a, 10)), "p50": float(np.percentile(a, 50)),
+            "p90": float(np.percentile(a, 90))}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -488,25 +507,103 @@ def time_e2e(case, wl, steps, flush, device):
     return {"ms": graph_ms, "eager_ms": eager_ms, "h2d": h2d, "d2h": d2h}
 
 
-def cpu_baseline(wl, seconds):
+def time_comparators(case, wl, flush, reps=20):
+    """Context only: the same base GEMMs through torch.matmul (cuBLAS), and
+    the whole layer as sequential passes in torch -- the base GEMM, then for
+    every adapter in the batch its rows gathered, multiplied by A^T and B^T,
+    scaled and added (the per-adapter loop the S-LoRA page contrasts with a
+    batched operator).  Eager launches, L2 flushed before each step, CUDA
+    events around each step; medians."""
+    import torch
+
+    x, Ws = case["x"], case["Ws"]
+    if not all(isinstance(W, torch.Tensor) for W in Ws):
+        return None
+    outs = [torch.empty((wl.M, W.shape[0]), dtype=x.dtype, device=x.device) for W in Ws]
+    ids = wl.row_adapter
+    groups = []
+    for p, proj in enumerate(wl.projections):
+        per = []
+        for s in wl.used_slots:
+            rows = torch.from_numpy(np.nonzero(ids == s)[0].astype(np.int64)).to(x.device)
+            A, B = wl.adapter(p, int(s))
+            per.append((rows, torch.from_numpy(A).to(x.dtype).to(x.device), torch.from_numpy(B).to(x.dtype).to(x.device),
+                        float(wl.alphas[s]) / float(wl.ranks[s])))
+        groups.append(per)
+
+    def base():
+        for W, o in zip(Ws, outs):
+            torch.matmul(x, W.t(), out=o)
+
+    def looped():
+        base()
+        for per, o in zip(groups, outs):
+            for rows, A, B, sc in per:
+                xr = x.index_select(0, rows)
+                o.index_add_(0, rows, torch.matmul(torch.matmul(xr, A.t()), B.t()), alpha=sc)
+
+    res = {}
+    for name, fn in (("cublas_base_gemm", base), ("torch_adapter_loop", looped)):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        med = statistics.median(ms)
+        res[name] = {"us": round(med * 1e3, 2), "tokens_per_s": round(wl.M / (med / 1e3), 1)}
+    flops = sum(2 * wl.M * W.shape[0] * wl.K for W in Ws)
+    res["cublas_base_gemm"]["tflops"] = round(flops / (res["cublas_base_gemm"]["us"] / 1e6) / 1e12, 1)
+    res["torch_adapter_loop"]["adapters"] = int(wl.used_slots.size)
+    return res
+
+
+SINGLE_THREAD_WORKLOADS = ("tiny_fp32", "decode_bgmv", "decode_70b_qv")
+
+
+def _oracle_rate(wl, seconds, threads):
+    """Rows per second of the float64 oracle over every projection, on a
+    seeded row sample sized so that one pass takes about a second."""
     import oracle
 
-    rows = np.arange(wl.M)
-    cores = oracle.usable_cores()
-    done = 0
+    rng = np.random.default_rng(0)
+    t = time.perf_counter()
+    for p in range(len(wl.projections)):
+        oracle.workload_forward(wl, p, rows=[0], threads=1)
+    row_s = max(time.perf_counter() - t, 1e-5)
+    n = int(max(1, min(wl.M, 1.0 * threads / row_s)))
+    done, reps = 0, 0
     t0 = time.perf_counter()
-    reps = 0
     while True:
+        rows = np.sort(rng.choice(wl.M, size=n, replace=False))
         for p in range(len(wl.projections)):
-            oracle.workload_forward(wl, p, rows=rows, threads=cores)
-        done += rows.size
+            oracle.workload_forward(wl, p, rows=rows, threads=threads)
+        done += n
         reps += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} pass(es) of all {wl.M} rows x {len(wl.projections)} projection(s), "
-                      f"float64 oracle, {cores} threads, {dt:.1f} s"}
+    return done / dt, f"{reps} pass(es) of {n} random rows of {wl.M} x {len(wl.projections)} projection(s), " \
+                      f"float64 oracle, {threads} thread(s), {dt:.1f} s"
+
+
+def cpu_baseline(wl, seconds):
+    import oracle
+
+    cores = oracle.usable_cores()
+    value, sample = _oracle_rate(wl, seconds, cores)
+    out = {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if wl.name in SINGLE_THREAD_WORKLOADS:
+        v1, s1 = _oracle_rate(wl, min(5.0, seconds / 2), 1)
+        out["single_thread"] = {"value": v1, "unit": "tokens/s", "cores": 1, "sample": s1}
+    return out
 
 
 def max_over_ranks(values, device):
@@ -575,6 +672,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local_rank
     res = time_device(case, wl, steps, warmup, flush, dev_index)
     torch.cuda.synchronize()
+    comparators = time_comparators(case, wl, flush) if world == 1 else None
     if world > 1:
         dist.barrier()
     total_ms = sum(res["step_ms"])
@@ -615,7 +713,8 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
     roof["algorithmic_bytes_per_call"] = b
     roof["algorithmic_flops_per_call"] = f
-    roof["time_share"] = round((gemm_ms if gemm_dominant else shrink_ms) / total_ms, 3) if total_ms else None
+    eager_total = sum(res["eager_ms"])
+    roof["time_share"] = round((gemm_ms if gemm_dominant else shrink_ms) / eager_total, 3) if eager_total else None
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -624,6 +723,7 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         "steps": steps,
         "warmup": warmup,
         "ms_per_step": round(total_ms / steps, 5),
+        "step_ms_percentiles": {k: round(v, 5) for k, v in percentiles(res["step_ms"]).items()},
         "replay_ms_per_step": round(sum(res["replay_ms"]) / steps, 5),
         "higher_is_better": True,
         "scaling": "weak",
@@ -649,10 +749,16 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
             "lora_gbs": round(alg["lora_bytes"] / lora_avg_s / 1e9, 1) if lora_avg_s > 0 else None,
             "lora_frac_hbm": round(alg["lora_bytes"] / lora_avg_s / 1e9 / peaks["hbm_gbs"], 4)
             if lora_avg_s > 0 else None,
+            "lora_bytes": alg["lora_bytes"],
+            "lora_bytes_fused_form": alg["lora_bytes_fused"],
+            "intermediate_bytes": alg["intermediate_bytes"],
             "gemm_us": round(gemm_avg_s * 1e6, 3),
             "gemm_tc_frac": round(alg["gemm_flops"] / gemm_avg_s / 1e12 / peaks["bf16_tflops"], 4),
             "gemm_hbm_frac": round(alg["gemm_bytes"] / gemm_avg_s / 1e9 / peaks["hbm_gbs"], 4),
+            "gemm_us_percentiles": {k: round(v * 1e3, 3) for k, v in percentiles(res["gemm_ms"]).items()},
+            "lora_us_percentiles": {k: round(v * 1e3, 3) for k, v in percentiles(res["shrink_ms"]).items()},
         },
+        "comparators": comparators,
         "e2e": {"value": round(whole_job_rate(wl.M * e2e_steps, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "launch": "CUDA graph of the step (copies and forward) replayed per step",

@@ -46,7 +46,8 @@
 extern "C" {
 #endif
 
-#define LORA_ABI_VERSION 4  /* 3: lora_proj_t.w_scale (int8 base weights); 4: w_bits (int4) */
+#define LORA_ABI_VERSION 5  /* 3: lora_proj_t.w_scale (int8 base weights); 4: w_bits (int4);
+                               5: lora_forward_args_t.scales (per-call scales) */
 #define LORA_BLOCK_ROWS 16
 #define LORA_MAX_PROJ 4
 
@@ -300,10 +301,23 @@ typedef struct lora_forward_args {
      * stage durations on the launching stream. */
     void *const *stage_events;
     int32_t num_stage_events; /* 0, or exactly 1 + 2*n_proj */
+    /* Optional per-call adapter scales: NULL, or device fp32 [max_slots]
+     * (16-byte aligned) used for this call in place of every projection's
+     * pool scales, so that row m of slot i gets scales[i] * B_i (A_i x[m]).
+     * The scale belongs with the adapter ("Adapter Residency When One
+     * Replica Serves Many Fine-Tunes", §"What the forward pass has to do
+     * differently"); this lets a caller change an adapter's strength per
+     * call without reloading it.  There is no per-call rank: a slot's rank
+     * is fixed by the blocks it was loaded into, whose rank-rows past that
+     * rank are zero; load the adapter again to change it. */
+    const float *scales;
 } lora_forward_args_t;
 
-/* Scratch bytes lora_linear_forward needs for these arguments (depends on
- * M, the projections' pools and the path chosen), 0 on invalid input. */
+/* Scratch bytes lora_linear_forward needs for these arguments, 0 on invalid
+ * input.  It depends on M, K, every projection's N and pool shape, the form
+ * of the row map and the kernels the call will take, so this function is the
+ * only exact measure of the need: size workspaces (and check calls against
+ * LORA_NOALLOC_SCRATCH_BYTES) with it, not with a formula. */
 size_t lora_forward_workspace_bytes(const lora_forward_args_t *args);
 
 /*
@@ -342,12 +356,14 @@ lora_status_t lora_linear_forward(const lora_forward_args_t *args, void *stream)
  * allocating library routine.
  * Limits and rules:
  *  - Returns LORA_ERR_WORKSPACE, launching nothing, when the call needs more
- *    scratch than LORA_NOALLOC_SCRATCH_BYTES (lora_forward_workspace_bytes
- *    gives the need: per projection M*max_rank*4 bytes plus, with segments,
- *    M*4 bytes, each rounded up to 256).
+ *    scratch than LORA_NOALLOC_SCRATCH_BYTES.  lora_forward_workspace_bytes
+ *    on the same arguments gives the need exactly (it includes the kernels'
+ *    intermediates, split-K partial tiles and counters, not only the rank-r
+ *    intermediate).
  *  - The first call on a device looks up that device's copy of the array
  *    (with the device current), so make that first call before starting
- *    any stream capture on the device.
+ *    any stream capture on the device.  The address is kept per CUDA
+ *    context: after a device reset the next call looks it up again.
  *  - Every call on a device shares the one array, and the array keeps
  *    whatever the last call left in it; the forward itself resets what must
  *    start from a known value.  Calls whose work overlaps on the GPU (for
@@ -364,6 +380,21 @@ lora_status_t lora_linear_forward_noalloc(const lora_forward_args_t *args, void 
  * the row, segment or block index the first error concerned.
  */
 lora_status_t lora_get_device_status(void *stream, int32_t *detail);
+
+/*
+ * Testing hook for the failure path of the kernels' bounded waits (no
+ * counterpart in the pages).  Arms the next lora_linear_forward call on any
+ * thread: in that call every split-K tile-counter wait of the tensor-core
+ * GEMM waits for one arrival more than the launch makes, giving up after
+ * limit_ns (1 ms .. 2 s) instead of the normal 2 s.  The waits then run out:
+ * the GEMM records LORA_ERR_DEVICE_TIMEOUT in the status word, writes no
+ * output for those tiles, releases its tensor memory and ends normally, so
+ * the context stays usable.  The arming is taken by the next call that
+ * passes validation and reaches the device; calls whose GEMM does not split
+ * K take it without effect.  limit_ns = 0 disarms.  Errors: INVALID_ARG
+ * (limit out of range).
+ */
+lora_status_t lora_test_arm_wait_timeout(uint64_t limit_ns);
 
 /* Static, human-readable name of a status code. */
 const char *lora_status_string(lora_status_t status);

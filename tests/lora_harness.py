@@ -20,6 +20,17 @@ from workloads import bf16_round
 BF16_TOL = 2e-2
 FP32_TOL = 1e-4
 
+# Guard regions around every output and the workspace of a forward: rows
+# above and below each output, columns past N in each row (ldo = N + 16),
+# and bytes on both sides of the workspace, all filled with a sentinel and
+# checked unchanged afterwards, so that a stray store past a tile edge fails
+# the test even where the output itself is right.
+GUARD_ROWS = 2
+GUARD_COLS = 16
+GUARD_BYTES = 4096
+SENTINEL = -7.75  # exact in bf16 and fp32
+WS_SENTINEL = 0xA5
+
 
 def row_tolerance(dtype: str, ref: np.ndarray) -> np.ndarray:
     amax = np.max(np.abs(ref), axis=1)
@@ -80,34 +91,80 @@ def device_inputs(wl, device="cuda"):
     return x, Ws
 
 
-def forward(wl, pools, mode: str = "bgmv", device="cuda", ids: Optional[np.ndarray] = None,
-            x=None, Ws=None, outs=None) -> List[np.ndarray]:
-    """Run lora_linear_forward through the C ABI; returns float32 outputs.
+def guarded_output(M: int, N: int, dtype: torch.dtype, device):
+    """An [M, N] output view (row stride N + GUARD_COLS) inside a buffer whose
+    other elements hold SENTINEL; the view itself is NaN-filled, so a missing
+    store shows too.  Returns (view, buffer)."""
+    buf = torch.full((M + 2 * GUARD_ROWS, N + GUARD_COLS), SENTINEL, dtype=dtype, device=device)
+    out = buf[GUARD_ROWS:GUARD_ROWS + M, :N]
+    out.fill_(float("nan"))
+    return out, buf
+
+
+def check_output_guard(buf: torch.Tensor, M: int, N: int, what: str) -> None:
+    g = buf.clone()
+    g[GUARD_ROWS:GUARD_ROWS + M, :N] = SENTINEL
+    bad = int((g != SENTINEL).sum())
+    assert bad == 0, f"{what}: {bad} guard elements around the output were overwritten"
+
+
+def guarded_workspace(nbytes: int, device):
+    """A workspace of nbytes inside a buffer with GUARD_BYTES of WS_SENTINEL
+    on both sides.  Returns (view, buffer)."""
+    buf = torch.full((nbytes + 2 * GUARD_BYTES,), WS_SENTINEL, dtype=torch.uint8, device=device)
+    return buf[GUARD_BYTES:GUARD_BYTES + nbytes], buf
+
+
+def check_workspace_guard(buf: torch.Tensor, what: str) -> None:
+    head, tail = buf[:GUARD_BYTES], buf[buf.numel() - GUARD_BYTES:]
+    bad = int((head != WS_SENTINEL).sum()) + int((tail != WS_SENTINEL).sum())
+    assert bad == 0, f"{what}: {bad} guard bytes around the workspace were overwritten"
+
+
+def index_args(wl, mode: str, ids: np.ndarray, device) -> dict:
+    """The row map of a forward in one of the three forms.
 
     mode "bgmv": per-row ids; "sgmv": host segmenter + permutation;
-    "sorted": the workload's own pre-sorted segments (no permutation).
+    "sorted": the workload's own pre-sorted segments (no permutation)."""
+    if mode == "bgmv":
+        return dict(row_adapter=torch.from_numpy(np.ascontiguousarray(ids, np.int32)).to(device))
+    if mode == "sgmv":
+        perm, offs, adp = segment_rows(ids, wl.num_slots)
+        return dict(seg_offsets=torch.from_numpy(offs).to(device), seg_adapter=torch.from_numpy(adp).to(device),
+                    perm=torch.from_numpy(perm).to(device))
+    if mode == "sorted":
+        return dict(seg_offsets=torch.from_numpy(wl.seg_offsets).to(device),
+                    seg_adapter=torch.from_numpy(wl.seg_adapter).to(device))
+    raise ValueError(mode)
+
+
+def forward(wl, pools, mode: str = "bgmv", device="cuda", ids: Optional[np.ndarray] = None,
+            x=None, Ws=None, outs=None, scales: Optional[torch.Tensor] = None) -> List[np.ndarray]:
+    """Run lora_linear_forward through the C ABI; returns float32 outputs.
+
+    mode: see index_args.  Unless ``outs`` is given, every output and the
+    workspace sit between guard regions that are checked after the call.
+    ``scales``: the call's own per-slot scales (device float32), or None.
     """
     td = torch_dtype(wl.dtype)
     if x is None or Ws is None:
         x, Ws = device_inputs(wl, device)
     ids = wl.row_adapter if ids is None else ids
+    bufs = None
     if outs is None:
-        outs = [torch.full((wl.M, p.N), float("nan"), dtype=td, device=device) for p in wl.projections]
+        made = [guarded_output(wl.M, p.N, td, device) for p in wl.projections]
+        outs, bufs = [o for o, _ in made], [b for _, b in made]
     projs = [(W, pool, out) for W, pool, out in zip(Ws, pools, outs)]
-    if mode == "bgmv":
-        call = LinearCall(x, projs, row_adapter=torch.from_numpy(np.ascontiguousarray(ids, np.int32)).to(device))
-    elif mode == "sgmv":
-        perm, offs, adp = segment_rows(ids, wl.num_slots)
-        call = LinearCall(x, projs, seg_offsets=torch.from_numpy(offs).to(device),
-                          seg_adapter=torch.from_numpy(adp).to(device),
-                          perm=torch.from_numpy(perm).to(device))
-    elif mode == "sorted":
-        call = LinearCall(x, projs, seg_offsets=torch.from_numpy(wl.seg_offsets).to(device),
-                          seg_adapter=torch.from_numpy(wl.seg_adapter).to(device))
-    else:
-        raise ValueError(mode)
+    index = index_args(wl, mode, ids, device)
+    need = LinearCall(x, projs, scales=scales, **index).workspace_bytes
+    ws, ws_buf = guarded_workspace(need, device)
+    call = LinearCall(x, projs, workspace=ws, scales=scales, **index)
     call()
     torch.cuda.synchronize()
+    check_workspace_guard(ws_buf, f"{wl.name} {mode}")
+    if bufs is not None:
+        for p, (b, proj) in enumerate(zip(bufs, wl.projections)):
+            check_output_guard(b, wl.M, proj.N, f"{wl.name} {mode} projection {p}")
     return [o.float().cpu().numpy() for o in outs]
 
 

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.lora_abi_version() == 4
+    assert L.lora_abi_version() == 5
     from adapter_gemm_linear_gb300._lib import STATUS_NAMES
     texts = {L.lora_status_string(c).decode() for c in STATUS_NAMES}
     assert len(texts) == len(STATUS_NAMES) and all(texts)
@@ -122,4 +122,15 @@ def test_forward_validation_without_device(L):
     assert L.lora_forward_workspace_bytes(ctypes.byref(args())) == 0
     # stage events: count must be 1 + 2*n_proj
     assert fwd(ctypes.byref(args(num_stage_events=2)), None) == 1
+    # per-call scales must be 16-byte aligned like every device pointer
+    assert fwd(ctypes.byref(args(scales=0x6004)), None) == 2
     assert L.lora_kernel_launches() == 0
+
+
+def test_wait_timeout_hook_range(L):
+    """The test hook accepts limits of 1 ms to 2 s, and 0 to disarm (left
+    disarmed here, so that no later forward in this process is affected)."""
+    assert L.lora_test_arm_wait_timeout(999_999) == 1
+    assert L.lora_test_arm_wait_timeout(2_000_000_001) == 1
+    assert L.lora_test_arm_wait_timeout(50_000_000) == 0
+    assert L.lora_test_arm_wait_timeout(0) == 0

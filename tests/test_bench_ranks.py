@@ -94,3 +94,44 @@ def test_algorithmic_bytes_of_quantized_base():
     assert bf16["gemm_bytes"] - i4["gemm_bytes"] == N * K * 3 // 2 - N * 4
     assert bf16["gemm_flops"] == i8["gemm_flops"] == i4["gemm_flops"] == 2 * wl.M * N * K
     assert bf16["lora_bytes"] == i8["lora_bytes"] == i4["lora_bytes"]
+
+
+def test_algorithmic_bytes_follow_the_method():
+    """The base GEMM's bytes are (NK + MK + MN) * 2 with no implementation
+    intermediate (34,603,008 for 64 x 4096 -> 4096, as worked out by hand);
+    the standalone LoRA bytes count each distinct adapter once, the adapted
+    rows of x and of y (read and written) and V written and read; the fp32
+    correction array is reported apart as an intermediate."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from workloads import make_config
+    wl = make_config("decode_bgmv")
+    a = bench.algorithmic(wl)
+    M, K, N = 64, 4096, 4096
+    assert a["gemm_bytes"] == (N * K + M * K + M * N) * 2 == 34_603_008
+    assert a["gemm_flops"] == 2 * M * N * K
+    distinct = np.unique(wl.row_adapter[wl.row_adapter >= 0]).size
+    Ma = int((wl.row_adapter >= 0).sum())
+    assert (distinct, Ma) == (a["distinct"], a["adapted_rows"])
+    assert a["lora_bytes"] == distinct * 16 * (K + N) * 2 + Ma * (K + 2 * N) * 2 + 2 * Ma * 16 * 4
+    assert a["lora_bytes_fused"] == distinct * 16 * (K + N) * 2 + 2 * Ma * 16 * 4
+    assert a["intermediate_bytes"] == 2 * M * N * 4
+    assert a["lora_flops"] == 2 * Ma * 16 * (K + N)
+    # large M: the shrink reads the distinct A's and the adapted rows of x and
+    # writes V; the GEMM's share adds the distinct B's and reads V
+    wl = make_config("prefill_sgmv")
+    a = bench.algorithmic(wl)
+    M = 8192
+    rd = int(sum(int(wl.ranks[s]) for s in np.unique(wl.row_adapter)))
+    rr = int(wl.ranks[wl.row_adapter].sum())
+    assert a["lora_bytes"] == rd * K * 2 + M * K * 2 + rr * 4
+    assert a["gemm_bytes"] == (N * K + M * K + M * N) * 2 + rd * N * 2 + rr * 4
+    assert a["gemm_flops"] == 2 * M * N * K
+
+
+def test_percentiles():
+    sys.path.insert(0, ROOT)
+    import bench
+    p = bench.percentiles(list(range(1, 101)))
+    assert p["p50"] == 50.5 and abs(p["p10"] - 10.9) < 1e-9 and abs(p["p90"] - 90.1) < 1e-9

@@ -19,11 +19,15 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _sample_rows(wl, n=48, seed=0):
+def _sample_rows(wl, n=48, seed=0, per_tile=0, tile=128):
     """Rows to check at full size: both ends, segment boundaries, base-only
-    rows, and a seeded random sample."""
+    rows, a seeded random sample, and ``per_tile`` seeded rows of every
+    ``tile``-row token tile (the large-M GEMM's unit along M)."""
     rng = np.random.default_rng(seed)
     rows = {0, wl.M - 1}
+    for t0 in range(0, wl.M, tile) if per_tile else ():
+        rows.update(int(r) for r in rng.choice(np.arange(t0, min(wl.M, t0 + tile)),
+                                                size=min(per_tile, min(wl.M, t0 + tile) - t0), replace=False))
     if wl.seg_offsets is not None:
         for o in wl.seg_offsets[1:-1]:
             rows.update({int(o) - 1, int(o)})
@@ -65,6 +69,25 @@ def test_integer_exact_bitwise(mode):
         want = H.oracle_bf16_bits(H.oracle_rows(wl, p))
         got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         assert np.array_equal(got, want), f"projection {p}: {np.sum(got != want)} outputs differ"
+
+
+@pytest.mark.parametrize("mode", ["sorted", "sgmv", "bgmv"])
+def test_integer_exact_prefill_geometry(mode):
+    """The prefill workload's geometry at a size the oracle finishes in
+    seconds: 2048 tokens in 16 sorted segments that straddle the 128-token
+    tiles, 16 slots with ranks {8, 16, 32, 64} (alpha = 2r) in scattered pool
+    blocks, 5% base-only rows.  Integer inputs, so the large-M path (the LoRA
+    term on the tensor cores) must be bit-exact for every row."""
+    wl = synth(M=2048, K=1024, Ns=[1032], num_slots=16, rank_choices=(8, 16, 32, 64), integer=True,
+               seed=2048, none_frac=0.05, mode="sgmv")
+    assert sorted(set(int(r) for r in wl.ranks)) == [8, 16, 32, 64]
+    straddle = [int(o) for o in wl.seg_offsets[1:-1] if int(o) % 128]
+    assert len(straddle) >= 8
+    pools = H.make_pools(wl, DEV, extra_blocks=29)
+    out = H.forward(wl, pools, mode)[0]
+    want = H.oracle_bf16_bits(H.oracle_rows(wl, 0))
+    got = torch.from_numpy(out).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want), f"{mode}: {np.sum(got != want)} outputs differ"
 
 
 @pytest.mark.parametrize("shape", [(64, 2048, (264, 520)), (37, 1024, (1032,)), (700, 192, (136,))])
@@ -237,10 +260,14 @@ def test_decode_bgmv_full():
 
 
 def test_prefill_sgmv_sampled():
+    """The full prefill workload: two rows of every 128-token tile (each
+    tile has its own slot range on the large-M path), the segment
+    boundaries and a random sample, against the oracle."""
     wl = make_config("prefill_sgmv")
     pools = H.make_pools(wl, DEV)
     out = H.forward(wl, pools, "sorted")[0]
-    rows = _sample_rows(wl)
+    rows = _sample_rows(wl, per_tile=2)
+    assert len(set(int(r) // 128 for r in rows)) == wl.M // 128
     H.assert_close("bf16", out[rows], H.oracle_rows(wl, 0, rows), "prefill_sgmv")
     assert not np.isnan(out).any()
 
@@ -264,14 +291,15 @@ def test_slora_mixed_sampled():
     assert not np.isnan(out).any()
 
 
-@pytest.mark.parametrize("cfg", ["tiny_fp32", "decode_bgmv", "slora_mixed"])
+@pytest.mark.parametrize("cfg", ["tiny_fp32", "decode_bgmv", "prefill_sgmv", "decode_70b_qv", "slora_mixed"])
 def test_mutations_fail_tolerance(cfg):
     """Outputs computed with a wrong assignment or scale must fail the
-    tolerance against the true oracle: (i) every id forced to -1, (ii) ids
-    rotated to another slot, (iii) every scale halved."""
+    tolerance against the true oracle, on every workload and every
+    projection: (i) every id forced to -1, (ii) ids rotated to another slot,
+    (iii) every scale halved.  The unmutated forward passes on the same rows,
+    so the tolerance separates the two."""
     wl = make_config(cfg)
     rows = _sample_rows(wl, n=32) if wl.M > 64 else np.arange(wl.M)
-    ref = H.oracle_rows(wl, 0, rows)
     ids = wl.row_adapter
     none = np.full_like(ids, -1)
     used = wl.used_slots
@@ -279,12 +307,17 @@ def test_mutations_fail_tolerance(cfg):
     for k, s in enumerate(used):
         rot[ids == s] = used[(k + 1) % used.size]
     pools = H.make_pools(wl, DEV)
-    out_none = H.forward(wl, pools, "bgmv", ids=none)[0]
-    out_rot = H.forward(wl, pools, "bgmv", ids=rot)[0]
+    outs_ok = H.forward(wl, pools, "bgmv")
+    outs_none = H.forward(wl, pools, "bgmv", ids=none)
+    outs_rot = H.forward(wl, pools, "bgmv", ids=rot)
+    del pools
     half = H.make_pools(wl, DEV, alpha_scale=0.5)
-    out_half = H.forward(wl, half, "bgmv")[0]
-    for name, out in (("none", out_none), ("rotated", out_rot), ("half scale", out_half)):
-        assert H.fails_tolerance(wl.dtype, out[rows], ref), f"{cfg}: mutation '{name}' passed"
+    outs_half = H.forward(wl, half, "bgmv")
+    for p in range(len(wl.projections)):
+        ref = H.oracle_rows(wl, p, rows)
+        H.assert_close(wl.dtype, outs_ok[p][rows], ref, f"{cfg} p{p} unmutated")
+        for name, outs in (("none", outs_none), ("rotated", outs_rot), ("half scale", outs_half)):
+            assert H.fails_tolerance(wl.dtype, outs[p][rows], ref), f"{cfg} p{p}: mutation '{name}' passed"
 
 
 def test_base_only_and_empty():
