@@ -456,18 +456,16 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         v.num_blocks = d.num_blocks;
         v.max_rank = d.max_rank;
         v.V = nullptr;
-        // large M in bf16 with few slot columns: the LoRA term joins the
-        // GEMM's K on the tensor cores (Vm, Bm; no fp32 V)
-        const int64_t cols = (static_cast<int64_t>(d.max_slots) * d.max_rank + 63) / 64 * 64;
-        v.ext_cols = (a->dtype == LORA_BF16 && a->M > 0 && !lora::plan_tc(a->M, d.N, a->K).swap &&
-                      cols <= lora::kExtMaxCols)
-                         ? static_cast<int32_t>(cols)
-                         : 0;
-        v.vm = v.bm = v.adense = nullptr;
-        v.tile_range = nullptr;
+        // large M in bf16: the LoRA term on the tensor cores, per token tile
+        // over the pool blocks its rows use (lora_tiles.cu); V (below) then
+        // serves only tiles that take the CUDA-core fallback
+        v.lora_tiles = (a->dtype == LORA_BF16 && a->M > 0 && !lora::plan_tc(a->M, d.N, a->K).swap) ? 1 : 0;
+        v.tile_plan = v.tile_counter = nullptr;
+        v.shrink_part = nullptr;
+        v.vt = nullptr;
+        v.shrink_grid = 0;
         ws->v_off[i] = off;
-        if (v.ext_cols == 0)
-            off += align_up(sizeof(float) * static_cast<size_t>(a->M) * d.max_rank * plan->v_parts, 256);
+        off += align_up(sizeof(float) * static_cast<size_t>(a->M) * d.max_rank * plan->v_parts, 256);
     }
     // slot ids of every pool must mean the same adapters
     for (int i = 1; i < a->n_proj; ++i)
@@ -510,24 +508,28 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     off += align_up(ycorr, 256);
     ws->group_off = off;
     if (ycorr) off += align_up(sizeof(int32_t) * lora::group_table_ints(a->M), 256);
-    // the tensor-core LoRA term of large M: Vm, Bm and the token tiles' slot
-    // ranges, shared by the projections
-    size_t vm = 0, bm = 0, ad = 0;
-    for (int i = 0; i < a->n_proj; ++i) {
-        const lora::ProjView &v = plan->proj[i];
-        if (v.ext_cols == 0) continue;
-        vm = std::max(vm, sizeof(uint16_t) * static_cast<size_t>(a->M) * 2 * v.ext_cols);
-        bm = std::max(bm, sizeof(uint16_t) * static_cast<size_t>(v.N) * v.ext_cols);
-        ad = std::max(ad, sizeof(uint16_t) * static_cast<size_t>(v.ext_cols) * a->K);
+    // the tensor-core LoRA term of large M: tile plans and counters, the
+    // shrink's partial tiles and Vt, shared by the projections (their kernels
+    // run one after the other on the stream)
+    size_t plan_b = 0, tcount_b = 0, spart_b = 0, vt_b = 0;
+    int sgrid = 0;
+    if (a->n_proj > 0 && plan->proj[0].lora_tiles) {
+        const size_t T = (static_cast<size_t>(a->M) + lora::kPlanRows - 1) / lora::kPlanRows;
+        plan_b = sizeof(int32_t) * T * lora::kPlanInts;
+        tcount_b = sizeof(int32_t) * T;
+        sgrid = lora::tc_shrink_grid(a->M, a->K);
+        spart_b = lora::tc_shrink_part_bytes(sgrid);
+        vt_b = sizeof(uint16_t) * T * lora::kPlanRows * lora::kVtCols;
     }
-    ws->vm_off = off;
-    off += align_up(vm, 256);
-    ws->bm_off = off;
-    off += align_up(bm, 256);
-    ws->adense_off = off;
-    off += align_up(ad, 256);
-    ws->range_off = off;
-    if (vm) off += align_up(sizeof(int32_t) * 2 * static_cast<size_t>((a->M + 127) / 128), 256);
+    for (int i = 0; i < a->n_proj; ++i) plan->proj[i].shrink_grid = plan->proj[i].lora_tiles ? sgrid : 0;
+    ws->plan_off = off;
+    off += align_up(plan_b, 256);
+    ws->tcount_off = off;
+    off += align_up(tcount_b, 256);
+    ws->spart_off = off;
+    off += align_up(spart_b, 256);
+    ws->vt_off = off;
+    off += align_up(vt_b, 256);
     ws->counter_off = off;  // last: the counters run to the end of the workspace
     off += align_up(cnt, 256);
     ws->total = off;
@@ -572,11 +574,11 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
     }
     plan.group_table = reinterpret_cast<int32_t *>(base + ws.group_off);
     for (int i = 0; i < plan.n_proj; ++i) {
-        if (plan.proj[i].ext_cols == 0) continue;
-        plan.proj[i].vm = base + ws.vm_off;
-        plan.proj[i].bm = base + ws.bm_off;
-        plan.proj[i].adense = base + ws.adense_off;
-        plan.proj[i].tile_range = reinterpret_cast<int32_t *>(base + ws.range_off);
+        if (!plan.proj[i].lora_tiles) continue;
+        plan.proj[i].tile_plan = reinterpret_cast<int32_t *>(base + ws.plan_off);
+        plan.proj[i].tile_counter = reinterpret_cast<int32_t *>(base + ws.tcount_off);
+        plan.proj[i].shrink_part = reinterpret_cast<float *>(base + ws.spart_off);
+        plan.proj[i].vt = base + ws.vt_off;
     }
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);
     plan.n_counters = static_cast<int32_t>((ws.total - ws.counter_off) / sizeof(int32_t));

@@ -74,15 +74,28 @@ struct ProjView {
     int32_t max_slots, bps, num_blocks, max_rank;
     float *V;              // workspace: [v_parts][M][max_rank] fp32
     float *ycorr;          // workspace: fp32 [M][N] LoRA correction of the small-M orientation
-    // large M, LoRA term on the tensor cores (ext_cols > 0): the GEMM's K runs
-    // on over [Vm_hi | Vm_lo] x [Bm | Bm]; slot s owns columns [s*max_rank, (s+1)*max_rank)
-    int32_t ext_cols;      // columns of Bm = of each half of Vm (a multiple of 64), 0: not used
-    void *vm;              // workspace: bf16 [M][2 ext_cols]: s_i V of the row's slot, hi and lo parts
-    void *bm;              // workspace: bf16 [N][ext_cols]: every slot's B, zero past its rank
-    void *adense;          // workspace: bf16 [ext_cols][K]: every slot's A rows, zero past its rank
-    int32_t *tile_range;   // workspace: [ceil(M/128)][2] lowest and highest slot of each token tile
+    // large M in bf16: the LoRA term on the tensor cores (lora_tiles.cu).  Per
+    // 128-token tile, the pool blocks of the slots its rows use (tile_plan);
+    // Vt holds s_i V of each row as bf16 hi and lo parts per block entry; the
+    // GEMM adds them times the blocks' B as extra MMAs.
+    int32_t lora_tiles;    // 1: this path (tile_plan, tile_counter, shrink_part, vt set)
+    int32_t *tile_plan;    // workspace: int32 [tiles][kPlanInts]
+    int32_t *tile_counter; // workspace: int32 [tiles], k-blocks summed per tile
+    float *shrink_part;    // workspace: fp32 partial tiles of the shrink, [shrink_grid][2][kPlanRows][256]
+    void *vt;              // workspace: bf16 [tiles * kPlanRows][kVtCols]
+    int32_t shrink_grid;   // CTAs of the tensor-core shrink
 };
-constexpr int kExtMaxCols = 2048;  // largest max_slots * max_rank (rounded to 64) for the extension
+
+// Large-M LoRA term (lora_tiles.cu).  A plan tile is the GEMM's token tile;
+// its record: [0] = nb, the pool blocks it lists (-1: more than
+// kPlanMaxBlocks, rows take the CUDA-core fallback), [kPlanBlkOff + e] = block
+// id and [kPlanSlotOff + e] = slot of entry e.
+constexpr int kPlanRows = 128;
+constexpr int kPlanMaxBlocks = 16;
+constexpr int kPlanInts = 48;
+constexpr int kPlanBlkOff = 16;
+constexpr int kPlanSlotOff = 32;
+constexpr int kVtCols = 2 * LORA_BLOCK_ROWS * kPlanMaxBlocks;  // hi parts, then lo parts
 
 // Rows grouped by adapter slot (device int32 arrays in the workspace):
 // count[0] = G groups; group g holds the sorted positions [start[g],
@@ -146,7 +159,7 @@ struct WorkspaceLayout {
     size_t part_off;              // fp32 split-K partial tiles (largest projection)
     size_t ycorr_off;             // fp32 [M][N] correction of the small-M orientation (largest projection)
     size_t group_off;             // int32 group table (small-M orientation)
-    size_t vm_off, bm_off, adense_off, range_off;  // large-M tensor-core LoRA term: Vm, Bm, A_dense, tile slot ranges
+    size_t plan_off, tcount_off, spart_off, vt_off;  // large-M tensor-core LoRA term
     size_t counter_off;           // int32 per output tile (split-K)
     size_t total;
 };
@@ -175,13 +188,13 @@ cudaError_t launch_forward(const ForwardPlan &plan, cudaStream_t stream);
 // Multiprocessors of the current device (cached per device; 148 if unknown).
 int device_sm_count();
 
-// Large M with the LoRA term on the tensor cores (lora_kernels.cu): Bm and
-// A_dense from the pool's blocks and the token tiles' slot ranges
-// (ext_prepare), then Vm by a GEMM x A_dense^T (launch_gemm_vm); the main
-// GEMM adds [Vm] x [Bm]^T.
-cudaError_t launch_ext_prepare(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
-// V of the large-M tensor-core path as a GEMM x A_dense^T into Vm (tc_gemm.cu).
-cudaError_t launch_gemm_vm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+// Large M with the LoRA term on the tensor cores (lora_tiles.cu): the tile
+// plan (block lists; per-row V of fallback tiles), then the tensor-core
+// shrink into Vt; the main GEMM adds Vt x B_block^T per listed block.
+int tc_shrink_grid(int32_t M, int32_t K);
+size_t tc_shrink_part_bytes(int grid);
+cudaError_t launch_tile_plan(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+cudaError_t launch_tc_shrink(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
 
 // The small-M LoRA path by adapter group (lora_grouped.cu): the rows' group
 // table (rows sorted by slot), then per projection the grouped shrink into

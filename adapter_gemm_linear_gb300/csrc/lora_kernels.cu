@@ -288,243 +288,6 @@ shrink_simt_kernel(const T *__restrict__ x, int32_t ldx, int32_t K, const int32_
 }
 
 // ---------------------------------------------------------------------------
-// bf16 shrink for the tensor-core path: V[m, 16t + j] = sum_k A_i[16t + j, k] x[m, k]
-// grid (M, blocks per slot), 256 threads, one row x one 16-row block per CTA.
-// Each thread takes 8 consecutive k per step and keeps kBatch steps of loads
-// (the x vector and the 16 A vectors of each step) in flight before using
-// them, so a CTA has up to 256 * kBatch * 17 * 16 bytes outstanding; with
-// K = 4096 and kBatch = 2 that is the whole 128 KiB block in one round trip.
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ float dot8_bf16(const uint4 &a, const float (&xv)[8], float acc) {
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        acc = fmaf(__uint_as_float(w[i] << 16), xv[2 * i], acc);
-        acc = fmaf(__uint_as_float(w[i] & 0xFFFF0000u), xv[2 * i + 1], acc);
-    }
-    return acc;
-}
-
-template <int kBatch>
-__global__ void __launch_bounds__(256)
-shrink_rows_bf16_kernel(const __nv_bfloat16 *__restrict__ x, int32_t ldx, int32_t K,
-                        const int32_t *__restrict__ row_slot, const __nv_bfloat16 *__restrict__ a_arena,
-                        const int32_t *__restrict__ table, const int32_t *__restrict__ ranks,
-                        int32_t max_slots, int32_t bps, int32_t num_blocks, float *__restrict__ V,
-                        int32_t ldv, unsigned long long *status, int32_t *__restrict__ counters,
-                        int32_t n_counters) {
-    constexpr int kThreadsS = 256;
-    const int32_t m = blockIdx.x;
-    const int32_t t = blockIdx.y;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in shrink_simt_kernel
-    // the split-K tile counters of the GEMM that follows start from zero
-    if (m == 0 && t == 0)
-        for (int32_t c = threadIdx.x; c < n_counters; c += kThreadsS) counters[c] = 0;
-    int32_t r;
-    float s;
-    const int32_t i = resolve_slot(row_slot[m], m, ranks, nullptr, max_slots, bps, &r, &s, status,
-                                   t == 0 && threadIdx.x == 0);
-    if (i < 0 || t * LORA_BLOCK_ROWS >= r) return;
-    const int32_t b = table[i * bps + t];
-    if (b < 0 || b >= num_blocks) {
-        if (threadIdx.x == 0) record_error(status, kDevBadBlock, static_cast<uint32_t>(i));
-        return;
-    }
-    const uint4 *A = reinterpret_cast<const uint4 *>(a_arena + static_cast<size_t>(b) * LORA_BLOCK_ROWS * K);
-    const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * ldx);
-    const int32_t K8 = K / 8;  // 16-byte vectors per row
-    float acc[LORA_BLOCK_ROWS];
-#pragma unroll
-    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = 0.0f;
-#pragma unroll 1
-    for (int32_t k0 = threadIdx.x; k0 < K8; k0 += kBatch * kThreadsS) {
-        uint4 xq[kBatch];
-        uint4 aq[kBatch][LORA_BLOCK_ROWS];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int32_t k = k0 + u * kThreadsS;
-            if (k < K8) {
-                xq[u] = __ldg(xr + k);
-#pragma unroll
-                for (int j = 0; j < LORA_BLOCK_ROWS; ++j) aq[u][j] = __ldg(A + static_cast<size_t>(j) * K8 + k);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            if (k0 + u * kThreadsS < K8) {
-                float xv[8];
-                const uint32_t w[4] = {xq[u].x, xq[u].y, xq[u].z, xq[u].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    xv[2 * q] = __uint_as_float(w[q] << 16);
-                    xv[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-                }
-#pragma unroll
-                for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = dot8_bf16(aq[u][j], xv, acc[j]);
-            }
-        }
-    }
-    __shared__ float red[kThreadsS / 32][LORA_BLOCK_ROWS];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
-        float v = acc[j];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[warp][j] = v;
-    }
-    __syncthreads();
-    if (threadIdx.x < LORA_BLOCK_ROWS) {
-        float v = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kThreadsS / 32; ++w) v += red[w][threadIdx.x];
-        V[static_cast<size_t>(m) * ldv + t * LORA_BLOCK_ROWS + threadIdx.x] = v;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Large M, LoRA term on the tensor cores: the GEMM's K extends over
-//   [Vm_hi | Vm_lo] (beside x) and [Bm | Bm] (beside W),
-// Bm[n][s*R + j] = B_s[n][j] (zero for j >= r_s and for empty slots or
-// corrupt block entries), Vm[m][s*R + j] = hi / lo bf16 parts of s_i V[m][j]
-// for the row's own slot s (zero elsewhere), R = the pool's max rank.  The
-// two bf16 parts carry about 16 significant bits of s_i V, so Vm Bm^T adds the
-// correction to the fp32 accumulator with the precision of an fp32 V.  V itself
-// is a GEMM x A_dense^T (tc_gemm.cu, vm mode) with A_dense[s*R + j] = A_s[j].
-// ---------------------------------------------------------------------------
-
-// Per-slot validity of the dense copies: the slot's rank blocks, or 0 when
-// the slot is empty or one of its block entries is corrupt (its rows then get
-// no correction, as on every other path).
-__device__ __forceinline__ int32_t dense_blocks(int32_t slot, const int32_t *table, const int32_t *ranks,
-                                                int32_t bps, int32_t num_blocks) {
-    const int32_t r = ranks[slot];
-    if (r <= 0 || r > bps * LORA_BLOCK_ROWS) return 0;
-    const int32_t nblk = (r + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
-    for (int32_t jb = 0; jb < nblk; ++jb) {
-        const int32_t blk = table[static_cast<size_t>(slot) * bps + jb];
-        if (blk < 0 || blk >= num_blocks) return 0;
-    }
-    return nblk;
-}
-
-struct ExtPrepareParams {
-    int32_t M, N, K, max_slots, R, ext_cols, bps, num_blocks;
-    const __nv_bfloat16 *a_arena, *b_arena;
-    const int32_t *table, *ranks, *row_slot;
-    __nv_bfloat16 *bm, *adense;
-    int32_t *tile_range;
-};
-
-// blockIdx.y selects the job, blockIdx.x walks it:
-//   0: Bm row n, slot s: the slot's R columns, 32 bytes (16 ranks of one pool
-//      block) at a time; slot index max_slots writes the zero padding;
-//   1: A_dense row c (slot c / R, rank c % R), 8 columns per thread;
-//   2: one warp per token tile: the lowest and highest slot its rows name.
-__global__ void __launch_bounds__(256) ext_prepare_kernel(const ExtPrepareParams p) {
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    if (blockIdx.y == 0) {
-        if (gid >= static_cast<int64_t>(p.N) * (p.max_slots + 1)) return;
-        const int32_t slot = static_cast<int32_t>(gid % (p.max_slots + 1));
-        const int32_t n = static_cast<int32_t>(gid / (p.max_slots + 1));
-        uint4 *dst_row = reinterpret_cast<uint4 *>(p.bm + static_cast<size_t>(n) * p.ext_cols);
-        if (slot == p.max_slots) {  // padding columns
-            for (int32_t c = p.max_slots * p.R; c < p.ext_cols; c += LORA_BLOCK_ROWS) {
-                dst_row[c / 8] = zero;
-                dst_row[c / 8 + 1] = zero;
-            }
-            return;
-        }
-        const int32_t nblk = dense_blocks(slot, p.table, p.ranks, p.bps, p.num_blocks);
-        for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < p.R; ++jb) {
-            uint4 q0 = zero, q1 = zero;
-            if (jb < nblk) {
-                const int32_t blk = p.table[static_cast<size_t>(slot) * p.bps + jb];
-                const uint4 *src =
-                    reinterpret_cast<const uint4 *>(p.b_arena + (static_cast<size_t>(blk) * p.N + n) * LORA_BLOCK_ROWS);
-                q0 = __ldg(src);
-                q1 = __ldg(src + 1);
-            }
-            const int32_t c = slot * p.R + jb * LORA_BLOCK_ROWS;
-            dst_row[c / 8] = q0;
-            dst_row[c / 8 + 1] = q1;
-        }
-    } else if (blockIdx.y == 1) {
-        const int32_t K8 = p.K / 8;
-        if (gid >= static_cast<int64_t>(p.ext_cols) * K8) return;
-        const int32_t c = static_cast<int32_t>(gid / K8);
-        const int32_t k8 = static_cast<int32_t>(gid % K8);
-        uint4 q = zero;
-        const int32_t slot = c / p.R, j = c % p.R;
-        if (slot < p.max_slots) {
-            const int32_t nblk = dense_blocks(slot, p.table, p.ranks, p.bps, p.num_blocks);
-            const int32_t jb = j / LORA_BLOCK_ROWS;
-            if (jb < nblk) {
-                const int32_t blk = p.table[static_cast<size_t>(slot) * p.bps + jb];
-                q = __ldg(reinterpret_cast<const uint4 *>(
-                          p.a_arena + (static_cast<size_t>(blk) * LORA_BLOCK_ROWS + j % LORA_BLOCK_ROWS) * p.K) +
-                      k8);
-            }
-        }
-        reinterpret_cast<uint4 *>(p.adense + static_cast<size_t>(c) * p.K)[k8] = q;
-    } else {
-        const int64_t tile = gid / 32;
-        const int lane = threadIdx.x & 31;
-        if (tile >= (p.M + 127) / 128) return;  // whole warps: 128 rows per tile
-        int32_t lo = 0x7fffffff, hi = -1;
-        for (int32_t i = lane; i < 128; i += 32) {
-            const int32_t m = static_cast<int32_t>(tile) * 128 + i;
-            if (m >= p.M) break;
-            const int32_t id = p.row_slot[m];
-            if (id >= 0 && id < p.max_slots) {
-                lo = min(lo, id);
-                hi = max(hi, id);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-        }
-        if (lane == 0) {
-            p.tile_range[2 * tile] = lo;
-            p.tile_range[2 * tile + 1] = hi;
-        }
-    }
-}
-
-cudaError_t launch_ext_prepare(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
-    ExtPrepareParams p;
-    p.M = plan.M;
-    p.N = v.N;
-    p.K = plan.K;
-    p.max_slots = v.max_slots;
-    p.R = v.max_rank;
-    p.ext_cols = v.ext_cols;
-    p.bps = v.bps;
-    p.num_blocks = v.num_blocks;
-    p.a_arena = static_cast<const __nv_bfloat16 *>(v.a_arena);
-    p.b_arena = static_cast<const __nv_bfloat16 *>(v.b_arena);
-    p.table = v.table;
-    p.ranks = v.ranks;
-    p.row_slot = plan.row_slot;
-    p.bm = static_cast<__nv_bfloat16 *>(v.bm);
-    p.adense = static_cast<__nv_bfloat16 *>(v.adense);
-    p.tile_range = v.tile_range;
-    const int block = 256;
-    const int64_t jobs[3] = {static_cast<int64_t>(v.N) * (v.max_slots + 1),
-                             static_cast<int64_t>(v.ext_cols) * (plan.K / 8),
-                             32 * static_cast<int64_t>((plan.M + 127) / 128)};
-    int64_t most = 0;
-    for (int64_t j : jobs) most = j > most ? j : most;
-    const int64_t gx = (most + block - 1) / block;
-    ext_prepare_kernel<<<dim3(static_cast<unsigned>(gx), 3), block, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
 // SIMT GEMM with the expand fused into the epilogue:
 // out[m, n] = sum_k x[m,k] W[n,k] + s_i * sum_j B_i[n, j] V[m, j]
 // 64x64 tile, 256 threads, 4x4 outputs per thread (rows ty+16a, cols tx+16b)
@@ -646,14 +409,6 @@ static cudaError_t launch_forward_simt(const ForwardPlan &plan, cudaStream_t str
     return cudaSuccess;
 }
 
-// bf16.  Small M (the GEMM's swapped orientation): per projection the LoRA
-// term into plan.ycorr (lora_grouped.cu) -- by one per-row kernel when each
-// row's A and B are cheap to read, else by the pipelined grouped shrink and
-// expand (lora_pipe.cu; for larger pools, the rows' group table and the
-// grouped kernels of lora_grouped.cu) -- then the GEMM, which adds it.  Large M: the
-// per-row shrink, then the GEMM, whose epilogue applies the expand.  The GEMM
-// is launched as a programmatic dependent of the kernel before it (see
-// tc_gemm.cu).
 // Several projections, each's LoRA term by the per-row kernel: one launch of
 // it for all of them, then the GEMMs, two projections per launch, each launch
 // a programmatic dependent of the kernel before it and with its own split-K
@@ -688,8 +443,16 @@ static cudaError_t launch_forward_fused_rows(const ForwardPlan &plan, cudaStream
     return cudaSuccess;
 }
 
+// bf16.  Small M (the GEMM's swapped orientation): per projection the LoRA
+// term into plan.ycorr (lora_grouped.cu) -- by one per-row kernel when each
+// row's A and B are cheap to read, else by the pipelined grouped shrink and
+// expand (lora_pipe.cu; for larger pools, the rows' group table and the
+// grouped kernels of lora_grouped.cu) -- then the GEMM, which adds it.  Large
+// M: the token tiles' block lists and the tensor-core shrink (lora_tiles.cu),
+// then the GEMM, which adds the expand as extra MMAs per listed pool block.
+// The GEMM is launched as a programmatic dependent of the kernel before it
+// (see tc_gemm.cu).
 static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t stream) {
-    using T = __nv_bfloat16;
     const bool swapped = plan_tc(plan.M, plan.proj[0].N, plan.K).swap;
     if (plan.fused_rows) return launch_forward_fused_rows(plan, stream);
     bool by_row = swapped;
@@ -719,25 +482,11 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
             e = launch_shrink_grouped(plan, v, gt, stream);
             if (e == cudaSuccess) e = launch_expand_grouped(plan, v, gt, stream);
             if (e != cudaSuccess) return e;
-        } else if (v.ext_cols > 0) {
-            e = launch_ext_prepare(plan, v, stream);
-            if (e == cudaSuccess) e = launch_gemm_vm(plan, v, stream);
-            if (e != cudaSuccess) return e;
         } else {
-            dim3 sgrid(plan.M, v.bps);
-            // few (row, block) pairs: the wide kernel that keeps a whole A
-            // block in flight per CTA; many: the narrow one, several CTAs per SM
-            if (static_cast<int64_t>(plan.M) * v.bps <= 4 * static_cast<int64_t>(device_sm_count()))
-                shrink_rows_bf16_kernel<2><<<sgrid, 256, 0, stream>>>(
-                    static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
-                    static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
-                    v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
-            else
-                shrink_simt_kernel<T><<<sgrid, 128, 0, stream>>>(
-                    static_cast<const T *>(plan.x), plan.ldx, plan.K, plan.row_slot,
-                    static_cast<const T *>(v.a_arena), v.table, v.ranks, v.max_slots, v.bps, v.num_blocks,
-                    v.V, v.max_rank, plan.status, plan.counters, plan.n_counters);
-            e = cudaGetLastError();
+            // large M: the tiles' block lists (and the per-row V of tiles
+            // whose adapters span too many blocks), then V on the tensor cores
+            e = launch_tile_plan(plan, v, stream);
+            if (e == cudaSuccess) e = launch_tc_shrink(plan, v, stream);
             if (e != cudaSuccess) return e;
         }
         if (plan.stage_events) {
@@ -746,7 +495,7 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
         }
         e = launch_gemm_lora_tc(plan, v, stream);
         if (e != cudaSuccess) return e;
-        count_launches((swapped && !by_row) || (!swapped && v.ext_cols > 0) ? 3 : 2);
+        count_launches(swapped && by_row ? 2 : 3);
         if (plan.stage_events) {
             e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[2 + 2 * p]), stream);
             if (e != cudaSuccess) return e;

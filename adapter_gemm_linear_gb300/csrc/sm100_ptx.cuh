@@ -235,6 +235,16 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
+// The same for a K-major tile stored with the 32-byte swizzle: rows of 32
+// bytes (16 bf16 along K: one MMA's K), groups of 8 rows 256 bytes apart
+// (stride byte offset), tile base 256-byte aligned, layout type 6 = 32-byte
+// swizzle.  Written by a TMA box of 16 columns with CU_TENSOR_MAP_SWIZZLE_32B.
+__device__ __forceinline__ uint64_t desc_kmajor_sw32(uint32_t smem_addr) {
+    return static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(256 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(6) << 61);
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16 with bf16 A and B, fp32 D,
 // both operands K-major, no negation: D format F32 (bits 4-5 = 1), A format
 // BF16 (7-9 = 1), B format BF16 (10-12 = 1), N >> 3 (17-22), M >> 4 (24-28).

@@ -1,13 +1,25 @@
 // Base GEMM on the 5th-generation tensor cores (tcgen05, fp32 accumulators in
-// TMEM, operands staged by TMA) with the LoRA term added in the epilogue:
+// TMEM, operands staged by TMA) with the LoRA term added before the rounding:
 //
 //   out[m, n] = round( sum_k x[m,k] W[n,k]  +  s_i * sum_j B_i[n,j] V[m,j] )
 //
 // where i is row m's adapter slot (none: no second term), V = A_i x is the
-// rank-r intermediate (fp32, from the shrink kernel), B_i's entries are
-// gathered through the pool's block table, and s_i = alpha_i / r_i.  The
-// correction is added to the fp32 accumulator, so each output is rounded to
-// bf16 exactly once.
+// rank-r intermediate and s_i = alpha_i / r_i.  The correction is added to
+// the fp32 accumulator, so each output is rounded to bf16 exactly once.
+//
+// Where the LoRA term comes from:
+//   small M (swapped orientation)  the LoRA kernels before this one write the
+//                whole correction as an fp32 [M][N] array (ycorr), added in
+//                the epilogue;
+//   large M (non-swapped)          the tensor cores add it: after a unit's
+//                main k-blocks come one step per pool block of its token
+//                tile's plan (lora_tiles.cu), two MMAs of K = 16 each, with
+//                A = the tile's s_i V as bf16 hi and lo parts (Vt, from the
+//                tensor-core shrink) and B = the block's 16 rank-columns of B
+//                for the unit's output columns, loaded straight from the
+//                pool's B arena; tiles whose adapters span more blocks than a
+//                plan lists take a CUDA-core expand in the epilogue (V per row
+//                from the plan kernel, B gathered through the block table).
 //
 // Persistent kernel: one CTA per SM walks a list of work units; a unit is an
 // output tile (and, for split-K, one K range of it).  Two orientations:
@@ -46,6 +58,7 @@
 #include "lora_device.cuh"
 #include "lora_internal.h"
 #include "sm100_ptx.cuh"
+#include "tensor_map.h"
 
 namespace lora {
 
@@ -60,7 +73,7 @@ constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kSmemLimit = 226 * 1024;   // dynamic shared memory per CTA (227 KiB opt-in maximum)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kEpiBarrier = 1;         // named barrier of the epilogue warps
-constexpr int kMaxUnitList = 256;      // shrink mode: active units one CTA can take
+constexpr uint32_t kVtBoxBytes = kBM * LORA_BLOCK_ROWS * 2;  // a [128 x 16] bf16 box of Vt
 constexpr int kTaBand = 8;             // non-swapped unit order: token tiles per band
 
 struct TcParams {
@@ -81,19 +94,14 @@ struct TcParams {
     size_t v_part_stride;   // elements between the planes
     float *part;        // split-K partial tiles [splits][tiles][BN][128] fp32 (splits > 1)
     const float *ycorr; // swapped orientation: fp32 [M][N] LoRA correction from the expand kernel
-    // non-swapped orientation, LoRA term on the tensor cores: extra k-blocks
-    // over [Vm_hi | Vm_lo] (A side) and [Bm | Bm] (B side); Vm is [M][2 ext_cols],
-    // Bm [N][ext_cols], slot s owning columns [s*ext_rank, (s+1)*ext_rank)
-    int32_t ext;             // 0: the epilogue applies the expand instead
-    int32_t ext_cols;        // columns per half of Vm (a multiple of kBK)
-    int32_t ext_rank;        // columns per slot (the pool's max rank)
-    const int32_t *tile_range;  // [token tiles][2]: lowest and highest slot of the tile's rows
-    // shrink mode (non-swapped, W = A_dense [ext_cols][K]): the tile's fp32
-    // result x A_dense^T becomes the hi and lo bf16 parts of s_i V in vm_out
-    // ([M][2 ext_cols]), masked to the row's own slot columns; units whose
-    // columns lie outside their token tile's slot range are skipped
-    int32_t vm_mode;
-    __nv_bfloat16 *vm_out;
+    // non-swapped orientation, LoRA term on the tensor cores: after the main
+    // k-blocks, one step per pool block e listed in the token tile's plan,
+    // two MMAs of K = 16: [Vt_hi | Vt_lo](tile rows, 16e:16e+16) (tma_va) times
+    // the block's 16 rank-columns of B for the tile's output columns (tma_vb,
+    // straight from the pool's B arena).  Tiles whose plan is -1 take the
+    // CUDA-core expand in the epilogue instead (V from the plan kernel).
+    int32_t lora_tiles;
+    const int32_t *tile_plan;  // [token tiles][kPlanInts]
     int32_t *counters;  // per tile, zero on entry (splits > 1)
     unsigned long long *status;
     // swapped orientation, two projections of the same x in one launch: W
@@ -137,14 +145,14 @@ struct Cfg {
     static constexpr uint32_t kABytes = kBM * kBK * 2;
     static constexpr uint32_t kBBytes = BN * kBK * 2;
     static constexpr uint32_t kQBytes = QUANT ? kBM * kBK : 0;  // int8 W staging
-    // ring + barriers + TMEM address + flags + unit list + alignment slack
-    static constexpr int kFixed = 1024 + (3 * 12 + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
+    // ring + barriers + TMEM address + flags + alignment slack
+    static constexpr int kFixed = 1024 + (3 * 12 + 4) * 8 + 16;
     static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes + kQBytes);
     static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
     static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                         : 2 * BN <= 256 ? 256 : 512;
     static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + kQBytes) +
-                                    ((QUANT ? 3 : 2) * kStages + 4) * 8 + 16 + (kMaxUnitList + 4) * 4;
+                                    ((QUANT ? 3 : 2) * kStages + 4) * 8 + 16;
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kStages >= 2, "ring too small");
     // swapped with a deep ring (narrow token tiles): k-blocks whose loads are
@@ -168,7 +176,7 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
     if (SWAP) {
         w.tb = r % p.tiles_b;
         w.ta = r / p.tiles_b;
-    } else if (!p.vm_mode && p.tiles_a > kTaBand) {
+    } else if (p.tiles_a > kTaBand) {
         // bands of kTaBand token tiles, each over all W tiles: a wave of CTAs
         // then streams a few MB of x (read from DRAM about once) while the W
         // tiles it shares stay in L2
@@ -213,24 +221,15 @@ __device__ __forceinline__ void epi_sync() {
 
 // --------------------------------------------------------------- producer
 
-// Extension k-blocks of token tile ta: the columns of the slots its rows use,
-// [lo, hi), in k-blocks [kb0, kb0 + n); every k-block runs twice (Vm_hi, Vm_lo).
-__device__ __forceinline__ void ext_kblocks(const TcParams &p, int32_t ta, int32_t *kb0, int32_t *n) {
-    const int32_t smin = p.tile_range[2 * ta], smax = p.tile_range[2 * ta + 1];
-    if (smax < smin) {
-        *kb0 = 0;
-        *n = 0;
-        return;
-    }
-    const int32_t lo = smin * p.ext_rank, hi = (smax + 1) * p.ext_rank;
-    *kb0 = lo / kBK;
-    *n = (hi + kBK - 1) / kBK - *kb0;
+// Extension steps of token tile ta: the pool blocks its plan lists (0 when
+// the tile has no adapter rows or takes the CUDA-core expand).
+__device__ __forceinline__ int32_t tile_ext_steps(const TcParams &p, int32_t ta) {
+    const int32_t nb = p.tile_plan[static_cast<size_t>(ta) * kPlanInts];
+    return nb > 0 ? nb : 0;
 }
 
-// The idx-th work unit of this CTA, or -1: every gridDim.x-th unit, or in
-// shrink mode the CTA's share of the active units (built in the prologue).
-__device__ __forceinline__ int32_t next_unit(const TcParams &p, const int32_t *unit_list, int32_t idx) {
-    if (p.vm_mode) return idx < unit_list[-1] ? unit_list[idx] : -1;
+// The idx-th work unit of this CTA (every gridDim.x-th unit), or -1.
+__device__ __forceinline__ int32_t next_unit(const TcParams &p, int32_t idx) {
     const int32_t u = blockIdx.x + idx * static_cast<int32_t>(gridDim.x);
     return u < p.num_units ? u : -1;
 }
@@ -246,30 +245,28 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                                              const CUtensorMap *tma_va, const CUtensorMap *tma_vb,
                                              const TcParams &p, uint8_t *sA, uint8_t *sB, uint8_t *sQ,
                                              uint64_t *full, uint64_t *empty,
-                                             volatile uint32_t *abort_flag, const int32_t *unit_list) {
+                                             volatile uint32_t *abort_flag) {
     using namespace sm100;
     using C = Cfg<SWAP, BN, QUANT>;
     int32_t it = 0;
-    if (p.vm_mode) grid_dependency_wait();  // A_dense comes from the kernel before
     for (int32_t idx = 0;; ++idx) {
-        const int32_t u = next_unit(p, unit_list, idx);
+        const int32_t u = next_unit(p, idx);
         if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
         const int32_t kb0 = w.ks * p.kb_per_split;
         const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
         const int32_t nmain = kb1 - kb0;
-        int32_t ekb0 = 0, ekn = 0, total = nmain;
+        int32_t total = nmain;
         // swapped: the W tile's projection (its tensor map) and row
         const bool second = SWAP && PAIR && w.ta >= p.tiles_a0;
         const CUtensorMap *map_a = second ? tma_va : tma_a;
         const int32_t row_a = (second ? w.ta - p.tiles_a0 : w.ta) * kBM;
         for (int32_t i = 0; i < total; ++i, ++it) {
-            if (!SWAP && p.ext && i == nmain - 1) {
-                // with the unit's last main k-block next: Vm and the tile
-                // ranges come from the shrink kernel
+            if (!SWAP && p.lora_tiles && i == nmain - 1) {
+                // with the unit's last main k-block next: the plan and Vt
+                // come from the kernels before
                 grid_dependency_wait();
-                ext_kblocks(p, w.ta, &ekb0, &ekn);
-                total = nmain + 2 * ekn;
+                total = nmain + tile_ext_steps(p, w.ta);
             }
             if (C::kLoadGroup > 1 && i % C::kLoadGroup == 0) {
                 // wait until the next kLoadGroup stages are all free,
@@ -290,9 +287,9 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                 *abort_flag = 1;
             }
             if (*abort_flag) return;
-            mbar_arrive_expect_tx(&full[s], (QUANT ? (p.w_bits == 4 ? C::kQBytes / 2 : C::kQBytes) : C::kABytes) +
-                                                C::kBBytes);
             if (i < nmain) {
+                mbar_arrive_expect_tx(&full[s], (QUANT ? (p.w_bits == 4 ? C::kQBytes / 2 : C::kQBytes) : C::kABytes) +
+                                                    C::kBBytes);
                 const int32_t kb = kb0 + i;
                 if (QUANT)  // int8 (or packed int4) W into the staging tile; the epilogue warps convert it
                     tma_load_2d(sQ + s * C::kQBytes, map_a, p.w_bits == 4 ? kb * (kBK / 2) : kb * kBK, row_a,
@@ -301,11 +298,16 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                     tma_load_2d(sA + s * C::kABytes, map_a, kb * kBK, row_a, &full[s]);
                 tma_load_2d(sB + s * C::kBBytes, tma_b, kb * kBK, w.tb * BN, &full[s]);
             } else {
-                // LoRA extension: k-block e of the slot columns, hi half then lo half of Vm
+                // LoRA step e: the tile's Vt hi and lo columns of block entry
+                // e (32-byte swizzle, side by side in the A area) and the
+                // block's B rows of this unit's output columns
                 const int32_t e = i - nmain;
-                const int32_t half = e / ekn, kb = ekb0 + e % ekn;
-                tma_load_2d(sA + s * C::kABytes, tma_va, half * p.ext_cols + kb * kBK, w.ta * kBM, &full[s]);
-                tma_load_2d(sB + s * C::kBBytes, tma_vb, kb * kBK, w.tb * BN, &full[s]);
+                const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e];
+                mbar_arrive_expect_tx(&full[s], 2 * kVtBoxBytes + BN * LORA_BLOCK_ROWS * 2);
+                tma_load_2d(sA + s * C::kABytes, tma_va, e * LORA_BLOCK_ROWS, w.ta * kBM, &full[s]);
+                tma_load_2d(sA + s * C::kABytes + kVtBoxBytes, tma_va, kVtCols / 2 + e * LORA_BLOCK_ROWS, w.ta * kBM,
+                            &full[s]);
+                tma_load_2d(sB + s * C::kBBytes, tma_vb, 0, blk * p.N + w.tb * BN, &full[s]);
             }
         }
     }
@@ -316,14 +318,13 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
 template <bool SWAP, int BN, bool QUANT = false>
 __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
                                         uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
-                                        uint32_t tmem_base, volatile uint32_t *abort_flag,
-                                        const int32_t *unit_list) {
+                                        uint32_t tmem_base, volatile uint32_t *abort_flag) {
     using namespace sm100;
     using C = Cfg<SWAP, BN, QUANT>;
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
     int32_t it = 0, t = 0;
     for (int32_t idx = 0;; ++idx) {
-        const int32_t u = next_unit(p, unit_list, idx);
+        const int32_t u = next_unit(p, idx);
         if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
         const int32_t kb0 = w.ks * p.kb_per_split;
@@ -335,13 +336,11 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
         tc_fence_after_sync();
         const uint32_t d = tmem_base + b * BN;
         for (int32_t kb = kb0; kb < kb1 && ok; ++kb, ++it) {
-            if (!SWAP && p.ext && kb == kb_main - 1) {
-                // the LoRA extension k-blocks follow the main ones in the ring
-                // (the tile ranges come from the shrink kernel)
+            if (!SWAP && p.lora_tiles && kb == kb_main - 1) {
+                // the LoRA steps follow the main k-blocks in the ring (the
+                // plan comes from the kernels before)
                 grid_dependency_wait();
-                int32_t ekb0, ekn;
-                ext_kblocks(p, w.ta, &ekb0, &ekn);
-                kb1 = kb_main + 2 * ekn;
+                kb1 = kb_main + tile_ext_steps(p, w.ta);
             }
             const int s = it % C::kStages;
             const uint32_t ph = (it / C::kStages) & 1;
@@ -353,11 +352,16 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
             tc_fence_after_sync();
             const uint32_t a_addr = smem_u32(sA + s * C::kABytes);
             const uint32_t b_addr = smem_u32(sB + s * C::kBBytes);
+            if (kb < kb_main) {
 #pragma unroll
-            for (int k = 0; k < kBK / kUmmaK; ++k)
-                mma_bf16_f32(d, desc_kmajor_sw128(a_addr + k * kUmmaK * 2),
-                             desc_kmajor_sw128(b_addr + k * kUmmaK * 2), idesc,
-                             (kb > kb0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < kBK / kUmmaK; ++k)
+                    mma_bf16_f32(d, desc_kmajor_sw128(a_addr + k * kUmmaK * 2),
+                                 desc_kmajor_sw128(b_addr + k * kUmmaK * 2), idesc,
+                                 (kb > kb0 || k > 0) ? 1u : 0u);
+            } else {  // LoRA step: Vt_hi and Vt_lo times the block's B, K = 16 each
+                mma_bf16_f32(d, desc_kmajor_sw32(a_addr), desc_kmajor_sw32(b_addr), idesc, 1u);
+                mma_bf16_f32(d, desc_kmajor_sw32(a_addr + kVtBoxBytes), desc_kmajor_sw32(b_addr), idesc, 1u);
+            }
             mma_commit(&empty[s]);
         }
         if (!ok || *abort_flag) {
@@ -465,7 +469,7 @@ template <bool SWAP, int BN, bool PAIR = false, bool QUANT = false>
 __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, const uint8_t *sQ, uint64_t *full,
                                              uint64_t *conv, uint64_t *tmem_full, uint64_t *tmem_empty,
                                              uint32_t tmem_base, volatile uint32_t *abort_flag,
-                                             volatile uint32_t *last_flag, const int32_t *unit_list) {
+                                             volatile uint32_t *last_flag) {
     using namespace sm100;
     using C = Cfg<SWAP, BN, QUANT>;
     constexpr int kGroups = kEpiWarps / 4;
@@ -478,7 +482,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int32_t t = 0, cit = 0;
     for (int32_t idx = 0;; ++idx) {
-        const int32_t u = next_unit(p, unit_list, idx);
+        const int32_t u = next_unit(p, idx);
         if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
         if (QUANT) {
@@ -676,60 +680,22 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
                 }
             }
         } else {
-            grid_dependency_wait();  // V comes from the shrink kernel
+            grid_dependency_wait();  // the plan and V come from the kernels before
             const int32_t m = w.ta * kBM + q * 32 + lane;
+            // the CUDA-core expand for rows of tiles whose adapters span too
+            // many pool blocks for the LoRA steps (or without the steps at all)
+            const bool per_row = !p.lora_tiles || p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts] < 0;
             int32_t r = 0, slot = -1;
             float s = 0.0f;
-            if (m < p.M)
+            if (per_row && m < p.M)
                 slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s, p.status,
                                     false);
-            if (p.vm_mode && slot >= 0) {
-                // a corrupt block entry drops the row's correction
-                bool okb = true;
-                for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
-                    const int32_t blk = p.table[static_cast<size_t>(slot) * p.bps + jb];
-                    okb &= blk >= 0 && blk < p.num_blocks;
-                }
-                if (!okb) slot = -1;
-            }
 #pragma unroll 1
             for (int c = grp; c < kChunks; c += kGroups) {
                 float acc[32];
                 load_tmem_chunk(col0 + c * 32, acc);
                 const int32_t n0 = w.tb * BN + c * 32;
-                if (p.vm_mode) {
-                    // columns n0 .. n0+31 of Vm: s_i V for the row's own slot, else 0
-                    if (m < p.M && n0 < p.N) {
-                        __nv_bfloat16 *hi_dst = p.vm_out + static_cast<size_t>(m) * 2 * p.ext_cols + n0;
-                        __nv_bfloat16 *lo_dst = hi_dst + p.ext_cols;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            float hv[8], lv[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int32_t col = n0 + g * 8 + e;
-                                const float val = (slot >= 0 && col / p.ext_rank == slot) ? s * acc[g * 8 + e] : 0.0f;
-                                const __nv_bfloat16 h = __float2bfloat16_rn(val);
-                                hv[e] = __bfloat162float(h);
-                                lv[e] = val - hv[e];
-                            }
-                            uint4 qh, ql;
-                            qh.x = pack_bf16x2(hv[0], hv[1]);
-                            qh.y = pack_bf16x2(hv[2], hv[3]);
-                            qh.z = pack_bf16x2(hv[4], hv[5]);
-                            qh.w = pack_bf16x2(hv[6], hv[7]);
-                            ql.x = pack_bf16x2(lv[0], lv[1]);
-                            ql.y = pack_bf16x2(lv[2], lv[3]);
-                            ql.z = pack_bf16x2(lv[4], lv[5]);
-                            ql.w = pack_bf16x2(lv[6], lv[7]);
-                            *reinterpret_cast<uint4 *>(hi_dst + g * 8) = qh;
-                            *reinterpret_cast<uint4 *>(lo_dst + g * 8) = ql;
-                        }
-                    }
-                    __syncwarp();
-                    continue;
-                }
-                if (!p.ext) rows_finish_chunk(p, slot, r, s, m, n0, acc);
+                if (per_row) rows_finish_chunk(p, slot, r, s, m, n0, acc);
                 if (m < p.M) {
                     __nv_bfloat16 *dst = p.out + static_cast<size_t>(m) * p.ldo + n0;
 #pragma unroll
@@ -778,7 +744,6 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
     volatile uint32_t *last_flag = tmem_slot + 2;
-    int32_t *unit_list = reinterpret_cast<int32_t *>(tmem_slot + 4) + 1;  // unit_list[-1] = its length
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -799,7 +764,7 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tma_a);
         prefetch_tensormap(&tma_b);
-        if (!SWAP && p.ext) {
+        if (!SWAP && p.lora_tiles) {
             prefetch_tensormap(&tma_va);
             prefetch_tensormap(&tma_vb);
         }
@@ -807,43 +772,6 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
-    }
-    if (p.vm_mode && warp == 2) {
-        // shrink mode: the active units (column tiles inside their token
-        // tile's slot range) in unit order; the j-th goes to CTA j % gridDim.x
-        grid_dependency_wait();  // the tile ranges come from the kernel before
-        int32_t base = 0;
-        for (int32_t t0 = 0; t0 < p.tiles_a; t0 += 32) {
-            const int32_t ta = t0 + lane;
-            int32_t cnt = 0, tb0 = 0;
-            if (ta < p.tiles_a) {
-                const int32_t smin = p.tile_range[2 * ta], smax = p.tile_range[2 * ta + 1];
-                if (smax >= smin) {
-                    tb0 = smin * p.ext_rank / BN;
-                    cnt = ((smax + 1) * p.ext_rank - 1) / BN - tb0 + 1;
-                }
-            }
-            int32_t incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            for (int32_t k = 0; k < cnt; ++k) {
-                const int32_t j = base + incl - cnt + k;
-                if (j % static_cast<int32_t>(gridDim.x) == static_cast<int32_t>(blockIdx.x)) {
-                    const int32_t pos = j / static_cast<int32_t>(gridDim.x);
-                    if (pos < kMaxUnitList) unit_list[pos] = (tb0 + k) * p.tiles_a + ta;  // see decode_unit
-                }
-            }
-            base += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) {
-            const int32_t g = static_cast<int32_t>(gridDim.x), bid = static_cast<int32_t>(blockIdx.x);
-            const int32_t mine = base > bid ? (base - bid + g - 1) / g : 0;
-            if (mine > kMaxUnitList) record_error(p.status, kDevTimeout, 9);
-            unit_list[-1] = mine < kMaxUnitList ? mine : kMaxUnitList;
-        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -853,15 +781,15 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     if (warp == 0) {
         if (lane == 0)
             run_producer<SWAP, BN, PAIR, QUANT>(&tma_a, &tma_b, &tma_va, &tma_vb, p, sA, sB, sQ, full, empty,
-                                                abort_flag, unit_list);
+                                                abort_flag);
     } else if (warp == 1) {
         if (lane == 0)
             // with int8 W the MMAs wait for the converted tile, not the load
             run_mma<SWAP, BN, QUANT>(p, sA, sB, QUANT ? conv : full, empty, tmem_full, tmem_empty, tmem_base,
-                                     abort_flag, unit_list);
+                                     abort_flag);
     } else {
         run_epilogue<SWAP, BN, PAIR, QUANT>(p, sA, sQ, full, conv, tmem_full, tmem_empty, tmem_base, abort_flag,
-                                            last_flag, unit_list);
+                                            last_flag);
     }
 
     tc_fence_before_sync();
@@ -874,59 +802,12 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// Row-major bf16 matrix [rows][cols] with row stride `ld` elements, tiled in
-// boxes of box_rows x 64 with the 128-byte swizzle; out-of-range elements of
-// a box read as zero.
-bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint64_t ld,
-                    uint32_t box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {ld * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-
-// Row-major byte matrix [rows][cols] (row stride `cols` bytes, a multiple of
-// 16) in boxes of box_rows x box_cols bytes without swizzle; out-of-range
-// elements read as zero.
-bool make_tmap_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                  uint32_t box_cols) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // v1: a second projection of the same x in the same launch (swapped
 // orientation only; tp plans both).  counters: the split-K tile counters of
 // this launch (NULL: the plan's).
 template <bool SWAP, int BN, bool PAIR = false, bool QUANT = false>
 cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcPlan &tp, cudaStream_t stream,
-                           bool vm_mode = false, const ProjView *v1 = nullptr, int32_t *counters = nullptr,
+                           const ProjView *v1 = nullptr, int32_t *counters = nullptr,
                            int64_t n_counters = 0) {
     using C = Cfg<SWAP, BN, QUANT>;
     auto kernel = tc_gemm_lora_kernel<SWAP, BN, PAIR, QUANT>;
@@ -948,7 +829,7 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     }
     CUtensorMap tx, tw;
     if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, SWAP ? BN : kBM)) return cudaErrorInvalidValue;
-    if (QUANT != (v.w_scale != nullptr) || (QUANT && (!SWAP || PAIR || vm_mode))) return cudaErrorInvalidValue;
+    if (QUANT != (v.w_scale != nullptr) || (QUANT && (!SWAP || PAIR))) return cudaErrorInvalidValue;
     if (QUANT) {  // int8 [N][K] bytes, or packed int4 [N][K/2]: 64 values of a row per box
         const bool i4 = v.w_bits == 4;
         if (!make_tmap_u8(&tw, v.W, v.N, i4 ? plan.K / 2 : plan.K, kBM, i4 ? kBK / 2 : kBK))
@@ -956,17 +837,21 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     } else if (!make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, SWAP ? kBM : BN)) {
         return cudaErrorInvalidValue;
     }
-    // LoRA extension operands (non-swapped orientation): [Vm_hi | Vm_lo] beside
-    // x, Bm beside W; unused maps are copies of the main ones
+    // LoRA steps (non-swapped orientation): Vt beside x, the pool's B arena
+    // ([num_blocks * N][16]) beside W, both in [rows x 16] boxes with the
+    // 32-byte swizzle; unused maps are copies of the main ones
     CUtensorMap tva = tx, tvb = tw;
-    const bool ext = !SWAP && !vm_mode && v.ext_cols > 0;
+    const bool tiles = !SWAP && v.lora_tiles;
     if (PAIR != (v1 != nullptr)) return cudaErrorInvalidValue;
-    if (v1) {  // the second projection's W in the slot of the extension's A-side map
-        if (!SWAP || vm_mode || !make_tmap_bf16(&tva, v1->W, v1->N, plan.K, plan.K, kBM)) return cudaErrorInvalidValue;
+    if (v1) {  // the second projection's W in the slot of the LoRA steps' A-side map
+        if (!SWAP || !make_tmap_bf16(&tva, v1->W, v1->N, plan.K, plan.K, kBM)) return cudaErrorInvalidValue;
     }
-    if (ext) {
-        if (!make_tmap_bf16(&tva, v.vm, plan.M, 2 * static_cast<uint64_t>(v.ext_cols), 2 * static_cast<uint64_t>(v.ext_cols), kBM) ||
-            !make_tmap_bf16(&tvb, v.bm, v.N, v.ext_cols, v.ext_cols, BN))
+    if (tiles) {
+        const uint64_t tiles_m = static_cast<uint64_t>((plan.M + kPlanRows - 1) / kPlanRows) * kPlanRows;
+        if (!v.vt || !v.tile_plan ||
+            !make_tmap_bf16(&tva, v.vt, tiles_m, kVtCols, kVtCols, kBM, LORA_BLOCK_ROWS, 32) ||
+            !make_tmap_bf16(&tvb, v.b_arena, static_cast<uint64_t>(v.num_blocks) * v.N, LORA_BLOCK_ROWS,
+                            LORA_BLOCK_ROWS, BN, LORA_BLOCK_ROWS, 32))
             return cudaErrorInvalidValue;
     }
     TcParams p;
@@ -995,12 +880,8 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.v_part_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.part = plan.part;
     p.ycorr = v.ycorr;
-    p.ext = ext ? 1 : 0;
-    p.ext_cols = v.ext_cols;
-    p.ext_rank = v.max_rank;
-    p.tile_range = v.tile_range;
-    p.vm_mode = vm_mode ? 1 : 0;
-    p.vm_out = vm_mode ? static_cast<__nv_bfloat16 *>(v.vm) : nullptr;
+    p.lora_tiles = tiles ? 1 : 0;
+    p.tile_plan = v.tile_plan;
     p.counters = counters ? counters : plan.counters;
     if (!counters) n_counters = plan.n_counters;
     p.status = plan.status;
@@ -1119,29 +1000,6 @@ TcPlan plan_tc_pair(int32_t M, int32_t N0, int32_t N1, int32_t K) {
     return t;
 }
 
-// The shrink of the large-M tensor-core path as a GEMM: x A_dense^T over the
-// slot columns of each token tile (other column tiles are skipped), written
-// to Vm as the hi and lo bf16 parts of s_i V (see TcParams::vm_mode).
-cudaError_t launch_gemm_vm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
-    if (v.ext_cols <= 0 || !v.adense || !v.vm || !v.tile_range) return cudaErrorInvalidValue;
-    TcPlan tp = plan_tc(plan.M, v.ext_cols, plan.K);
-    if (tp.swap) return cudaErrorInvalidValue;
-    tp.bn = 64;  // one slot of a rank-64 pool per column tile
-    tp.tiles_b = (v.ext_cols + 63) / 64;
-    tp.splits = 1;
-    tp.kb_per_split = tp.num_kb;
-    tp.units = tp.tiles_a * tp.tiles_b;
-    const int sms = device_sm_count();
-    tp.grid = tp.units < sms ? tp.units : sms;
-    ProjView vv = v;
-    vv.W = v.adense;
-    vv.w_scale = nullptr;
-    vv.N = v.ext_cols;
-    vv.out = nullptr;
-    vv.ldo = v.ext_cols;
-    return launch_variant<false, 64>(plan, vv, tp, stream, true);
-}
-
 cudaError_t launch_gemm_lora_tc_pair(const ForwardPlan &plan, const ProjView &v0, const ProjView *v1,
                                      int32_t *counters, int64_t n_counters, cudaStream_t stream) {
     const TcPlan tp = v1 ? plan_tc_pair(plan.M, v0.N, v1->N, plan.K) : plan_tc(plan.M, v0.N, plan.K);
@@ -1149,23 +1007,23 @@ cudaError_t launch_gemm_lora_tc_pair(const ForwardPlan &plan, const ProjView &v0
     if (v0.w_scale || (v1 && v1->w_scale)) {  // int8 W: one projection, token tiles of 32 or 64
         if (v1) return cudaErrorInvalidValue;
         if (tp.bn == 32)
-            return launch_variant<true, 32, false, true>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+            return launch_variant<true, 32, false, true>(plan, v0, tp, stream, nullptr, counters, n_counters);
         if (tp.bn == 64)
-            return launch_variant<true, 64, false, true>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+            return launch_variant<true, 64, false, true>(plan, v0, tp, stream, nullptr, counters, n_counters);
         return cudaErrorInvalidValue;
     }
     // pairs: tiles of at least 128 tokens (the narrower variants keep their
     // register count low enough to share an SM with the per-row kernel)
     if (v1) {
-        if (tp.bn == 128) return launch_variant<true, 128, true>(plan, v0, tp, stream, false, v1, counters, n_counters);
-        if (tp.bn == 256) return launch_variant<true, 256, true>(plan, v0, tp, stream, false, v1, counters, n_counters);
+        if (tp.bn == 128) return launch_variant<true, 128, true>(plan, v0, tp, stream, v1, counters, n_counters);
+        if (tp.bn == 256) return launch_variant<true, 256, true>(plan, v0, tp, stream, v1, counters, n_counters);
         return cudaErrorInvalidValue;
     }
     switch (tp.bn) {
-        case 32: return launch_variant<true, 32>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
-        case 64: return launch_variant<true, 64>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
-        case 128: return launch_variant<true, 128>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
-        default: return launch_variant<true, 256>(plan, v0, tp, stream, false, nullptr, counters, n_counters);
+        case 32: return launch_variant<true, 32>(plan, v0, tp, stream, nullptr, counters, n_counters);
+        case 64: return launch_variant<true, 64>(plan, v0, tp, stream, nullptr, counters, n_counters);
+        case 128: return launch_variant<true, 128>(plan, v0, tp, stream, nullptr, counters, n_counters);
+        default: return launch_variant<true, 256>(plan, v0, tp, stream, nullptr, counters, n_counters);
     }
 }
 

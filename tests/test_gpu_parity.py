@@ -90,6 +90,25 @@ def test_integer_exact_prefill_geometry(mode):
     assert np.array_equal(got, want), f"{mode}: {np.sum(got != want)} outputs differ"
 
 
+@pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
+def test_integer_exact_large_m_tile_fallback(mode):
+    """Large M where some 128-token tiles name adapters spanning more than 16
+    pool blocks (rows in no order: up to 12 slots of rank 48-64 per tile) and
+    take the CUDA-core fallback, while the tiles of the sorted first half take
+    the tensor-core LoRA steps; one call, every row bit-exact."""
+    wl = synth(M=900, K=256, Ns=[264, 136], num_slots=12, rank_choices=(48, 64), integer=True, seed=900,
+               none_frac=0.1)
+    ids = wl.row_adapter.copy()
+    half = ids[:450]
+    ids[:450] = np.sort(half)  # the first half sorted: few slots per tile
+    pools = H.make_pools(wl, DEV, extra_blocks=7)
+    outs = H.forward(wl, pools, mode, ids=ids)
+    for p in range(2):
+        want = H.oracle_bf16_bits(H.oracle_rows(wl, p, ids=ids))
+        got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), f"{mode} projection {p}: {np.sum(got != want)} outputs differ"
+
+
 @pytest.mark.parametrize("shape", [(64, 2048, (264, 520)), (37, 1024, (1032,)), (700, 192, (136,))])
 def test_integer_exact_split_k_and_orientations(shape):
     """Bit-exact through the split-K reduction (few tokens, long K: several

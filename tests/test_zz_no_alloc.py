@@ -51,7 +51,7 @@ def _index(wl, mode):
 CASES = {
     "per_row_two_proj": dict(M=128, K=1024, Ns=[256, 520], rank_choices=(8, 16)),
     "grouped": dict(M=300, K=520, Ns=[392, 136], rank_choices=(1, 7, 16, 33, 64)),
-    "pipelined": dict(M=480, K=2056, Ns=[1032], rank_choices=(16, 64, 128)),
+    "pipelined": dict(M=480, K=1600, Ns=[520], rank_choices=(16, 64, 128)),
     "large_m": dict(M=1100, K=512, Ns=[264, 136], rank_choices=(8, 16, 32, 64)),
     "int8_base": dict(M=64, K=1024, Ns=[520], rank_choices=(8, 16), wq=8),
     "int4_base": dict(M=48, K=1024, Ns=[264], rank_choices=(16,), wq=4),
