@@ -460,8 +460,8 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
         // over the pool blocks its rows use (lora_tiles.cu); V (below) then
         // serves only tiles that take the CUDA-core fallback
         v.lora_tiles = (a->dtype == LORA_BF16 && a->M > 0 && !lora::plan_tc(a->M, d.N, a->K).swap) ? 1 : 0;
-        v.tile_plan = v.tile_counter = nullptr;
-        v.shrink_part = nullptr;
+        v.tile_plan = nullptr;
+        v.vacc = nullptr;
         v.vt = nullptr;
         v.shrink_grid = 0;
         ws->v_off[i] = off;
@@ -508,26 +508,23 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     off += align_up(ycorr, 256);
     ws->group_off = off;
     if (ycorr) off += align_up(sizeof(int32_t) * lora::group_table_ints(a->M), 256);
-    // the tensor-core LoRA term of large M: tile plans and counters, the
-    // shrink's partial tiles and Vt, shared by the projections (their kernels
-    // run one after the other on the stream)
-    size_t plan_b = 0, tcount_b = 0, spart_b = 0, vt_b = 0;
+    // the tensor-core LoRA term of large M: tile plans, the V accumulator and
+    // Vt, shared by the projections (their kernels run one after the other
+    // on the stream)
+    size_t plan_b = 0, vacc_b = 0, vt_b = 0;
     int sgrid = 0;
     if (a->n_proj > 0 && plan->proj[0].lora_tiles) {
         const size_t T = (static_cast<size_t>(a->M) + lora::kPlanRows - 1) / lora::kPlanRows;
         plan_b = sizeof(int32_t) * T * lora::kPlanInts;
-        tcount_b = sizeof(int32_t) * T;
         sgrid = lora::tc_shrink_grid(a->M, a->K);
-        spart_b = lora::tc_shrink_part_bytes(sgrid);
+        vacc_b = lora::tc_shrink_acc_bytes(a->M);
         vt_b = sizeof(uint16_t) * T * lora::kPlanRows * lora::kVtCols;
     }
     for (int i = 0; i < a->n_proj; ++i) plan->proj[i].shrink_grid = plan->proj[i].lora_tiles ? sgrid : 0;
     ws->plan_off = off;
     off += align_up(plan_b, 256);
-    ws->tcount_off = off;
-    off += align_up(tcount_b, 256);
-    ws->spart_off = off;
-    off += align_up(spart_b, 256);
+    ws->vacc_off = off;
+    off += align_up(vacc_b, 256);
     ws->vt_off = off;
     off += align_up(vt_b, 256);
     ws->counter_off = off;  // last: the counters run to the end of the workspace
@@ -576,8 +573,7 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
     for (int i = 0; i < plan.n_proj; ++i) {
         if (!plan.proj[i].lora_tiles) continue;
         plan.proj[i].tile_plan = reinterpret_cast<int32_t *>(base + ws.plan_off);
-        plan.proj[i].tile_counter = reinterpret_cast<int32_t *>(base + ws.tcount_off);
-        plan.proj[i].shrink_part = reinterpret_cast<float *>(base + ws.spart_off);
+        plan.proj[i].vacc = reinterpret_cast<float *>(base + ws.vacc_off);
         plan.proj[i].vt = base + ws.vt_off;
     }
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);

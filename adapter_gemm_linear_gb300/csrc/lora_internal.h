@@ -78,10 +78,9 @@ struct ProjView {
     // 128-token tile, the pool blocks of the slots its rows use (tile_plan);
     // Vt holds s_i V of each row as bf16 hi and lo parts per block entry; the
     // GEMM adds them times the blocks' B as extra MMAs.
-    int32_t lora_tiles;    // 1: this path (tile_plan, tile_counter, shrink_part, vt set)
+    int32_t lora_tiles;    // 1: this path (tile_plan, vacc, vt set)
     int32_t *tile_plan;    // workspace: int32 [tiles][kPlanInts]
-    int32_t *tile_counter; // workspace: int32 [tiles], k-blocks summed per tile
-    float *shrink_part;    // workspace: fp32 partial tiles of the shrink, [shrink_grid][2][kPlanRows][256]
+    float *vacc;           // workspace: fp32 V accumulator, [tiles][256][kPlanRows] (column-major per tile)
     void *vt;              // workspace: bf16 [tiles * kPlanRows][kVtCols]
     int32_t shrink_grid;   // CTAs of the tensor-core shrink
 };
@@ -159,7 +158,7 @@ struct WorkspaceLayout {
     size_t part_off;              // fp32 split-K partial tiles (largest projection)
     size_t ycorr_off;             // fp32 [M][N] correction of the small-M orientation (largest projection)
     size_t group_off;             // int32 group table (small-M orientation)
-    size_t plan_off, tcount_off, spart_off, vt_off;  // large-M tensor-core LoRA term
+    size_t plan_off, vacc_off, vt_off;  // large-M tensor-core LoRA term
     size_t counter_off;           // int32 per output tile (split-K)
     size_t total;
 };
@@ -192,8 +191,9 @@ int device_sm_count();
 // plan (block lists; per-row V of fallback tiles), then the tensor-core
 // shrink into Vt; the main GEMM adds Vt x B_block^T per listed block.
 int tc_shrink_grid(int32_t M, int32_t K);
-size_t tc_shrink_part_bytes(int grid);
+size_t tc_shrink_acc_bytes(int32_t M);
 cudaError_t launch_tile_plan(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+// The shrink and the convert kernel after it (Vt, and V of fallback tiles).
 cudaError_t launch_tc_shrink(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
 
 // The small-M LoRA path by adapter group (lora_grouped.cu): the rows' group
