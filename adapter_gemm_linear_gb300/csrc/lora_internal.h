@@ -80,16 +80,17 @@ struct ProjView {
     // GEMM adds them times the blocks' B as extra MMAs.
     int32_t lora_tiles;    // 1: this path (tile_plan, vacc, vt set)
     int32_t *tile_plan;    // workspace: int32 [tiles][kPlanInts]
-    float *vacc;           // workspace: fp32 V accumulator, [tiles][256][kPlanRows] (column-major per tile)
+    float *vacc;           // workspace: fp32 V accumulator, [plan tiles][256 columns][kPlanRows] (column-major per tile)
     void *vt;              // workspace: bf16 [tiles * kPlanRows][kVtCols]
     int32_t shrink_grid;   // CTAs of the tensor-core shrink
 };
 
-// Large-M LoRA term (lora_tiles.cu).  A plan tile is the GEMM's token tile;
+// Large-M LoRA term (lora_tiles.cu).  A plan tile is 256 tokens: the token
+// tile of the two-SM GEMM, two tiles of the one-SM GEMM and of the shrink;
 // its record: [0] = nb, the pool blocks it lists (-1: more than
 // kPlanMaxBlocks, rows take the CUDA-core fallback), [kPlanBlkOff + e] = block
 // id and [kPlanSlotOff + e] = slot of entry e.
-constexpr int kPlanRows = 128;
+constexpr int kPlanRows = 256;
 constexpr int kPlanMaxBlocks = 16;
 constexpr int kPlanInts = 48;
 constexpr int kPlanBlkOff = 16;

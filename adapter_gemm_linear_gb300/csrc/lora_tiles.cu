@@ -1,8 +1,8 @@
 // The LoRA term of the large-M (prefill) orientation on the tensor cores,
 // reading the adapters straight from the paged pool.
 //
-// The GEMM of tc_gemm.cu takes 128 tokens per tile.  For each such tile this
-// file builds
+// A plan tile is 256 tokens (the token tile of the two-SM GEMM).  For each
+// plan tile this file builds
 //
 //   tile_plan_kernel   the tile's block list: the distinct adapter slots its
 //                      rows name, in ascending order, and for each the pool
@@ -12,8 +12,9 @@
 //                      needs more (rows in no useful order) is marked for the
 //                      CUDA-core fallback, whose per-row V this kernel
 //                      computes itself.
-//   tc_shrink_kernel   V = x_tile A_list^T on tcgen05: the MMA's A operand is
-//                      the tile's 128 x rows, its B operand the tile's block
+//   tc_shrink_kernel   V = x_tile A_list^T on tcgen05, per 128-row half of a
+//                      plan tile: the MMA's A operand is the half's 128 x
+//                      rows, its B operand the plan tile's block
 //                      list -- one 16-row TMA box per pool block, stacked in
 //                      shared memory -- so N = 16 nb.  The (tile, k-block)
 //                      pairs of all tiles with adapters are split into
@@ -70,10 +71,11 @@ constexpr int kShrinkMaxSegs = 64;      // segments (tile pieces) one CTA may ta
 constexpr int kMinPairs = 4;            // fewest (tile, k-block) pairs a CTA takes
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kAccCols = 16 * kPlanMaxBlocks;  // 256: TMEM columns of one accumulator
-constexpr uint32_t kXBytes = kPlanRows * kBK * 2;  // 16 KiB x box per k-block
+constexpr int kSubRows = 128;           // rows of the shrink's MMA (M): half a plan tile
+constexpr uint32_t kXBytes = kSubRows * kBK * 2;  // 16 KiB x box per k-block
 constexpr int kConvertSplit = 4;        // CTAs per tile of the convert kernel
 
-static_assert(kPlanRows == 128, "one MMA M of 128 token rows per plan tile");
+static_assert(kPlanRows == 2 * kSubRows, "a plan tile is two shrink tiles");
 static_assert(kShrinkXStages % kShrinkXGroup == 0, "x groups tile the ring");
 static_assert(kAccCols <= 256, "the MMA's N is at most 256");
 
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(256) tile_plan_kernel(const TilePlanParams p) 
 // ------------------------------------------------------------------ shrink
 
 struct ShrinkParams {
-    int32_t M, T, num_kb;
+    int32_t M, T, num_kb;  // T: 128-row sub-tiles (two per plan tile)
     const int32_t *plan;
     float *vacc;          // [T][kAccCols][kPlanRows] fp32 accumulator (column-major per tile)
     unsigned long long *status;
@@ -213,7 +215,7 @@ __device__ __forceinline__ void a_ring_layout(const Seg *seg, int32_t nseg, cons
                                               int32_t *stages, uint32_t *stage_bytes) {
     int32_t nb_max = 1;
     for (int32_t i = 0; i < nseg; ++i) {
-        const int32_t nb = plan[static_cast<size_t>(seg[i].tile) * kPlanInts];
+        const int32_t nb = plan[static_cast<size_t>(seg[i].tile >> 1) * kPlanInts];
         nb_max = nb > nb_max ? nb : nb_max;
     }
     const int32_t sb = nb_max * LORA_BLOCK_ROWS * kBK * 2;
@@ -261,7 +263,7 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
     }
     if (warp == 2) {
         // This CTA's share of the (tile, k-block) pairs: a contiguous range of
-        // equal length over all tiles (every pair streams one x box from DRAM;
+        // equal length over all 128-row sub-tiles (every pair streams one x box from DRAM;
         // the pool blocks mostly hit L2).  It needs no plan, so x streams
         // while the plan kernel before this one is still running; tiles
         // without adapter rows are loaded and skipped.
@@ -322,7 +324,7 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
                     }
                     if (sh.abort_flag) break;
                     mbar_arrive_expect_tx(&sh.xfull[s], kXBytes);
-                    tma_load_2d(ring + s * kXBytes, &tma_x, kb * kBK, sg.tile * kPlanRows, &sh.xfull[s]);
+                    tma_load_2d(ring + s * kXBytes, &tma_x, kb * kBK, sg.tile * kSubRows, &sh.xfull[s]);
                 }
             }
         }
@@ -336,7 +338,7 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
             int32_t it = 0;
             for (int32_t si = 0; si < nseg && !sh.abort_flag; ++si) {
                 const Seg sg = sh.seg[si];
-                const int32_t *plan = p.plan + static_cast<size_t>(sg.tile) * kPlanInts;
+                const int32_t *plan = p.plan + static_cast<size_t>(sg.tile >> 1) * kPlanInts;
                 const int32_t nb = plan[0];
                 if (nb <= 0) continue;  // no adapter rows (or the fallback): x only
                 int32_t blk[kPlanMaxBlocks];
@@ -370,7 +372,7 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
             bool ok = true;
             for (int32_t si = 0; si < nseg && ok; ++si) {
                 const Seg sg = sh.seg[si];
-                const int32_t nb = p.plan[static_cast<size_t>(sg.tile) * kPlanInts];
+                const int32_t nb = p.plan[static_cast<size_t>(sg.tile >> 1) * kPlanInts];
                 if (nb <= 0) {
                     // a tile without blocks: release its x stages unused
                     for (int32_t kb = sg.kb0; kb < sg.kb1; ++kb, ++ix) {
@@ -389,7 +391,7 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
                 if (!ok) record_error(p.status, kDevTimeout, 22);
                 tc_fence_after_sync();
                 const uint32_t d = sh.tmem_base + b * kAccCols;
-                const uint32_t idesc = idesc_bf16_f32(kPlanRows, nb * LORA_BLOCK_ROWS);
+                const uint32_t idesc = idesc_bf16_f32(kSubRows, nb * LORA_BLOCK_ROWS);
                 for (int32_t kb = sg.kb0; kb < sg.kb1 && ok; ++kb, ++ix, ++ia) {
                     const int sx = ix % kShrinkXStages, sa = ia % a_stages;
                     if (!mbar_wait_bounded(&sh.xfull[sx], (ix / kShrinkXStages) & 1, kWaitNs) ||
@@ -398,7 +400,6 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
                         ok = false;
                         break;
                     }
-                    tc_fence_after_sync();
                     const uint32_t a_addr = smem_u32(ring + sx * kXBytes);
                     const uint32_t b_addr = smem_u32(aring + static_cast<size_t>(sa) * a_stage_bytes);
 #pragma unroll
@@ -421,8 +422,8 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // thread r holds tile row r: its values of column j go to
-        // vacc[tile][j][r], so each warp's reductions cover 128 contiguous bytes
+        // thread r holds sub-tile row r: its values of column j go to
+        // vacc[plan tile][j][row], so each warp's reductions cover 128 contiguous bytes
         const int q = warp & 3;  // TMEM lane quarter of this warp
         const int r = q * 32 + lane;
         const uint32_t lane_addr = sh.tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -431,7 +432,7 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
         int32_t act = 0;
         for (int32_t si = 0; si < nseg; ++si) {
             const Seg sg = sh.seg[si];
-            const int32_t ncols = p.plan[static_cast<size_t>(sg.tile) * kPlanInts] * LORA_BLOCK_ROWS;
+            const int32_t ncols = p.plan[static_cast<size_t>(sg.tile >> 1) * kPlanInts] * LORA_BLOCK_ROWS;
             if (ncols <= 0) continue;
             const int b = act & 1;
             const bool ok = mbar_wait_bounded(&sh.tmem_full[b], (act >> 1) & 1, kWaitNs);
@@ -442,8 +443,8 @@ tc_shrink_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constan
             }
             if (!shrink_epi_all(ok && !sh.abort_flag)) break;  // uniform over the epilogue warps
             tc_fence_after_sync();
-            const bool row_ok = sg.tile * kPlanRows + r < p.M;
-            float *dst = p.vacc + static_cast<size_t>(sg.tile) * kAccCols * kPlanRows + r;
+            const bool row_ok = sg.tile * kSubRows + r < p.M;
+            float *dst = p.vacc + static_cast<size_t>(sg.tile >> 1) * kAccCols * kPlanRows + (sg.tile & 1) * kSubRows + r;
             for (int32_t c0 = 0; c0 < ncols; c0 += 32) {
                 uint32_t raw[32];
                 tmem_ld_32x32b_x32(lane_addr + b * kAccCols + c0, raw);
@@ -486,8 +487,9 @@ struct ConvertParams {
 };
 
 // grid (T, kConvertSplit): CTA (t, y) takes block entries e = y, y + 4, ...
-// of tile t (thread: row r, 8 of the entry's 16 columns), or, for a tile
-// marked for the fallback, rows y, y + 4, ... (one warp per row, lanes over k).
+// of plan tile t (thread: row r of the tile, the entry's 16 columns), or,
+// for a tile marked for the fallback, rows y, y + 4, ... (one warp per row,
+// lanes over k).
 __global__ void __launch_bounds__(256) tile_convert_kernel(const ConvertParams p) {
     // the GEMM (a programmatic dependent) may launch and stream W; it reads Vt
     // and V only after this grid has completed
@@ -497,7 +499,7 @@ __global__ void __launch_bounds__(256) tile_convert_kernel(const ConvertParams p
     const int32_t *plan = p.plan + static_cast<size_t>(t) * kPlanInts;
     const int32_t nb = plan[0];
     if (nb > 0) {
-        const int r = threadIdx.x & (kPlanRows - 1), h = threadIdx.x >> 7;
+        const int r = threadIdx.x;  // row of the plan tile
         const int32_t m = t * kPlanRows + r;
         if (m >= p.M) return;
         int32_t rr;
@@ -506,16 +508,15 @@ __global__ void __launch_bounds__(256) tile_convert_kernel(const ConvertParams p
                                           false);
         const float *src = p.vacc + static_cast<size_t>(t) * kAccCols * kPlanRows + r;
         __nv_bfloat16 *hi_row = p.vt + static_cast<size_t>(m) * kVtCols;
-#pragma unroll 2
         for (int32_t e = y; e < nb; e += kConvertSplit) {
-            const int32_t c0 = e * LORA_BLOCK_ROWS + h * 8;
-            float v[8];
+            float v[LORA_BLOCK_ROWS];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + static_cast<size_t>(c0 + i) * kPlanRows);
+            for (int i = 0; i < LORA_BLOCK_ROWS; ++i)
+                v[i] = __ldcg(src + static_cast<size_t>(e * LORA_BLOCK_ROWS + i) * kPlanRows);
             const bool own = slot >= 0 && plan[kPlanSlotOff + e] == slot;
-            uint32_t hw[4], lw[4];
+            uint32_t hw[8], lw[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 float h2[2], l2[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -528,8 +529,12 @@ __global__ void __launch_bounds__(256) tile_convert_kernel(const ConvertParams p
                 hw[i] = *reinterpret_cast<const uint32_t *>(&hh);
                 lw[i] = *reinterpret_cast<const uint32_t *>(&ll);
             }
-            *reinterpret_cast<uint4 *>(hi_row + c0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(hi_row + kVtCols / 2 + c0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            uint4 *hd = reinterpret_cast<uint4 *>(hi_row + e * LORA_BLOCK_ROWS);
+            uint4 *ld = reinterpret_cast<uint4 *>(hi_row + kVtCols / 2 + e * LORA_BLOCK_ROWS);
+            hd[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            hd[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+            ld[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            ld[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
         }
         return;
     }
@@ -588,7 +593,7 @@ __global__ void __launch_bounds__(256) tile_convert_kernel(const ConvertParams p
 }  // namespace
 
 int tc_shrink_grid(int32_t M, int32_t K) {
-    const int64_t T = (M + kPlanRows - 1) / kPlanRows;
+    const int64_t T = (M + kSubRows - 1) / kSubRows;
     const int64_t pairs = T * ((K + kBK - 1) / kBK);
     int64_t g = pairs / kMinPairs;
     const int sms = device_sm_count();
@@ -655,13 +660,13 @@ cudaError_t launch_tc_shrink(const ForwardPlan &plan, const ProjView &v, cudaStr
     }
     if (!v.tile_plan || !v.vacc || !v.vt || v.shrink_grid <= 0) return cudaErrorInvalidValue;
     CUtensorMap tx, ta;
-    if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, kPlanRows)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, kSubRows)) return cudaErrorInvalidValue;
     if (!make_tmap_bf16(&ta, v.a_arena, static_cast<uint64_t>(v.num_blocks) * LORA_BLOCK_ROWS, plan.K, plan.K,
                         LORA_BLOCK_ROWS))
         return cudaErrorInvalidValue;
     ShrinkParams p;
     p.M = plan.M;
-    p.T = (plan.M + kPlanRows - 1) / kPlanRows;
+    p.T = (plan.M + kSubRows - 1) / kSubRows;
     p.num_kb = (plan.K + kBK - 1) / kBK;
     p.plan = v.tile_plan;
     p.vacc = v.vacc;
@@ -690,8 +695,8 @@ cudaError_t launch_tc_shrink(const ForwardPlan &plan, const ProjView &v, cudaStr
     c.V = v.V;
     c.status = plan.status;
     void *cargs[] = {&c};
-    return launch_pdl(reinterpret_cast<const void *>(tile_convert_kernel), dim3(p.T, kConvertSplit), 256, 0, cargs,
-                      stream);
+    return launch_pdl(reinterpret_cast<const void *>(tile_convert_kernel),
+                      dim3((plan.M + kPlanRows - 1) / kPlanRows, kConvertSplit), kPlanRows, 0, cargs, stream);
 }
 
 }  // namespace lora

@@ -221,10 +221,11 @@ __device__ __forceinline__ void epi_sync() {
 
 // --------------------------------------------------------------- producer
 
-// Extension steps of token tile ta: the pool blocks its plan lists (0 when
-// the tile has no adapter rows or takes the CUDA-core expand).
+// Extension steps of token tile ta: the pool blocks the plan of its 256-row
+// plan tile lists (0 when that has no adapter rows or takes the CUDA-core
+// expand).
 __device__ __forceinline__ int32_t tile_ext_steps(const TcParams &p, int32_t ta) {
-    const int32_t nb = p.tile_plan[static_cast<size_t>(ta) * kPlanInts];
+    const int32_t nb = p.tile_plan[static_cast<size_t>(ta / (kPlanRows / kBM)) * kPlanInts];
     return nb > 0 ? nb : 0;
 }
 
@@ -302,7 +303,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
                 // e (32-byte swizzle, side by side in the A area) and the
                 // block's B rows of this unit's output columns
                 const int32_t e = i - nmain;
-                const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e];
+                const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta / (kPlanRows / kBM)) * kPlanInts + kPlanBlkOff + e];
                 mbar_arrive_expect_tx(&full[s], 2 * kVtBoxBytes + BN * LORA_BLOCK_ROWS * 2);
                 tma_load_2d(sA + s * C::kABytes, tma_va, e * LORA_BLOCK_ROWS, w.ta * kBM, &full[s]);
                 tma_load_2d(sA + s * C::kABytes + kVtBoxBytes, tma_va, kVtCols / 2 + e * LORA_BLOCK_ROWS, w.ta * kBM,
@@ -349,7 +350,9 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
                 ok = false;
                 break;
             }
-            tc_fence_after_sync();
+            // a tile converted by the epilogue threads (QUANT) was written through
+            // the generic proxy; TMA-filled stages need no fence
+            if (QUANT) tc_fence_after_sync();
             const uint32_t a_addr = smem_u32(sA + s * C::kABytes);
             const uint32_t b_addr = smem_u32(sB + s * C::kBBytes);
             if (kb < kb_main) {
@@ -684,7 +687,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
             const int32_t m = w.ta * kBM + q * 32 + lane;
             // the CUDA-core expand for rows of tiles whose adapters span too
             // many pool blocks for the LoRA steps (or without the steps at all)
-            const bool per_row = !p.lora_tiles || p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts] < 0;
+            const bool per_row = !p.lora_tiles || p.tile_plan[static_cast<size_t>(w.ta / (kPlanRows / kBM)) * kPlanInts] < 0;
             int32_t r = 0, slot = -1;
             float s = 0.0f;
             if (per_row && m < p.M)
@@ -797,6 +800,321 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+
+// --------------------------------------------------------------- two-SM kernel (large M)
+//
+// Large M in bf16 with at least 256 output columns: one MMA over a pair of
+// CTAs (a cluster of two, tcgen05 cta_group::2).  A pair tile is 256 tokens x
+// kPairBN output columns; CTA r of the pair loads its 128 token rows of x and
+// its kPairBN/2 rows of W per k-block (32 KiB instead of the 48 KiB a
+// 128 x 256 tile takes on one SM), the even CTA issues the MMAs (M = 256,
+// N = kPairBN) over both CTAs' shared memory, and each CTA's Tensor Memory
+// holds the accumulator rows of its 128 tokens.  Both CTAs' loads signal the
+// even CTA's `full` barrier; its MMA completions signal both CTAs' `empty`
+// and `tmem_full` barriers; both CTAs' epilogues signal its `tmem_empty`.
+// After the main k-blocks come the LoRA steps of the pair tile's plan, in
+// the same split (Vt rows per CTA, half of the block's B rows per CTA).
+
+constexpr int kPairM = 2 * kBM;   // tokens per pair tile
+constexpr int kPairBN = 256;      // output columns per pair tile (the MMA's N)
+constexpr int kPairBand = 4;      // unit order: pair tiles per band (as kTaBand for one SM)
+
+struct PairCfg {
+    static constexpr uint32_t kABytes = kBM * kBK * 2;              // this CTA's 128 rows of x
+    static constexpr uint32_t kBBytes = (kPairBN / 2) * kBK * 2;    // this CTA's half of the W tile
+    static constexpr uint32_t kOutBytes = kBM * kBK * 2;            // an output staging buffer: 128 rows x 64 columns
+    static constexpr int kOutBufs = 2;
+    static constexpr int kFixed = 1024 + kOutBufs * static_cast<int>(kOutBytes) + (2 * 12 + 4) * 8 + 16;
+    static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes);
+    static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
+    static constexpr uint32_t kTmemCols = 2 * kPairBN;              // two accumulators
+    static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) +
+                                    kOutBufs * kOutBytes + (2 * kStages + 4) * 8 + 16;
+    static_assert(kSmem <= kSmemLimit, "shared memory over budget");
+    static_assert(kTmemCols <= 512, "two accumulators in Tensor Memory");
+    static_assert(kABytes >= 2 * kVtBoxBytes, "a LoRA step's Vt boxes fit the A area");
+};
+
+__device__ __forceinline__ Unit decode_pair_unit(int32_t u, const TcParams &p) {
+    Unit w;
+    w.ks = 0;
+    if (p.tiles_a > kPairBand) {
+        const int32_t per = kPairBand * p.tiles_b;
+        const int32_t band = u / per, q = u % per;
+        const int32_t rows = min(kPairBand, p.tiles_a - band * kPairBand);
+        w.ta = band * kPairBand + q % rows;
+        w.tb = q / rows;
+    } else {
+        w.ta = u % p.tiles_a;
+        w.tb = u / p.tiles_a;
+    }
+    return w;
+}
+
+// Units of this pair (every (gridDim.x / 2)-th), or -1.
+__device__ __forceinline__ int32_t next_pair_unit(const TcParams &p, int32_t idx) {
+    const int32_t u = static_cast<int32_t>(blockIdx.x >> 1) + idx * static_cast<int32_t>(gridDim.x >> 1);
+    return u < p.num_units ? u : -1;
+}
+
+__device__ __forceinline__ int32_t pair_ext_steps(const TcParams &p, int32_t ta) {
+    const int32_t nb = p.tile_plan[static_cast<size_t>(ta) * kPlanInts];
+    return nb > 0 ? nb : 0;
+}
+
+__device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, const CUtensorMap *tma_w,
+                                                  const CUtensorMap *tma_vt, const CUtensorMap *tma_bb,
+                                                  const TcParams &p, uint32_t rank, uint8_t *sA, uint8_t *sB,
+                                                  uint64_t *full, uint64_t *empty, volatile uint32_t *abort_flag) {
+    using namespace sm100;
+    using C = PairCfg;
+    int32_t it = 0;
+    for (int32_t idx = 0;; ++idx) {
+        const int32_t u = next_pair_unit(p, idx);
+        if (u < 0) break;
+        const Unit w = decode_pair_unit(u, p);
+        const int32_t nmain = p.num_kb;
+        int32_t total = nmain;
+        const int32_t row = w.ta * kPairM + static_cast<int32_t>(rank) * kBM;
+        for (int32_t i = 0; i < total; ++i, ++it) {
+            if (p.lora_tiles && i == nmain - 1) {
+                grid_dependency_wait();  // the plan and Vt come from the kernels before
+                total = nmain + pair_ext_steps(p, w.ta);
+            }
+            const int s = it % C::kStages;
+            if (!mbar_wait_bounded(&empty[s], ((it / C::kStages) & 1) ^ 1, kWaitLimitNs)) {
+                record_error(p.status, kDevTimeout, 11);
+                *abort_flag = 1;
+            }
+            if (*abort_flag) return;
+            // the stage is free in both CTAs once the even CTA's MMAs have read
+            // it: that CTA's producer, which has just waited for it, tells the other
+            if (rank == 0 && it >= C::kStages) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&empty[s]), 1));
+            const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's barrier
+            if (i < nmain) {
+                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (C::kABytes + C::kBBytes));
+                tma_load_2d_pair(sA + s * C::kABytes, tma_x, i * kBK, row, fb);
+                tma_load_2d_pair(sB + s * C::kBBytes, tma_w, i * kBK, w.tb * kPairBN + static_cast<int32_t>(rank) * (kPairBN / 2),
+                                 fb);
+            } else {
+                const int32_t e = i - nmain;
+                const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e];
+                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (2 * kVtBoxBytes + (kPairBN / 2) * LORA_BLOCK_ROWS * 2));
+                tma_load_2d_pair(sA + s * C::kABytes, tma_vt, e * LORA_BLOCK_ROWS, row, fb);
+                tma_load_2d_pair(sA + s * C::kABytes + kVtBoxBytes, tma_vt, kVtCols / 2 + e * LORA_BLOCK_ROWS, row, fb);
+                tma_load_2d_pair(sB + s * C::kBBytes, tma_bb, 0,
+                                 blk * p.N + w.tb * kPairBN + static_cast<int32_t>(rank) * (kPairBN / 2), fb);
+            }
+        }
+    }
+}
+
+// The even CTA's MMA issuer.
+__device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
+                                             uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
+                                             uint32_t tmem_base, volatile uint32_t *abort_flag) {
+    using namespace sm100;
+    using C = PairCfg;
+    constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kPairBN);
+    int32_t it = 0, t = 0;
+    for (int32_t idx = 0;; ++idx) {
+        const int32_t u = next_pair_unit(p, idx);
+        if (u < 0) break;
+        const Unit w = decode_pair_unit(u, p);
+        const int32_t nmain = p.num_kb;
+        int32_t total = nmain;
+        const int b = t & 1;
+        bool ok = mbar_wait_bounded(&tmem_empty[b], ((t >> 1) & 1) ^ 1, kWaitLimitNs);
+        if (!ok) record_error(p.status, kDevTimeout, 12);
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + b * kPairBN;
+        for (int32_t i = 0; i < total && ok; ++i, ++it) {
+            if (p.lora_tiles && i == nmain - 1) {
+                grid_dependency_wait();
+                total = nmain + pair_ext_steps(p, w.ta);
+            }
+            const int s = it % C::kStages;
+            if (!mbar_wait_bounded(&full[s], (it / C::kStages) & 1, kWaitLimitNs)) {
+                record_error(p.status, kDevTimeout, 13);
+                ok = false;
+                break;
+            }
+            const uint32_t a_addr = smem_u32(sA + s * C::kABytes);
+            const uint32_t b_addr = smem_u32(sB + s * C::kBBytes);
+            if (i < nmain) {
+#pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k)
+                    mma_bf16_f32_pair(d, desc_kmajor_sw128(a_addr + k * kUmmaK * 2),
+                                      desc_kmajor_sw128(b_addr + k * kUmmaK * 2), idesc, (i > 0 || k > 0) ? 1u : 0u);
+            } else {  // LoRA step: Vt_hi and Vt_lo times the block's B, K = 16 each
+                mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr), desc_kmajor_sw32(b_addr), idesc, 1u);
+                mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr + kVtBoxBytes), desc_kmajor_sw32(b_addr), idesc, 1u);
+            }
+            // the stage is free once these MMAs have read it (the producer of this
+            // CTA passes that on to the other CTA's)
+            mma_commit_pair(mapa_shared(smem_u32(&empty[s]), 0));
+        }
+        if (!ok || *abort_flag) {
+            *abort_flag = 1;
+            // wake both epilogues so they can unwind
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[b]), 0));
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[b]), 1));
+            return;
+        }
+        mma_commit_pair(mapa_shared(smem_u32(&tmem_full[b]), 0));
+        mma_commit_pair(mapa_shared(smem_u32(&tmem_full[b]), 1));
+        ++t;
+    }
+}
+
+// Epilogue of both CTAs: for each unit, the 256 accumulator columns in four
+// chunks of 64: every warp reads 32 of them for its 32 rows from TMEM, adds
+// the CUDA-core expand where the tile needs it, and writes bf16 into a
+// shared-memory staging buffer laid out as a 128-byte-swizzled [128 x 64]
+// box; one thread then stores the box with TMA (rows past M and columns past
+// N are clipped).  Two staging buffers alternate.
+__device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUtensorMap *tma_out, uint32_t rank,
+                                                  uint8_t *sOut, uint64_t *tmem_full, uint64_t *tmem_empty,
+                                                  uint32_t tmem_base, volatile uint32_t *abort_flag) {
+    using namespace sm100;
+    using C = PairCfg;
+    const int warp = threadIdx.x >> 5;
+    const int q = warp & 3;
+    const int grp = (warp - 2) >> 2;  // which 32 of a chunk's 64 columns
+    const int lane = threadIdx.x & 31;
+    const int et = threadIdx.x - 64;
+    const int row = q * 32 + lane;    // row of this CTA's 128
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    grid_dependency_wait();  // the plan and the fallback V come from the kernels before
+    int32_t t = 0, chunk_no = 0;
+    for (int32_t idx = 0;; ++idx) {
+        const int32_t u = next_pair_unit(p, idx);
+        if (u < 0) break;
+        const Unit w = decode_pair_unit(u, p);
+        const int b = t & 1;
+        bool ok = mbar_wait_bounded(&tmem_full[b], (t >> 1) & 1, kWaitLimitNs);
+        if (!ok) {
+            record_error(p.status, kDevTimeout, 14);
+            *abort_flag = 1;
+        }
+        if (!epi_all(ok && !*abort_flag)) break;  // uniform over the epilogue warps
+        tc_fence_after_sync();
+        const uint32_t col0 = lane_addr + b * kPairBN;
+        const int32_t m0 = w.ta * kPairM + static_cast<int32_t>(rank) * kBM;
+        const int32_t m = m0 + row;
+        const bool per_row = !p.lora_tiles || p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts] < 0;
+        int32_t r = 0, slot = -1;
+        float s = 0.0f;
+        if (per_row && m < p.M)
+            slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s, p.status, false);
+#pragma unroll 1
+        for (int j = 0; j < kPairBN / kBK; ++j, ++chunk_no) {
+            float acc[32];
+            load_tmem_chunk(col0 + j * kBK + grp * 32, acc);
+            const int32_t n0 = w.tb * kPairBN + j * kBK;
+            if (per_row) rows_finish_chunk(p, slot, r, s, m, n0 + grp * 32, acc);
+            uint8_t *buf = sOut + (chunk_no & 1) * C::kOutBytes;
+            // the store that last read this buffer (two chunks back) must be done
+            if (et == 0) bulk_wait_group_read<C::kOutBufs - 1>();
+            epi_sync();
+            uint8_t *dst_row = buf + row * (kBK * 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint4 v;
+                v.x = pack_bf16x2(acc[i * 8 + 0], acc[i * 8 + 1]);
+                v.y = pack_bf16x2(acc[i * 8 + 2], acc[i * 8 + 3]);
+                v.z = pack_bf16x2(acc[i * 8 + 4], acc[i * 8 + 5]);
+                v.w = pack_bf16x2(acc[i * 8 + 6], acc[i * 8 + 7]);
+                // 16-byte piece c of the row lands at c ^ (row % 8): the 128-byte swizzle
+                const int c = grp * 4 + i;
+                *reinterpret_cast<uint4 *>(dst_row + ((c ^ (row & 7)) << 4)) = v;
+            }
+            fence_proxy_async_shared();  // the TMA store reads the buffer through the async proxy
+            epi_sync();
+            if (et == 0) {
+                tma_store_2d(tma_out, n0, m0, buf);
+                bulk_commit_group();
+            }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));  // the even CTA's barrier
+        ++t;
+    }
+    if (et == 0) bulk_wait_group_all();  // the staging buffers must outlive the stores
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ CUtensorMap tma_w,
+                    const __grid_constant__ CUtensorMap tma_vt, const __grid_constant__ CUtensorMap tma_bb,
+                    const __grid_constant__ CUtensorMap tma_out, const TcParams p) {
+    using namespace sm100;
+    using C = PairCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + C::kStages * C::kABytes;
+    uint8_t *sOut = sB + C::kStages * C::kBBytes;  // output staging, 1024-byte aligned
+    uint64_t *full = reinterpret_cast<uint64_t *>(sOut + C::kOutBufs * C::kOutBytes);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tmem_full = empty + C::kStages;  // [2]
+    uint64_t *tmem_empty = tmem_full + 2;      // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 2);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+    const uint32_t rank = cluster_ctarank();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tmem_full[b], 1);
+            mbar_init(&tmem_empty[b], 2 * kEpiWarps);  // the epilogue warps of both CTAs
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tma_x);
+        prefetch_tensormap(&tma_w);
+        prefetch_tensormap(&tma_out);
+        if (p.lora_tiles) {
+            prefetch_tensormap(&tma_vt);
+            prefetch_tensormap(&tma_bb);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, C::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    // both CTAs' barriers initialised and Tensor Memory allocated before any
+    // signal crosses the pair
+    tc_fence_before_sync();
+    cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) run_pair_producer(&tma_x, &tma_w, &tma_vt, &tma_bb, p, rank, sA, sB, full, empty, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) run_pair_mma(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
+    } else {
+        run_pair_epilogue(p, &tma_out, rank, sOut, tmem_full, tmem_empty, tmem_base, abort_flag);
+    }
+
+    // no CTA leaves while the other may still signal its barriers or read its
+    // shared memory through the pair MMA
+    tc_fence_before_sync();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, C::kTmemCols);
     }
 }
 
@@ -924,6 +1242,91 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     return cudaLaunchKernelEx(&cfg, kernel, tx, tw, tva, tvb, p);
 }
 
+
+// The two-SM GEMM of the large-M orientation (see tc_gemm_pair_kernel): as
+// many pairs as can be resident at once (a cluster needs two SMs of one
+// GPC), each walking every (pairs)-th unit.
+cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
+    using C = PairCfg;
+    static std::mutex mu;
+    static uint64_t done_ctx[128] = {};
+    static int max_pairs[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    int pairs_cap = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        uint64_t ctx = done_ctx[dev];
+        if (first_use_in_context(&ctx)) {
+            e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmem));
+            if (e != cudaSuccess) return e;
+            cudaLaunchConfig_t oc = {};
+            oc.gridDim = dim3(2 * 128);
+            oc.blockDim = dim3(kThreads);
+            oc.dynamicSmemBytes = C::kSmem;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel, &oc);
+            if (e != cudaSuccess || n < 1) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+            max_pairs[dev] = n;
+            done_ctx[dev] = current_context_id();
+        }
+        pairs_cap = max_pairs[dev];
+    }
+    if (!v.lora_tiles || !v.vt || !v.tile_plan) return cudaErrorInvalidValue;
+    CUtensorMap tx, tw, tvt, tbb, tout;
+    const uint64_t tiles_m = static_cast<uint64_t>((plan.M + kPlanRows - 1) / kPlanRows) * kPlanRows;
+    if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, kBM) ||
+        !make_tmap_bf16(&tout, v.out, plan.M, v.N, v.ldo, kBM) ||
+        !make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, kPairBN / 2) ||
+        !make_tmap_bf16(&tvt, v.vt, tiles_m, kVtCols, kVtCols, kBM, LORA_BLOCK_ROWS, 32) ||
+        !make_tmap_bf16(&tbb, v.b_arena, static_cast<uint64_t>(v.num_blocks) * v.N, LORA_BLOCK_ROWS, LORA_BLOCK_ROWS,
+                        kPairBN / 2, LORA_BLOCK_ROWS, 32))
+        return cudaErrorInvalidValue;
+    TcParams p = {};
+    p.M = plan.M;
+    p.N = v.N;
+    p.K = plan.K;
+    p.num_kb = (plan.K + kBK - 1) / kBK;
+    p.kb_per_split = p.num_kb;
+    p.splits = 1;
+    p.tiles_a = (plan.M + kPairM - 1) / kPairM;
+    p.tiles_b = (v.N + kPairBN - 1) / kPairBN;
+    p.num_units = p.tiles_a * p.tiles_b;
+    p.out = static_cast<__nv_bfloat16 *>(v.out);
+    p.ldo = v.ldo;
+    p.row_slot = plan.row_slot;
+    p.b_arena = static_cast<const __nv_bfloat16 *>(v.b_arena);
+    p.table = v.table;
+    p.ranks = v.ranks;
+    p.scales = v.scales;
+    p.max_slots = v.max_slots;
+    p.bps = v.bps;
+    p.num_blocks = v.num_blocks;
+    p.V = v.V;
+    p.ldv = v.max_rank;
+    p.v_parts = 1;
+    p.v_part_stride = static_cast<size_t>(plan.M) * v.max_rank;
+    p.lora_tiles = 1;
+    p.tile_plan = v.tile_plan;
+    p.status = plan.status;
+    p.tiles_a0 = p.tiles_a;
+    const int pairs = p.num_units < pairs_cap ? p.num_units : pairs_cap;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, tx, tw, tvt, tbb, tout, p);
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -1038,6 +1441,8 @@ cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cuda
             default: return launch_variant<true, 256>(plan, v, tp, stream);
         }
     }
+    // large M with at least one full pair tile of columns: the two-SM kernel
+    if (v.lora_tiles && v.N >= kPairBN) return launch_pair_gemm(plan, v, stream);
     if (tp.bn == 128) return launch_variant<false, 128>(plan, v, tp, stream);
     return launch_variant<false, 256>(plan, v, tp, stream);
 }
