@@ -580,12 +580,22 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
     plan.n_counters = static_cast<int32_t>((ws.total - ws.counter_off) / sizeof(int32_t));
     cudaStream_t st = as_stream(stream);
     plan.test_wait_limit_ns = g_test_wait_limit_ns.exchange(0);
+    plan.seg_offsets = plan.seg_adapter = nullptr;
+    plan.num_segs = 0;
+    plan.rows_in_plan = false;
     if (plan.stage_events &&
         cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[0]), st) != cudaSuccess)
         return LORA_ERR_CUDA;
     if (args->row_adapter) {
         if (!aligned16(args->row_adapter)) return LORA_ERR_ALIGNMENT;
         plan.row_slot = args->row_adapter;
+    } else if (!args->perm && plan.proj[0].lora_tiles) {
+        // the large-M path's plan kernel turns the segments into row slots itself
+        plan.row_slot = reinterpret_cast<int32_t *>(base + ws.row_slot_off);
+        plan.seg_offsets = args->seg_offsets;
+        plan.seg_adapter = args->seg_adapter;
+        plan.num_segs = args->num_segs;
+        plan.rows_in_plan = true;
     } else {
         int32_t *row_slot = reinterpret_cast<int32_t *>(base + ws.row_slot_off);
         if (cudaMemsetAsync(row_slot, 0xFF, sizeof(int32_t) * plan.M, st) != cudaSuccess)

@@ -147,6 +147,11 @@ struct ForwardPlan {
     // lora_test_arm_wait_timeout: 0, or the time limit of this call's split-K
     // counter waits, which then wait for one arrival more than any launch makes
     uint64_t test_wait_limit_ns;
+    // sorted segments without a permutation on the large-M path: the tile plan
+    // kernel derives every row's slot from them and writes row_slot itself
+    const int32_t *seg_offsets, *seg_adapter;
+    int32_t num_segs;
+    bool rows_in_plan;
 };
 
 // Count of kernels launched by the library (lora_kernel_launches).

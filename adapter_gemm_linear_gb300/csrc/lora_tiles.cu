@@ -16,10 +16,11 @@
 //                      plan tile: the MMA's A operand is the half's 128 x
 //                      rows, its B operand the plan tile's block
 //                      list -- one 16-row TMA box per pool block, stacked in
-//                      shared memory -- so N = 16 nb.  The (tile, k-block)
-//                      pairs of all tiles with adapters are split into
-//                      contiguous ranges of equal load (bytes), one per CTA,
-//                      so every SM streams x for the same time;
+//                      shared memory -- so N = 16 nb.  The (half tile,
+//                      k-block) pairs of all tiles are split into contiguous
+//                      ranges of equal length, one per CTA, so every SM
+//                      streams the same number of x boxes (halves without
+//                      adapter rows are loaded and skipped);
 //                      each CTA adds its part of a tile into an fp32
 //                      accumulator (zeroed by the plan kernel) with coalesced
 //                      reductions, so no CTA waits for another.
@@ -82,6 +83,11 @@ static_assert(kAccCols <= 256, "the MMA's N is at most 256");
 struct TilePlanParams {
     int32_t M, T;
     const int32_t *row_slot;
+    // sorted segments without a permutation: each row's slot from them,
+    // written to row_slot_out (NULL: row_slot holds the slots already)
+    const int32_t *seg_offsets, *seg_adapter;
+    int32_t num_segs;
+    int32_t *row_slot_out;
     const int32_t *table, *ranks;
     int32_t max_slots, bps, num_blocks;
     int32_t *plan;     // [T][kPlanInts]
@@ -97,34 +103,63 @@ struct TilePlanParams {
 // mark the tile (-1) for the CUDA-core fallback.  Then the CTA zeroes the
 // accumulator columns of the listed blocks.
 __global__ void __launch_bounds__(256) tile_plan_kernel(const TilePlanParams p) {
+    static_assert(kPlanRows == 256, "one thread per row of the plan tile");
     __shared__ int32_t s_nb;
+    __shared__ int32_t s_slot[kPlanRows];
     const int32_t t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *plan = p.plan + static_cast<size_t>(t) * kPlanInts;
+    // the shrink (a programmatic dependent) may launch at once: its x stream
+    // needs no plan, and it reads the plan and adds into the accumulator only
+    // after this grid has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    {
+        // every thread resolves one row's slot (errors recorded here, once per row)
+        const int32_t m = t * kPlanRows + threadIdx.x;
+        int32_t id = -1;
+        if (p.row_slot_out) {
+            // segment s covers positions [off[s], off[s+1]); the row's segment is
+            // the last one starting at or before it (offsets must not decrease
+            // and must lie within [0, M]; the first tile's CTA checks them)
+            const int32_t S = p.num_segs;
+            if (t == 0)
+                for (int32_t i = threadIdx.x; i <= S; i += blockDim.x) {
+                    const int32_t o = p.seg_offsets[i];
+                    if (o < 0 || o > p.M || (i > 0 && p.seg_offsets[i - 1] > o))
+                        record_error(p.status, kDevBadSegment, static_cast<uint32_t>(i));
+                }
+            if (m < p.M && S > 0 && p.seg_offsets[0] <= m) {
+                int32_t lo = 0, hi = S;
+                while (lo < hi) {
+                    const int32_t mid = (lo + hi + 1) >> 1;
+                    if (p.seg_offsets[mid] <= m) lo = mid; else hi = mid - 1;
+                }
+                if (lo < S && m < p.seg_offsets[lo + 1]) id = p.seg_adapter[lo];
+            }
+            if (m < p.M) p.row_slot_out[m] = id;
+        } else if (m < p.M) {
+            id = p.row_slot[m];
+        }
+        const int32_t rk = (id >= 0 && id < p.max_slots) ? p.ranks[id] : 0;
+        int32_t mine = INT_MAX;
+        if (id != -1 && m < p.M) {
+            if (id < -1 || id >= p.max_slots)
+                record_error(p.status, kDevBadAdapter, static_cast<uint32_t>(m));
+            else if (rk <= 0)
+                record_error(p.status, kDevEmptySlot, static_cast<uint32_t>(m));
+            else if (rk > p.bps * LORA_BLOCK_ROWS)
+                record_error(p.status, kDevBadBlock, static_cast<uint32_t>(id));
+            else
+                mine = id;
+        }
+        s_slot[threadIdx.x] = mine;
+    }
+    __syncthreads();
     if (warp == 0) {
         constexpr int kRowsPerLane = kPlanRows / 32;
-        int32_t id[kRowsPerLane], rk[kRowsPerLane], mine[kRowsPerLane];
+        int32_t mine[kRowsPerLane];
 #pragma unroll
-        for (int i = 0; i < kRowsPerLane; ++i) {
-            const int32_t m = t * kPlanRows + i * 32 + lane;
-            id[i] = m < p.M ? p.row_slot[m] : -1;
-        }
-#pragma unroll
-        for (int i = 0; i < kRowsPerLane; ++i) rk[i] = (id[i] >= 0 && id[i] < p.max_slots) ? p.ranks[id[i]] : 0;
-#pragma unroll
-        for (int i = 0; i < kRowsPerLane; ++i) {
-            const int32_t m = t * kPlanRows + i * 32 + lane;
-            mine[i] = INT_MAX;
-            if (id[i] == -1 || m >= p.M) continue;
-            if (id[i] < -1 || id[i] >= p.max_slots)
-                record_error(p.status, kDevBadAdapter, static_cast<uint32_t>(m));
-            else if (rk[i] <= 0)
-                record_error(p.status, kDevEmptySlot, static_cast<uint32_t>(m));
-            else if (rk[i] > p.bps * LORA_BLOCK_ROWS)
-                record_error(p.status, kDevBadBlock, static_cast<uint32_t>(id[i]));
-            else
-                mine[i] = id[i];
-        }
+        for (int i = 0; i < kRowsPerLane; ++i) mine[i] = s_slot[i * 32 + lane];
         int32_t last = -1, nb = 0;
         bool overflow = false;
         while (true) {
@@ -158,9 +193,6 @@ __global__ void __launch_bounds__(256) tile_plan_kernel(const TilePlanParams p) 
         }
     }
     __syncthreads();
-    // the shrink (a programmatic dependent) may launch; it reads the plan and
-    // adds into the accumulator only after this grid has completed
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int32_t n4 = s_nb > 0 ? s_nb * LORA_BLOCK_ROWS * kPlanRows / 4 : 0;
     float4 *acc = reinterpret_cast<float4 *>(p.vacc + static_cast<size_t>(t) * kAccCols * kPlanRows);
     for (int32_t i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -637,6 +669,10 @@ cudaError_t launch_tile_plan(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.plan = v.tile_plan;
     p.vacc = v.vacc;
     p.status = plan.status;
+    p.seg_offsets = plan.seg_offsets;
+    p.seg_adapter = plan.seg_adapter;
+    p.num_segs = plan.num_segs;
+    p.row_slot_out = plan.rows_in_plan ? const_cast<int32_t *>(plan.row_slot) : nullptr;
     if (!p.plan || !p.vacc) return cudaErrorInvalidValue;
     tile_plan_kernel<<<p.T, 256, 0, stream>>>(p);
     return cudaGetLastError();

@@ -57,7 +57,7 @@ DEFAULT_CONFIG = "prefill_sgmv"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_SOURCES = ["tc_gemm.cu", "sm100_ptx.cuh", "lora_device.cuh", "lora_internal.h"]
+GEMM_SOURCES = ["tc_gemm.cu", "sm100_ptx.cuh", "lora_device.cuh", "lora_internal.h", "tensor_map.cu", "tensor_map.h"]
 
 
 def parse_args():
@@ -216,7 +216,7 @@ def algorithmic(wl, w_bits=0):
         else:
             gb = base + rd * N * eb + rr * 4
             lb = rd * K * eb + Ma * K * eb + rr * 4
-            inter = 0
+            inter = large_m_intermediates(wl, N)
         out["gemm_bytes"] += gb
         out["gemm_flops"] += 2 * M * N * K
         out["lora_bytes"] += lb
@@ -226,6 +226,25 @@ def algorithmic(wl, w_bits=0):
         out["per_proj"].append({"N": N, "gemm_bytes": gb, "gemm_flops": 2 * M * N * K, "lora_bytes": lb})
     out.update(st)
     return out
+
+
+PLAN_ROWS = 256  # tokens per plan tile of the library's large-M LoRA path
+PAIR_BN = 256    # output columns per tile of its two-SM GEMM
+
+
+def large_m_intermediates(wl, N):
+    """Bytes of the large-M path's own intermediates for one projection: per
+    256-token tile, the fp32 V accumulator of the pool blocks its rows use
+    (written by reductions and read once) and Vt, its bf16 hi and lo parts
+    (written once, read by every one of the GEMM's column tiles)."""
+    ids = wl.row_adapter
+    blocks = 0
+    for t0 in range(0, wl.M, PLAN_ROWS):
+        used = np.unique(ids[t0:t0 + PLAN_ROWS])
+        blocks += sum(-(-int(wl.ranks[s]) // 16) for s in used if s >= 0)
+    cols = 16 * blocks  # accumulator columns over all tiles
+    col_tiles = -(-N // PAIR_BN)
+    return cols * PLAN_ROWS * 4 * 2 + cols * PLAN_ROWS * 2 * 2 * (1 + col_tiles)
 
 
 def percentiles(values):

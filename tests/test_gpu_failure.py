@@ -99,3 +99,27 @@ def test_scales_must_be_float32():
     with pytest.raises(ValueError):
         LinearCall(x, [(Ws[0], pools[0], out)], row_adapter=torch.zeros(8, dtype=torch.int32, device=DEV),
                    scales=torch.ones(2, dtype=torch.float64, device=DEV))
+
+
+@pytest.mark.parametrize("M", [300, 1100])
+def test_bad_segment_offsets_reported(M):
+    """Decreasing segment offsets are reported as LORA_ERR_SEGMENTS with the
+    offending index, by the segments-to-rows kernel (300 rows) and by the
+    large-M plan kernel that reads pre-sorted segments itself (1100 rows)."""
+    wl = synth(M=M, K=256, Ns=[264], num_slots=3, rank_choices=(16,), seed=5, none_frac=0.0)
+    pools = H.make_pools(wl, DEV, slots=range(3))
+    x, Ws = H.device_inputs(wl)
+    out = torch.empty((M, 264), dtype=torch.bfloat16, device=DEV)
+    offs = torch.tensor([0, M // 2, M // 4, M], dtype=torch.int32, device=DEV)  # decreasing at index 2
+    adp = torch.tensor([0, 1, 2], dtype=torch.int32, device=DEV)
+    device_status()
+    LinearCall(x, [(Ws[0], pools[0], out)], seg_offsets=offs, seg_adapter=adp)()
+    torch.cuda.synchronize()
+    assert device_status() == (8, 2)
+    # valid offsets afterwards: no error, and the oracle's result
+    offs = torch.tensor([0, M // 4, M // 2, M], dtype=torch.int32, device=DEV)
+    LinearCall(x, [(Ws[0], pools[0], out)], seg_offsets=offs, seg_adapter=adp)()
+    torch.cuda.synchronize()
+    assert device_status() == (0, 0)
+    ids = np.repeat(np.arange(3, dtype=np.int32), [M // 4, M // 2 - M // 4, M - M // 2])
+    H.assert_close("bf16", out.float().cpu().numpy(), H.oracle_rows(wl, 0, ids=ids), f"segments M={M}")
