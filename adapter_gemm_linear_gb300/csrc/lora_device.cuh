@@ -83,4 +83,74 @@ struct VecTraits<__nv_bfloat16> {
     }
 };
 
+// Vt entry e of one row (the large-M LoRA path): the block's 16 values
+// s * v[j] as bf16 hi parts at columns [16e, 16e + 16) and the bf16 of what
+// each hi part leaves (lo) at [kVtCols / 2 + 16e, ...), or zeros when the
+// block is not the row's own adapter's (own false).
+__device__ __forceinline__ void store_vt_entry(__nv_bfloat16 *vt_row, int32_t e, const float *v, bool own, float s) {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float h2[2], l2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float val = own ? s * v[2 * i + u] : 0.0f;
+            h2[u] = __bfloat162float(__float2bfloat16_rn(val));
+            l2[u] = val - h2[u];
+        }
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(h2[0], h2[1]);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(l2[0], l2[1]);
+        hw[i] = *reinterpret_cast<const uint32_t *>(&hh);
+        lw[i] = *reinterpret_cast<const uint32_t *>(&ll);
+    }
+    uint4 *hd = reinterpret_cast<uint4 *>(vt_row + e * LORA_BLOCK_ROWS);
+    uint4 *ld = reinterpret_cast<uint4 *>(vt_row + kVtCols / 2 + e * LORA_BLOCK_ROWS);
+    hd[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    hd[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    ld[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    ld[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+}
+
+// V[m][0, r) = A_slot x[m] for one row on CUDA cores, by one warp (lanes
+// over k in 8-wide pieces, then a butterfly sum): the fallback of the
+// large-M path for tiles whose adapters span too many pool blocks.  The
+// slot's table entries must already be checked to lie in [0, num_blocks).
+// K must be a multiple of 8.  Rank-rows past r are zero in the pool, so the
+// whole last block is computed and written.
+__device__ __forceinline__ void row_v_by_warp(const __nv_bfloat16 *x_row, int32_t K, const __nv_bfloat16 *a_arena,
+                                              const int32_t *slot_blocks, int32_t r, float *v_row, int lane) {
+    const int32_t K8 = K / 8;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x_row);
+    for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
+        const int32_t blk = slot_blocks[jb];
+        const uint4 *ab = reinterpret_cast<const uint4 *>(a_arena + static_cast<size_t>(blk) * LORA_BLOCK_ROWS * K);
+        float acc[LORA_BLOCK_ROWS];
+#pragma unroll
+        for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = 0.0f;
+        for (int32_t k8 = lane; k8 < K8; k8 += 32) {
+            float xv[8];
+            VecTraits<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(xr + k8), xv);
+#pragma unroll
+            for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
+                float av[8];
+                VecTraits<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(ab + static_cast<size_t>(j) * K8 + k8),
+                                               av);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[j] = fmaf(av[e], xv[e], acc[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+        }
+        if (lane < LORA_BLOCK_ROWS) {
+            float v = 0.0f;
+#pragma unroll
+            for (int j = 0; j < LORA_BLOCK_ROWS; ++j) v = lane == j ? acc[j] : v;
+            v_row[jb * LORA_BLOCK_ROWS + lane] = v;
+        }
+    }
+}
+
 }  // namespace lora

@@ -511,16 +511,29 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     // the tensor-core LoRA term of large M: tile plans, the V accumulator and
     // Vt, shared by the projections (their kernels run one after the other
     // on the stream)
+    // (the fp32 region: the shrink's accumulator for projections whose GEMM
+    // is the one-SM kernel, the K-slices of V for the two-SM kernel, which
+    // computes V itself)
     size_t plan_b = 0, vacc_b = 0, vt_b = 0;
     int sgrid = 0;
     if (a->n_proj > 0 && plan->proj[0].lora_tiles) {
         const size_t T = (static_cast<size_t>(a->M) + lora::kPlanRows - 1) / lora::kPlanRows;
         plan_b = sizeof(int32_t) * T * lora::kPlanInts;
-        sgrid = lora::tc_shrink_grid(a->M, a->K);
-        vacc_b = lora::tc_shrink_acc_bytes(a->M);
         vt_b = sizeof(uint16_t) * T * lora::kPlanRows * lora::kVtCols;
+        bool shrink = false, pair = false;
+        for (int i = 0; i < a->n_proj; ++i) {
+            const bool pg = lora::pair_gemm_takes(plan->proj[i]);
+            shrink = shrink || !pg;
+            pair = pair || pg;
+        }
+        if (shrink) {
+            sgrid = lora::tc_shrink_grid(a->M, a->K);
+            vacc_b = lora::tc_shrink_acc_bytes(a->M);
+        }
+        if (pair) vacc_b = std::max(vacc_b, lora::pair_vpart_bytes(a->M));  // the same region, used in turn
     }
-    for (int i = 0; i < a->n_proj; ++i) plan->proj[i].shrink_grid = plan->proj[i].lora_tiles ? sgrid : 0;
+    for (int i = 0; i < a->n_proj; ++i)
+        plan->proj[i].shrink_grid = plan->proj[i].lora_tiles && !lora::pair_gemm_takes(plan->proj[i]) ? sgrid : 0;
     ws->plan_off = off;
     off += align_up(plan_b, 256);
     ws->vacc_off = off;
@@ -573,7 +586,7 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
     for (int i = 0; i < plan.n_proj; ++i) {
         if (!plan.proj[i].lora_tiles) continue;
         plan.proj[i].tile_plan = reinterpret_cast<int32_t *>(base + ws.plan_off);
-        plan.proj[i].vacc = reinterpret_cast<float *>(base + ws.vacc_off);
+        plan.proj[i].vacc = ws.vt_off > ws.vacc_off ? reinterpret_cast<float *>(base + ws.vacc_off) : nullptr;
         plan.proj[i].vt = base + ws.vt_off;
     }
     plan.counters = reinterpret_cast<int32_t *>(base + ws.counter_off);

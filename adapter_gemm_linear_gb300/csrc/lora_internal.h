@@ -88,11 +88,18 @@ struct ProjView {
 // Large-M LoRA term (lora_tiles.cu).  A plan tile is 256 tokens: the token
 // tile of the two-SM GEMM, two tiles of the one-SM GEMM and of the shrink;
 // its record: [0] = nb, the pool blocks it lists (-1: more than
-// kPlanMaxBlocks, rows take the CUDA-core fallback), [kPlanBlkOff + e] = block
-// id and [kPlanSlotOff + e] = slot of entry e.
+// kPlanMaxBlocks, rows take the CUDA-core fallback), [kPlanReadyOff] = how
+// many CTAs of the two-SM GEMM have written the tile's Vt (or fallback V),
+// [kPlanPartOff + r] = how many K-slices of the tile's V the GEMM's CTAs of
+// rank r have finished, [kPlanStoredOff + r] = how many of those have stored
+// their partial sums (all five zeroed by the plan kernel),
+// [kPlanBlkOff + e] = block id and [kPlanSlotOff + e] = slot of entry e.
 constexpr int kPlanRows = 256;
 constexpr int kPlanMaxBlocks = 16;
 constexpr int kPlanInts = 48;
+constexpr int kPlanReadyOff = 1;
+constexpr int kPlanPartOff = 2;    // two entries, one per CTA rank of a pair
+constexpr int kPlanStoredOff = 4;  // two entries likewise
 constexpr int kPlanBlkOff = 16;
 constexpr int kPlanSlotOff = 32;
 constexpr int kVtCols = 2 * LORA_BLOCK_ROWS * kPlanMaxBlocks;  // hi parts, then lo parts
@@ -234,6 +241,12 @@ cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaS
 // Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K);
 cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+// Large M: whether the projection's GEMM is the two-SM kernel, which also
+// computes the LoRA term's V itself (only the plan kernel runs before it);
+// otherwise the shrink and convert kernels of lora_tiles.cu run first.
+bool pair_gemm_takes(const ProjView &v);
+// Its fp32 scratch for the K-slices of V (in ProjView::vacc): bytes for M rows.
+size_t pair_vpart_bytes(int32_t M);
 // Swapped orientation: projections v0 and (if not NULL) v1 of the same x in
 // one launch, with its own split-K tile counters.
 TcPlan plan_tc_pair(int32_t M, int32_t N0, int32_t N1, int32_t K);

@@ -483,10 +483,11 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
             if (e == cudaSuccess) e = launch_expand_grouped(plan, v, gt, stream);
             if (e != cudaSuccess) return e;
         } else {
-            // large M: the tiles' block lists, V on the tensor cores, Vt (and
-            // the per-row V of tiles whose adapters span too many blocks)
+            // large M: the tiles' block lists; then, unless the two-SM GEMM
+            // computes it itself, V on the tensor cores and Vt (and the per-row
+            // V of tiles whose adapters span too many blocks)
             e = launch_tile_plan(plan, v, stream);
-            if (e == cudaSuccess) e = launch_tc_shrink(plan, v, stream);
+            if (e == cudaSuccess && !pair_gemm_takes(v)) e = launch_tc_shrink(plan, v, stream);
             if (e != cudaSuccess) return e;
         }
         if (plan.stage_events) {
@@ -495,7 +496,7 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
         }
         e = launch_gemm_lora_tc(plan, v, stream);
         if (e != cudaSuccess) return e;
-        count_launches(swapped ? (by_row ? 2 : 3) : 4);
+        count_launches(swapped ? (by_row ? 2 : 3) : (pair_gemm_takes(v) ? 2 : 4));
         if (plan.stage_events) {
             e = cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[2 + 2 * p]), stream);
             if (e != cudaSuccess) return e;

@@ -91,7 +91,7 @@ struct TilePlanParams {
     const int32_t *table, *ranks;
     int32_t max_slots, bps, num_blocks;
     int32_t *plan;     // [T][kPlanInts]
-    float *vacc;       // [T][kAccCols][kPlanRows] fp32, zeroed here for the listed blocks
+    float *vacc;       // [T][kAccCols][kPlanRows] fp32, zeroed here for the listed blocks (NULL: none)
     unsigned long long *status;
 };
 
@@ -189,10 +189,16 @@ __global__ void __launch_bounds__(256) tile_plan_kernel(const TilePlanParams p) 
         }
         if (lane == 0) {
             plan[0] = overflow ? -1 : nb;
+            plan[kPlanReadyOff] = 0;
+            plan[kPlanPartOff] = 0;
+            plan[kPlanPartOff + 1] = 0;
+            plan[kPlanStoredOff] = 0;
+            plan[kPlanStoredOff + 1] = 0;
             s_nb = overflow ? -1 : nb;
         }
     }
     __syncthreads();
+    if (!p.vacc) return;  // the two-SM GEMM computes V itself, without the accumulator
     const int32_t n4 = s_nb > 0 ? s_nb * LORA_BLOCK_ROWS * kPlanRows / 4 : 0;
     float4 *acc = reinterpret_cast<float4 *>(p.vacc + static_cast<size_t>(t) * kAccCols * kPlanRows);
     for (int32_t i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -545,35 +551,13 @@ __global__ void __launch_bounds__(256) tile_convert_kernel(const ConvertParams p
 #pragma unroll
             for (int i = 0; i < LORA_BLOCK_ROWS; ++i)
                 v[i] = __ldcg(src + static_cast<size_t>(e * LORA_BLOCK_ROWS + i) * kPlanRows);
-            const bool own = slot >= 0 && plan[kPlanSlotOff + e] == slot;
-            uint32_t hw[8], lw[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float h2[2], l2[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const float val = own ? s * v[2 * i + u] : 0.0f;
-                    h2[u] = __bfloat162float(__float2bfloat16_rn(val));
-                    l2[u] = val - h2[u];
-                }
-                const __nv_bfloat162 hh = __floats2bfloat162_rn(h2[0], h2[1]);
-                const __nv_bfloat162 ll = __floats2bfloat162_rn(l2[0], l2[1]);
-                hw[i] = *reinterpret_cast<const uint32_t *>(&hh);
-                lw[i] = *reinterpret_cast<const uint32_t *>(&ll);
-            }
-            uint4 *hd = reinterpret_cast<uint4 *>(hi_row + e * LORA_BLOCK_ROWS);
-            uint4 *ld = reinterpret_cast<uint4 *>(hi_row + kVtCols / 2 + e * LORA_BLOCK_ROWS);
-            hd[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            hd[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-            ld[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            ld[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+            store_vt_entry(hi_row, e, v, slot >= 0 && plan[kPlanSlotOff + e] == slot, s);
         }
         return;
     }
     if (nb == 0) return;
     // fallback tile: V[m][j] = sum_k A_i[j][k] x[m][k], one warp per row, lanes over k
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int32_t K8 = p.K / 8;
     for (int32_t i = y + kConvertSplit * warp; i < kPlanRows; i += kConvertSplit * 8) {
         const int32_t m = t * kPlanRows + i;
         if (m >= p.M) break;
@@ -588,37 +572,8 @@ __global__ void __launch_bounds__(256) tile_convert_kernel(const ConvertParams p
             blocks_ok &= blk >= 0 && blk < p.num_blocks;
         }
         if (!blocks_ok) continue;  // reported by the plan kernel; the epilogue drops the row's correction
-        const uint4 *xr = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(m) * p.ldx);
-        for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < r; ++jb) {
-            const int32_t blk = p.table[static_cast<size_t>(slot) * p.bps + jb];
-            const uint4 *ab = reinterpret_cast<const uint4 *>(p.a_arena + static_cast<size_t>(blk) * LORA_BLOCK_ROWS * p.K);
-            float acc[LORA_BLOCK_ROWS];
-#pragma unroll
-            for (int j = 0; j < LORA_BLOCK_ROWS; ++j) acc[j] = 0.0f;
-            for (int32_t k8 = lane; k8 < K8; k8 += 32) {
-                float xv[8];
-                VecTraits<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(xr + k8), xv);
-#pragma unroll
-                for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
-                    float av[8];
-                    VecTraits<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(ab + static_cast<size_t>(j) * K8 + k8), av);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[j] = fmaf(av[e], xv[e], acc[j]);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < LORA_BLOCK_ROWS; ++j) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
-            }
-            // rank-rows past r are zero in the pool, so every entry of the block is finite
-            if (lane < LORA_BLOCK_ROWS) {
-                float v = 0.0f;
-#pragma unroll
-                for (int j = 0; j < LORA_BLOCK_ROWS; ++j) v = lane == j ? acc[j] : v;
-                p.V[static_cast<size_t>(m) * p.max_rank + jb * LORA_BLOCK_ROWS + lane] = v;
-            }
-        }
+        row_v_by_warp(p.x + static_cast<size_t>(m) * p.ldx, p.K, p.a_arena, p.table + static_cast<size_t>(slot) * p.bps,
+                      r, p.V + static_cast<size_t>(m) * p.max_rank, lane);
     }
 }
 
@@ -667,13 +622,13 @@ cudaError_t launch_tile_plan(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.bps = v.bps;
     p.num_blocks = v.num_blocks;
     p.plan = v.tile_plan;
-    p.vacc = v.vacc;
+    p.vacc = pair_gemm_takes(v) ? nullptr : v.vacc;  // the two-SM GEMM needs no accumulator
     p.status = plan.status;
     p.seg_offsets = plan.seg_offsets;
     p.seg_adapter = plan.seg_adapter;
     p.num_segs = plan.num_segs;
     p.row_slot_out = plan.rows_in_plan ? const_cast<int32_t *>(plan.row_slot) : nullptr;
-    if (!p.plan || !p.vacc) return cudaErrorInvalidValue;
+    if (!p.plan) return cudaErrorInvalidValue;
     tile_plan_kernel<<<p.T, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }

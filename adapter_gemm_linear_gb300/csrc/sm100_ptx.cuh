@@ -21,6 +21,12 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same for global memory: generic-proxy writes of this thread (or
+// acquired from another) before later async-proxy accesses (TMA loads).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -295,6 +301,15 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(mbar_cluster_addr)
         : "memory");
+}
+
+// Prefetch the box at (c0, c1) of a tensor map into L2 (no shared memory,
+// no barrier; boxes past the tensor's bounds fetch only what lies inside).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 // Arrive on an mbarrier of either CTA of the pair without ordering any of

@@ -120,6 +120,19 @@ struct TcParams {
     // only when armed for a test, so that the waits run out) and their limit
     int32_t counter_extra;
     uint64_t counter_wait_ns;
+    // two-SM kernel: V items, kVSplit per token tile (v_units tiles), each
+    // computes one K-slice of the tile's V = x A_list^T into v_part; the last
+    // slice of a CTA's rows to finish writes their Vt (vt_out), or for a
+    // fallback tile the slices write the per-row V (v_rows, from x and the A
+    // arena); then the plan's ready entry (plan_rw) counts the CTA
+    int32_t v_units;
+    __nv_bfloat16 *vt_out;
+    float *v_rows;
+    float *v_part;  // fp32 [v_units][kVSplit][256 rows][256 columns]: the K-slices of V
+    int32_t *plan_rw;
+    const __nv_bfloat16 *x;
+    int32_t ldx;
+    const __nv_bfloat16 *a_arena;
 };
 
 // The projection of a swapped W tile (second: the launch's second
@@ -817,10 +830,31 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
 // and `tmem_full` barriers; both CTAs' epilogues signal its `tmem_empty`.
 // After the main k-blocks come the LoRA steps of the pair tile's plan, in
 // the same split (Vt rows per CTA, half of the block's B rows per CTA).
+//
+// The LoRA term's V is computed here too, by V items: kVSplit per token
+// tile, each V = x_tile A_list^T over one K-slice with the same pair MMA (M
+// = 256 tokens, N = 32 ceil(nb/2): CTA r stacks blocks [r h, r h + h) of the
+// tile's list, h = ceil(nb/2), from 16-row boxes of the pool's A arena).
+// The slices of a CTA's rows count their arrival (a per-tile, per-rank
+// counter in the plan); all but the last store their fp32 slice, and the
+// last adds those to its own, writes the rows' Vt -- hi and lo bf16 parts of
+// s_i V masked to each row's own slot -- and counts the CTA in the plan's
+// ready entry; a main unit's producer waits for both CTAs' counts before it
+// loads Vt for the LoRA steps.  Tiles whose
+// plan overflowed get the per-row V on CUDA cores from their V items'
+// epilogues instead (rows split between the slices), which the main units'
+// epilogues wait for.  V items come first in every pair's sequence (so
+// every wait points to work that never waits), dealt first to the pairs
+// with one main unit fewer, up to kVSplit each, then to the others; all pairs
+// are resident at once (the grid is at most the resident cluster count), so
+// every wait ends.
 
 constexpr int kPairM = 2 * kBM;   // tokens per pair tile
 constexpr int kPairBN = 256;      // output columns per pair tile (the MMA's N)
 constexpr int kPairBand = 4;      // unit order: pair tiles per band (as kTaBand for one SM)
+constexpr uint32_t kBlockBoxBytes = LORA_BLOCK_ROWS * kBK * 2;  // one pool block's 16 A rows of a k-block
+constexpr int kVSplit = 2;        // K-slices of a token tile's V (V items per tile)
+static_assert(kPairM == kPlanRows, "a pair tile is a plan tile");
 
 struct PairCfg {
     static constexpr uint32_t kABytes = kBM * kBK * 2;              // this CTA's 128 rows of x
@@ -836,6 +870,8 @@ struct PairCfg {
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kTmemCols <= 512, "two accumulators in Tensor Memory");
     static_assert(kABytes >= 2 * kVtBoxBytes, "a LoRA step's Vt boxes fit the A area");
+    static_assert((kPairBN / 2) * kBK * 2 >= ((kPlanMaxBlocks + 1) / 2) * kBlockBoxBytes,
+                  "a CTA's half of a V unit's block list fits the B area");
 };
 
 __device__ __forceinline__ Unit decode_pair_unit(int32_t u, const TcParams &p) {
@@ -854,10 +890,37 @@ __device__ __forceinline__ Unit decode_pair_unit(int32_t u, const TcParams &p) {
     return w;
 }
 
-// Units of this pair (every (gridDim.x / 2)-th), or -1.
+// Unit idx of this pair, or -1.  Codes: u < num_units is a main unit (every
+// G-th for G pairs, in the band order of decode_pair_unit), num_units + v the
+// V item v (token tile v / kVSplit, K-slice v % kVSplit).  A pair takes its V
+// items first.  V items are dealt in order of v: first up to kVSplit to each
+// pair with one main unit fewer (pairs [G - light, G), the last pair first;
+// every pair when G divides num_units), then one at a time to all pairs from
+// the first on.
 __device__ __forceinline__ int32_t next_pair_unit(const TcParams &p, int32_t idx) {
-    const int32_t u = static_cast<int32_t>(blockIdx.x >> 1) + idx * static_cast<int32_t>(gridDim.x >> 1);
+    const int32_t G = static_cast<int32_t>(gridDim.x >> 1), P = static_cast<int32_t>(blockIdx.x >> 1);
+    const int32_t NV = p.v_units * kVSplit;
+    int32_t nv = 0;
+    if (NV > 0) {
+        const int32_t rem = p.num_units % G;
+        const int32_t light = rem == 0 ? G : G - rem;
+        const int32_t n1 = min(NV, light * kVSplit);
+        const int32_t j = G - 1 - P;  // this pair's place among the light ones
+        const int32_t c1 = (j < light && j < n1) ? (n1 - j + light - 1) / light : 0;
+        if (idx < c1) return p.num_units + j + idx * light;
+        const int32_t n2 = NV - n1;
+        const int32_t c2 = P < n2 ? (n2 - P + G - 1) / G : 0;
+        if (idx < c1 + c2) return p.num_units + n1 + P + (idx - c1) * G;
+        nv = c1 + c2;
+    }
+    const int32_t u = P + (idx - nv) * G;
     return u < p.num_units ? u : -1;
+}
+
+// K-slice s of a V item: k-blocks [kb0, kb1) (empty when num_kb < kVSplit).
+__device__ __forceinline__ void vslice_kblocks(const TcParams &p, int32_t s, int32_t *kb0, int32_t *kb1) {
+    *kb0 = s * p.num_kb / kVSplit;
+    *kb1 = (s + 1) * p.num_kb / kVSplit;
 }
 
 __device__ __forceinline__ int32_t pair_ext_steps(const TcParams &p, int32_t ta) {
@@ -865,109 +928,336 @@ __device__ __forceinline__ int32_t pair_ext_steps(const TcParams &p, int32_t ta)
     return nb > 0 ? nb : 0;
 }
 
+// Main units of this pair (they follow its V items in next_pair_unit).
+__device__ __forceinline__ int32_t pair_main_count(const TcParams &p) {
+    const int32_t G = static_cast<int32_t>(gridDim.x >> 1), P = static_cast<int32_t>(blockIdx.x >> 1);
+    return P < p.num_units ? (p.num_units - P + G - 1) / G : 0;
+}
+
+// The order of the two phases (0: the main k-blocks, 1: the LoRA steps) of
+// this pair's main units: slot -> (main unit k, phase).  The first two
+// units' main k-blocks both come before their LoRA steps, so that those,
+// which wait for the tiles' V, start one unit later (the two accumulators
+// hold both units meanwhile); then each unit's phases follow one another.
+__device__ __forceinline__ void pair_main_phase(int32_t slot, int32_t n_main, int32_t *k, int32_t *phase) {
+    if (n_main >= 2 && slot < 4) {
+        *k = slot & 1;
+        *phase = slot >> 1;
+    } else {
+        *k = slot >> 1;
+        *phase = slot & 1;
+    }
+}
+
 __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, const CUtensorMap *tma_w,
                                                   const CUtensorMap *tma_vt, const CUtensorMap *tma_bb,
-                                                  const TcParams &p, uint32_t rank, uint8_t *sA, uint8_t *sB,
-                                                  uint64_t *full, uint64_t *empty, volatile uint32_t *abort_flag) {
+                                                  const CUtensorMap *tma_pa, const TcParams &p, uint32_t rank,
+                                                  uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
+                                                  volatile uint32_t *abort_flag) {
     using namespace sm100;
     using C = PairCfg;
-    int32_t it = 0;
-    for (int32_t idx = 0;; ++idx) {
+    int32_t it = 0, idx = 0;
+    // Wait for stage `it` to be free in both CTAs (the even CTA's MMAs have
+    // read it: that CTA's producer, which has just waited for it, tells the
+    // other); false when the pair gives up.
+    auto acquire_stage = [&](int32_t site) -> bool {
+        const int s = it % C::kStages;
+        if (!mbar_wait_bounded(&empty[s], ((it / C::kStages) & 1) ^ 1, kWaitLimitNs)) {
+            record_error(p.status, kDevTimeout, site);
+            *abort_flag = 1;
+        }
+        if (*abort_flag) return false;
+        if (rank == 0 && it >= C::kStages) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&empty[s]), 1));
+        return true;
+    };
+    for (;; ++idx) {  // V items: x and this CTA's half of the tile's block list, one K-slice
         const int32_t u = next_pair_unit(p, idx);
-        if (u < 0) break;
-        const Unit w = decode_pair_unit(u, p);
-        const int32_t nmain = p.num_kb;
-        int32_t total = nmain;
-        const int32_t row = w.ta * kPairM + static_cast<int32_t>(rank) * kBM;
-        for (int32_t i = 0; i < total; ++i, ++it) {
-            if (p.lora_tiles && i == nmain - 1) {
-                grid_dependency_wait();  // the plan and Vt come from the kernels before
-                total = nmain + pair_ext_steps(p, w.ta);
-            }
+        if (u < p.num_units) break;  // the main units (or the end) follow
+        const int32_t ta = (u - p.num_units) / kVSplit;
+        int32_t kb0, kb1;
+        vslice_kblocks(p, (u - p.num_units) % kVSplit, &kb0, &kb1);
+        grid_dependency_wait();  // the plan comes from the kernel before
+        const int32_t *plan = p.tile_plan + static_cast<size_t>(ta) * kPlanInts;
+        const int32_t nb = plan[0];
+        if (nb <= 0) continue;  // nothing for the tensor cores
+        const int32_t h = (nb + 1) >> 1;
+        const int32_t e0 = static_cast<int32_t>(rank) * h, e1 = min(nb, e0 + h);
+        const int32_t row = ta * kPairM + static_cast<int32_t>(rank) * kBM;
+        for (int32_t i = kb0; i < kb1; ++i, ++it) {
+            if (!acquire_stage(15)) return;
             const int s = it % C::kStages;
-            if (!mbar_wait_bounded(&empty[s], ((it / C::kStages) & 1) ^ 1, kWaitLimitNs)) {
-                record_error(p.status, kDevTimeout, 11);
-                *abort_flag = 1;
-            }
-            if (*abort_flag) return;
-            // the stage is free in both CTAs once the even CTA's MMAs have read
-            // it: that CTA's producer, which has just waited for it, tells the other
-            if (rank == 0 && it >= C::kStages) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&empty[s]), 1));
             const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's barrier
-            if (i < nmain) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kABytes + static_cast<uint32_t>(nb) * kBlockBoxBytes);
+            tma_load_2d_pair(sA + s * C::kABytes, tma_x, i * kBK, row, fb);
+            for (int32_t e = e0; e < e1; ++e)
+                tma_load_2d_pair(sB + s * C::kBBytes + (e - e0) * kBlockBoxBytes, tma_pa, i * kBK,
+                                 plan[kPlanBlkOff + e] * LORA_BLOCK_ROWS, fb);
+        }
+    }
+    const int32_t nv = idx, n_main = pair_main_count(p);
+    for (int32_t slot = 0; slot < 2 * n_main; ++slot) {
+        int32_t k, phase;
+        pair_main_phase(slot, n_main, &k, &phase);
+        const Unit w = decode_pair_unit(next_pair_unit(p, nv + k), p);
+        const int32_t row = w.ta * kPairM + static_cast<int32_t>(rank) * kBM;
+        const int32_t n0 = w.tb * kPairBN + static_cast<int32_t>(rank) * (kPairBN / 2);  // this CTA's W rows
+        if (phase == 0) {
+            for (int32_t i = 0; i < p.num_kb; ++i, ++it) {
+                if (!acquire_stage(11)) return;
+                const int s = it % C::kStages;
+                const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
                 if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (C::kABytes + C::kBBytes));
                 tma_load_2d_pair(sA + s * C::kABytes, tma_x, i * kBK, row, fb);
-                tma_load_2d_pair(sB + s * C::kBBytes, tma_w, i * kBK, w.tb * kPairBN + static_cast<int32_t>(rank) * (kPairBN / 2),
-                                 fb);
-            } else {
-                const int32_t e = i - nmain;
-                const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e];
-                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (2 * kVtBoxBytes + (kPairBN / 2) * LORA_BLOCK_ROWS * 2));
-                tma_load_2d_pair(sA + s * C::kABytes, tma_vt, e * LORA_BLOCK_ROWS, row, fb);
-                tma_load_2d_pair(sA + s * C::kABytes + kVtBoxBytes, tma_vt, kVtCols / 2 + e * LORA_BLOCK_ROWS, row, fb);
-                tma_load_2d_pair(sB + s * C::kBBytes, tma_bb, 0,
-                                 blk * p.N + w.tb * kPairBN + static_cast<int32_t>(rank) * (kPairBN / 2), fb);
+                tma_load_2d_pair(sB + s * C::kBBytes, tma_w, i * kBK, n0, fb);
             }
+            continue;
+        }
+        grid_dependency_wait();  // the plan comes from the kernel before
+        const int32_t ext = pair_ext_steps(p, w.ta);
+        if (ext == 0) continue;
+        // the tile's Vt comes from its V items (both CTAs of some pair)
+        if (!wait_counter_at_least(p.tile_plan + static_cast<size_t>(w.ta) * kPlanInts + kPlanReadyOff, 2,
+                                   kWaitLimitNs)) {
+            record_error(p.status, kDevTimeout, 16);
+            *abort_flag = 1;
+            return;
+        }
+        fence_proxy_async_global();  // the TMA loads below read what generic stores wrote
+        for (int32_t e = 0; e < ext; ++e, ++it) {
+            if (!acquire_stage(11)) return;
+            const int s = it % C::kStages;
+            const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+            const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e];
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (2 * kVtBoxBytes + (kPairBN / 2) * LORA_BLOCK_ROWS * 2));
+            tma_load_2d_pair(sA + s * C::kABytes, tma_vt, e * LORA_BLOCK_ROWS, row, fb);
+            tma_load_2d_pair(sA + s * C::kABytes + kVtBoxBytes, tma_vt, kVtCols / 2 + e * LORA_BLOCK_ROWS, row, fb);
+            tma_load_2d_pair(sB + s * C::kBBytes, tma_bb, 0, blk * p.N + n0, fb);
         }
     }
 }
 
-// The even CTA's MMA issuer.
+// The even CTA's MMA issuer: the V items, then the phases of the main units
+// in the order of pair_main_phase (the same stage order as the producers').
+// Unit number t (V items and main units in their sequence order) uses
+// accumulator t & 1.
 __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
                                              uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
                                              uint32_t tmem_base, volatile uint32_t *abort_flag) {
     using namespace sm100;
     using C = PairCfg;
-    constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kPairBN);
-    int32_t it = 0, t = 0;
-    for (int32_t idx = 0;; ++idx) {
-        const int32_t u = next_pair_unit(p, idx);
-        if (u < 0) break;
-        const Unit w = decode_pair_unit(u, p);
-        const int32_t nmain = p.num_kb;
-        int32_t total = nmain;
-        const int b = t & 1;
-        bool ok = mbar_wait_bounded(&tmem_empty[b], ((t >> 1) & 1) ^ 1, kWaitLimitNs);
+    constexpr uint32_t idesc_main = idesc_bf16_f32(kPairM, kPairBN);
+    int32_t it = 0, idx = 0;
+    // wake both epilogues for accumulator b so they can unwind
+    auto give_up = [&](int b) {
+        *abort_flag = 1;
+        mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[b]), 0));
+        mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[b]), 1));
+    };
+    auto claim_accumulator = [&](int32_t t) -> bool {
+        const bool ok = mbar_wait_bounded(&tmem_empty[t & 1], ((t >> 1) & 1) ^ 1, kWaitLimitNs);
         if (!ok) record_error(p.status, kDevTimeout, 12);
         tc_fence_after_sync();
-        const uint32_t d = tmem_base + b * kPairBN;
-        for (int32_t i = 0; i < total && ok; ++i, ++it) {
-            if (p.lora_tiles && i == nmain - 1) {
-                grid_dependency_wait();
-                total = nmain + pair_ext_steps(p, w.ta);
-            }
-            const int s = it % C::kStages;
-            if (!mbar_wait_bounded(&full[s], (it / C::kStages) & 1, kWaitLimitNs)) {
-                record_error(p.status, kDevTimeout, 13);
-                ok = false;
-                break;
-            }
-            const uint32_t a_addr = smem_u32(sA + s * C::kABytes);
-            const uint32_t b_addr = smem_u32(sB + s * C::kBBytes);
-            if (i < nmain) {
-#pragma unroll
-                for (int k = 0; k < kBK / kUmmaK; ++k)
-                    mma_bf16_f32_pair(d, desc_kmajor_sw128(a_addr + k * kUmmaK * 2),
-                                      desc_kmajor_sw128(b_addr + k * kUmmaK * 2), idesc, (i > 0 || k > 0) ? 1u : 0u);
-            } else {  // LoRA step: Vt_hi and Vt_lo times the block's B, K = 16 each
-                mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr), desc_kmajor_sw32(b_addr), idesc, 1u);
-                mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr + kVtBoxBytes), desc_kmajor_sw32(b_addr), idesc, 1u);
-            }
-            // the stage is free once these MMAs have read it (the producer of this
-            // CTA passes that on to the other CTA's)
-            mma_commit_pair(mapa_shared(smem_u32(&empty[s]), 0));
+        return ok;
+    };
+    auto wait_stage = [&]() -> bool {
+        const int s = it % C::kStages;
+        if (!mbar_wait_bounded(&full[s], (it / C::kStages) & 1, kWaitLimitNs)) {
+            record_error(p.status, kDevTimeout, 13);
+            return false;
         }
-        if (!ok || *abort_flag) {
-            *abort_flag = 1;
-            // wake both epilogues so they can unwind
-            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[b]), 0));
-            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[b]), 1));
-            return;
-        }
+        return true;
+    };
+    // the stage is free once these MMAs have read it (the producer of this
+    // CTA passes that on to the other CTA's)
+    auto release_stage = [&]() { mma_commit_pair(mapa_shared(smem_u32(&empty[it % C::kStages]), 0)); };
+    auto finish_unit = [&](int b) {
         mma_commit_pair(mapa_shared(smem_u32(&tmem_full[b]), 0));
         mma_commit_pair(mapa_shared(smem_u32(&tmem_full[b]), 1));
-        ++t;
+    };
+    for (;; ++idx) {  // V items: N = 32 ceil(nb / 2), one K-slice, no LoRA steps
+        const int32_t u = next_pair_unit(p, idx);
+        if (u < p.num_units) break;
+        const int32_t t = idx, b = t & 1;
+        const int32_t ta = (u - p.num_units) / kVSplit;
+        int32_t kb0, kb1;
+        vslice_kblocks(p, (u - p.num_units) % kVSplit, &kb0, &kb1);
+        grid_dependency_wait();
+        const int32_t nb = p.tile_plan[static_cast<size_t>(ta) * kPlanInts];
+        const int32_t total = nb > 0 ? kb1 - kb0 : 0;
+        const uint32_t idesc = idesc_bf16_f32(kPairM, nb > 0 ? 32 * ((nb + 1) >> 1) : 32);
+        if (!claim_accumulator(t)) return give_up(b);
+        const uint32_t d = tmem_base + b * kPairBN;
+        for (int32_t i = 0; i < total; ++i, ++it) {
+            if (!wait_stage()) return give_up(b);
+            const uint32_t a_addr = smem_u32(sA + (it % C::kStages) * C::kABytes);
+            const uint32_t b_addr = smem_u32(sB + (it % C::kStages) * C::kBBytes);
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+                mma_bf16_f32_pair(d, desc_kmajor_sw128(a_addr + k * kUmmaK * 2), desc_kmajor_sw128(b_addr + k * kUmmaK * 2),
+                                  idesc, (i > 0 || k > 0) ? 1u : 0u);
+            release_stage();
+        }
+        if (*abort_flag) return give_up(b);
+        finish_unit(b);
     }
+    const int32_t nv = idx, n_main = pair_main_count(p);
+    for (int32_t slot = 0; slot < 2 * n_main; ++slot) {
+        int32_t k, phase;
+        pair_main_phase(slot, n_main, &k, &phase);
+        const int32_t t = nv + k, b = t & 1;
+        const uint32_t d = tmem_base + b * kPairBN;
+        if (phase == 0) {
+            if (!claim_accumulator(t)) return give_up(b);
+            for (int32_t i = 0; i < p.num_kb; ++i, ++it) {
+                if (!wait_stage()) return give_up(b);
+                const uint32_t a_addr = smem_u32(sA + (it % C::kStages) * C::kABytes);
+                const uint32_t b_addr = smem_u32(sB + (it % C::kStages) * C::kBBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+                    mma_bf16_f32_pair(d, desc_kmajor_sw128(a_addr + kk * kUmmaK * 2),
+                                      desc_kmajor_sw128(b_addr + kk * kUmmaK * 2), idesc_main, (i > 0 || kk > 0) ? 1u : 0u);
+                release_stage();
+            }
+            continue;
+        }
+        const Unit w = decode_pair_unit(next_pair_unit(p, nv + k), p);
+        grid_dependency_wait();
+        const int32_t ext = pair_ext_steps(p, w.ta);
+        for (int32_t e = 0; e < ext; ++e, ++it) {  // LoRA step: Vt_hi and Vt_lo times the block's B, K = 16 each
+            if (!wait_stage()) return give_up(b);
+            const uint32_t a_addr = smem_u32(sA + (it % C::kStages) * C::kABytes);
+            const uint32_t b_addr = smem_u32(sB + (it % C::kStages) * C::kBBytes);
+            mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr), desc_kmajor_sw32(b_addr), idesc_main, 1u);
+            mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr + kVtBoxBytes), desc_kmajor_sw32(b_addr), idesc_main, 1u);
+            release_stage();
+        }
+        if (*abort_flag) return give_up(b);
+        finish_unit(b);
+    }
+}
+
+// Epilogue of V item v in CTA `rank` (row: this thread's row of the CTA's
+// 128, warp_e: its index among the eight epilogue warps, grp: which half of
+// the 32-column chunks it reads).  Accumulator column 16e + j holds rank-row
+// j of block e of the tile's list (CTA 0's B rows first).  The slices of a
+// CTA's rows count their arrival; all but the last store their fp32 slice
+// (row-major, [256 rows][256 columns] per slice) and count that; the last
+// waits for those stores, adds them to its own slice, still in Tensor
+// Memory, writes the rows' Vt and publishes.  For a fallback tile the
+// slices compute their share of the rows' per-row V first instead.
+__device__ __forceinline__ void run_pair_v_epilogue(const TcParams &p, int32_t v, uint32_t rank, uint32_t col0,
+                                                    int row, int warp_e, int grp, int lane,
+                                                    volatile uint32_t *v_last) {
+    using namespace sm100;
+    const int32_t ta = v / kVSplit, sl = v % kVSplit;
+    const int32_t *plan = p.tile_plan + static_cast<size_t>(ta) * kPlanInts;
+    int32_t *counts = p.plan_rw + static_cast<size_t>(ta) * kPlanInts;
+    const int32_t nb = plan[0];
+    const int32_t m0 = ta * kPairM + static_cast<int32_t>(rank) * kBM;
+    const int32_t m = m0 + row;
+    const int32_t prow = static_cast<int32_t>(rank) * kBM + row;  // row of the 256-row slice
+    const size_t slice_elems = static_cast<size_t>(kPlanRows) * kPlanRows;
+    float *tile_part = p.v_part + static_cast<size_t>(ta) * kVSplit * slice_elems;
+    int32_t kb0, kb1;
+    vslice_kblocks(p, sl, &kb0, &kb1);
+    const bool own_slice = kb1 > kb0;  // this item accumulated something
+    const int32_t h = (nb + 1) >> 1;
+    // the row's slot and scale now, while nothing waits on them
+    int32_t r = 0, slot = -1;
+    float sc = 0.0f;
+    if (nb > 0 && m < p.M)
+        slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &sc, p.status, false);
+    if (nb < 0) {
+        // rows in no useful order: V of each row on CUDA cores, one warp per
+        // row, this slice's share of the CTA's rows
+        const int32_t lo = sl * kBM / kVSplit, hi = (sl + 1) * kBM / kVSplit;
+#pragma unroll 1
+        for (int32_t i = lo + warp_e; i < hi; i += kEpiWarps) {
+            const int32_t mi = m0 + i;
+            if (mi >= p.M) break;
+            int32_t ri = 0;
+            float si = 0.0f;
+            const int32_t slot_i =
+                resolve_slot(p.row_slot[mi], mi, p.ranks, nullptr, p.max_slots, p.bps, &ri, &si, p.status, false);
+            if (slot_i < 0) continue;
+            const int32_t *blocks = p.table + static_cast<size_t>(slot_i) * p.bps;
+            bool blocks_ok = true;
+            for (int32_t jb = 0; jb * LORA_BLOCK_ROWS < ri; ++jb) blocks_ok &= blocks[jb] >= 0 && blocks[jb] < p.num_blocks;
+            if (!blocks_ok) continue;  // reported by the plan kernel; the epilogue drops the row's correction
+            row_v_by_warp(p.x + static_cast<size_t>(mi) * p.ldx, p.K, p.a_arena, blocks, ri,
+                          p.v_rows + static_cast<size_t>(mi) * p.ldv, lane);
+        }
+    }
+    epi_sync();
+    if (threadIdx.x == 64) *v_last = atomicAdd(counts + kPlanPartOff + rank, 1) == kVSplit - 1 ? 1u : 0u;
+    epi_sync();
+    if (!*v_last) {
+        if (nb > 0 && own_slice) {
+            float *dst_row = tile_part + sl * slice_elems + static_cast<size_t>(prow) * kPlanRows;
+#pragma unroll 1
+            for (int32_t c = grp; c < h; c += 2) {
+                float acc[32];
+                load_tmem_chunk(col0 + c * 32, acc);
+                float4 *dst = reinterpret_cast<float4 *>(dst_row + c * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    __stcg(dst + i, make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]));
+            }
+        }
+        __threadfence();
+        epi_sync();
+        if (threadIdx.x == 64) atomicAdd(counts + kPlanStoredOff + rank, 1);
+        return;
+    }
+    // the last slice: the others' partial sums, then Vt
+    if (threadIdx.x == 64) {
+        if (!wait_counter_at_least(counts + kPlanStoredOff + rank, kVSplit - 1, kWaitLimitNs))
+            record_error(p.status, kDevTimeout, 18);
+        __threadfence();
+    }
+    epi_sync();
+    if (nb > 0) {
+        __nv_bfloat16 *vt_row = p.vt_out + static_cast<size_t>(m) * kVtCols;
+#pragma unroll 1
+        for (int32_t c = grp; c < h; c += 2) {  // 32 columns: blocks 2c and 2c + 1
+            float acc[32];
+            if (own_slice) {
+                load_tmem_chunk(col0 + c * 32, acc);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+            }
+            if (m < p.M) {
+#pragma unroll
+                for (int q = 0; q < kVSplit; ++q) {
+                    int32_t q0, q1;
+                    vslice_kblocks(p, q, &q0, &q1);
+                    if (q == sl || q1 <= q0) continue;
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        tile_part + q * slice_elems + static_cast<size_t>(prow) * kPlanRows + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 f = __ldcg(src + i);
+                        acc[4 * i] += f.x;
+                        acc[4 * i + 1] += f.y;
+                        acc[4 * i + 2] += f.z;
+                        acc[4 * i + 3] += f.w;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int32_t e = 2 * c + u;
+                    if (e < nb) store_vt_entry(vt_row, e, acc + 16 * u, slot >= 0 && plan[kPlanSlotOff + e] == slot, sc);
+                }
+            }
+        }
+    }
+    // publish: this CTA's rows are written (the main units read Vt through
+    // TMA loads, V through plain loads)
+    fence_proxy_async_global();
+    __threadfence();
+    epi_sync();
+    if (threadIdx.x == 64) atomicAdd(counts + kPlanReadyOff, 1);
 }
 
 // Epilogue of both CTAs: for each unit, the 256 accumulator columns in four
@@ -978,7 +1268,8 @@ __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uin
 // N are clipped).  Two staging buffers alternate.
 __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUtensorMap *tma_out, uint32_t rank,
                                                   uint8_t *sOut, uint64_t *tmem_full, uint64_t *tmem_empty,
-                                                  uint32_t tmem_base, volatile uint32_t *abort_flag) {
+                                                  uint32_t tmem_base, volatile uint32_t *abort_flag,
+                                                  volatile uint32_t *v_last) {
     using namespace sm100;
     using C = PairCfg;
     const int warp = threadIdx.x >> 5;
@@ -988,12 +1279,11 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
     const int et = threadIdx.x - 64;
     const int row = q * 32 + lane;    // row of this CTA's 128
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    grid_dependency_wait();  // the plan and the fallback V come from the kernels before
+    grid_dependency_wait();  // the plan comes from the kernel before
     int32_t t = 0, chunk_no = 0;
     for (int32_t idx = 0;; ++idx) {
         const int32_t u = next_pair_unit(p, idx);
         if (u < 0) break;
-        const Unit w = decode_pair_unit(u, p);
         const int b = t & 1;
         bool ok = mbar_wait_bounded(&tmem_full[b], (t >> 1) & 1, kWaitLimitNs);
         if (!ok) {
@@ -1003,9 +1293,28 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
         if (!epi_all(ok && !*abort_flag)) break;  // uniform over the epilogue warps
         tc_fence_after_sync();
         const uint32_t col0 = lane_addr + b * kPairBN;
+        if (u >= p.num_units) {
+            run_pair_v_epilogue(p, u - p.num_units, rank, col0, row, warp - 2, grp, lane, v_last);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+            ++t;
+            continue;
+        }
+        const Unit w = decode_pair_unit(u, p);
         const int32_t m0 = w.ta * kPairM + static_cast<int32_t>(rank) * kBM;
         const int32_t m = m0 + row;
         const bool per_row = !p.lora_tiles || p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts] < 0;
+        if (per_row && p.v_units > 0) {
+            // the rows' V comes from the tile's V unit
+            const bool ready = wait_counter_at_least(p.tile_plan + static_cast<size_t>(w.ta) * kPlanInts + kPlanReadyOff,
+                                                     2, kWaitLimitNs);
+            if (!ready) {
+                record_error(p.status, kDevTimeout, 17);
+                *abort_flag = 1;
+            }
+            if (!epi_all(ready && !*abort_flag)) break;
+        }
         int32_t r = 0, slot = -1;
         float s = 0.0f;
         if (per_row && m < p.M)
@@ -1050,7 +1359,8 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ CUtensorMap tma_w,
                     const __grid_constant__ CUtensorMap tma_vt, const __grid_constant__ CUtensorMap tma_bb,
-                    const __grid_constant__ CUtensorMap tma_out, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tma_pa, const __grid_constant__ CUtensorMap tma_out,
+                    const TcParams p) {
     using namespace sm100;
     using C = PairCfg;
     extern __shared__ uint8_t smem_raw[];
@@ -1065,6 +1375,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_cons
     uint64_t *tmem_empty = tmem_full + 2;      // [2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
+    volatile uint32_t *v_last = tmem_slot + 2;  // a V item's epilogue: this slice was the last
     const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1087,6 +1398,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_cons
         if (p.lora_tiles) {
             prefetch_tensormap(&tma_vt);
             prefetch_tensormap(&tma_bb);
+            prefetch_tensormap(&tma_pa);
         }
     }
     if (warp == 1) {
@@ -1101,11 +1413,12 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_cons
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) run_pair_producer(&tma_x, &tma_w, &tma_vt, &tma_bb, p, rank, sA, sB, full, empty, abort_flag);
+        if (lane == 0)
+            run_pair_producer(&tma_x, &tma_w, &tma_vt, &tma_bb, &tma_pa, p, rank, sA, sB, full, empty, abort_flag);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) run_pair_mma(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
     } else {
-        run_pair_epilogue(p, &tma_out, rank, sOut, tmem_full, tmem_empty, tmem_base, abort_flag);
+        run_pair_epilogue(p, &tma_out, rank, sOut, tmem_full, tmem_empty, tmem_base, abort_flag, v_last);
     }
 
     // no CTA leaves while the other may still signal its barriers or read its
@@ -1275,15 +1588,17 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
         }
         pairs_cap = max_pairs[dev];
     }
-    if (!v.lora_tiles || !v.vt || !v.tile_plan) return cudaErrorInvalidValue;
-    CUtensorMap tx, tw, tvt, tbb, tout;
+    if (!v.lora_tiles || !v.vt || !v.tile_plan || !v.V || !v.vacc) return cudaErrorInvalidValue;
+    CUtensorMap tx, tw, tvt, tbb, tpa, tout;
     const uint64_t tiles_m = static_cast<uint64_t>((plan.M + kPlanRows - 1) / kPlanRows) * kPlanRows;
     if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, kBM) ||
         !make_tmap_bf16(&tout, v.out, plan.M, v.N, v.ldo, kBM) ||
         !make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, kPairBN / 2) ||
         !make_tmap_bf16(&tvt, v.vt, tiles_m, kVtCols, kVtCols, kBM, LORA_BLOCK_ROWS, 32) ||
         !make_tmap_bf16(&tbb, v.b_arena, static_cast<uint64_t>(v.num_blocks) * v.N, LORA_BLOCK_ROWS, LORA_BLOCK_ROWS,
-                        kPairBN / 2, LORA_BLOCK_ROWS, 32))
+                        kPairBN / 2, LORA_BLOCK_ROWS, 32) ||
+        !make_tmap_bf16(&tpa, v.a_arena, static_cast<uint64_t>(v.num_blocks) * LORA_BLOCK_ROWS, plan.K, plan.K,
+                        LORA_BLOCK_ROWS))
         return cudaErrorInvalidValue;
     TcParams p = {};
     p.M = plan.M;
@@ -1313,7 +1628,16 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.tile_plan = v.tile_plan;
     p.status = plan.status;
     p.tiles_a0 = p.tiles_a;
-    const int pairs = p.num_units < pairs_cap ? p.num_units : pairs_cap;
+    p.v_units = p.tiles_a;
+    p.vt_out = static_cast<__nv_bfloat16 *>(v.vt);
+    p.v_rows = v.V;
+    p.v_part = v.vacc;
+    p.plan_rw = v.tile_plan;
+    p.x = static_cast<const __nv_bfloat16 *>(plan.x);
+    p.ldx = plan.ldx;
+    p.a_arena = static_cast<const __nv_bfloat16 *>(v.a_arena);
+    const int total_units = p.num_units + p.v_units * kVSplit;
+    const int pairs = total_units < pairs_cap ? total_units : pairs_cap;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(kThreads);
@@ -1324,7 +1648,7 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, tx, tw, tvt, tbb, tout, p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, tx, tw, tvt, tbb, tpa, tout, p);
 }
 
 }  // namespace
@@ -1430,6 +1754,13 @@ cudaError_t launch_gemm_lora_tc_pair(const ForwardPlan &plan, const ProjView &v0
     }
 }
 
+bool pair_gemm_takes(const ProjView &v) { return v.lora_tiles && !v.w_scale && v.N >= kPairBN; }
+
+size_t pair_vpart_bytes(int32_t M) {
+    const size_t T = (static_cast<size_t>(M) + kPairM - 1) / kPairM;
+    return sizeof(float) * T * kVSplit * kPlanRows * kPlanRows;
+}
+
 cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
     if (v.w_scale) return launch_gemm_lora_tc_pair(plan, v, nullptr, nullptr, 0, stream);
     const TcPlan tp = plan_tc(plan.M, v.N, plan.K);
@@ -1442,7 +1773,7 @@ cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cuda
         }
     }
     // large M with at least one full pair tile of columns: the two-SM kernel
-    if (v.lora_tiles && v.N >= kPairBN) return launch_pair_gemm(plan, v, stream);
+    if (pair_gemm_takes(v)) return launch_pair_gemm(plan, v, stream);
     if (tp.bn == 128) return launch_variant<false, 128>(plan, v, tp, stream);
     return launch_variant<false, 256>(plan, v, tp, stream);
 }

@@ -6,8 +6,11 @@ of the workload: the LoRA kernels, then the tensor-core base GEMM that adds
 the LoRA term before rounding.  For M <= 512 (the GEMM's swapped
 orientation) the LoRA kernels write the whole correction s_i B_i A_i x as an
 fp32 [M][N] array (per-row kernel, or the adapter-grouped shrink and
-expand); for larger M the per-row shrink writes V and the GEMM's epilogue
-applies the expand.  Prints ONE JSON line per workload (default: the
+expand).  For larger M a plan kernel lists each 256-token tile's pool
+blocks; then the two-SM GEMM computes V itself (tensor-core V items over
+the same x) and adds the expand as extra MMAs from the pool's B blocks, or,
+with fewer than 256 output columns, a tensor-core shrink and a convert
+kernel compute V before the one-SM GEMM.  Prints ONE JSON line per workload (default: the
 prefill SGMV workload, 8192 tokens of a 4096->4096 projection in 16 sorted
 segments over adapters of ranks {8, 16, 32, 64}: the largest workload, and
 the one whose base GEMM is bound by the tensor cores).
@@ -186,8 +189,12 @@ def algorithmic(wl, w_bits=0):
     distinct adapters and produce the correction the GEMM adds):
         sum_distinct r (K + N) eb + M_a (K + 2N) eb + 2 M_a r 4
     (adapters once each, the adapted rows of x read and of y read and
-    written, the rank-r intermediate written and read).  Large M (the shrink
-    is its own kernel, the expand runs inside the GEMM): the shrink's share,
+    written, the rank-r intermediate written and read).  Large M with the
+    two-SM GEMM ("pair": shrink and expand inside the GEMM, only the tile
+    plans before it): the GEMM's bytes are the base bytes plus the fused
+    form below, its flops 2MNK plus the LoRA flops; the plan kernel's bytes
+    are the row ids and the plans.  Large M otherwise ("rows": the shrink is
+    its own kernel, the expand runs inside the GEMM): the shrink's share,
         sum_distinct r K eb + M_a K eb + M_a r 4,
     and the GEMM's share, sum_distinct r N eb + M_a r 4, beside the base
     bytes.  The fused form of the LoRA bytes (x and y shared with the base
@@ -203,40 +210,50 @@ def algorithmic(wl, w_bits=0):
     wb = {8: 1, 4: 0.5}.get(w_bits, eb)  # bytes per base weight
     M, K = wl.M, wl.K
     swapped = wl.dtype == "bf16" and M <= SWAPPED_MAX_M
+    pair = wl.dtype == "bf16" and not swapped and not w_bits and all(p.N >= PAIR_BN for p in wl.projections)
     out = {"gemm_bytes": 0, "gemm_flops": 0, "lora_bytes": 0, "lora_flops": 0, "lora_bytes_fused": 0,
-           "intermediate_bytes": 0, "per_proj": [], "orientation": "swapped" if swapped else "rows"}
+           "intermediate_bytes": 0, "per_proj": [],
+           "orientation": "swapped" if swapped else "pair" if pair else "rows"}
     Ma, rd, rr = st["adapted_rows"], st["sum_r_distinct"], st["sum_r_rows"]
     for p in wl.projections:
         N = p.N
         base = int(N * K * wb) + (N * 4 if w_bits else 0) + (M * K + M * N) * eb
         fused = rd * (K + N) * eb + 2 * rr * 4
+        gf, lf = 2 * M * N * K, 2 * rr * (K + N)
         if swapped:
             gb, lb = base, rd * (K + N) * eb + Ma * (K + 2 * N) * eb + 2 * rr * 4
             inter = 2 * M * N * 4  # the fp32 correction array
+        elif pair:
+            gb, lb = base + fused, 4 * M + 48 * 4 * (-(-M // PLAN_ROWS))
+            gf, lf = gf + lf, 0
+            inter = large_m_intermediates(wl, N, pair=True)
         else:
             gb = base + rd * N * eb + rr * 4
             lb = rd * K * eb + Ma * K * eb + rr * 4
             inter = large_m_intermediates(wl, N)
         out["gemm_bytes"] += gb
-        out["gemm_flops"] += 2 * M * N * K
+        out["gemm_flops"] += gf
         out["lora_bytes"] += lb
         out["lora_bytes_fused"] += fused
-        out["lora_flops"] += 2 * rr * (K + N)
+        out["lora_flops"] += lf
         out["intermediate_bytes"] += inter
-        out["per_proj"].append({"N": N, "gemm_bytes": gb, "gemm_flops": 2 * M * N * K, "lora_bytes": lb})
+        out["per_proj"].append({"N": N, "gemm_bytes": gb, "gemm_flops": gf, "lora_bytes": lb})
     out.update(st)
     return out
 
 
 PLAN_ROWS = 256  # tokens per plan tile of the library's large-M LoRA path
 PAIR_BN = 256    # output columns per tile of its two-SM GEMM
+V_SLICES = 2     # K-slices of a tile's V in the two-SM GEMM
 
 
-def large_m_intermediates(wl, N):
+def large_m_intermediates(wl, N, pair=False):
     """Bytes of the large-M path's own intermediates for one projection: per
-    256-token tile, the fp32 V accumulator of the pool blocks its rows use
-    (written by reductions and read once) and Vt, its bf16 hi and lo parts
-    (written once, read by every one of the GEMM's column tiles)."""
+    256-token tile, the fp32 V of the pool blocks its rows use -- with the
+    two-SM GEMM, all K-slices but one written and read once; otherwise an
+    accumulator written by reductions and read once -- and Vt, its bf16 hi
+    and lo parts (written once, read by every one of the GEMM's column
+    tiles)."""
     ids = wl.row_adapter
     blocks = 0
     for t0 in range(0, wl.M, PLAN_ROWS):
@@ -244,7 +261,8 @@ def large_m_intermediates(wl, N):
         blocks += sum(-(-int(wl.ranks[s]) // 16) for s in used if s >= 0)
     cols = 16 * blocks  # accumulator columns over all tiles
     col_tiles = -(-N // PAIR_BN)
-    return cols * PLAN_ROWS * 4 * 2 + cols * PLAN_ROWS * 2 * 2 * (1 + col_tiles)
+    fp32 = cols * PLAN_ROWS * 4 * 2 * ((V_SLICES - 1) if pair else 1)
+    return fp32 + cols * PLAN_ROWS * 2 * 2 * (1 + col_tiles)
 
 
 def percentiles(values):
@@ -715,7 +733,8 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     gemm_dominant = gemm_ms >= shrink_ms
     if gemm_dominant:
         b, f, t = alg["gemm_bytes"], alg["gemm_flops"], gemm_avg_s
-        kernel = "tc_gemm_lora_kernel"
+        kernel = "tc_gemm_pair_kernel (V items and LoRA steps inside)" if alg["orientation"] == "pair" \
+            else "tc_gemm_lora_kernel"
     else:
         b, f, t = alg["lora_bytes"], alg["lora_flops"], lora_avg_s
         kernel = ("lora_rows_kernel, or pipe_shrink_kernel + pipe_expand_kernel (max_rank <= 128), or "

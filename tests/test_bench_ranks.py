@@ -118,16 +118,31 @@ def test_algorithmic_bytes_follow_the_method():
     assert a["lora_bytes_fused"] == distinct * 16 * (K + N) * 2 + 2 * Ma * 16 * 4
     assert a["intermediate_bytes"] == 2 * M * N * 4
     assert a["lora_flops"] == 2 * Ma * 16 * (K + N)
-    # large M: the shrink reads the distinct A's and the adapted rows of x and
-    # writes V; the GEMM's share adds the distinct B's and reads V
+    # large M with the two-SM GEMM (N >= 256): the whole LoRA term is inside
+    # the GEMM, whose bytes are the base bytes plus the distinct adapters'
+    # A and B and V written and read (x and y shared with the base), and
+    # whose flops add 2 r (K + N) per adapted row; before it only the tile
+    # plans are made (the row ids read, 48 ints per 256-token tile written)
     wl = make_config("prefill_sgmv")
     a = bench.algorithmic(wl)
     M = 8192
     rd = int(sum(int(wl.ranks[s]) for s in np.unique(wl.row_adapter)))
     rr = int(wl.ranks[wl.row_adapter].sum())
+    assert a["orientation"] == "pair"
+    assert a["gemm_bytes"] == (N * K + M * K + M * N) * 2 + rd * (K + N) * 2 + 2 * rr * 4
+    assert a["gemm_flops"] == 2 * M * N * K + 2 * rr * (K + N)
+    assert a["lora_bytes"] == 4 * M + 48 * 4 * (M // 256) and a["lora_flops"] == 0
+    # large M with fewer than 256 output columns: the shrink reads the
+    # distinct A's and the adapted rows of x and writes V; the GEMM's share
+    # adds the distinct B's and reads V
+    import copy
+    wl2 = copy.deepcopy(wl)
+    wl2.projections[0].N = 136
+    a = bench.algorithmic(wl2)
+    assert a["orientation"] == "rows"
     assert a["lora_bytes"] == rd * K * 2 + M * K * 2 + rr * 4
-    assert a["gemm_bytes"] == (N * K + M * K + M * N) * 2 + rd * N * 2 + rr * 4
-    assert a["gemm_flops"] == 2 * M * N * K
+    assert a["gemm_bytes"] == (136 * K + M * K + M * 136) * 2 + rd * 136 * 2 + rr * 4
+    assert a["gemm_flops"] == 2 * M * 136 * K
 
 
 def test_percentiles():
