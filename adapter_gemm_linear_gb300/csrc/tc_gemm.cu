@@ -1139,12 +1139,13 @@ __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uin
 // Epilogue of V item v in CTA `rank` (row: this thread's row of the CTA's
 // 128, warp_e: its index among the eight epilogue warps, grp: which half of
 // the 32-column chunks it reads).  Accumulator column 16e + j holds rank-row
-// j of block e of the tile's list (CTA 0's B rows first).  The slices of a
-// CTA's rows count their arrival; all but the last store their fp32 slice
-// (row-major, [256 rows][256 columns] per slice) and count that; the last
-// waits for those stores, adds them to its own slice, still in Tensor
-// Memory, writes the rows' Vt and publishes.  For a fallback tile the
-// slices compute their share of the rows' per-row V first instead.
+// j of block e of the tile's list (CTA 0's B rows first).  Every slice of a
+// CTA's rows stores its fp32 sums (row-major, [256 rows][256 columns] per
+// slice) and then counts itself; the last to count adds the others' sums to
+// its own, still in Tensor Memory, writes the rows' Vt and publishes.  No
+// slice waits for another pair, so a V item never holds its accumulator
+// for longer than its own work.  For a fallback tile the slices compute
+// their share of the rows' per-row V instead.
 __device__ __forceinline__ void run_pair_v_epilogue(const TcParams &p, int32_t v, uint32_t rank, uint32_t col0,
                                                     int row, int warp_e, int grp, int lane,
                                                     volatile uint32_t *v_last) {
@@ -1188,34 +1189,29 @@ __device__ __forceinline__ void run_pair_v_epilogue(const TcParams &p, int32_t v
                           p.v_rows + static_cast<size_t>(mi) * p.ldv, lane);
         }
     }
-    epi_sync();
-    if (threadIdx.x == 64) *v_last = atomicAdd(counts + kPlanPartOff + rank, 1) == kVSplit - 1 ? 1u : 0u;
-    epi_sync();
-    if (!*v_last) {
-        if (nb > 0 && own_slice) {
-            float *dst_row = tile_part + sl * slice_elems + static_cast<size_t>(prow) * kPlanRows;
+    if (nb > 0 && own_slice) {
+        float *dst_row = tile_part + sl * slice_elems + static_cast<size_t>(prow) * kPlanRows;
 #pragma unroll 1
-            for (int32_t c = grp; c < h; c += 2) {
-                float acc[32];
-                load_tmem_chunk(col0 + c * 32, acc);
-                float4 *dst = reinterpret_cast<float4 *>(dst_row + c * 32);
+        for (int32_t c = grp; c < h; c += 2) {
+            float acc[32];
+            load_tmem_chunk(col0 + c * 32, acc);
+            float4 *dst = reinterpret_cast<float4 *>(dst_row + c * 32);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    __stcg(dst + i, make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]));
-            }
+            for (int i = 0; i < 8; ++i)
+                __stcg(dst + i, make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]));
         }
-        __threadfence();
-        epi_sync();
-        if (threadIdx.x == 64) atomicAdd(counts + kPlanStoredOff + rank, 1);
-        return;
     }
-    // the last slice: the others' partial sums, then Vt
+    // count this slice (every writer fences, one thread counts); the last
+    // one goes on after an acquiring fence
+    __threadfence();
+    epi_sync();
     if (threadIdx.x == 64) {
-        if (!wait_counter_at_least(counts + kPlanStoredOff + rank, kVSplit - 1, kWaitLimitNs))
-            record_error(p.status, kDevTimeout, 18);
+        const bool last = atomicAdd(counts + kPlanPartOff + rank, 1) == kVSplit - 1;
         __threadfence();
+        *v_last = last ? 1u : 0u;
     }
     epi_sync();
+    if (!*v_last) return;
     if (nb > 0) {
         __nv_bfloat16 *vt_row = p.vt_out + static_cast<size_t>(m) * kVtCols;
 #pragma unroll 1
