@@ -91,13 +91,16 @@ struct ProjView {
 // kPlanMaxBlocks, rows take the CUDA-core fallback), [kPlanReadyOff] = how
 // many CTAs of the two-SM GEMM have written the tile's Vt (or fallback V),
 // [kPlanPartOff + r] = how many K-slices of the tile's V the GEMM's CTAs of
-// rank r have stored (all three zeroed by the plan kernel),
+// rank r have stored, and in tile 0's record [kPlanQueueOff] = the main
+// units the two-SM GEMM has handed out past its first round (all zeroed by
+// the plan kernel),
 // [kPlanBlkOff + e] = block id and [kPlanSlotOff + e] = slot of entry e.
 constexpr int kPlanRows = 256;
 constexpr int kPlanMaxBlocks = 16;
 constexpr int kPlanInts = 48;
 constexpr int kPlanReadyOff = 1;
 constexpr int kPlanPartOff = 2;  // two entries, one per CTA rank of a pair
+constexpr int kPlanQueueOff = 4;
 constexpr int kPlanBlkOff = 16;
 constexpr int kPlanSlotOff = 32;
 constexpr int kVtCols = 2 * LORA_BLOCK_ROWS * kPlanMaxBlocks;  // hi parts, then lo parts

@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(256) tile_plan_kernel(const TilePlanParams p) 
             plan[kPlanReadyOff] = 0;
             plan[kPlanPartOff] = 0;
             plan[kPlanPartOff + 1] = 0;
+            plan[kPlanQueueOff] = 0;
             s_nb = overflow ? -1 : nb;
         }
     }

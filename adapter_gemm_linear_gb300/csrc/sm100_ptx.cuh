@@ -84,6 +84,31 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// The same wait with cluster-scope acquire: for data that a thread of the
+// other CTA of the pair wrote before a release.cluster arrive.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Wait until the int at `ptr` (global memory, written by other CTAs with
 // atomics) is at least `target`, giving up after `limit_ns`.
 __device__ __forceinline__ bool wait_counter_at_least(const int32_t *ptr, int32_t target, uint64_t limit_ns) {
@@ -310,6 +335,11 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t 
                      reinterpret_cast<uint64_t>(map)),
                  "r"(c0), "r"(c1)
                  : "memory");
+}
+
+// Store a 32-bit value to shared memory of either CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // Arrive on an mbarrier of either CTA of the pair without ordering any of

@@ -129,6 +129,7 @@ struct TcParams {
     __nv_bfloat16 *vt_out;
     float *v_rows;
     float *v_part;  // fp32 [v_units][kVSplit][256 rows][256 columns]: the K-slices of V
+    int32_t *queue;  // main units handed out past the first round (zero on entry)
     int32_t *plan_rw;
     const __nv_bfloat16 *x;
     int32_t ldx;
@@ -854,6 +855,8 @@ constexpr int kPairBN = 256;      // output columns per pair tile (the MMA's N)
 constexpr int kPairBand = 4;      // unit order: pair tiles per band (as kTaBand for one SM)
 constexpr uint32_t kBlockBoxBytes = LORA_BLOCK_ROWS * kBK * 2;  // one pool block's 16 A rows of a k-block
 constexpr int kVSplit = 2;        // K-slices of a token tile's V (V items per tile)
+constexpr int kUnitRing = 4;      // main-unit ids in flight from the even CTA's producer to the other roles
+constexpr int kUnitReaders = 2 + 2 * kEpiWarps;  // MMA warp, the odd CTA's producer, both CTAs' epilogue warps
 static_assert(kPairM == kPlanRows, "a pair tile is a plan tile");
 
 struct PairCfg {
@@ -861,12 +864,13 @@ struct PairCfg {
     static constexpr uint32_t kBBytes = (kPairBN / 2) * kBK * 2;    // this CTA's half of the W tile
     static constexpr uint32_t kOutBytes = kBM * kBK * 2;            // an output staging buffer: 128 rows x 64 columns
     static constexpr int kOutBufs = 2;
-    static constexpr int kFixed = 1024 + kOutBufs * static_cast<int>(kOutBytes) + (2 * 12 + 4) * 8 + 16;
+    static constexpr int kBarBytes = (2 * 12 + 4 + 2 * kUnitRing) * 8 + 16 + 4 * kUnitRing;
+    static constexpr int kFixed = 1024 + kOutBufs * static_cast<int>(kOutBytes) + kBarBytes;
     static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes);
     static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
     static constexpr uint32_t kTmemCols = 2 * kPairBN;              // two accumulators
     static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) +
-                                    kOutBufs * kOutBytes + (2 * kStages + 4) * 8 + 16;
+                                    kOutBufs * kOutBytes + (2 * kStages + 4 + 2 * kUnitRing) * 8 + 16 + 4 * kUnitRing;
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kTmemCols <= 512, "two accumulators in Tensor Memory");
     static_assert(kABytes >= 2 * kVtBoxBytes, "a LoRA step's Vt boxes fit the A area");
@@ -890,31 +894,89 @@ __device__ __forceinline__ Unit decode_pair_unit(int32_t u, const TcParams &p) {
     return w;
 }
 
-// Unit idx of this pair, or -1.  Codes: u < num_units is a main unit (every
-// G-th for G pairs, in the band order of decode_pair_unit), num_units + v the
-// V item v (token tile v / kVSplit, K-slice v % kVSplit).  A pair takes its V
-// items first.  V items are dealt in order of v: first up to kVSplit to each
-// pair with one main unit fewer (pairs [G - light, G), the last pair first;
-// every pair when G divides num_units), then one at a time to all pairs from
-// the first on.
-__device__ __forceinline__ int32_t next_pair_unit(const TcParams &p, int32_t idx) {
+// V item idx of this pair (token tile v / kVSplit, K-slice v % kVSplit), or
+// -1 after its last.  A pair takes its V items before its main units; they
+// are dealt one at a time from the last pair down (the main units, handed
+// out on demand, even out the rest).
+__device__ __forceinline__ int32_t pair_v_item(const TcParams &p, int32_t idx) {
     const int32_t G = static_cast<int32_t>(gridDim.x >> 1), P = static_cast<int32_t>(blockIdx.x >> 1);
-    const int32_t NV = p.v_units * kVSplit;
-    int32_t nv = 0;
-    if (NV > 0) {
-        const int32_t rem = p.num_units % G;
-        const int32_t light = rem == 0 ? G : G - rem;
-        const int32_t n1 = min(NV, light * kVSplit);
-        const int32_t j = G - 1 - P;  // this pair's place among the light ones
-        const int32_t c1 = (j < light && j < n1) ? (n1 - j + light - 1) / light : 0;
-        if (idx < c1) return p.num_units + j + idx * light;
-        const int32_t n2 = NV - n1;
-        const int32_t c2 = P < n2 ? (n2 - P + G - 1) / G : 0;
-        if (idx < c1 + c2) return p.num_units + n1 + P + (idx - c1) * G;
-        nv = c1 + c2;
-    }
-    const int32_t u = P + (idx - nv) * G;
+    const int32_t v = (G - 1 - P) + idx * G;
+    return v < p.v_units * kVSplit ? v : -1;
+}
+
+// The main units of a pair: unit k of its sequence is P for k = 0 (every
+// pair's first, fixed), then units G, G + 1, ... in band order, handed out
+// one at a time from the queue counter to whichever pair asks first, so that
+// a pair slowed by its V items takes fewer; -1 ends the sequence.  The even
+// CTA's producer fetches them and passes them to the other roles of both
+// CTAs through a ring of kUnitRing ids in shared memory.
+__device__ __forceinline__ int32_t fetch_main_unit(const TcParams &p, int32_t k) {
+    const int32_t G = static_cast<int32_t>(gridDim.x >> 1), P = static_cast<int32_t>(blockIdx.x >> 1);
+    if (k == 0) return P < p.num_units ? P : -1;
+    grid_dependency_wait();  // the counter is zeroed by the kernel before
+    const int32_t u = G + atomicAdd(p.queue, 1);
     return u < p.num_units ? u : -1;
+}
+
+struct UnitRing {
+    volatile int32_t *ids;  // [kUnitRing]
+    uint64_t *full;         // [kUnitRing]: an id is there (count 1)
+    uint64_t *empty;        // [kUnitRing], the even CTA's: every reader has it (count kUnitReaders)
+};
+
+// The even CTA's producer: put main unit k's id into both CTAs' rings.
+__device__ __forceinline__ bool ring_publish(const TcParams &p, const UnitRing &r, int32_t k, int32_t u) {
+    using namespace sm100;
+    const int slot = k % kUnitRing;
+    if (!mbar_wait_cluster_bounded(&r.empty[slot], ((k / kUnitRing) & 1) ^ 1, kWaitLimitNs)) {
+        record_error(p.status, kDevTimeout, 19);
+        return false;
+    }
+    r.ids[slot] = u;
+    st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int32_t *>(&r.ids[slot])), 1), static_cast<uint32_t>(u));
+    mbar_arrive_cluster(mapa_shared(smem_u32(&r.full[slot]), 0));
+    mbar_arrive_cluster(mapa_shared(smem_u32(&r.full[slot]), 1));
+    return true;
+}
+
+// Every other role: main unit k's id (-1 at the end, or when the wait gives
+// up).  Each reading warp then tells the even CTA's producer once
+// (ring_done), after all of its threads have read it.
+__device__ __forceinline__ int32_t ring_read(const TcParams &p, const UnitRing &r, int32_t k) {
+    using namespace sm100;
+    const int slot = k % kUnitRing;
+    if (!mbar_wait_cluster_bounded(&r.full[slot], (k / kUnitRing) & 1, kWaitLimitNs)) {
+        record_error(p.status, kDevTimeout, 20);
+        return -1;
+    }
+    return r.ids[slot];
+}
+
+__device__ __forceinline__ void ring_done(const UnitRing &r, int32_t k) {
+    using namespace sm100;
+    mbar_arrive_cluster(mapa_shared(smem_u32(&r.empty[k % kUnitRing]), 0));
+}
+
+// The phases (0: main k-blocks, 1: LoRA steps) of main units k = 0, 1, ... in
+// the order every role takes them: both phase-0s of the first two units
+// before their phase-1s (the LoRA steps, which wait for the tiles' V, start
+// one unit later; the two accumulators hold both units meanwhile), then each
+// unit's two phases in turn.  get(k) gives unit k's id (-1: none), phase(u, k,
+// ph) runs a phase and returns false when the pair gives up.
+template <typename Get, typename Phase>
+__device__ __forceinline__ void for_each_main_phase(Get &&get, Phase &&phase) {
+    const int32_t u0 = get(0);
+    if (u0 < 0 || !phase(u0, 0, 0)) return;
+    const int32_t u1 = get(1);
+    if (u1 < 0) {
+        phase(u0, 0, 1);
+        return;
+    }
+    if (!phase(u1, 1, 0) || !phase(u0, 0, 1) || !phase(u1, 1, 1)) return;
+    for (int32_t k = 2;; ++k) {
+        const int32_t u = get(k);
+        if (u < 0 || !phase(u, k, 0) || !phase(u, k, 1)) return;
+    }
 }
 
 // K-slice s of a V item: k-blocks [kb0, kb1) (empty when num_kb < kVSplit).
@@ -928,32 +990,11 @@ __device__ __forceinline__ int32_t pair_ext_steps(const TcParams &p, int32_t ta)
     return nb > 0 ? nb : 0;
 }
 
-// Main units of this pair (they follow its V items in next_pair_unit).
-__device__ __forceinline__ int32_t pair_main_count(const TcParams &p) {
-    const int32_t G = static_cast<int32_t>(gridDim.x >> 1), P = static_cast<int32_t>(blockIdx.x >> 1);
-    return P < p.num_units ? (p.num_units - P + G - 1) / G : 0;
-}
-
-// The order of the two phases (0: the main k-blocks, 1: the LoRA steps) of
-// this pair's main units: slot -> (main unit k, phase).  The first two
-// units' main k-blocks both come before their LoRA steps, so that those,
-// which wait for the tiles' V, start one unit later (the two accumulators
-// hold both units meanwhile); then each unit's phases follow one another.
-__device__ __forceinline__ void pair_main_phase(int32_t slot, int32_t n_main, int32_t *k, int32_t *phase) {
-    if (n_main >= 2 && slot < 4) {
-        *k = slot & 1;
-        *phase = slot >> 1;
-    } else {
-        *k = slot >> 1;
-        *phase = slot & 1;
-    }
-}
-
 __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, const CUtensorMap *tma_w,
                                                   const CUtensorMap *tma_vt, const CUtensorMap *tma_bb,
                                                   const CUtensorMap *tma_pa, const TcParams &p, uint32_t rank,
                                                   uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
-                                                  volatile uint32_t *abort_flag) {
+                                                  const UnitRing &ring, volatile uint32_t *abort_flag) {
     using namespace sm100;
     using C = PairCfg;
     int32_t it = 0, idx = 0;
@@ -971,11 +1012,11 @@ __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, cons
         return true;
     };
     for (;; ++idx) {  // V items: x and this CTA's half of the tile's block list, one K-slice
-        const int32_t u = next_pair_unit(p, idx);
-        if (u < p.num_units) break;  // the main units (or the end) follow
-        const int32_t ta = (u - p.num_units) / kVSplit;
+        const int32_t v = pair_v_item(p, idx);
+        if (v < 0) break;
+        const int32_t ta = v / kVSplit;
         int32_t kb0, kb1;
-        vslice_kblocks(p, (u - p.num_units) % kVSplit, &kb0, &kb1);
+        vslice_kblocks(p, v % kVSplit, &kb0, &kb1);
         grid_dependency_wait();  // the plan comes from the kernel before
         const int32_t *plan = p.tile_plan + static_cast<size_t>(ta) * kPlanInts;
         const int32_t nb = plan[0];
@@ -994,37 +1035,43 @@ __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, cons
                                  plan[kPlanBlkOff + e] * LORA_BLOCK_ROWS, fb);
         }
     }
-    const int32_t nv = idx, n_main = pair_main_count(p);
-    for (int32_t slot = 0; slot < 2 * n_main; ++slot) {
-        int32_t k, phase;
-        pair_main_phase(slot, n_main, &k, &phase);
-        const Unit w = decode_pair_unit(next_pair_unit(p, nv + k), p);
+    auto get = [&](int32_t k) -> int32_t {
+        if (rank == 1) {
+            const int32_t u = ring_read(p, ring, k);
+            ring_done(ring, k);
+            return u;
+        }
+        const int32_t u = fetch_main_unit(p, k);
+        return ring_publish(p, ring, k, u) ? u : -1;
+    };
+    auto phase = [&](int32_t u, int32_t, int32_t ph) -> bool {
+        const Unit w = decode_pair_unit(u, p);
         const int32_t row = w.ta * kPairM + static_cast<int32_t>(rank) * kBM;
         const int32_t n0 = w.tb * kPairBN + static_cast<int32_t>(rank) * (kPairBN / 2);  // this CTA's W rows
-        if (phase == 0) {
+        if (ph == 0) {
             for (int32_t i = 0; i < p.num_kb; ++i, ++it) {
-                if (!acquire_stage(11)) return;
+                if (!acquire_stage(11)) return false;
                 const int s = it % C::kStages;
                 const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
                 if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (C::kABytes + C::kBBytes));
                 tma_load_2d_pair(sA + s * C::kABytes, tma_x, i * kBK, row, fb);
                 tma_load_2d_pair(sB + s * C::kBBytes, tma_w, i * kBK, n0, fb);
             }
-            continue;
+            return true;
         }
         grid_dependency_wait();  // the plan comes from the kernel before
         const int32_t ext = pair_ext_steps(p, w.ta);
-        if (ext == 0) continue;
+        if (ext == 0) return true;
         // the tile's Vt comes from its V items (both CTAs of some pair)
         if (!wait_counter_at_least(p.tile_plan + static_cast<size_t>(w.ta) * kPlanInts + kPlanReadyOff, 2,
                                    kWaitLimitNs)) {
             record_error(p.status, kDevTimeout, 16);
             *abort_flag = 1;
-            return;
+            return false;
         }
         fence_proxy_async_global();  // the TMA loads below read what generic stores wrote
         for (int32_t e = 0; e < ext; ++e, ++it) {
-            if (!acquire_stage(11)) return;
+            if (!acquire_stage(11)) return false;
             const int s = it % C::kStages;
             const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
             const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e];
@@ -1033,16 +1080,20 @@ __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, cons
             tma_load_2d_pair(sA + s * C::kABytes + kVtBoxBytes, tma_vt, kVtCols / 2 + e * LORA_BLOCK_ROWS, row, fb);
             tma_load_2d_pair(sB + s * C::kBBytes, tma_bb, 0, blk * p.N + n0, fb);
         }
-    }
+        return true;
+    };
+    for_each_main_phase(get, phase);
 }
 
 // The even CTA's MMA issuer: the V items, then the phases of the main units
-// in the order of pair_main_phase (the same stage order as the producers').
+// in the order of for_each_main_phase (the same stage order as the
+// producers').
 // Unit number t (V items and main units in their sequence order) uses
 // accumulator t & 1.
 __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
                                              uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
-                                             uint32_t tmem_base, volatile uint32_t *abort_flag) {
+                                             const UnitRing &ring, uint32_t tmem_base,
+                                             volatile uint32_t *abort_flag) {
     using namespace sm100;
     using C = PairCfg;
     constexpr uint32_t idesc_main = idesc_bf16_f32(kPairM, kPairBN);
@@ -1075,12 +1126,12 @@ __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uin
         mma_commit_pair(mapa_shared(smem_u32(&tmem_full[b]), 1));
     };
     for (;; ++idx) {  // V items: N = 32 ceil(nb / 2), one K-slice, no LoRA steps
-        const int32_t u = next_pair_unit(p, idx);
-        if (u < p.num_units) break;
+        const int32_t v = pair_v_item(p, idx);
+        if (v < 0) break;
         const int32_t t = idx, b = t & 1;
-        const int32_t ta = (u - p.num_units) / kVSplit;
+        const int32_t ta = v / kVSplit;
         int32_t kb0, kb1;
-        vslice_kblocks(p, (u - p.num_units) % kVSplit, &kb0, &kb1);
+        vslice_kblocks(p, v % kVSplit, &kb0, &kb1);
         grid_dependency_wait();
         const int32_t nb = p.tile_plan[static_cast<size_t>(ta) * kPlanInts];
         const int32_t total = nb > 0 ? kb1 - kb0 : 0;
@@ -1100,16 +1151,25 @@ __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uin
         if (*abort_flag) return give_up(b);
         finish_unit(b);
     }
-    const int32_t nv = idx, n_main = pair_main_count(p);
-    for (int32_t slot = 0; slot < 2 * n_main; ++slot) {
-        int32_t k, phase;
-        pair_main_phase(slot, n_main, &k, &phase);
+    const int32_t nv = idx;
+    auto get = [&](int32_t k) -> int32_t {
+        const int32_t u = ring_read(p, ring, k);
+        ring_done(ring, k);
+        return u;
+    };
+    auto phase = [&](int32_t u, int32_t k, int32_t ph) -> bool {
         const int32_t t = nv + k, b = t & 1;
         const uint32_t d = tmem_base + b * kPairBN;
-        if (phase == 0) {
-            if (!claim_accumulator(t)) return give_up(b);
+        if (ph == 0) {
+            if (!claim_accumulator(t)) {
+                give_up(b);
+                return false;
+            }
             for (int32_t i = 0; i < p.num_kb; ++i, ++it) {
-                if (!wait_stage()) return give_up(b);
+                if (!wait_stage()) {
+                    give_up(b);
+                    return false;
+                }
                 const uint32_t a_addr = smem_u32(sA + (it % C::kStages) * C::kABytes);
                 const uint32_t b_addr = smem_u32(sB + (it % C::kStages) * C::kBBytes);
 #pragma unroll
@@ -1118,22 +1178,30 @@ __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uin
                                       desc_kmajor_sw128(b_addr + kk * kUmmaK * 2), idesc_main, (i > 0 || kk > 0) ? 1u : 0u);
                 release_stage();
             }
-            continue;
+            return true;
         }
-        const Unit w = decode_pair_unit(next_pair_unit(p, nv + k), p);
+        const Unit w = decode_pair_unit(u, p);
         grid_dependency_wait();
         const int32_t ext = pair_ext_steps(p, w.ta);
         for (int32_t e = 0; e < ext; ++e, ++it) {  // LoRA step: Vt_hi and Vt_lo times the block's B, K = 16 each
-            if (!wait_stage()) return give_up(b);
+            if (!wait_stage()) {
+                give_up(b);
+                return false;
+            }
             const uint32_t a_addr = smem_u32(sA + (it % C::kStages) * C::kABytes);
             const uint32_t b_addr = smem_u32(sB + (it % C::kStages) * C::kBBytes);
             mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr), desc_kmajor_sw32(b_addr), idesc_main, 1u);
             mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr + kVtBoxBytes), desc_kmajor_sw32(b_addr), idesc_main, 1u);
             release_stage();
         }
-        if (*abort_flag) return give_up(b);
+        if (*abort_flag) {
+            give_up(b);
+            return false;
+        }
         finish_unit(b);
-    }
+        return true;
+    };
+    for_each_main_phase(get, phase);
 }
 
 // Epilogue of V item v in CTA `rank` (row: this thread's row of the CTA's
@@ -1264,8 +1332,8 @@ __device__ __forceinline__ void run_pair_v_epilogue(const TcParams &p, int32_t v
 // N are clipped).  Two staging buffers alternate.
 __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUtensorMap *tma_out, uint32_t rank,
                                                   uint8_t *sOut, uint64_t *tmem_full, uint64_t *tmem_empty,
-                                                  uint32_t tmem_base, volatile uint32_t *abort_flag,
-                                                  volatile uint32_t *v_last) {
+                                                  const UnitRing &ring, uint32_t tmem_base,
+                                                  volatile uint32_t *abort_flag, volatile uint32_t *v_last) {
     using namespace sm100;
     using C = PairCfg;
     const int warp = threadIdx.x >> 5;
@@ -1276,9 +1344,18 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
     const int row = q * 32 + lane;    // row of this CTA's 128
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     grid_dependency_wait();  // the plan comes from the kernel before
-    int32_t t = 0, chunk_no = 0;
+    int32_t t = 0, chunk_no = 0, nv = 0;
+    while (pair_v_item(p, nv) >= 0) ++nv;
     for (int32_t idx = 0;; ++idx) {
-        const int32_t u = next_pair_unit(p, idx);
+        // V items first, then the main units from the ring
+        int32_t u;
+        if (idx < nv) {
+            u = p.num_units + pair_v_item(p, idx);
+        } else {
+            u = ring_read(p, ring, idx - nv);
+            __syncwarp();
+            if (lane == 0) ring_done(ring, idx - nv);
+        }
         if (u < 0) break;
         const int b = t & 1;
         bool ok = mbar_wait_bounded(&tmem_full[b], (t >> 1) & 1, kWaitLimitNs);
@@ -1369,9 +1446,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_cons
     uint64_t *empty = full + C::kStages;
     uint64_t *tmem_full = empty + C::kStages;  // [2]
     uint64_t *tmem_empty = tmem_full + 2;      // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 2);
+    UnitRing ring;
+    ring.full = tmem_empty + 2;                // [kUnitRing]
+    ring.empty = ring.full + kUnitRing;        // [kUnitRing]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ring.empty + kUnitRing);
     volatile uint32_t *abort_flag = tmem_slot + 1;
     volatile uint32_t *v_last = tmem_slot + 2;  // a V item's epilogue: this slice was the last
+    ring.ids = reinterpret_cast<volatile int32_t *>(tmem_slot + 4);  // [kUnitRing]
     const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1383,6 +1464,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_cons
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tmem_full[b], 1);
             mbar_init(&tmem_empty[b], 2 * kEpiWarps);  // the epilogue warps of both CTAs
+        }
+        for (int i = 0; i < kUnitRing; ++i) {
+            mbar_init(&ring.full[i], 1);
+            mbar_init(&ring.empty[i], kUnitReaders);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -1410,11 +1495,12 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_cons
 
     if (warp == 0) {
         if (lane == 0)
-            run_pair_producer(&tma_x, &tma_w, &tma_vt, &tma_bb, &tma_pa, p, rank, sA, sB, full, empty, abort_flag);
+            run_pair_producer(&tma_x, &tma_w, &tma_vt, &tma_bb, &tma_pa, p, rank, sA, sB, full, empty, ring, abort_flag);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) run_pair_mma(p, sA, sB, full, empty, tmem_full, tmem_empty, tmem_base, abort_flag);
+        if (lane == 0 && rank == 0)
+            run_pair_mma(p, sA, sB, full, empty, tmem_full, tmem_empty, ring, tmem_base, abort_flag);
     } else {
-        run_pair_epilogue(p, &tma_out, rank, sOut, tmem_full, tmem_empty, tmem_base, abort_flag, v_last);
+        run_pair_epilogue(p, &tma_out, rank, sOut, tmem_full, tmem_empty, ring, tmem_base, abort_flag, v_last);
     }
 
     // no CTA leaves while the other may still signal its barriers or read its
@@ -1628,6 +1714,7 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.vt_out = static_cast<__nv_bfloat16 *>(v.vt);
     p.v_rows = v.V;
     p.v_part = v.vacc;
+    p.queue = v.tile_plan + kPlanQueueOff;
     p.plan_rw = v.tile_plan;
     p.x = static_cast<const __nv_bfloat16 *>(plan.x);
     p.ldx = plan.ldx;
