@@ -878,8 +878,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    from workloads import CONFIG_NAMES
-    names = list(CONFIG_NAMES[1:]) if args.config == "all" else [args.config]
+    from workloads import CONFIG_NAMES, WIDENING_NAMES
+    names = list(CONFIG_NAMES[1:]) + list(WIDENING_NAMES) if args.config == "all" else [args.config]
     if args.impl == "reference":
         if rank != 0:
             return 0

@@ -2,8 +2,9 @@
 oracle on the same seeded inputs.
 
 Small cases span several output tiles with ragged tails in M, N and K; the
-five named workloads run at full size with the oracle evaluated on every row
-(small ones) or on sampled rows (large ones).  Integer-valued cases must be
+five named workloads and the two of other target modules run at full size
+with the oracle evaluated on every row (small ones) or on sampled rows
+(large ones).  Integer-valued cases must be
 bit-exact; mutation cases check that the tolerance is not vacuous.
 """
 
@@ -310,7 +311,32 @@ def test_slora_mixed_sampled():
     assert not np.isnan(out).any()
 
 
-@pytest.mark.parametrize("cfg", ["tiny_fp32", "decode_bgmv", "prefill_sgmv", "decode_70b_qv", "slora_mixed"])
+def test_decode_70b_qkv_sampled():
+    """q, k and v of a 70B layer in one call (k and v 1024 wide, GQA), rank-64
+    adapters on all three."""
+    wl = make_config("decode_70b_qkv")
+    pools = H.make_pools(wl, DEV)
+    outs = H.forward(wl, pools, "bgmv")
+    rows = _sample_rows(wl, n=64)
+    for p in range(3):
+        H.assert_close("bf16", outs[p][rows], H.oracle_rows(wl, p, rows), f"decode_70b_qkv p{p}")
+        assert not np.isnan(outs[p]).any()
+
+
+def test_prefill_down_proj_sampled():
+    """A down projection (K = 13824 > N = 5120) at prefill size: two rows of
+    every 256-token tile, the segment boundaries and a random sample."""
+    wl = make_config("prefill_down_proj")
+    pools = H.make_pools(wl, DEV)
+    out = H.forward(wl, pools, "sorted")[0]
+    rows = _sample_rows(wl, per_tile=2, tile=256)
+    assert len(set(int(r) // 256 for r in rows)) == wl.M // 256
+    H.assert_close("bf16", out[rows], H.oracle_rows(wl, 0, rows), "prefill_down_proj")
+    assert not np.isnan(out).any()
+
+
+@pytest.mark.parametrize("cfg", ["tiny_fp32", "decode_bgmv", "prefill_sgmv", "decode_70b_qv", "slora_mixed",
+                                 "decode_70b_qkv", "prefill_down_proj"])
 def test_mutations_fail_tolerance(cfg):
     """Outputs computed with a wrong assignment or scale must fail the
     tolerance against the true oracle, on every workload and every

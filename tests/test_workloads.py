@@ -86,3 +86,20 @@ def test_synth_integer_and_sgmv():
 def test_config_names():
     assert len(CONFIG_NAMES) == 5
 
+
+def test_widening_workloads():
+    """The other target modules: q, k, v of a 70B layer in one call (GQA: k
+    and v 1024 wide) and a down projection with K > N, reachable by name and
+    by index after the five."""
+    from workloads import WIDENING_NAMES
+    assert WIDENING_NAMES == ("decode_70b_qkv", "prefill_down_proj")
+    q = make_config("decode_70b_qkv")
+    assert [p.N for p in q.projections] == [8192, 1024, 1024] and q.K == 8192 and q.M == 256
+    assert set(q.ranks.tolist()) == {64} and float(q.alphas[0]) == 128.0
+    assert (q.row_adapter == -1).sum() == 13
+    assert make_config(5).row_adapter.tolist() == q.row_adapter.tolist()
+    d = make_config("prefill_down_proj")
+    assert d.K == 13824 and d.projections[0].N == 5120 and d.K > d.projections[0].N
+    assert d.seg_offsets[0] == 0 and d.seg_offsets[-1] == 4096 and d.mode == "sgmv"
+    assert np.array_equal(np.repeat(d.seg_adapter, np.diff(d.seg_offsets)), d.row_adapter)
+

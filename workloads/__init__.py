@@ -10,6 +10,7 @@ another one.
 
 from .configs import (  # noqa: F401
     CONFIG_NAMES,
+    WIDENING_NAMES,
     Projection,
     Workload,
     bf16_round,

@@ -1,5 +1,6 @@
-"""The five synthetic workloads of the multi-adapter LoRA linear layer, plus a
-parametric generator for small parity cases.
+"""The five synthetic workloads of the multi-adapter LoRA linear layer, two
+more for other target modules, and a parametric generator for small parity
+cases.
 
 Shapes and distributions follow the workloads described on the pages (see
 "S-LoRA: what the paper actually says…", §"Batched LoRA computation"; "LoRA
@@ -15,6 +16,18 @@ prefill_sgmv    bf16    x 8192x4096, W 4096x4096, 16 slots rank {8..64}, a=2r
 decode_70b_qv   bf16    x 256x8192, W_q 8192x8192 + W_v 1024x8192, 128 slots
 slora_mixed     bf16    x 512x5120, W 13824x5120, 2048 slots rank {8..128}
 ==============  ======  ======================================================
+
+Other target modules (WIDENING_NAMES; "Your LoRA Adapters Are Thrashing Your
+GPUs", §02 "Which layers to adapt" and "Concrete parameter counts for a 70B
+model"):
+
+=================  ======  ===================================================
+decode_70b_qkv     bf16    x 256x8192, W_q 8192x8192, W_k and W_v 1024x8192
+                           (GQA) in one call, 64 slots rank 64, alpha 128
+prefill_down_proj  bf16    x 4096x13824, W 5120x13824 (K > N: the down
+                           projection of the slora_mixed model's FFN), 16
+                           slots rank {8..64}, SGMV segments
+=================  ======  ===================================================
 
 Value recipe: x ~ N(0, 1); W ~ N(0, variance 1/K); A and B ~ N(0, std 0.02);
 bf16 configurations round every drawn value once, to nearest-even, to bf16,
@@ -36,6 +49,11 @@ CONFIG_NAMES = (
     "prefill_sgmv",
     "decode_70b_qv",
     "slora_mixed",
+)
+
+WIDENING_NAMES = (
+    "decode_70b_qkv",
+    "prefill_down_proj",
 )
 
 _ROOT_SEED = 0
@@ -174,12 +192,13 @@ def _normal(rng, shape, std, dtype):
 
 
 def make_config(name_or_index) -> Workload:
-    """Build one of the five named workloads (deterministic, seed 0)."""
-    if isinstance(name_or_index, int):
-        idx = name_or_index
-    else:
-        idx = CONFIG_NAMES.index(name_or_index)
-    builder = [_tiny_fp32, _decode_bgmv, _prefill_sgmv, _decode_70b_qv, _slora_mixed][idx]
+    """Build one of the named workloads (deterministic, seed 0): the five of
+    CONFIG_NAMES (by name or index 0-4) or one of WIDENING_NAMES (by name, or
+    index 5 on)."""
+    names = CONFIG_NAMES + WIDENING_NAMES
+    idx = name_or_index if isinstance(name_or_index, int) else names.index(name_or_index)
+    builder = [_tiny_fp32, _decode_bgmv, _prefill_sgmv, _decode_70b_qv, _slora_mixed,
+               _decode_70b_qkv, _prefill_down_proj][idx]
     return builder(idx)
 
 
@@ -274,6 +293,51 @@ def _slora_mixed(c: int) -> Workload:
         description="S-LoRA-scale mixed batch: bf16 5120->13824, 2048 slots ranks "
                     "{8..128} alpha 2r, 512 rows over 200 adapters (power law s=1.0), "
                     "26 rows base-only",
+    )
+
+
+def _decode_70b_qkv(c: int) -> Workload:
+    M, K, S = 256, 8192, 64
+    x = _normal(_rng(c, 0), (M, K), 1.0, "bf16")
+    Wq = _normal(_rng(c, 1), (8192, K), 1.0 / np.sqrt(K), "bf16")
+    Wk = _normal(_rng(c, 3), (1024, K), 1.0 / np.sqrt(K), "bf16")
+    Wv = _normal(_rng(c, 4), (1024, K), 1.0 / np.sqrt(K), "bf16")
+    rid = _rng(c, 2)
+    none_rows = rid.choice(M, size=int(round(0.05 * M)), replace=False)
+    slot_of_rank = rid.permutation(S)
+    ids = slot_of_rank[_zipf_rank(rid, S, 1.1, M)].astype(np.int32)
+    ids[none_rows] = -1
+    return Workload(
+        name="decode_70b_qkv", dtype="bf16", M=M, K=K, x=x,
+        projections=[Projection("q_proj", 8192, Wq, (c, 100)),
+                     Projection("k_proj", 1024, Wk, (c, 101)),
+                     Projection("v_proj", 1024, Wv, (c, 102))],
+        num_slots=S, ranks=np.full(S, 64, np.int32), alphas=np.full(S, 128.0, np.float32),
+        row_adapter=ids, mode="bgmv", free_list_seed=0x5EED0 + c,
+        description="70B-shaped decode, rank-64 Q+K+V adapters: bf16 hidden 8192, q 8192->8192, "
+                    "k and v 8192->1024 (GQA) in one call, 256 rows, 64 slots alpha 128, "
+                    "ids Zipf(1.1), 13 rows base-only",
+    )
+
+
+def _prefill_down_proj(c: int) -> Workload:
+    M, K, N, S = 4096, 13824, 5120, 16
+    x = _normal(_rng(c, 0), (M, K), 1.0, "bf16")
+    W = _normal(_rng(c, 1), (N, K), 1.0 / np.sqrt(K), "bf16")
+    rr = _rng(c, 2)
+    ranks = rr.choice(np.array([8, 16, 32, 64]), size=S).astype(np.int32)
+    lengths = _largest_remainder(rr.geometric(1.0 / 256.0, size=S), M)
+    seg_offsets = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    seg_adapter = np.arange(S, dtype=np.int32)
+    ids = np.repeat(seg_adapter, lengths).astype(np.int32)
+    return Workload(
+        name="prefill_down_proj", dtype="bf16", M=M, K=K, x=x,
+        projections=[Projection("down_proj", N, W, (c, 100))],
+        num_slots=S, ranks=ranks, alphas=(2.0 * ranks).astype(np.float32),
+        row_adapter=ids, mode="sgmv", seg_offsets=seg_offsets, seg_adapter=seg_adapter,
+        free_list_seed=0x5EED0 + c,
+        description="prefill SGMV of a down projection (K > N): bf16 13824->5120, 4096 tokens "
+                    "in 16 sorted segments (geometric lengths, mean 256), ranks {8,16,32,64}, alpha 2r",
     )
 
 
