@@ -851,7 +851,8 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
 // every wait ends.
 
 constexpr int kPairM = 2 * kBM;   // tokens per pair tile
-constexpr int kPairBN = 256;      // output columns per pair tile (the MMA's N)
+constexpr int kPairBN = 256;      // output columns per pair tile of the large-M path (the MMA's N)
+constexpr int kPairAcc = 256;     // Tensor Memory columns of one accumulator
 constexpr int kPairBand = 4;      // unit order: pair tiles per band (as kTaBand for one SM)
 constexpr uint32_t kBlockBoxBytes = LORA_BLOCK_ROWS * kBK * 2;  // one pool block's 16 A rows of a k-block
 constexpr int kVSplit = 2;        // K-slices of a token tile's V (V items per tile)
@@ -859,23 +860,27 @@ constexpr int kUnitRing = 4;      // main-unit ids in flight from the even CTA's
 constexpr int kUnitReaders = 2 + 2 * kEpiWarps;  // MMA warp, the odd CTA's producer, both CTAs' epilogue warps
 static_assert(kPairM == kPlanRows, "a pair tile is a plan tile");
 
+template <int BN>
 struct PairCfg {
+    // the V items stack a CTA's half of a tile's block list in the B area,
+    // which takes the 128 W rows of a 256-column tile
+    static_assert(BN == 256, "pair tiles of 256 output columns");
     static constexpr uint32_t kABytes = kBM * kBK * 2;              // this CTA's 128 rows of x
-    static constexpr uint32_t kBBytes = (kPairBN / 2) * kBK * 2;    // this CTA's half of the W tile
+    static constexpr uint32_t kBBytes = (BN / 2) * kBK * 2;         // this CTA's half of the W tile
     static constexpr uint32_t kOutBytes = kBM * kBK * 2;            // an output staging buffer: 128 rows x 64 columns
     static constexpr int kOutBufs = 2;
     static constexpr int kBarBytes = (2 * 12 + 4 + 2 * kUnitRing) * 8 + 16 + 4 * kUnitRing;
     static constexpr int kFixed = 1024 + kOutBufs * static_cast<int>(kOutBytes) + kBarBytes;
     static constexpr int kStages0 = (kSmemLimit - kFixed) / static_cast<int>(kABytes + kBBytes);
     static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
-    static constexpr uint32_t kTmemCols = 2 * kPairBN;              // two accumulators
+    static constexpr uint32_t kTmemCols = 2 * kPairAcc;             // two accumulators (V items use up to 256 columns)
     static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) +
                                     kOutBufs * kOutBytes + (2 * kStages + 4 + 2 * kUnitRing) * 8 + 16 + 4 * kUnitRing;
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kTmemCols <= 512, "two accumulators in Tensor Memory");
     static_assert(kABytes >= 2 * kVtBoxBytes, "a LoRA step's Vt boxes fit the A area");
-    static_assert((kPairBN / 2) * kBK * 2 >= ((kPlanMaxBlocks + 1) / 2) * kBlockBoxBytes,
-                  "a CTA's half of a V unit's block list fits the B area");
+    static_assert(kBBytes >= ((kPlanMaxBlocks + 1) / 2) * kBlockBoxBytes,
+                  "a CTA's half of a V item's block list fits the B area");
 };
 
 __device__ __forceinline__ Unit decode_pair_unit(int32_t u, const TcParams &p) {
@@ -985,18 +990,21 @@ __device__ __forceinline__ void vslice_kblocks(const TcParams &p, int32_t s, int
     *kb1 = (s + 1) * p.num_kb / kVSplit;
 }
 
+// LoRA steps of a main unit of token tile ta (none without the tile plans).
 __device__ __forceinline__ int32_t pair_ext_steps(const TcParams &p, int32_t ta) {
+    if (!p.lora_tiles) return 0;
     const int32_t nb = p.tile_plan[static_cast<size_t>(ta) * kPlanInts];
     return nb > 0 ? nb : 0;
 }
 
+template <int BN>
 __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, const CUtensorMap *tma_w,
                                                   const CUtensorMap *tma_vt, const CUtensorMap *tma_bb,
                                                   const CUtensorMap *tma_pa, const TcParams &p, uint32_t rank,
                                                   uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                                                   const UnitRing &ring, volatile uint32_t *abort_flag) {
     using namespace sm100;
-    using C = PairCfg;
+    using C = PairCfg<BN>;
     int32_t it = 0, idx = 0;
     // Wait for stage `it` to be free in both CTAs (the even CTA's MMAs have
     // read it: that CTA's producer, which has just waited for it, tells the
@@ -1047,7 +1055,7 @@ __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, cons
     auto phase = [&](int32_t u, int32_t, int32_t ph) -> bool {
         const Unit w = decode_pair_unit(u, p);
         const int32_t row = w.ta * kPairM + static_cast<int32_t>(rank) * kBM;
-        const int32_t n0 = w.tb * kPairBN + static_cast<int32_t>(rank) * (kPairBN / 2);  // this CTA's W rows
+        const int32_t n0 = w.tb * BN + static_cast<int32_t>(rank) * (BN / 2);  // this CTA's W rows
         if (ph == 0) {
             for (int32_t i = 0; i < p.num_kb; ++i, ++it) {
                 if (!acquire_stage(11)) return false;
@@ -1075,7 +1083,7 @@ __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, cons
             const int s = it % C::kStages;
             const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
             const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e];
-            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (2 * kVtBoxBytes + (kPairBN / 2) * LORA_BLOCK_ROWS * 2));
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (2 * kVtBoxBytes + (BN / 2) * LORA_BLOCK_ROWS * 2));
             tma_load_2d_pair(sA + s * C::kABytes, tma_vt, e * LORA_BLOCK_ROWS, row, fb);
             tma_load_2d_pair(sA + s * C::kABytes + kVtBoxBytes, tma_vt, kVtCols / 2 + e * LORA_BLOCK_ROWS, row, fb);
             tma_load_2d_pair(sB + s * C::kBBytes, tma_bb, 0, blk * p.N + n0, fb);
@@ -1090,13 +1098,14 @@ __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, cons
 // producers').
 // Unit number t (V items and main units in their sequence order) uses
 // accumulator t & 1.
+template <int BN>
 __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full,
                                              uint64_t *empty, uint64_t *tmem_full, uint64_t *tmem_empty,
                                              const UnitRing &ring, uint32_t tmem_base,
                                              volatile uint32_t *abort_flag) {
     using namespace sm100;
-    using C = PairCfg;
-    constexpr uint32_t idesc_main = idesc_bf16_f32(kPairM, kPairBN);
+    using C = PairCfg<BN>;
+    constexpr uint32_t idesc_main = idesc_bf16_f32(kPairM, BN);
     int32_t it = 0, idx = 0;
     // wake both epilogues for accumulator b so they can unwind
     auto give_up = [&](int b) {
@@ -1137,7 +1146,7 @@ __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uin
         const int32_t total = nb > 0 ? kb1 - kb0 : 0;
         const uint32_t idesc = idesc_bf16_f32(kPairM, nb > 0 ? 32 * ((nb + 1) >> 1) : 32);
         if (!claim_accumulator(t)) return give_up(b);
-        const uint32_t d = tmem_base + b * kPairBN;
+        const uint32_t d = tmem_base + b * kPairAcc;
         for (int32_t i = 0; i < total; ++i, ++it) {
             if (!wait_stage()) return give_up(b);
             const uint32_t a_addr = smem_u32(sA + (it % C::kStages) * C::kABytes);
@@ -1159,7 +1168,7 @@ __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uin
     };
     auto phase = [&](int32_t u, int32_t k, int32_t ph) -> bool {
         const int32_t t = nv + k, b = t & 1;
-        const uint32_t d = tmem_base + b * kPairBN;
+        const uint32_t d = tmem_base + b * kPairAcc;
         if (ph == 0) {
             if (!claim_accumulator(t)) {
                 give_up(b);
@@ -1330,12 +1339,13 @@ __device__ __forceinline__ void run_pair_v_epilogue(const TcParams &p, int32_t v
 // shared-memory staging buffer laid out as a 128-byte-swizzled [128 x 64]
 // box; one thread then stores the box with TMA (rows past M and columns past
 // N are clipped).  Two staging buffers alternate.
+template <int BN>
 __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUtensorMap *tma_out, uint32_t rank,
                                                   uint8_t *sOut, uint64_t *tmem_full, uint64_t *tmem_empty,
                                                   const UnitRing &ring, uint32_t tmem_base,
                                                   volatile uint32_t *abort_flag, volatile uint32_t *v_last) {
     using namespace sm100;
-    using C = PairCfg;
+    using C = PairCfg<BN>;
     const int warp = threadIdx.x >> 5;
     const int q = warp & 3;
     const int grp = (warp - 2) >> 2;  // which 32 of a chunk's 64 columns
@@ -1365,7 +1375,7 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
         }
         if (!epi_all(ok && !*abort_flag)) break;  // uniform over the epilogue warps
         tc_fence_after_sync();
-        const uint32_t col0 = lane_addr + b * kPairBN;
+        const uint32_t col0 = lane_addr + b * kPairAcc;
         if (u >= p.num_units) {
             run_pair_v_epilogue(p, u - p.num_units, rank, col0, row, warp - 2, grp, lane, v_last);
             tc_fence_before_sync();
@@ -1377,7 +1387,9 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
         const Unit w = decode_pair_unit(u, p);
         const int32_t m0 = w.ta * kPairM + static_cast<int32_t>(rank) * kBM;
         const int32_t m = m0 + row;
-        const bool per_row = !p.lora_tiles || p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts] < 0;
+        // the CUDA-core expand for tiles whose plan overflowed (with ycorr the
+        // LoRA term is already in it)
+        const bool per_row = p.lora_tiles && p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts] < 0;
         if (per_row && p.v_units > 0) {
             // the rows' V comes from the tile's V unit
             const bool ready = wait_counter_at_least(p.tile_plan + static_cast<size_t>(w.ta) * kPlanInts + kPlanReadyOff,
@@ -1393,10 +1405,10 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
         if (per_row && m < p.M)
             slot = resolve_slot(p.row_slot[m], m, p.ranks, p.scales, p.max_slots, p.bps, &r, &s, p.status, false);
 #pragma unroll 1
-        for (int j = 0; j < kPairBN / kBK; ++j, ++chunk_no) {
+        for (int j = 0; j < BN / kBK; ++j, ++chunk_no) {
             float acc[32];
             load_tmem_chunk(col0 + j * kBK + grp * 32, acc);
-            const int32_t n0 = w.tb * kPairBN + j * kBK;
+            const int32_t n0 = w.tb * BN + j * kBK;
             if (per_row) rows_finish_chunk(p, slot, r, s, m, n0 + grp * 32, acc);
             uint8_t *buf = sOut + (chunk_no & 1) * C::kOutBytes;
             // the store that last read this buffer (two chunks back) must be done
@@ -1429,13 +1441,14 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
     if (et == 0) bulk_wait_group_all();  // the staging buffers must outlive the stores
 }
 
+template <int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ CUtensorMap tma_w,
                     const __grid_constant__ CUtensorMap tma_vt, const __grid_constant__ CUtensorMap tma_bb,
                     const __grid_constant__ CUtensorMap tma_pa, const __grid_constant__ CUtensorMap tma_out,
                     const TcParams p) {
     using namespace sm100;
-    using C = PairCfg;
+    using C = PairCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -1495,12 +1508,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_cons
 
     if (warp == 0) {
         if (lane == 0)
-            run_pair_producer(&tma_x, &tma_w, &tma_vt, &tma_bb, &tma_pa, p, rank, sA, sB, full, empty, ring, abort_flag);
+            run_pair_producer<BN>(&tma_x, &tma_w, &tma_vt, &tma_bb, &tma_pa, p, rank, sA, sB, full, empty, ring,
+                                  abort_flag);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0)
-            run_pair_mma(p, sA, sB, full, empty, tmem_full, tmem_empty, ring, tmem_base, abort_flag);
+            run_pair_mma<BN>(p, sA, sB, full, empty, tmem_full, tmem_empty, ring, tmem_base, abort_flag);
     } else {
-        run_pair_epilogue(p, &tma_out, rank, sOut, tmem_full, tmem_empty, ring, tmem_base, abort_flag, v_last);
+        run_pair_epilogue<BN>(p, &tma_out, rank, sOut, tmem_full, tmem_empty, ring, tmem_base, abort_flag, v_last);
     }
 
     // no CTA leaves while the other may still signal its barriers or read its
@@ -1640,9 +1654,11 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
 
 // The two-SM GEMM of the large-M orientation (see tc_gemm_pair_kernel): as
 // many pairs as can be resident at once (a cluster needs two SMs of one
-// GPC), each walking every (pairs)-th unit.
+// GPC).
+template <int BN>
 cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
-    using C = PairCfg;
+    using C = PairCfg<BN>;
+    auto kernel = tc_gemm_pair_kernel<BN>;
     static std::mutex mu;
     static uint64_t done_ctx[128] = {};
     static int max_pairs[128] = {};
@@ -1655,15 +1671,14 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
         std::lock_guard<std::mutex> lock(mu);
         uint64_t ctx = done_ctx[dev];
         if (first_use_in_context(&ctx)) {
-            e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(C::kSmem));
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
             if (e != cudaSuccess) return e;
             cudaLaunchConfig_t oc = {};
             oc.gridDim = dim3(2 * 128);
             oc.blockDim = dim3(kThreads);
             oc.dynamicSmemBytes = C::kSmem;
             int n = 0;
-            e = cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel, &oc);
+            e = cudaOccupancyMaxActiveClusters(&n, kernel, &oc);
             if (e != cudaSuccess || n < 1) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
             max_pairs[dev] = n;
             done_ctx[dev] = current_context_id();
@@ -1675,10 +1690,10 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     const uint64_t tiles_m = static_cast<uint64_t>((plan.M + kPlanRows - 1) / kPlanRows) * kPlanRows;
     if (!make_tmap_bf16(&tx, plan.x, plan.M, plan.K, plan.ldx, kBM) ||
         !make_tmap_bf16(&tout, v.out, plan.M, v.N, v.ldo, kBM) ||
-        !make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, kPairBN / 2) ||
+        !make_tmap_bf16(&tw, v.W, v.N, plan.K, plan.K, BN / 2) ||
         !make_tmap_bf16(&tvt, v.vt, tiles_m, kVtCols, kVtCols, kBM, LORA_BLOCK_ROWS, 32) ||
-        !make_tmap_bf16(&tbb, v.b_arena, static_cast<uint64_t>(v.num_blocks) * v.N, LORA_BLOCK_ROWS, LORA_BLOCK_ROWS,
-                        kPairBN / 2, LORA_BLOCK_ROWS, 32) ||
+        !make_tmap_bf16(&tbb, v.b_arena, static_cast<uint64_t>(v.num_blocks) * v.N, LORA_BLOCK_ROWS,
+                        LORA_BLOCK_ROWS, BN / 2, LORA_BLOCK_ROWS, 32) ||
         !make_tmap_bf16(&tpa, v.a_arena, static_cast<uint64_t>(v.num_blocks) * LORA_BLOCK_ROWS, plan.K, plan.K,
                         LORA_BLOCK_ROWS))
         return cudaErrorInvalidValue;
@@ -1690,7 +1705,7 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.kb_per_split = p.num_kb;
     p.splits = 1;
     p.tiles_a = (plan.M + kPairM - 1) / kPairM;
-    p.tiles_b = (v.N + kPairBN - 1) / kPairBN;
+    p.tiles_b = (v.N + BN - 1) / BN;
     p.num_units = p.tiles_a * p.tiles_b;
     p.out = static_cast<__nv_bfloat16 *>(v.out);
     p.ldo = v.ldo;
@@ -1706,10 +1721,10 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.ldv = v.max_rank;
     p.v_parts = 1;
     p.v_part_stride = static_cast<size_t>(plan.M) * v.max_rank;
-    p.lora_tiles = 1;
-    p.tile_plan = v.tile_plan;
     p.status = plan.status;
     p.tiles_a0 = p.tiles_a;
+    p.lora_tiles = 1;
+    p.tile_plan = v.tile_plan;
     p.v_units = p.tiles_a;
     p.vt_out = static_cast<__nv_bfloat16 *>(v.vt);
     p.v_rows = v.V;
@@ -1731,7 +1746,7 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, tx, tw, tvt, tbb, tpa, tout, p);
+    return cudaLaunchKernelEx(&cfg, kernel, tx, tw, tvt, tbb, tpa, tout, p);
 }
 
 }  // namespace
@@ -1856,7 +1871,7 @@ cudaError_t launch_gemm_lora_tc(const ForwardPlan &plan, const ProjView &v, cuda
         }
     }
     // large M with at least one full pair tile of columns: the two-SM kernel
-    if (pair_gemm_takes(v)) return launch_pair_gemm(plan, v, stream);
+    if (pair_gemm_takes(v)) return launch_pair_gemm<kPairBN>(plan, v, stream);
     if (tp.bn == 128) return launch_variant<false, 128>(plan, v, tp, stream);
     return launch_variant<false, 256>(plan, v, tp, stream);
 }

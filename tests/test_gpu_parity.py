@@ -40,7 +40,8 @@ def _sample_rows(wl, n=48, seed=0, per_tile=0, tile=128):
 
 @pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
 @pytest.mark.parametrize("shape", [(300, 520, 392), (130, 1024, 264), (1, 64, 8), (257, 136, 1000),
-                                   (64, 2048, 520), (17, 4096, 136), (600, 256, 200), (520, 1024, 2056)])
+                                   (64, 2048, 520), (17, 4096, 136), (600, 256, 200), (520, 1024, 2056),
+                                   (480, 1024, 2056), (400, 512, 6152)])
 def test_small_mixed_ranks(shape, mode):
     M, K, N = shape
     wl = synth(M=M, K=K, Ns=[N], num_slots=7, rank_choices=(1, 7, 16, 33, 64), seed=M + K + N)
@@ -110,11 +111,12 @@ def test_integer_exact_large_m_tile_fallback(mode):
         assert np.array_equal(got, want), f"{mode} projection {p}: {np.sum(got != want)} outputs differ"
 
 
-@pytest.mark.parametrize("shape", [(64, 2048, (264, 520)), (37, 1024, (1032,)), (700, 192, (136,))])
+@pytest.mark.parametrize("shape", [(64, 2048, (264, 520)), (37, 1024, (1032,)), (700, 192, (136,)),
+                                   (448, 320, (2064,))])
 def test_integer_exact_split_k_and_orientations(shape):
     """Bit-exact through the split-K reduction (few tokens, long K: several
-    CTAs share each output tile) and the non-swapped orientation (many
-    tokens)."""
+    CTAs share each output tile), the swapped orientation near its row
+    limit (448 tokens) and the non-swapped orientation (many tokens)."""
     M, K, Ns = shape
     wl = synth(M=M, K=K, Ns=list(Ns), num_slots=6, rank_choices=(4, 16, 32), integer=True,
                seed=M + K, none_frac=0.2)

@@ -46,8 +46,9 @@ def _index(wl, mode):
 # Each case takes a different layout of the scratch memory: the per-row
 # LoRA kernel with one correction array per projection (two projections in
 # one call); the pipelined grouped kernels (V planes, correction array, split-K
-# partial tiles and counters); the large-M path (the LoRA term as extra GEMM
-# k-blocks, with its intermediates); int8 and int4 base weights.
+# partial tiles and counters); the large-M path (tile plans, V slices and Vt
+# for the two-SM GEMM, the shrink's accumulator for the one-SM GEMM); int8
+# and int4 base weights.
 CASES = {
     "per_row_two_proj": dict(M=128, K=1024, Ns=[256, 520], rank_choices=(8, 16)),
     "grouped": dict(M=300, K=520, Ns=[392, 136], rank_choices=(1, 7, 16, 33, 64)),
