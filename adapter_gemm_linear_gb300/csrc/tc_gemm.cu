@@ -856,6 +856,7 @@ constexpr int kPairAcc = 256;     // Tensor Memory columns of one accumulator
 constexpr int kPairBand = 4;      // unit order: pair tiles per band (as kTaBand for one SM)
 constexpr uint32_t kBlockBoxBytes = LORA_BLOCK_ROWS * kBK * 2;  // one pool block's 16 A rows of a k-block
 constexpr int kVSplit = 2;        // K-slices of a token tile's V (V items per tile)
+constexpr int kLoraPerStage = 2;  // pool blocks of a main unit's LoRA steps per ring stage
 constexpr int kUnitRing = 4;      // main-unit ids in flight from the even CTA's producer to the other roles
 constexpr int kUnitReaders = 2 + 2 * kEpiWarps;  // MMA warp, the odd CTA's producer, both CTAs' epilogue warps
 static_assert(kPairM == kPlanRows, "a pair tile is a plan tile");
@@ -878,7 +879,9 @@ struct PairCfg {
                                     kOutBufs * kOutBytes + (2 * kStages + 4 + 2 * kUnitRing) * 8 + 16 + 4 * kUnitRing;
     static_assert(kSmem <= kSmemLimit, "shared memory over budget");
     static_assert(kTmemCols <= 512, "two accumulators in Tensor Memory");
-    static_assert(kABytes >= 2 * kVtBoxBytes, "a LoRA step's Vt boxes fit the A area");
+    static constexpr uint32_t kLoraBBytes = (BN / 2) * LORA_BLOCK_ROWS * 2;  // a block's B box of this CTA
+    static_assert(kABytes >= kLoraPerStage * 2 * kVtBoxBytes, "a stage's Vt boxes fit the A area");
+    static_assert(kBBytes >= kLoraPerStage * kLoraBBytes, "a stage's B boxes fit the B area");
     static_assert(kBBytes >= ((kPlanMaxBlocks + 1) / 2) * kBlockBoxBytes,
                   "a CTA's half of a V item's block list fits the B area");
 };
@@ -1078,15 +1081,21 @@ __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, cons
             return false;
         }
         fence_proxy_async_global();  // the TMA loads below read what generic stores wrote
-        for (int32_t e = 0; e < ext; ++e, ++it) {
+        // kLoraPerStage pool blocks per stage: their Vt hi and lo boxes side by
+        // side in the A area, their B boxes in the B area
+        for (int32_t e = 0; e < ext; e += kLoraPerStage, ++it) {
             if (!acquire_stage(11)) return false;
             const int s = it % C::kStages;
             const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-            const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e];
-            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (2 * kVtBoxBytes + (BN / 2) * LORA_BLOCK_ROWS * 2));
-            tma_load_2d_pair(sA + s * C::kABytes, tma_vt, e * LORA_BLOCK_ROWS, row, fb);
-            tma_load_2d_pair(sA + s * C::kABytes + kVtBoxBytes, tma_vt, kVtCols / 2 + e * LORA_BLOCK_ROWS, row, fb);
-            tma_load_2d_pair(sB + s * C::kBBytes, tma_bb, 0, blk * p.N + n0, fb);
+            const int32_t eb = min(kLoraPerStage, ext - e);
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * eb * (2 * kVtBoxBytes + C::kLoraBBytes));
+            for (int32_t j = 0; j < eb; ++j) {
+                const int32_t blk = p.tile_plan[static_cast<size_t>(w.ta) * kPlanInts + kPlanBlkOff + e + j];
+                uint8_t *va = sA + s * C::kABytes + j * 2 * kVtBoxBytes;
+                tma_load_2d_pair(va, tma_vt, (e + j) * LORA_BLOCK_ROWS, row, fb);
+                tma_load_2d_pair(va + kVtBoxBytes, tma_vt, kVtCols / 2 + (e + j) * LORA_BLOCK_ROWS, row, fb);
+                tma_load_2d_pair(sB + s * C::kBBytes + j * C::kLoraBBytes, tma_bb, 0, blk * p.N + n0, fb);
+            }
         }
         return true;
     };
@@ -1192,15 +1201,21 @@ __device__ __forceinline__ void run_pair_mma(const TcParams &p, uint8_t *sA, uin
         const Unit w = decode_pair_unit(u, p);
         grid_dependency_wait();
         const int32_t ext = pair_ext_steps(p, w.ta);
-        for (int32_t e = 0; e < ext; ++e, ++it) {  // LoRA step: Vt_hi and Vt_lo times the block's B, K = 16 each
+        // LoRA steps, kLoraPerStage pool blocks per stage: Vt_hi and Vt_lo
+        // times the block's B, K = 16 each
+        for (int32_t e = 0; e < ext; e += kLoraPerStage, ++it) {
             if (!wait_stage()) {
                 give_up(b);
                 return false;
             }
             const uint32_t a_addr = smem_u32(sA + (it % C::kStages) * C::kABytes);
             const uint32_t b_addr = smem_u32(sB + (it % C::kStages) * C::kBBytes);
-            mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr), desc_kmajor_sw32(b_addr), idesc_main, 1u);
-            mma_bf16_f32_pair(d, desc_kmajor_sw32(a_addr + kVtBoxBytes), desc_kmajor_sw32(b_addr), idesc_main, 1u);
+            const int32_t eb = min(kLoraPerStage, ext - e);
+            for (int32_t j = 0; j < eb; ++j) {
+                const uint32_t va = a_addr + j * 2 * kVtBoxBytes, vb = b_addr + j * C::kLoraBBytes;
+                mma_bf16_f32_pair(d, desc_kmajor_sw32(va), desc_kmajor_sw32(vb), idesc_main, 1u);
+                mma_bf16_f32_pair(d, desc_kmajor_sw32(va + kVtBoxBytes), desc_kmajor_sw32(vb), idesc_main, 1u);
+            }
             release_stage();
         }
         if (*abort_flag) {
