@@ -92,6 +92,19 @@ def test_integer_exact_prefill_geometry(mode):
     assert np.array_equal(got, want), f"{mode}: {np.sum(got != want)} outputs differ"
 
 
+def test_integer_exact_many_units():
+    """More 256 x 256 units (8 token tiles x 20 column tiles = 160) than two
+    rounds of the pairs, so most are handed out on demand, with LoRA steps
+    on every tile; integer inputs, every output bit-exact."""
+    wl = synth(M=2048, K=192, Ns=[5120], num_slots=16, rank_choices=(8, 16, 32, 64), integer=True,
+               seed=5120, none_frac=0.05, mode="sgmv")
+    pools = H.make_pools(wl, DEV, extra_blocks=11)
+    out = H.forward(wl, pools, "sorted")[0]
+    want = H.oracle_bf16_bits(H.oracle_rows(wl, 0))
+    got = torch.from_numpy(out).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want), f"{np.sum(got != want)} outputs differ"
+
+
 @pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
 def test_integer_exact_large_m_tile_fallback(mode):
     """Large M where some 128-token tiles name adapters spanning more than 16
