@@ -41,8 +41,11 @@ def _sample_rows(wl, n=48, seed=0, per_tile=0, tile=128):
 @pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
 @pytest.mark.parametrize("shape", [(300, 520, 392), (130, 1024, 264), (1, 64, 8), (257, 136, 1000),
                                    (64, 2048, 520), (17, 4096, 136), (600, 256, 200), (520, 1024, 2056),
-                                   (480, 1024, 2056), (400, 512, 6152)])
+                                   (480, 1024, 2056), (400, 512, 6152), (700, 1000, 520), (600, 64, 264)])
 def test_small_mixed_ranks(shape, mode):
+    """(700, 1000, 520): the two-SM GEMM with a ragged last k-block (the V
+    items' K-slices of 8 and 8 k-blocks, the last one partly past K); (600,
+    64, 264): one k-block, so one of a tile's two V slices is empty."""
     M, K, N = shape
     wl = synth(M=M, K=K, Ns=[N], num_slots=7, rank_choices=(1, 7, 16, 33, 64), seed=M + K + N)
     pools = H.make_pools(wl, DEV)
