@@ -95,17 +95,23 @@ struct TilePlanParams {
     unsigned long long *status;
 };
 
-// One CTA per token tile.  Warp 0 resolves the rows' slots (errors are
-// recorded here, once per row) and lists the tile's distinct slots -- a
-// repeated warp minimum over the slots above the last one listed -- with
-// their pool blocks (a slot with a block entry out of range is reported and
-// left out: its rows get no correction).  More than kPlanMaxBlocks blocks
-// mark the tile (-1) for the CUDA-core fallback.  Then the CTA zeroes the
-// accumulator columns of the listed blocks.
+// One CTA per token tile.  Every thread resolves one row's slot (errors are
+// recorded here, once per row) and fetches the slot's rank and first
+// kPlanPrefetch block-table entries into shared memory, all in parallel.
+// Warp 0 then lists the tile's distinct slots -- a repeated warp minimum over
+// the slots above the last one listed -- with their pool blocks, read from
+// a row of that slot in shared memory (a slot with a block entry out of range
+// is reported and left out: its rows get no correction).  More than
+// kPlanMaxBlocks blocks mark the tile (-1) for the CUDA-core fallback.  On
+// the one-SM path the CTA then zeroes the accumulator columns of the listed
+// blocks.
 __global__ void __launch_bounds__(256) tile_plan_kernel(const TilePlanParams p) {
     static_assert(kPlanRows == 256, "one thread per row of the plan tile");
+    constexpr int kPlanPrefetch = 4;  // table entries fetched per row (ranks up to 64)
     __shared__ int32_t s_nb;
     __shared__ int32_t s_slot[kPlanRows];
+    __shared__ int32_t s_rank[kPlanRows];
+    __shared__ int32_t s_tbl[kPlanRows][kPlanPrefetch];
     const int32_t t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *plan = p.plan + static_cast<size_t>(t) * kPlanInts;
@@ -153,6 +159,11 @@ __global__ void __launch_bounds__(256) tile_plan_kernel(const TilePlanParams p) 
                 mine = id;
         }
         s_slot[threadIdx.x] = mine;
+        s_rank[threadIdx.x] = mine == INT_MAX ? 0 : rk;
+        const int32_t nblk = mine == INT_MAX ? 0 : (rk + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
+#pragma unroll
+        for (int i = 0; i < kPlanPrefetch; ++i)
+            s_tbl[threadIdx.x][i] = i < nblk ? p.table[static_cast<size_t>(mine) * p.bps + i] : 0;
     }
     __syncthreads();
     if (warp == 0) {
@@ -171,8 +182,17 @@ __global__ void __launch_bounds__(256) tile_plan_kernel(const TilePlanParams p) 
             for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
             if (cand == INT_MAX) break;
             last = cand;
-            const int32_t nblk = (p.ranks[cand] + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
-            const int32_t blk = lane < nblk ? p.table[static_cast<size_t>(cand) * p.bps + lane] : 0;
+            // a row of slot cand: its rank and first table entries are in shared memory
+            int32_t mrow = -1;
+#pragma unroll
+            for (int i = kRowsPerLane - 1; i >= 0; --i)
+                if (mine[i] == cand) mrow = i * 32 + lane;
+            const uint32_t holders = __ballot_sync(0xffffffffu, mrow >= 0);
+            const int32_t row = __shfl_sync(0xffffffffu, mrow, __ffs(holders) - 1);
+            const int32_t nblk = (s_rank[row] + LORA_BLOCK_ROWS - 1) / LORA_BLOCK_ROWS;
+            const int32_t blk = lane < nblk ? (lane < kPlanPrefetch ? s_tbl[row][lane]
+                                                                    : p.table[static_cast<size_t>(cand) * p.bps + lane])
+                                            : 0;
             if (__any_sync(0xffffffffu, lane < nblk && (blk < 0 || blk >= p.num_blocks))) {
                 if (lane == 0) record_error(p.status, kDevBadBlock, static_cast<uint32_t>(cand));
                 continue;
