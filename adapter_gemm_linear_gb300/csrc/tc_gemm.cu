@@ -821,34 +821,39 @@ tc_gemm_lora_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
 // --------------------------------------------------------------- two-SM kernel (large M)
 //
 // Large M in bf16 with at least 256 output columns: one MMA over a pair of
-// CTAs (a cluster of two, tcgen05 cta_group::2).  A pair tile is 256 tokens x
-// kPairBN output columns; CTA r of the pair loads its 128 token rows of x and
-// its kPairBN/2 rows of W per k-block (32 KiB instead of the 48 KiB a
-// 128 x 256 tile takes on one SM), the even CTA issues the MMAs (M = 256,
-// N = kPairBN) over both CTAs' shared memory, and each CTA's Tensor Memory
-// holds the accumulator rows of its 128 tokens.  Both CTAs' loads signal the
-// even CTA's `full` barrier; its MMA completions signal both CTAs' `empty`
-// and `tmem_full` barriers; both CTAs' epilogues signal its `tmem_empty`.
+// CTAs (a cluster of two, tcgen05 cta_group::2).  A main unit is a pair tile
+// of 256 tokens x kPairBN output columns; CTA r of the pair loads its 128
+// token rows of x and its kPairBN/2 rows of W per k-block (32 KiB instead of
+// the 48 KiB a 128 x 256 tile takes on one SM), the even CTA issues the MMAs
+// (M = 256, N = kPairBN) over both CTAs' shared memory, and each CTA's
+// Tensor Memory holds the accumulator rows of its 128 tokens.  Both CTAs'
+// loads signal the even CTA's `full` barrier; its MMA completions signal its
+// `empty` barrier (its producer passes each release on to the odd CTA) and
+// both CTAs' `tmem_full`; both CTAs' epilogues signal its `tmem_empty`.
 // After the main k-blocks come the LoRA steps of the pair tile's plan, in
-// the same split (Vt rows per CTA, half of the block's B rows per CTA).
+// the same split (Vt rows per CTA, half of the block's B rows per CTA), two
+// pool blocks per ring stage.
 //
 // The LoRA term's V is computed here too, by V items: kVSplit per token
 // tile, each V = x_tile A_list^T over one K-slice with the same pair MMA (M
 // = 256 tokens, N = 32 ceil(nb/2): CTA r stacks blocks [r h, r h + h) of the
 // tile's list, h = ceil(nb/2), from 16-row boxes of the pool's A arena).
-// The slices of a CTA's rows count their arrival (a per-tile, per-rank
-// counter in the plan); all but the last store their fp32 slice, and the
-// last adds those to its own, writes the rows' Vt -- hi and lo bf16 parts of
-// s_i V masked to each row's own slot -- and counts the CTA in the plan's
-// ready entry; a main unit's producer waits for both CTAs' counts before it
-// loads Vt for the LoRA steps.  Tiles whose
-// plan overflowed get the per-row V on CUDA cores from their V items'
-// epilogues instead (rows split between the slices), which the main units'
-// epilogues wait for.  V items come first in every pair's sequence (so
-// every wait points to work that never waits), dealt first to the pairs
-// with one main unit fewer, up to kVSplit each, then to the others; all pairs
-// are resident at once (the grid is at most the resident cluster count), so
-// every wait ends.
+// Every slice of a CTA's rows stores its fp32 sums and then counts itself (a
+// per-tile, per-rank counter in the plan); the last to count adds the others
+// to its own, writes the rows' Vt -- hi and lo bf16 parts of s_i V masked to
+// each row's own slot -- and counts the CTA in the plan's ready entry; a
+// main unit's producer waits for both CTAs' counts before it loads Vt for
+// the LoRA steps.  Tiles whose plan overflowed get the per-row V on CUDA
+// cores from their V items' epilogues instead (rows split between the
+// slices), which the main units' epilogues wait for.
+//
+// Order of work: a pair takes its V items first (dealt one at a time from the
+// last pair down), then its main units, handed out on demand (fetch_main_unit)
+// so that the pairs' work evens out; the first two main units of a pair run
+// both main loops before their LoRA steps (for_each_main_phase).  V items
+// wait for nothing but their own loads and precede every main unit, so every
+// wait points to work that never waits, and all pairs are resident at once
+// (the grid is at most the resident cluster count): every wait ends.
 
 constexpr int kPairM = 2 * kBM;   // tokens per pair tile
 constexpr int kPairBN = 256;      // output columns per pair tile of the large-M path (the MMA's N)
