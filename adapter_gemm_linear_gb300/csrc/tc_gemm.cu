@@ -116,8 +116,9 @@ struct TcParams {
     // q int8 (w_bits 8) or packed int4, two per byte, low nibble first (4)
     const float *w_scale;
     int32_t w_bits;
-    // split-K tile-counter waits: the arrivals expected beyond `splits` (1
-    // only when armed for a test, so that the waits run out) and their limit
+    // split-K tile-counter waits (and the two-SM kernel's Vt ready waits):
+    // the arrivals expected beyond the real ones (1 only when armed for a
+    // test, so that the waits run out) and their limit
     int32_t counter_extra;
     uint64_t counter_wait_ns;
     // two-SM kernel: V items, kVSplit per token tile (v_units tiles), each
@@ -1079,8 +1080,8 @@ __device__ __forceinline__ void run_pair_producer(const CUtensorMap *tma_x, cons
         const int32_t ext = pair_ext_steps(p, w.ta);
         if (ext == 0) return true;
         // the tile's Vt comes from its V items (both CTAs of some pair)
-        if (!wait_counter_at_least(p.tile_plan + static_cast<size_t>(w.ta) * kPlanInts + kPlanReadyOff, 2,
-                                   kWaitLimitNs)) {
+        if (!wait_counter_at_least(p.tile_plan + static_cast<size_t>(w.ta) * kPlanInts + kPlanReadyOff,
+                                   2 + p.counter_extra, p.counter_wait_ns)) {
             record_error(p.status, kDevTimeout, 16);
             *abort_flag = 1;
             return false;
@@ -1413,7 +1414,7 @@ __device__ __forceinline__ void run_pair_epilogue(const TcParams &p, const CUten
         if (per_row && p.v_units > 0) {
             // the rows' V comes from the tile's V unit
             const bool ready = wait_counter_at_least(p.tile_plan + static_cast<size_t>(w.ta) * kPlanInts + kPlanReadyOff,
-                                                     2, kWaitLimitNs);
+                                                     2 + p.counter_extra, p.counter_wait_ns);
             if (!ready) {
                 record_error(p.status, kDevTimeout, 17);
                 *abort_flag = 1;
@@ -1751,6 +1752,9 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.v_part = v.vacc;
     p.queue = v.tile_plan + kPlanQueueOff;
     p.plan_rw = v.tile_plan;
+    // armed for a test: the Vt ready waits expect one count more than comes
+    p.counter_extra = plan.test_wait_limit_ns ? 1 : 0;
+    p.counter_wait_ns = plan.test_wait_limit_ns ? plan.test_wait_limit_ns : kWaitLimitNs;
     p.x = static_cast<const __nv_bfloat16 *>(plan.x);
     p.ldx = plan.ldx;
     p.a_arena = static_cast<const __nv_bfloat16 *>(v.a_arena);

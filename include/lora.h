@@ -385,14 +385,16 @@ lora_status_t lora_get_device_status(void *stream, int32_t *detail);
  * Testing hook for the failure path of the kernels' bounded waits (no
  * counterpart in the pages).  Arms the next lora_linear_forward call on any
  * thread: in that call every split-K tile-counter wait of the tensor-core
- * GEMM waits for one arrival more than the launch makes, giving up after
- * limit_ns (1 ms .. 2 s) instead of the normal 2 s.  The waits then run out:
- * the GEMM records LORA_ERR_DEVICE_TIMEOUT in the status word, writes no
- * output for those tiles, releases its tensor memory and ends normally, so
- * the context stays usable.  The arming is taken by the next call that
- * passes validation and reaches the device; calls whose GEMM does not split
- * K take it without effect.  limit_ns = 0 disarms.  Errors: INVALID_ARG
- * (limit out of range).
+ * GEMM (small M), and every wait of the large-M two-SM GEMM for a token
+ * tile's LoRA intermediate, waits for one arrival more than the launch makes,
+ * giving up after limit_ns (1 ms .. 2 s) instead of the normal 2 s.  The
+ * waits then run out: the GEMM records LORA_ERR_DEVICE_TIMEOUT in the status
+ * word, writes no output for the tiles it could not finish, releases its
+ * tensor memory and ends normally (after its other bounded waits, up to a
+ * few seconds), so the context stays usable.  The arming is taken by the
+ * next call that passes validation and reaches the device; calls with
+ * neither kind of wait take it without effect.  limit_ns = 0 disarms.
+ * Errors: INVALID_ARG (limit out of range).
  */
 lora_status_t lora_test_arm_wait_timeout(uint64_t limit_ns);
 

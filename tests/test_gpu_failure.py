@@ -1,8 +1,9 @@
 """Failure paths and per-call options of lora_linear_forward on the GPU.
 
 - A bounded wait that runs out: the test hook makes the split-K tile-counter
-  waits of the next forward expect an arrival that never comes, with a 20 ms
-  limit.  The GEMM must report LORA_ERR_DEVICE_TIMEOUT through the status
+  waits (small M) or the waits for a token tile's LoRA intermediate (the
+  large-M two-SM GEMM) of the next forward expect an arrival that never
+  comes, with a 20 ms limit.  The GEMM must report LORA_ERR_DEVICE_TIMEOUT through the status
   word, leave the tiles it could not finish unwritten, release its tensor
   memory and end; the next forward on the same context must be right.  No
   GPU fault is involved: every wait is bounded and the kernel returns.
@@ -41,6 +42,27 @@ def test_wait_timeout_reports_and_recovers():
     out = H.forward(wl, pools, "bgmv")[0]
     assert device_status() == (0, 0)
     H.assert_close("bf16", out, H.oracle_rows(wl, 0), "after the timed-out forward")
+
+
+VT_READY_SITE = 16  # detail the two-SM GEMM records for its wait on a tile's LoRA intermediate
+
+
+def test_wait_timeout_two_sm_gemm():
+    """The large-M two-SM GEMM armed the same way: its producers' waits for a
+    token tile's Vt expect one count more than the V items give.  The first
+    one runs out after 20 ms; the kernel records the timeout, its other
+    roles give up within their own bounded waits, and it ends; a normal
+    forward right after on the same context is right."""
+    wl = synth(M=1100, K=512, Ns=[264], num_slots=6, rank_choices=(8, 16, 32), seed=93, mode="sgmv")
+    pools = H.make_pools(wl, DEV)
+    assert device_status() == (0, 0)
+    arm_test_wait_timeout(20_000_000)
+    H.forward(wl, pools, "sorted")
+    st, detail = device_status()
+    assert st == LORA_ERR_DEVICE_TIMEOUT and detail == VT_READY_SITE, (st, detail)
+    out = H.forward(wl, pools, "sorted")[0]
+    assert device_status() == (0, 0)
+    H.assert_close("bf16", out, H.oracle_rows(wl, 0), "after the timed-out two-SM forward")
 
 
 def _scaled_oracle(wl, p, factors, rows=None):
