@@ -508,6 +508,8 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     off += align_up(ycorr, 256);
     ws->group_off = off;
     if (ycorr) off += align_up(sizeof(int32_t) * lora::group_table_ints(a->M), 256);
+    ws->pipe_group_off = off;
+    if (ycorr && a->M <= lora::kPipeMaxRows) off += align_up(lora::pipe_group_bytes() * a->n_proj, 256);
     // the tensor-core LoRA term of large M: tile plans, the V accumulator and
     // Vt, shared by the projections (their kernels run one after the other
     // on the stream)
@@ -583,6 +585,7 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
         }
     }
     plan.group_table = reinterpret_cast<int32_t *>(base + ws.group_off);
+    plan.pipe_groups = base + ws.pipe_group_off;
     for (int i = 0; i < plan.n_proj; ++i) {
         if (!plan.proj[i].lora_tiles) continue;
         plan.proj[i].tile_plan = reinterpret_cast<int32_t *>(base + ws.plan_off);

@@ -145,6 +145,7 @@ struct ForwardPlan {
     float *part;                // workspace: split-K partial tiles
     float *ycorr;               // workspace: fp32 [M][N] LoRA correction (small-M orientation)
     int32_t *group_table;       // workspace: GroupTable storage (small-M orientation)
+    void *pipe_groups;          // workspace: one row grouping per projection for the pipelined kernels
     int32_t *counters;          // workspace: split-K tile counters, zeroed by the shrink
     int32_t n_counters;         // entries of `counters`
     int v_parts;                // K-slice planes of V the shrink writes
@@ -172,6 +173,7 @@ struct WorkspaceLayout {
     size_t part_off;              // fp32 split-K partial tiles (largest projection)
     size_t ycorr_off;             // fp32 [M][N] correction of the small-M orientation (largest projection)
     size_t group_off;             // int32 group table (small-M orientation)
+    size_t pipe_group_off;        // the pipelined kernels' row groupings, one per projection
     size_t plan_off, vacc_off, vt_off;  // large-M tensor-core LoRA term
     size_t counter_off;           // int32 per output tile (split-K)
     size_t total;
@@ -236,6 +238,10 @@ cudaError_t launch_expand_grouped(const ForwardPlan &plan, const ProjView &v, co
 // of V with rows in sorted order, the expand plan.ycorr.  For M <=
 // kPipeMaxRows and pools of max_rank <= kPipeMaxRank.
 bool pipe_grouped_supported(int32_t M, int32_t max_rank);
+// The rows grouped by adapter once per forward for every projection (one CTA
+// each, into plan.pipe_groups), read by both pipelined kernels.
+size_t pipe_group_bytes();
+cudaError_t launch_pipe_group(const ForwardPlan &plan, cudaStream_t stream);
 cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
 cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
 

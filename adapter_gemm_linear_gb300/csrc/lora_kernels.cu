@@ -458,11 +458,17 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
     bool by_row = swapped;
     for (int p = 0; p < plan.n_proj; ++p)
         by_row = by_row && row_lora_preferred(plan.M, plan.K, plan.proj[p].N, plan.proj[p].max_rank);
-    // the pipelined grouped kernels group the rows themselves
+    // the pipelined grouped kernels read one grouping per projection,
+    // made by one launch before them
     bool piped = swapped && !by_row;
     for (int p = 0; p < plan.n_proj; ++p) piped = piped && pipe_grouped_supported(plan.M, plan.proj[p].max_rank);
     GroupTable gt{};
     cudaError_t e = cudaSuccess;
+    if (piped) {  // the rows grouped by adapter once, for every projection
+        e = launch_pipe_group(plan, stream);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+    }
     if (swapped && !by_row && !piped) {
         gt = group_table_at(plan.group_table, plan.M);
         e = launch_group_rows(plan, gt, plan.proj[0].max_slots, stream);

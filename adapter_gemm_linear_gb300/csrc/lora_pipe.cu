@@ -9,11 +9,12 @@
 // (MBGMV/MBGMM over a paged pool), with the rows sorted by adapter as in the
 // Punica SGMV description, laid out for this GPU:
 //
-//   * Every CTA sorts the rows by (rank blocks descending, slot) itself, a
-//     bitonic sort of 512 keys mostly in registers, and cuts the groups
-//     into chunks of at most 16 positions.  Both kernels derive the same
-//     order, so no table goes through global memory and no launch is spent
-//     on it.
+//   * One small launch per forward (pipe_group_kernel, a CTA per
+//     projection) sorts the rows by (rank blocks descending, slot), a
+//     bitonic sort of 512 keys mostly in registers, cuts the groups into
+//     chunks of at most 16 positions and writes the chunk table; every CTA
+//     of both kernels copies its projection's table into shared memory, so
+//     the sort is not repeated per CTA and per projection.
 //   * A producer warp streams the adapter data with untiled TMA bulk copies
 //     into a ring of shared-memory stages (mbarrier full/empty pairs); eight
 //     consumer warps do the arithmetic.  The pool's layouts make every piece
@@ -263,6 +264,61 @@ __device__ void group_rows_in_cta(GroupSmem &gs, int32_t M, const int32_t *row_s
     __syncthreads();
 }
 
+// One projection's row grouping as pipe_group_kernel leaves it in global
+// memory: the fields of GroupSmem that the pipelined kernels read.
+struct PipeGroupTable {
+    int32_t n_chunks;
+    int32_t pos_row[kPipeMaxRows];
+    int32_t c_begin[kPipeMaxRows + 1];
+    int32_t c_slot[kPipeMaxRows];
+    int32_t c_nblk[kPipeMaxRows];
+};
+
+// A CTA's copy of a grouping table (every thread calls it).
+__device__ void load_group_table(GroupSmem &gs, const PipeGroupTable *t, int32_t M) {
+    const int tid = threadIdx.x, T = blockDim.x;
+    const int32_t C = t->n_chunks;
+    for (int32_t i = tid; i < M; i += T) gs.pos_row[i] = t->pos_row[i];
+    for (int32_t i = tid; i <= C; i += T) gs.c_begin[i] = t->c_begin[i];
+    for (int32_t i = tid; i < C; i += T) {
+        gs.c_slot[i] = t->c_slot[i];
+        gs.c_nblk[i] = t->c_nblk[i];
+    }
+    if (tid == 0) gs.n_chunks = C;
+    __syncthreads();
+}
+
+struct PipeGroupParams {
+    int32_t M;
+    const int32_t *row_slot;
+    const int32_t *ranks[LORA_MAX_PROJ];
+    int32_t max_slots[LORA_MAX_PROJ], bps[LORA_MAX_PROJ];
+    PipeGroupTable *tables;  // [projections]
+    unsigned long long *status;
+};
+
+// CTA q groups the rows for projection q (the ranks come from its pool) and
+// writes the table both pipelined kernels of that projection read; invalid
+// ids are recorded once, by CTA 0.
+__global__ void __launch_bounds__(kPipeThreads, 1) pipe_group_kernel(const PipeGroupParams p) {
+    __shared__ GroupSmem gs;
+    // the row ids may come from the kernel before (segments to rows)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int q = blockIdx.x;
+    group_rows_in_cta(gs, p.M, p.row_slot, p.ranks[q], p.max_slots[q], p.bps[q], p.status, q == 0);
+    PipeGroupTable *t = p.tables + q;
+    const int tid = threadIdx.x, T = blockDim.x;
+    const int32_t C = gs.n_chunks;
+    for (int32_t i = tid; i < p.M; i += T) t->pos_row[i] = gs.pos_row[i];
+    for (int32_t i = tid; i <= C; i += T) t->c_begin[i] = gs.c_begin[i];
+    for (int32_t i = tid; i < C; i += T) {
+        t->c_slot[i] = gs.c_slot[i];
+        t->c_nblk[i] = gs.c_nblk[i];
+    }
+    if (tid == 0) t->n_chunks = C;
+}
+
 // Lane j's block id of chunk c (its slot's table entry j; 0 past the chunk's
 // rank blocks, past the last chunk, or for rows without an adapter).  The
 // producers load the next chunk's ids while they stream the current one.
@@ -299,6 +355,7 @@ struct PipeShrinkParams {
     size_t plane_stride;   // elements between planes
     int32_t *counters;     // split-K tile counters of the GEMM that follows, zeroed here
     int32_t n_counters;
+    const PipeGroupTable *group;  // the rows grouped by adapter (pipe_group_kernel)
     unsigned long long *status;
 };
 
@@ -333,7 +390,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_shrink_kernel(const Pipe
         fence_mbar_init();
         issued_s = 0;
     }
-    group_rows_in_cta(gs, p.M, p.row_slot, p.ranks, p.max_slots, p.bps, p.status, false);
+    load_group_table(gs, p.group, p.M);
     const int32_t C = gs.n_chunks;
     for (int32_t c = tid; c < C; c += kPipeThreads) gs.c_pre[c] = gs.c_nblk[c] * p.ksplit;
     __syncthreads();
@@ -528,6 +585,7 @@ struct PipeExpandParams {
     int32_t vslot_floats;  // ksplit * kChunkRows * ldv
     int32_t n_vslots;      // 2 .. kExpMaxVSlots
     float *ycorr;          // [M][N]
+    const PipeGroupTable *group;  // the rows grouped by adapter (pipe_group_kernel)
     unsigned long long *status;
 };
 
@@ -574,7 +632,9 @@ __global__ void __launch_bounds__(kExpThreads, 1) pipe_expand_kernel(const PipeE
         fence_mbar_init();
         issued_s = 0;
     }
-    group_rows_in_cta(gs, p.M, p.row_slot, p.ranks, p.max_slots, p.bps, p.status, blockIdx.x == 0);
+    // the grouping comes from pipe_group_kernel, which completed before the
+    // shrink this grid follows passed its own grid-dependency wait
+    load_group_table(gs, p.group, p.M);
     const int32_t C = gs.n_chunks;
     const int32_t n_ranges = (p.N + kExpCols - 1) / kExpCols;
     // cost of an item in quarter stages: 4 per rank block (its B copy and
@@ -944,6 +1004,43 @@ static int32_t pipe_kc_len(int32_t K, int32_t ksplit) {
     return len;
 }
 
+size_t pipe_group_bytes() { return sizeof(PipeGroupTable); }
+
+// Projection v's grouping table in plan.pipe_groups (null if v is not one of
+// the plan's projections or there is no table region).
+static const PipeGroupTable *pipe_group_of(const ForwardPlan &plan, const ProjView &v) {
+    const ptrdiff_t q = &v - plan.proj;
+    if (!plan.pipe_groups || q < 0 || q >= plan.n_proj) return nullptr;
+    return static_cast<const PipeGroupTable *>(plan.pipe_groups) + q;
+}
+
+cudaError_t launch_pipe_group(const ForwardPlan &plan, cudaStream_t stream) {
+    if (plan.M <= 0) return cudaSuccess;
+    if (plan.M > kPipeMaxRows || !plan.pipe_groups || plan.n_proj < 1 || plan.n_proj > LORA_MAX_PROJ)
+        return cudaErrorInvalidValue;
+    PipeGroupParams p;
+    p.M = plan.M;
+    p.row_slot = plan.row_slot;
+    for (int q = 0; q < plan.n_proj; ++q) {
+        p.ranks[q] = plan.proj[q].ranks;
+        p.max_slots[q] = plan.proj[q].max_slots;
+        p.bps[q] = plan.proj[q].bps;
+    }
+    p.tables = static_cast<PipeGroupTable *>(plan.pipe_groups);
+    p.status = plan.status;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.n_proj);
+    cfg.blockDim = dim3(kPipeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pipe_group_kernel, p);
+}
+
 cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
     if (plan.M <= 0) return cudaSuccess;
     if (!pipe_grouped_supported(plan.M, v.max_rank) || plan.v_parts < 1 || plan.v_parts > kMaxVPlanes)
@@ -969,6 +1066,8 @@ cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView &v, cudaS
     p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.counters = plan.counters;
     p.n_counters = plan.n_counters;
+    p.group = pipe_group_of(plan, v);
+    if (!p.group) return cudaErrorInvalidValue;
     p.status = plan.status;
     return launch_pipe(pipe_shrink_kernel, p, kPipeThreads, kShrSmem, kShrSmem, stream);
 }
@@ -994,6 +1093,8 @@ cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaS
     p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
     p.vslot_floats = kChunkRows * v.max_rank;
     p.ycorr = v.ycorr;
+    p.group = pipe_group_of(plan, v);
+    if (!p.group) return cudaErrorInvalidValue;
     p.status = plan.status;
     const size_t vbytes = sizeof(float) * static_cast<size_t>(p.vslot_floats);
     const size_t room = kExpSmemMax - static_cast<size_t>(kExpStages) * kExpStageBytes;
