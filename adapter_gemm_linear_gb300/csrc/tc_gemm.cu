@@ -483,6 +483,64 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
 // Epilogue warps: warp w (2..2+kEpiWarps-1) may access TMEM lane quarter
 // w % 4; the kEpiWarps / 4 warps sharing a quarter take turns over the
 // 32-column chunks.
+// Split-K finish of the swapped orientation: each thread sums four adjacent
+// output columns (16-byte loads of the tile's partial slices and of the
+// correction; N and ldo are multiples of 8, which the host checks), the
+// eight token lanes of the epilogue step through this split's share of the
+// tokens [e_begin, e_end), and every load of a batch of kR tokens is in
+// flight before the sums.
+template <int BN, bool PAIR, bool QUANT>
+__device__ __forceinline__ void finish_split_vec4(const TcParams &p, const ProjTile<PAIR> &pt, int32_t tb,
+                                                  const float *tile_part, size_t split_stride, int32_t e_begin,
+                                                  int32_t e_end, int et) {
+    constexpr int kR = BN <= 64 ? 2 : 4;  // within the narrow variants' register cap
+    constexpr int kLanes = kEpiThreads / (kBM / 4);  // token lanes: 8
+    const int cq = et % (kBM / 4), tr = et / (kBM / 4);
+    const int32_t nn0 = pt.ta * kBM + 4 * cq;
+    if (nn0 >= pt.N()) return;  // N % 4 == 0: the group is wholly inside or outside
+    const float *col = tile_part + 4 * cq;
+    const float4 wsc = QUANT ? __ldg(reinterpret_cast<const float4 *>(p.w_scale + nn0)) : make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll 1
+    for (int32_t e0 = e_begin + tr; e0 < e_end; e0 += kLanes * kR) {
+        float4 a[kR], sp[kR];
+#pragma unroll
+        for (int r = 0; r < kR; ++r) {
+            const int32_t e = e0 + kLanes * r, m = tb * BN + e;
+            a[r] = (e < e_end && m < p.M)
+                       ? __ldcg(reinterpret_cast<const float4 *>(pt.ycorr() + static_cast<size_t>(m) * pt.N() + nn0))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            sp[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll 2
+        for (int32_t ks = 0; ks < p.splits; ++ks) {
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const int32_t e = e0 + kLanes * r;
+                if (e < e_end) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(col + ks * split_stride +
+                                                                            static_cast<size_t>(e) * kBM));
+                    sp[r].x += v.x;
+                    sp[r].y += v.y;
+                    sp[r].z += v.z;
+                    sp[r].w += v.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kR; ++r) {
+            const int32_t e = e0 + kLanes * r, m = tb * BN + e;
+            if (e >= e_end || m >= p.M) continue;
+            // the int8 W row's scale multiplies the base sum only
+            uint2 o;
+            o.x = pack_bf16x2(QUANT ? fmaf(sp[r].x, wsc.x, a[r].x) : a[r].x + sp[r].x,
+                              QUANT ? fmaf(sp[r].y, wsc.y, a[r].y) : a[r].y + sp[r].y);
+            o.y = pack_bf16x2(QUANT ? fmaf(sp[r].z, wsc.z, a[r].z) : a[r].z + sp[r].z,
+                              QUANT ? fmaf(sp[r].w, wsc.w, a[r].w) : a[r].w + sp[r].w);
+            *reinterpret_cast<uint2 *>(pt.out() + static_cast<size_t>(m) * pt.ldo() + nn0) = o;
+        }
+    }
+}
+
 template <bool SWAP, int BN, bool PAIR = false, bool QUANT = false>
 __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, const uint8_t *sQ, uint64_t *full,
                                              uint64_t *conv, uint64_t *tmem_full, uint64_t *tmem_empty,
@@ -657,44 +715,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
                     const int32_t per = (BN + p.splits - 1) / p.splits;
                     const int32_t e_begin = w.ks * per;
                     const int32_t e_end = min(BN, e_begin + per);
-                    const int n_local = et % kBM;
-                    const int32_t nn = pt.ta * kBM + n_local;
-                    const float *first = p.part + tile * kTileElems + n_local;
-                    const size_t split_stride = tiles * kTileElems;
-#pragma unroll 1
-                    for (int32_t e0 = e_begin + et / kBM; e0 < e_end; e0 += 4 * (kEpiThreads / kBM)) {
-                        float a[4];
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int32_t e = e0 + v * (kEpiThreads / kBM);
-                            const int32_t m = w.tb * BN + e;
-                            a[v] = (e < e_end && m < p.M && nn < pt.N())
-                                       ? __ldcg(pt.ycorr() + static_cast<size_t>(m) * pt.N() + nn)
-                                       : 0.0f;
-                        }
-                        float sp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-                        for (int32_t ks = 0; ks < p.splits; ++ks) {
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                const int32_t e = e0 + v * (kEpiThreads / kBM);
-                                if (e < e_end) sp[v] += __ldcg(first + ks * split_stride + e * kBM);
-                            }
-                        }
-                        // the int8 W row's scale multiplies the base sum only
-                        const float wsc = QUANT ? (nn < pt.N() ? __ldg(p.w_scale + nn) : 0.0f) : 1.0f;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) a[v] = QUANT ? fmaf(sp[v], wsc, a[v]) : a[v] + sp[v];
-                        if (nn < pt.N()) {
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                const int32_t e = e0 + v * (kEpiThreads / kBM);
-                                const int32_t m = w.tb * BN + e;
-                                if (e < e_end && m < p.M)
-                                    pt.out()[static_cast<size_t>(m) * pt.ldo() + nn] = __float2bfloat16_rn(a[v]);
-                            }
-                        }
-                    }
+                    finish_split_vec4<BN, PAIR, QUANT>(p, pt, w.tb, p.part + tile * kTileElems, tiles * kTileElems,
+                                                       e_begin, e_end, et);
                 }
             }
         } else {
@@ -1814,11 +1836,13 @@ TcPlan plan_tc(int32_t M, int32_t N, int32_t K) {
     t.num_kb = (K + kBK - 1) / kBK;
     t.swap = M <= 512;
     if (t.swap) {
-        // tokens per tile: 256 above 256 tokens (an MMA of 128 W rows x 256
-        // tokens needs less shared-memory operand bandwidth per flop than 128
-        // x 128; measured 78 -> 75 us on 512 x 5120 -> 13824, while 256 tokens
-        // in one tile lost to two of 128 on 8192 -> 8192)
-        t.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 256 ? 128 : 256;
+        // tokens per tile: 256 above 128 tokens.  An MMA of 128 W rows x 256
+        // tokens issues half the instructions per flop of 128 x 128 (the MMA
+        // warp, not the loads, sets the pace of 128 x 128 tiles), and one
+        // token tile reads each W row once: the 70B q+v call (256 tokens,
+        // 8192 -> 9216, split-K 2) went 78.3 -> 74.1 us per step once the
+        // split-K finish kept several loads in flight per thread
+        t.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
         t.tiles_a = (N + kBM - 1) / kBM;
         t.tiles_b = (M + t.bn - 1) / t.bn;
         swapped_splits(&t, sms);

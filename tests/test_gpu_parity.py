@@ -128,11 +128,13 @@ def test_integer_exact_large_m_tile_fallback(mode):
 
 
 @pytest.mark.parametrize("shape", [(64, 2048, (264, 520)), (37, 1024, (1032,)), (700, 192, (136,)),
-                                   (448, 320, (2064,))])
+                                   (448, 320, (2064,)), (200, 2048, (1032,)), (256, 4096, (520, 264))])
 def test_integer_exact_split_k_and_orientations(shape):
     """Bit-exact through the split-K reduction (few tokens, long K: several
     CTAs share each output tile), the swapped orientation near its row
-    limit (448 tokens) and the non-swapped orientation (many tokens)."""
+    limit (448 tokens) and the non-swapped orientation (many tokens); 200
+    and 256 tokens take one 256-token tile (a ragged token tail, and two
+    projections in one launch)."""
     M, K, Ns = shape
     wl = synth(M=M, K=K, Ns=list(Ns), num_slots=6, rank_choices=(4, 16, 32), integer=True,
                seed=M + K, none_frac=0.2)
