@@ -184,6 +184,8 @@ struct TcPlan {
     bool swap;            // W rows on the TMEM lanes, tokens as the MMA's N
     int bn;               // MMA N (tokens when swapped, output columns otherwise)
     int num_kb, kb_per_split, splits;
+    int full_units;       // units that are whole tiles (the rest: split_tiles tiles in `splits` K ranges)
+    int split_tiles;
     int tiles_a, tiles_b, units, grid;
     size_t part_bytes, counter_bytes;  // split-K partial tiles and tile counters
 };

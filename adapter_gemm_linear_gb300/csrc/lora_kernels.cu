@@ -430,7 +430,7 @@ static cudaError_t launch_forward_fused_rows(const ForwardPlan &plan, cudaStream
         if (i > 0 && (e = record(1 + 2 * i)) != cudaSuccess) return e;
         const TcPlan tp = pair ? plan_tc_pair(plan.M, plan.proj[i].N, plan.proj[i + 1].N, plan.K)
                                : plan_tc(plan.M, plan.proj[i].N, plan.K);
-        const int64_t ntiles = tp.splits > 1 ? static_cast<int64_t>(tp.tiles_a) * tp.tiles_b : 0;
+        const int64_t ntiles = tp.split_tiles;
         if (coff + ntiles > plan.n_counters) return cudaErrorInvalidValue;
         e = launch_gemm_lora_tc_pair(plan, plan.proj[i], pair ? &plan.proj[i + 1] : nullptr, plan.counters + coff,
                                      plan.n_counters - coff, stream);

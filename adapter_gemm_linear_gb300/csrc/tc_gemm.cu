@@ -79,6 +79,9 @@ constexpr int kTaBand = 8;             // non-swapped unit order: token tiles pe
 struct TcParams {
     int32_t M, N, K;
     int32_t num_kb, kb_per_split, splits;
+    // units [0, full_units) are whole tiles over all of K; the rest are the
+    // split_tiles tiles after them, each in `splits` K ranges (split-K)
+    int32_t full_units, split_tiles;
     int32_t tiles_a, tiles_b, num_units;
     __nv_bfloat16 *out;
     int32_t ldo;
@@ -177,17 +180,26 @@ struct Cfg {
 
 struct Unit {
     int32_t ta, tb, ks;
+    int32_t st;  // split-K: the tile's index among the split tiles; -1: the unit is the whole tile
 };
 
 // Units are numbered with the split fastest; for the swapped orientation the
 // token tiles of one W tile come next (so they run at the same time and share
 // the W tile through L2), for the non-swapped one the x tiles of one W tile
-// within a band of kTaBand token tiles.
+// within a band of kTaBand token tiles.  The first full_units units are whole
+// tiles; the split tiles follow them.
 template <bool SWAP>
 __device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
     Unit w;
-    w.ks = u % p.splits;
-    const int32_t r = u / p.splits;
+    int32_t r = u;
+    w.ks = 0;
+    w.st = -1;
+    if (u >= p.full_units) {
+        const int32_t v = u - p.full_units;
+        w.ks = v % p.splits;
+        r = p.full_units + v / p.splits;
+        if (p.splits > 1) w.st = v / p.splits;
+    }
     if (SWAP) {
         w.tb = r % p.tiles_b;
         w.ta = r / p.tiles_b;
@@ -205,6 +217,12 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const TcParams &p) {
         w.tb = r / p.tiles_a;
     }
     return w;
+}
+
+// The k-blocks [kb0, kb1) of unit w.
+__device__ __forceinline__ void unit_kblocks(const TcParams &p, const Unit &w, int32_t *kb0, int32_t *kb1) {
+    *kb0 = w.st < 0 ? 0 : w.ks * p.kb_per_split;
+    *kb1 = w.st < 0 ? p.num_kb : min(*kb0 + p.kb_per_split, p.num_kb);
 }
 
 // Byte `j` of w as two signed int4 (low nibble first), converted exactly to
@@ -269,8 +287,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tma_a, const CUt
         const int32_t u = next_unit(p, idx);
         if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
-        const int32_t kb0 = w.ks * p.kb_per_split;
-        const int32_t kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+        int32_t kb0, kb1;
+        unit_kblocks(p, w, &kb0, &kb1);
         const int32_t nmain = kb1 - kb0;
         int32_t total = nmain;
         // swapped: the W tile's projection (its tensor map) and row
@@ -343,8 +361,8 @@ __device__ __forceinline__ void run_mma(const TcParams &p, uint8_t *sA, uint8_t 
         const int32_t u = next_unit(p, idx);
         if (u < 0) break;
         const Unit w = decode_unit<SWAP>(u, p);
-        const int32_t kb0 = w.ks * p.kb_per_split;
-        const int32_t kb_main = min(kb0 + p.kb_per_split, p.num_kb);
+        int32_t kb0, kb_main;
+        unit_kblocks(p, w, &kb0, &kb_main);
         int32_t kb1 = kb_main;
         const int b = t & 1;
         bool ok = mbar_wait_bounded(&tmem_empty[b], ((t >> 1) & 1) ^ 1, kWaitLimitNs);
@@ -566,8 +584,9 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
             // the bf16 A tile, laid out as a TMA load with the 128-byte
             // swizzle leaves it (16-byte chunk c of row r at chunk c ^ (r % 8)).
             // Thread et converts half hh of row r's 64 values.
-            const int32_t kb0 = w.ks * p.kb_per_split;
-            const int32_t nk = min(kb0 + p.kb_per_split, p.num_kb) - kb0;
+            int32_t kb0, kb1;
+            unit_kblocks(p, w, &kb0, &kb1);
+            const int32_t nk = kb1 - kb0;
             const int r = et >> 1, hh = et & 1;
             for (int32_t i = 0; i < nk; ++i, ++cit) {
                 const int s = cit % C::kStages;
@@ -618,7 +637,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
         float yc[SWAP ? kPre : 1][32];
         const ProjTile<PAIR> pt(p, w.ta);
         const int32_t n_sw = pt.ta * kBM + q * 32 + lane;
-        if (SWAP && p.splits == 1) {
+        if (SWAP && w.st < 0) {
             grid_dependency_wait();  // ycorr comes from the expand kernel
 #pragma unroll
             for (int ci = 0; ci < kPre; ++ci) {
@@ -642,7 +661,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
         if (SWAP) {
             const int32_t n = pt.ta * kBM + q * 32 + lane;
             const bool n_ok = n < pt.N();
-            if (p.splits == 1) {
+            if (w.st < 0) {
 #pragma unroll
                 for (int ci = 0; ci < kMyChunks; ++ci) {
                     const int c = grp + ci * kGroups;
@@ -682,10 +701,10 @@ __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, con
                 // partial tile to this split's slice; once every split of the
                 // tile has stored its slice, each sums the slices and the
                 // correction over its own range of the tile's tokens.  All
-                // splits of a tile run at once: split-K is planned only when
-                // the units fit in one wave of the grid.
-                const size_t tile = static_cast<size_t>(w.ta) * p.tiles_b + w.tb;
-                const size_t tiles = static_cast<size_t>(p.tiles_a) * p.tiles_b;
+                // splits of a tile run at once: the split units are the last
+                // round of the grid, one per CTA at most.
+                const size_t tile = static_cast<size_t>(w.st);
+                const size_t tiles = static_cast<size_t>(p.split_tiles);
                 constexpr size_t kTileElems = static_cast<size_t>(BN) * kBM;
                 float *mine = p.part + (w.ks * tiles + tile) * kTileElems + q * 32 + lane;
 #pragma unroll 1
@@ -1631,6 +1650,8 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
     p.num_kb = tp.num_kb;
     p.kb_per_split = tp.kb_per_split;
     p.splits = tp.splits;
+    p.full_units = tp.full_units;
+    p.split_tiles = tp.split_tiles;
     p.tiles_a = tp.tiles_a;
     p.tiles_b = tp.tiles_b;
     p.num_units = tp.units;
@@ -1673,9 +1694,10 @@ cudaError_t launch_variant(const ForwardPlan &plan, const ProjView &v, const TcP
         p.ycorr1 = v1->ycorr;
     }
     // the splits of a tile wait for one another, so they must all be resident:
-    // split-K needs every unit in the first wave of the grid
-    if (tp.splits > 1 && (!plan.part || !p.counters || tp.units > tp.grid ||
-                          n_counters < static_cast<int64_t>(tp.tiles_a) * tp.tiles_b))
+    // the split units form the grid's last round (whole rounds of whole
+    // tiles before them), at most one per CTA
+    if (tp.splits > 1 && (!plan.part || !p.counters || tp.full_units % tp.grid != 0 ||
+                          tp.units - tp.full_units > tp.grid || n_counters < tp.split_tiles))
         return cudaErrorInvalidValue;
     // programmatic dependent of the shrink kernel before it on the stream:
     // the CTAs may start (and stream W and x) while the shrink finishes; the
@@ -1747,6 +1769,8 @@ cudaError_t launch_pair_gemm(const ForwardPlan &plan, const ProjView &v, cudaStr
     p.num_kb = (plan.K + kBK - 1) / kBK;
     p.kb_per_split = p.num_kb;
     p.splits = 1;
+    p.full_units = 0;
+    p.split_tiles = 0;
     p.tiles_a = (plan.M + kPairM - 1) / kPairM;
     p.tiles_b = (v.N + BN - 1) / BN;
     p.num_units = p.tiles_a * p.tiles_b;
@@ -1809,24 +1833,39 @@ int device_sm_count() {
     return cache[dev];
 }
 
-// Split-K of the swapped orientation: enough splits to give every SM a unit,
-// each at least four k-blocks long, at most 16.
+// Split-K of the swapped orientation, each split at least four k-blocks
+// long, at most 16: with fewer tiles than SMs, enough splits to give every
+// SM a unit; with more, whole rounds of whole tiles and then, when the last
+// round would leave at least half of the SMs idle, its tiles split along K
+// over all of them (every CTA takes at most one split unit, so the splits of
+// a tile are resident together).
 static void swapped_splits(TcPlan *t, int sms) {
     const int tiles = t->tiles_a * t->tiles_b;
-    int s = tiles >= sms ? 1 : sms / tiles;
-    s = s < 1 ? 1 : s;
+    const int left = tiles % sms;
+    int s = 1;
+    t->full_units = 0;
+    if (tiles < sms) {
+        s = sms / tiles;
+    } else if (left != 0 && 2 * left <= sms) {
+        s = sms / left;
+        t->full_units = tiles - left;
+    }
     const int max_s = t->num_kb / 4 > 0 ? t->num_kb / 4 : 1;
     if (s > max_s) s = max_s;
     if (s > 16) s = 16;
+    if (s < 1) s = 1;
     t->kb_per_split = (t->num_kb + s - 1) / s;
     t->splits = (t->num_kb + t->kb_per_split - 1) / t->kb_per_split;
+    if (t->splits == 1) t->full_units = 0;
 }
 
 static void finish_plan(TcPlan *t, int sms) {
-    t->units = t->tiles_a * t->tiles_b * t->splits;
+    const int tiles = t->tiles_a * t->tiles_b;
+    t->split_tiles = t->splits > 1 ? tiles - t->full_units : 0;
+    t->units = t->full_units + (tiles - t->full_units) * t->splits;
     t->grid = t->units < sms ? t->units : sms;
-    t->part_bytes = t->splits > 1 ? sizeof(float) * static_cast<size_t>(t->splits) * t->tiles_a * t->tiles_b * t->bn * kBM : 0;
-    t->counter_bytes = t->splits > 1 ? sizeof(int32_t) * static_cast<size_t>(t->tiles_a) * t->tiles_b : 0;
+    t->part_bytes = sizeof(float) * static_cast<size_t>(t->splits) * t->split_tiles * t->bn * kBM;
+    t->counter_bytes = sizeof(int32_t) * static_cast<size_t>(t->split_tiles);
 }
 
 // Orientation, tile width and split-K factor for an M x N x K problem.
