@@ -222,6 +222,7 @@ def test_integer_exact_many_tiles(shape):
     ((128, 1024, (256, 512, 264)), 3),         # a pair and a single GEMM launch, both split-K (own tile counters)
     ((256, 2048, (1024, 1040, 512, 520)), 3),  # two pairs
     ((448, 512, (4096, 1024)), 2),             # a pair with 256-token tiles
+    ((300, 1024, (8192, 2048)), 2),            # a pair with more tiles than SMs: the last round split along K
 ])
 def test_fused_projection_launches(shape, launches, mode):
     """Several projections whose LoRA terms go through the per-row kernel:
