@@ -475,21 +475,28 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     // after the other on the stream)
     // With the fused per-row path every projection keeps its own correction
     // array and each GEMM launch (two projections) its own tile counters.
+    // With the pipelined pairs every projection keeps its own correction array
+    // and the pairs' GEMM launches, one after the other, share the counters.
     size_t part = 0, cnt = 0, ycorr = 0;
     plan->fused_rows = false;
+    plan->piped_pairs = false;
     if (a->dtype == LORA_BF16 && a->M > 0) {
         int32_t Ns[LORA_MAX_PROJ], ranks[LORA_MAX_PROJ];
+        bool any_quant = false;
         for (int i = 0; i < a->n_proj; ++i) {
             Ns[i] = a->proj[i].pool->d.N;
             ranks[i] = a->proj[i].pool->d.max_rank;
+            any_quant = any_quant || a->proj[i].w_scale != nullptr;
         }
         plan->fused_rows = lora::fuse_row_projections(a->M, a->K, a->n_proj, Ns, ranks);
-        if (plan->fused_rows) {
+        plan->piped_pairs =
+            !plan->fused_rows && lora::pipe_pair_projections(a->M, a->K, a->n_proj, Ns, ranks, any_quant);
+        if (plan->fused_rows || plan->piped_pairs) {
             for (int i = 0; i < a->n_proj; i += 2) {
                 const lora::TcPlan tp = i + 1 < a->n_proj ? lora::plan_tc_pair(a->M, Ns[i], Ns[i + 1], a->K)
                                                           : lora::plan_tc(a->M, Ns[i], a->K);
                 part = std::max(part, tp.part_bytes);
-                cnt += tp.counter_bytes;
+                cnt = plan->fused_rows ? cnt + tp.counter_bytes : std::max(cnt, tp.counter_bytes);
             }
             for (int i = 0; i < a->n_proj; ++i)
                 ycorr += align_up(sizeof(float) * static_cast<size_t>(a->M) * Ns[i], 256);
@@ -580,7 +587,8 @@ static lora_status_t linear_forward(const lora_forward_args_t *args, void *strea
     {
         size_t yoff = ws.ycorr_off;
         for (int i = 0; i < plan.n_proj; ++i) {
-            plan.proj[i].ycorr = reinterpret_cast<float *>(base + (plan.fused_rows ? yoff : ws.ycorr_off));
+            plan.proj[i].ycorr =
+                reinterpret_cast<float *>(base + (plan.fused_rows || plan.piped_pairs ? yoff : ws.ycorr_off));
             yoff += align_up(sizeof(float) * static_cast<size_t>(plan.M) * plan.proj[i].N, 256);
         }
     }

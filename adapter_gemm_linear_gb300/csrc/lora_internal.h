@@ -153,6 +153,10 @@ struct ForwardPlan {
     // of it for all projections (each its own ycorr), then the GEMMs two
     // projections per launch (each launch its own split-K counters)
     bool fused_rows;
+    // small M, every projection's LoRA term by the pipelined grouped kernels:
+    // the projections two at a time, both LoRA terms (each its own ycorr) and
+    // then one GEMM launch for the two
+    bool piped_pairs;
     // lora_test_arm_wait_timeout: 0, or the time limit of this call's split-K
     // counter waits, which then wait for one arrival more than any launch makes
     uint64_t test_wait_limit_ns;
@@ -240,6 +244,11 @@ cudaError_t launch_expand_grouped(const ForwardPlan &plan, const ProjView &v, co
 // of V with rows in sorted order, the expand plan.ycorr.  For M <=
 // kPipeMaxRows and pools of max_rank <= kPipeMaxRank.
 bool pipe_grouped_supported(int32_t M, int32_t max_rank);
+// Whether a call of n projections takes the pipelined kernels with the GEMMs
+// two projections per launch (ForwardPlan::piped_pairs): small M, LoRA terms
+// not all for the per-row kernel, every pool within the pipelined kernels'
+// rank limit, no quantized base weights.
+bool pipe_pair_projections(int32_t M, int32_t K, int n, const int32_t *N, const int32_t *max_rank, bool any_quant);
 // The rows grouped by adapter once per forward for every projection (one CTA
 // each, into plan.pipe_groups), read by both pipelined kernels.
 size_t pipe_group_bytes();

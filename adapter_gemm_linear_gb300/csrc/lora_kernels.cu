@@ -443,6 +443,41 @@ static cudaError_t launch_forward_fused_rows(const ForwardPlan &plan, cudaStream
     return cudaSuccess;
 }
 
+// Several projections whose LoRA terms go through the pipelined grouped
+// kernels: the rows grouped once, then the projections two at a time -- each
+// one's shrink and expand (its own ycorr) and one GEMM launch for the pair, a
+// programmatic dependent of the second expand.  The split-K counters are
+// shared: every shrink zeroes them after the launch before it has ended.
+// Stage events: each projection's LoRA stage covers its shrink and expand,
+// the GEMM stage of the second of a pair the pair's launch (the first's is
+// empty).
+static cudaError_t launch_forward_piped_pairs(const ForwardPlan &plan, cudaStream_t stream) {
+    auto record = [&](int i) -> cudaError_t {
+        return plan.stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[i]), stream)
+                                 : cudaSuccess;
+    };
+    cudaError_t e = launch_pipe_group(plan, stream);
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    for (int i = 0; i < plan.n_proj; i += 2) {
+        const bool pair = i + 1 < plan.n_proj;
+        for (int q = i; q <= (pair ? i + 1 : i); ++q) {
+            e = launch_pipe_shrink(plan, plan.proj[q], stream);
+            if (e == cudaSuccess) e = launch_pipe_expand(plan, plan.proj[q], stream);
+            if (e != cudaSuccess) return e;
+            count_launches(2);
+            if ((e = record(1 + 2 * q)) != cudaSuccess) return e;
+            if (q == i && pair && (e = record(2 + 2 * q)) != cudaSuccess) return e;
+        }
+        e = launch_gemm_lora_tc_pair(plan, plan.proj[i], pair ? &plan.proj[i + 1] : nullptr, plan.counters,
+                                     plan.n_counters, stream);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        if ((e = record(pair ? 4 + 2 * i : 2 + 2 * i)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 // bf16.  Small M (the GEMM's swapped orientation): per projection the LoRA
 // term into plan.ycorr (lora_grouped.cu) -- by one per-row kernel when each
 // row's A and B are cheap to read, else by the pipelined grouped shrink and
@@ -455,6 +490,7 @@ static cudaError_t launch_forward_fused_rows(const ForwardPlan &plan, cudaStream
 static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t stream) {
     const bool swapped = plan_tc(plan.M, plan.proj[0].N, plan.K).swap;
     if (plan.fused_rows) return launch_forward_fused_rows(plan, stream);
+    if (plan.piped_pairs) return launch_forward_piped_pairs(plan, stream);
     bool by_row = swapped;
     for (int p = 0; p < plan.n_proj; ++p)
         by_row = by_row && row_lora_preferred(plan.M, plan.K, plan.proj[p].N, plan.proj[p].max_rank);

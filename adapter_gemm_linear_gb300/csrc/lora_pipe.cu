@@ -958,6 +958,16 @@ __global__ void __launch_bounds__(kExpThreads, 1) pipe_expand_kernel(const PipeE
 
 bool pipe_grouped_supported(int32_t M, int32_t max_rank) { return M <= kPipeMaxRows && max_rank <= kPipeMaxRank; }
 
+bool pipe_pair_projections(int32_t M, int32_t K, int n, const int32_t *N, const int32_t *max_rank, bool any_quant) {
+    if (n < 2 || any_quant || M <= 0 || !plan_tc(M, N[0], K).swap) return false;
+    bool all_rows = true;
+    for (int i = 0; i < n; ++i) {
+        if (!pipe_grouped_supported(M, max_rank[i])) return false;
+        all_rows = all_rows && row_lora_preferred(M, K, N[i], max_rank[i]);
+    }
+    return !all_rows;
+}
+
 namespace {
 
 // Persistent grid of one CTA per SM, launched as a programmatic dependent of

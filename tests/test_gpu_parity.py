@@ -203,6 +203,33 @@ def test_pipelined_grouped_integer_exact():
         assert np.array_equal(got, want), f"projection {p}: {np.sum(got != want)} outputs differ"
 
 
+@pytest.mark.parametrize("mode", ["bgmv", "sgmv"])
+@pytest.mark.parametrize("shape, launches", [
+    ((300, 4096, (1032, 264)), 6),          # one pair: the grouping, two shrinks and expands, one GEMM
+    ((256, 4096, (2048, 512, 520)), 9),     # a pair and a single projection
+])
+def test_pipelined_projection_pairs(shape, launches, mode):
+    """Several projections whose LoRA terms go through the pipelined kernels:
+    the rows grouped once, each projection's shrink and expand into its own
+    correction array, then one GEMM launch per two projections (SGMV adds
+    the segments-to-rows kernel).  Integer inputs: every projection
+    bit-exact."""
+    from adapter_gemm_linear_gb300 import kernel_launches
+    M, K, Ns = shape
+    wl = synth(M=M, K=K, Ns=list(Ns), num_slots=11, rank_choices=(16, 64, 128), integer=True, seed=M + K,
+               none_frac=0.1, zipf_s=1.2)
+    pools = H.make_pools(wl, DEV)
+    H.forward(wl, pools, mode)
+    torch.cuda.synchronize()
+    before = kernel_launches()
+    outs = H.forward(wl, pools, mode)
+    assert kernel_launches() - before == launches + (1 if mode == "sgmv" else 0)
+    for p in range(len(Ns)):
+        want = H.oracle_bf16_bits(H.oracle_rows(wl, p))
+        got = torch.from_numpy(outs[p]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), f"{shape} projection {p}: {np.sum(got != want)} outputs differ"
+
+
 @pytest.mark.parametrize("shape", [(300, 1024, 9856), (400, 2056, 9992)])
 def test_integer_exact_many_tiles(shape):
     """Swapped GEMM with 256-token tiles and more tiles than SMs (a short last
