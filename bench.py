@@ -31,7 +31,10 @@ with pinned host buffers: the host->device copy of x and the row ids and the
 device->host copy of the outputs are inside each timed step, all on one
 stream of the caller's (not the legacy default stream).  The step is captured
 in a CUDA graph and replayed (`e2e.value`); issued from the host call by call
-it gives `e2e.eager_value`.
+it gives `e2e.eager_value`.  `e2e.streamed_value` streams the steps as a
+serving loop would: two buffer sets, the copy-in of step i + 1 and the
+copy-out of step i - 1 on streams of their own beside the forward of step i,
+timed from the first copy-in to the last copy-out.
 
 --impl reference times the float64 CPU oracle on the host cores on a bounded
 row sample of the same workload (the reference arm of this comparison).
@@ -303,16 +306,16 @@ def build_case(wl, device, w_bits=0):
     if w_bits:  # symmetric per-row int8 / int4 of the same weights
         Ws = [(Int8Weight if w_bits == 8 else Int4Weight).quantize(W) for W in Ws]
     outs = [torch.empty((wl.M, p.N), dtype=td, device=device) for p in wl.projections]
+    seg = None
     if wl.mode == "sgmv":
-        offs = torch.from_numpy(wl.seg_offsets).to(device)
-        adp = torch.from_numpy(wl.seg_adapter).to(device)
-        call = LinearCall(x, list(zip(Ws, pools, outs)), seg_offsets=offs, seg_adapter=adp)
+        seg = (torch.from_numpy(wl.seg_offsets).to(device), torch.from_numpy(wl.seg_adapter).to(device))
+        call = LinearCall(x, list(zip(Ws, pools, outs)), seg_offsets=seg[0], seg_adapter=seg[1])
         ids = None
     else:
         ids = torch.from_numpy(wl.row_adapter).to(device)
         call = LinearCall(x, list(zip(Ws, pools, outs)), row_adapter=ids)
     torch.cuda.synchronize(device)
-    return {"pools": pools, "x": x, "Ws": Ws, "outs": outs, "ids": ids, "call": call}
+    return {"pools": pools, "x": x, "Ws": Ws, "outs": outs, "ids": ids, "seg": seg, "call": call}
 
 
 class L2Flush:
@@ -544,6 +547,70 @@ def time_e2e(case, wl, steps, flush, device):
     return {"ms": graph_ms, "eager_ms": eager_ms, "h2d": h2d, "d2h": d2h}
 
 
+def time_e2e_streamed(case, wl, steps):
+    """Through the C ABI with pinned host buffers, as a serving loop streams
+    its batches: two device buffer sets, the copy-in of step i + 1 (x and the
+    row ids) and the copy-out of step i - 1 (the outputs) on streams of their
+    own beside the forward of step i.  Every step moves its own bytes both
+    ways; the time runs from the first copy-in to the last copy-out."""
+    import torch
+    from adapter_gemm_linear_gb300 import LinearCall
+
+    x_host = torch.from_numpy(wl.x).to(case["x"].dtype).pin_memory()
+    ids_host = None if case["ids"] is None else torch.from_numpy(wl.row_adapter).pin_memory()
+    x1 = torch.empty_like(case["x"])
+    outs1 = [torch.empty_like(o) for o in case["outs"]]
+    if case["seg"] is not None:
+        call1 = LinearCall(x1, list(zip(case["Ws"], case["pools"], outs1)), seg_offsets=case["seg"][0],
+                           seg_adapter=case["seg"][1])
+        ids1 = None
+    else:
+        ids1 = torch.empty_like(case["ids"])
+        call1 = LinearCall(x1, list(zip(case["Ws"], case["pools"], outs1)), row_adapter=ids1)
+    bufs = [(case["x"], case["ids"], case["outs"], case["call"]), (x1, ids1, outs1, call1)]
+    outs_host = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in case["outs"]] for _ in range(2)]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    for s in (s_in, s_comp, s_out):
+        s.wait_stream(torch.cuda.current_stream())
+
+    def issue(i):
+        b = i % 2
+        x, ids, outs, call = bufs[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(comp_done[b])  # the forward two steps back has read x_b
+            x.copy_(x_host, non_blocking=True)
+            if ids is not None:
+                ids.copy_(ids_host, non_blocking=True)
+            in_done[b].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(in_done[b])
+            s_comp.wait_event(out_done[b])  # the copy-out two steps back has read outs_b
+            call()
+            comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            for o, oh in zip(outs, outs_host[b]):
+                oh.copy_(o, non_blocking=True)
+            out_done[b].record(s_out)
+
+    for i in range(4):
+        issue(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    for i in range(steps):
+        issue(i)
+    end.record(s_out)
+    end.synchronize()
+    ms = start.elapsed_time(end)
+    torch.cuda.synchronize()
+    torch.cuda.current_stream().wait_stream(s_out)
+    return ms
+
+
 def time_comparators(case, wl, flush, reps=20):
     """Context only: the same base GEMMs through torch.matmul (cuBLAS), and
     the whole layer as sequential passes in torch -- the base GEMM, then for
@@ -717,8 +784,10 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     shrink_ms = sum(res["shrink_ms"])
     e2e_steps = max(3, min(steps, 200))
     e2e = time_e2e(case, wl, e2e_steps, flush, device)
+    e2e_streamed_ms = time_e2e_streamed(case, wl, e2e_steps)
     loads = time_adapter_loads(wl, device) if world == 1 else None
-    total_ms, e2e_ms, e2e_eager_ms = max_over_ranks([total_ms, e2e["ms"], e2e["eager_ms"]], device)
+    total_ms, e2e_ms, e2e_eager_ms, e2e_streamed_ms = max_over_ranks(
+        [total_ms, e2e["ms"], e2e["eager_ms"], e2e_streamed_ms], device)
     if rank != 0:
         return None
 
@@ -800,7 +869,10 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
         "e2e": {"value": round(whole_job_rate(wl.M * e2e_steps, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "launch": "CUDA graph of the step (copies and forward) replayed per step",
-                "eager_value": round(whole_job_rate(wl.M * e2e_steps, world, e2e_eager_ms), 1)},
+                "eager_value": round(whole_job_rate(wl.M * e2e_steps, world, e2e_eager_ms), 1),
+                "streamed_value": round(whole_job_rate(wl.M * e2e_steps, world, e2e_streamed_ms), 1),
+                "streamed_launch": "two buffer sets; copy-in of step i+1 and copy-out of step i-1 on their "
+                                   "own streams beside the forward of step i"},
         "adapter_load": loads,
         "gpu_launches": int(res["launches"]),
         "kernels_per_step": int(res["kernels_per_call"]),
