@@ -64,6 +64,9 @@ PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_SOURCES = ["tc_gemm.cu", "sm100_ptx.cuh", "lora_device.cuh", "lora_internal.h", "tensor_map.cu", "tensor_map.h"]
+# the small-M LoRA stage's kernels and their launch sequence
+LORA_SOURCES = ["lora_pipe.cu", "lora_grouped.cu", "lora_kernels.cu", "sm100_ptx.cuh", "lora_device.cuh",
+                "lora_internal.h"]
 
 
 def parse_args():
@@ -96,26 +99,31 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def gemm_source_hash() -> str:
+def source_hash(names) -> str:
     h = hashlib.sha256()
-    for name in GEMM_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "adapter_gemm_linear_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """dram bytes per launch of the GEMM kernel from a committed ncu capture,
-    if it was taken on the current kernel source."""
+def gemm_source_hash() -> str:
+    return source_hash(GEMM_SOURCES)
+
+
+def ncu_traffic(workload: str, stage: str = "gemm"):
+    """dram bytes from a committed ncu capture, if it was taken on the
+    current kernel sources: per launch of the GEMM kernel (stage "gemm"), or
+    per forward summed over the small-M LoRA stage's kernels (stage "lora")."""
     try:
         with open(TRAFFIC_PATH) as f:
             entries = json.load(f)
     except (OSError, ValueError):
         return None
-    src = gemm_source_hash()
+    src = source_hash(GEMM_SOURCES if stage == "gemm" else LORA_SOURCES)
     for e in entries.get("entries", []):
-        if e.get("workload") == workload and e.get("source_hash") == src:
-            return e.get("dram_bytes_per_launch")
+        if e.get("workload") == workload and e.get("stage", "gemm") == stage and e.get("source_hash") == src:
+            return e.get("dram_bytes_per_launch" if stage == "gemm" else "dram_bytes_per_forward")
     return None
 
 
@@ -815,7 +823,12 @@ def run_gpu(cfg_name, args, rank, world, local_rank):
     else:
         roof = {"bound": "hbm", "achieved": round(b / t / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ncu_traffic(wl.name + (f"+int{w_bits}w" if w_bits else "")) if gemm_dominant else None
+    if gemm_dominant:
+        roof["traffic"] = ncu_traffic(wl.name + (f"+int{w_bits}w" if w_bits else ""))
+        roof["traffic_scope"] = "per launch of the GEMM kernel"
+    else:
+        roof["traffic"] = None if w_bits else ncu_traffic(wl.name, "lora")
+        roof["traffic_scope"] = "per forward, the LoRA stage's kernels summed"
     roof["kernel"] = kernel
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
     roof["algorithmic_bytes_per_call"] = b
