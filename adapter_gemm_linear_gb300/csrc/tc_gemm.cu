@@ -26,15 +26,19 @@
 //   non-swapped  (large M): the MMA's M = 128 token rows of x, its N = BN
 //                columns of W; TMEM lane = token, TMEM column = output column.
 //   swapped      (small M): the MMA's M = 128 rows of W (output columns), its
-//                N = BN tokens; TMEM lane = output column, column = token.  With
-//                few tokens this puts W's rows on the 128 lanes, and split-K
-//                spreads each tile's K range over several CTAs so that ~all
-//                SMs stream W.  The correction comes precomputed from the
-//                grouped expand kernel as an fp32 [M][N] array (ycorr) and is
-//                added before the rounding.  Under split-K each split stores its
-//                fp32 partial tile to an L2-resident slice and bumps a per-tile
-//                counter; when the count is complete every split sums the
-//                slices and ycorr over its own range of tokens and stores bf16.
+//                N = BN tokens (up to 256: one tile for up to 256 tokens, so
+//                each MMA instruction does the most work); TMEM lane = output
+//                column, column = token.  With few tokens this puts W's rows on
+//                the 128 lanes, and split-K spreads each tile's K range over
+//                several CTAs so that ~all SMs stream W; with more tiles than
+//                SMs only the last round's tiles are split, over all of them.
+//                The correction comes precomputed from the LoRA kernels as an
+//                fp32 [M][N] array (ycorr) and is added before the rounding.
+//                Under split-K each split stores its fp32 partial tile to an
+//                L2-resident slice and bumps a per-tile counter; when the count
+//                is complete every split sums the slices and ycorr over its own
+//                range of tokens (four columns per thread, several tokens'
+//                loads in flight) and stores bf16.
 // Warp roles:
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per
 //               k-block into a shared-memory ring (128-byte swizzle);
@@ -498,9 +502,6 @@ __device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&acc)[32]
     for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(raw[e]);
 }
 
-// Epilogue warps: warp w (2..2+kEpiWarps-1) may access TMEM lane quarter
-// w % 4; the kEpiWarps / 4 warps sharing a quarter take turns over the
-// 32-column chunks.
 // Split-K finish of the swapped orientation: each thread sums four adjacent
 // output columns (16-byte loads of the tile's partial slices and of the
 // correction; N and ldo are multiples of 8, which the host checks), the
@@ -559,6 +560,9 @@ __device__ __forceinline__ void finish_split_vec4(const TcParams &p, const ProjT
     }
 }
 
+// Epilogue warps: warp w (2..2+kEpiWarps-1) may access TMEM lane quarter
+// w % 4; the kEpiWarps / 4 warps sharing a quarter take turns over the
+// 32-column chunks.
 template <bool SWAP, int BN, bool PAIR = false, bool QUANT = false>
 __device__ __forceinline__ void run_epilogue(const TcParams &p, uint8_t *sA, const uint8_t *sQ, uint64_t *full,
                                              uint64_t *conv, uint64_t *tmem_full, uint64_t *tmem_empty,
