@@ -462,19 +462,13 @@ def time_device(case, wl, steps, warmup, flush, clocks_index):
             "launches": kernels_per_call * steps, "kernels_per_call": kernels_per_call, "clocks": clocks}
 
 
-def time_adapter_loads(wl, device, reps=8):
-    """Pool residency: time to load one adapter of the workload's largest
-    rank into a slot of its first projection's pool shape, by source --
-    staged pageable host memory (synchronous), page-locked host memory read
-    by the scatter kernel over the host link (asynchronous), and device
-    memory.  Each load is followed by an unload; times are medians."""
+def _time_loads(K, N, r, td, device, reps):
+    """Median load time of one rank-r adapter (K -> N) into a pool slot from
+    each source; every load is followed by an unload."""
     import torch
     from adapter_gemm_linear_gb300 import LoraPool
 
-    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
-    K, N = wl.K, wl.projections[0].N
-    r = max(16, -(-int(wl.ranks.max()) // 16) * 16)
-    nbytes = r * (K + N) * (2 if wl.dtype == "bf16" else 4)
+    nbytes = r * (K + N) * (2 if td == torch.bfloat16 else 4)
     pool = LoraPool(K, N, 2, r, r // 16, dtype=td, device=device)
     gen = torch.Generator().manual_seed(7)
     A = (torch.randn(r, K, generator=gen) * 0.02).to(td)
@@ -496,6 +490,24 @@ def time_adapter_loads(wl, device, reps=8):
         out[name] = {"ms": round(med, 4), "gbs": round(nbytes / (med / 1e3) / 1e9, 2)}
     torch.cuda.synchronize()
     pool.close()
+    return out
+
+
+def time_adapter_loads(wl, device, reps=8):
+    """Pool residency: time to load one adapter of the workload's largest
+    rank into a slot of its first projection's pool shape, by source --
+    staged pageable host memory (synchronous), page-locked host memory read
+    by the scatter kernel over the host link (asynchronous), and device
+    memory -- and the same for an adapter of the residency page's size
+    (rank 1024 on an 8192 -> 28672 projection, 75.5 MB)."""
+    import torch
+
+    td = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    r = max(16, -(-int(wl.ranks.max()) // 16) * 16)
+    out = _time_loads(wl.K, wl.projections[0].N, r, td, device, reps)
+    big = _time_loads(8192, 28672, 1024, torch.bfloat16, device, reps)
+    big["shape"] = "rank 1024, 8192 -> 28672"
+    out["page_scale"] = big
     return out
 
 
