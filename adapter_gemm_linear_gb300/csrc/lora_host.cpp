@@ -475,8 +475,8 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
     // after the other on the stream)
     // With the fused per-row path every projection keeps its own correction
     // array and each GEMM launch (two projections) its own tile counters.
-    // With the pipelined pairs every projection keeps its own correction array
-    // and the pairs' GEMM launches, one after the other, share the counters.
+    // So does the pipelined path with several projections (one LoRA launch
+    // for all of them, then the GEMMs two projections per launch).
     size_t part = 0, cnt = 0, ycorr = 0;
     plan->fused_rows = false;
     plan->piped_pairs = false;
@@ -496,7 +496,7 @@ static lora_status_t plan_forward(const lora_forward_args_t *a, lora::ForwardPla
                 const lora::TcPlan tp = i + 1 < a->n_proj ? lora::plan_tc_pair(a->M, Ns[i], Ns[i + 1], a->K)
                                                           : lora::plan_tc(a->M, Ns[i], a->K);
                 part = std::max(part, tp.part_bytes);
-                cnt = plan->fused_rows ? cnt + tp.counter_bytes : std::max(cnt, tp.counter_bytes);
+                cnt += tp.counter_bytes;
             }
             for (int i = 0; i < a->n_proj; ++i)
                 ycorr += align_up(sizeof(float) * static_cast<size_t>(a->M) * Ns[i], 256);

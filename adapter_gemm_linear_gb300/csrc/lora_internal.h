@@ -154,8 +154,9 @@ struct ForwardPlan {
     // projections per launch (each launch its own split-K counters)
     bool fused_rows;
     // small M, every projection's LoRA term by the pipelined grouped kernels:
-    // the projections two at a time, both LoRA terms (each its own ycorr) and
-    // then one GEMM launch for the two
+    // one shrink and one expand launch for all projections (each its own
+    // ycorr), then the GEMMs two projections per launch (each launch its own
+    // split-K counters)
     bool piped_pairs;
     // lora_test_arm_wait_timeout: 0, or the time limit of this call's split-K
     // counter waits, which then wait for one arrival more than any launch makes
@@ -253,8 +254,11 @@ bool pipe_pair_projections(int32_t M, int32_t K, int n, const int32_t *N, const 
 // each, into plan.pipe_groups), read by both pipelined kernels.
 size_t pipe_group_bytes();
 cudaError_t launch_pipe_group(const ForwardPlan &plan, cudaStream_t stream);
-cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
-cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream);
+// The pipelined shrink (expand) of projections vs[0..n) (elements of
+// plan.proj) in one launch, the SMs split between them by the bytes of A (B)
+// a row's adapter brings at most.
+cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView *const *vs, int n, cudaStream_t stream);
+cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView *const *vs, int n, cudaStream_t stream);
 
 // Tensor-core base GEMM with the fused expand epilogue (tc_gemm.cu), bf16.
 TcPlan plan_tc(int32_t M, int32_t N, int32_t K);

@@ -444,35 +444,40 @@ static cudaError_t launch_forward_fused_rows(const ForwardPlan &plan, cudaStream
 }
 
 // Several projections whose LoRA terms go through the pipelined grouped
-// kernels: the rows grouped once, then the projections two at a time -- each
-// one's shrink and expand (its own ycorr) and one GEMM launch for the pair, a
-// programmatic dependent of the second expand.  The split-K counters are
-// shared: every shrink zeroes them after the launch before it has ended.
-// Stage events: each projection's LoRA stage covers its shrink and expand,
-// the GEMM stage of the second of a pair the pair's launch (the first's is
-// empty).
+// kernels: the rows grouped once, one shrink and one expand launch for all of
+// them (the SMs split between the projections, each its own ycorr), then the
+// GEMMs two projections per launch, each launch a programmatic dependent of
+// the kernel before it with its own split-K tile counters (all zeroed by the
+// shrink).  Stage events: the LoRA stage of projection 0 covers the LoRA
+// launches, the GEMM stage of the second of a pair the pair's launch; the
+// other stages are empty.
 static cudaError_t launch_forward_piped_pairs(const ForwardPlan &plan, cudaStream_t stream) {
     auto record = [&](int i) -> cudaError_t {
         return plan.stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(plan.stage_events[i]), stream)
                                  : cudaSuccess;
     };
+    const ProjView *vs[LORA_MAX_PROJ];
+    for (int q = 0; q < plan.n_proj; ++q) vs[q] = &plan.proj[q];
     cudaError_t e = launch_pipe_group(plan, stream);
+    if (e == cudaSuccess) e = launch_pipe_shrink(plan, vs, plan.n_proj, stream);
+    if (e == cudaSuccess) e = launch_pipe_expand(plan, vs, plan.n_proj, stream);
     if (e != cudaSuccess) return e;
-    count_launches(1);
+    count_launches(3);
+    if ((e = record(1)) != cudaSuccess) return e;
+    int64_t coff = 0;
     for (int i = 0; i < plan.n_proj; i += 2) {
         const bool pair = i + 1 < plan.n_proj;
-        for (int q = i; q <= (pair ? i + 1 : i); ++q) {
-            e = launch_pipe_shrink(plan, plan.proj[q], stream);
-            if (e == cudaSuccess) e = launch_pipe_expand(plan, plan.proj[q], stream);
-            if (e != cudaSuccess) return e;
-            count_launches(2);
-            if ((e = record(1 + 2 * q)) != cudaSuccess) return e;
-            if (q == i && pair && (e = record(2 + 2 * q)) != cudaSuccess) return e;
-        }
-        e = launch_gemm_lora_tc_pair(plan, plan.proj[i], pair ? &plan.proj[i + 1] : nullptr, plan.counters,
-                                     plan.n_counters, stream);
+        if (i > 0 && (e = record(1 + 2 * i)) != cudaSuccess) return e;
+        if (pair && ((e = record(2 + 2 * i)) != cudaSuccess || (e = record(3 + 2 * i)) != cudaSuccess)) return e;
+        const TcPlan tp = pair ? plan_tc_pair(plan.M, plan.proj[i].N, plan.proj[i + 1].N, plan.K)
+                               : plan_tc(plan.M, plan.proj[i].N, plan.K);
+        const int64_t ntiles = tp.split_tiles;
+        if (coff + ntiles > plan.n_counters) return cudaErrorInvalidValue;
+        e = launch_gemm_lora_tc_pair(plan, plan.proj[i], pair ? &plan.proj[i + 1] : nullptr, plan.counters + coff,
+                                     plan.n_counters - coff, stream);
         if (e != cudaSuccess) return e;
         count_launches(1);
+        coff += ntiles;
         if ((e = record(pair ? 4 + 2 * i : 2 + 2 * i)) != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -517,8 +522,9 @@ static cudaError_t launch_forward_tc(const ForwardPlan &plan, cudaStream_t strea
             e = launch_lora_rows(plan, v, stream);
             if (e != cudaSuccess) return e;
         } else if (piped) {
-            e = launch_pipe_shrink(plan, v, stream);
-            if (e == cudaSuccess) e = launch_pipe_expand(plan, v, stream);
+            const ProjView *one[1] = {&v};
+            e = launch_pipe_shrink(plan, one, 1, stream);
+            if (e == cudaSuccess) e = launch_pipe_expand(plan, one, 1, stream);
             if (e != cudaSuccess) return e;
         } else if (swapped) {
             e = launch_shrink_grouped(plan, v, gt, stream);

@@ -28,6 +28,9 @@
 //   * Each CTA takes a contiguous share of the work items balanced by cost:
 //     shrink items (chunk, rank block, K slice) cost the same; expand items
 //     (chunk, 1024 columns) cost by their rank blocks and rows.
+//   * One launch of each kernel serves every projection of the call: the
+//     CTAs are split between the projections by the bytes of A (B) a row's
+//     adapter brings, and each projection's CTAs share out its items.
 //
 // Every mbarrier wait is bounded (kDevTimeout), and a CTA that gave up waits,
 // again bounded, for its bulk copies in flight before it exits.
@@ -359,12 +362,35 @@ struct PipeShrinkParams {
     unsigned long long *status;
 };
 
+// One launch of a pipelined kernel over several projections of the same x:
+// CTAs [cta_begin[q], cta_begin[q + 1]) serve projection q, each with its own
+// parameters (pool, V, ycorr, grouping table).
+template <typename P>
+struct PipeMulti {
+    P proj[LORA_MAX_PROJ];
+    int32_t n_proj;
+    int32_t cta_begin[LORA_MAX_PROJ + 1];
+};
+
+// This CTA's projection, its index among that projection's CTAs and their count.
+template <typename P>
+__device__ __forceinline__ const P &pipe_projection(const PipeMulti<P> &m, int32_t *cta, int32_t *ncta) {
+    int q = 0;
+    while (q + 1 < m.n_proj && static_cast<int32_t>(blockIdx.x) >= m.cta_begin[q + 1]) ++q;
+    *cta = static_cast<int32_t>(blockIdx.x) - m.cta_begin[q];
+    *ncta = m.cta_begin[q + 1] - m.cta_begin[q];
+    return m.proj[q];
+}
+
 // Work items u = (chunk, rank block jb, K slice kc), kc fastest; the CTA takes
 // items [u_lo, u_hi).  An item is streamed in stages of kShrStageK k: the
 // block's 16 A rows and the chunk's x rows.  Consumer warp w takes the
 // stage's 16-k steps w, w + 8, ...; at the item's last stage the warps' 16 x
 // 16 partial tiles are summed through shared memory and stored to plane kc.
-__global__ void __launch_bounds__(kPipeThreads, 1) pipe_shrink_kernel(const PipeShrinkParams p) {
+__global__ void __launch_bounds__(kPipeThreads, 1)
+pipe_shrink_kernel(const __grid_constant__ PipeMulti<PipeShrinkParams> pm) {
+    int32_t cta, ncta;
+    const PipeShrinkParams p = pipe_projection(pm, &cta, &ncta);  // in registers: read in the hot loops
     extern __shared__ __align__(128) uint8_t pipe_smem[];
     __shared__ GroupSmem gs;
     __shared__ __align__(8) uint64_t full[kShrStages], empty[kShrStages], redbar[2];
@@ -397,8 +423,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) pipe_shrink_kernel(const Pipe
     const int32_t total = cta_scan_inplace(gs.c_pre, C, gs.warp_tot);
     if (tid == 0) gs.c_pre[C] = total;
     __syncthreads();
-    const int32_t u_lo = static_cast<int32_t>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
-    const int32_t u_hi = static_cast<int32_t>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
+    const int32_t u_lo = static_cast<int32_t>(static_cast<int64_t>(cta) * total / ncta);
+    const int32_t u_hi = static_cast<int32_t>(static_cast<int64_t>(cta + 1) * total / ncta);
 
     if (warp == kPipeConsumerWarps) {
         // ---- producer warp: lanes 0-15 copy the A rows, lanes 16-31 the x rows
@@ -608,7 +634,10 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uin
 // 8, ... of the range: out[n, i] += B[n, 16 jb + j] V[i, 16 jb + j] as 16 x 8 x
 // 16 tiles for the chunk's two halves of 8 positions.  Items of rows without
 // an adapter (or with a corrupt block entry) write zeros.
-__global__ void __launch_bounds__(kExpThreads, 1) pipe_expand_kernel(const PipeExpandParams p) {
+__global__ void __launch_bounds__(kExpThreads, 1)
+pipe_expand_kernel(const __grid_constant__ PipeMulti<PipeExpandParams> pm) {
+    int32_t cta, ncta;
+    const PipeExpandParams p = pipe_projection(pm, &cta, &ncta);  // in registers: read in the hot loops
     extern __shared__ __align__(128) uint8_t pipe_smem[];
     __shared__ GroupSmem gs;
     __shared__ __align__(8) uint64_t full[kExpStages], empty[kExpStages], vempty[kExpMaxVSlots];
@@ -648,8 +677,8 @@ __global__ void __launch_bounds__(kExpThreads, 1) pipe_expand_kernel(const PipeE
     if (tid == 0) gs.c_pre[C] = wsum;
     __syncthreads();
     const int64_t total = static_cast<int64_t>(n_ranges) * wsum;
-    const int64_t c_lo = static_cast<int64_t>(blockIdx.x) * total / gridDim.x;
-    const int64_t c_hi = static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x;
+    const int64_t c_lo = static_cast<int64_t>(cta) * total / ncta;
+    const int64_t c_hi = static_cast<int64_t>(cta + 1) * total / ncta;
 
     if (warp == kExpWarps) {
         // ---- producer warp
@@ -1051,67 +1080,113 @@ cudaError_t launch_pipe_group(const ForwardPlan &plan, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, pipe_group_kernel, p);
 }
 
-cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
-    if (plan.M <= 0) return cudaSuccess;
-    if (!pipe_grouped_supported(plan.M, v.max_rank) || plan.v_parts < 1 || plan.v_parts > kMaxVPlanes)
-        return cudaErrorInvalidValue;
-    PipeShrinkParams p;
-    p.M = plan.M;
-    p.K = plan.K;
-    p.ldx = plan.ldx;
-    p.x = static_cast<const __nv_bfloat16 *>(plan.x);
-    p.row_slot = plan.row_slot;
-    p.a_arena = static_cast<const __nv_bfloat16 *>(v.a_arena);
-    p.table = v.table;
-    p.ranks = v.ranks;
-    p.max_slots = v.max_slots;
-    p.bps = v.bps;
-    p.num_blocks = v.num_blocks;
-    p.V = v.V;
-    p.ldv = v.max_rank;
-    // one item covers all of K (in kShrStageK stages), so V is one plane:
-    // the expand then fetches one V piece per item instead of one per slice
-    p.ksplit = 1;
-    p.kc_len = pipe_kc_len(plan.K, 1);
-    p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
-    p.counters = plan.counters;
-    p.n_counters = plan.n_counters;
-    p.group = pipe_group_of(plan, v);
-    if (!p.group) return cudaErrorInvalidValue;
-    p.status = plan.status;
-    return launch_pipe(pipe_shrink_kernel, p, kPipeThreads, kShrSmem, kShrSmem, stream);
+// Split the grid's CTAs between n projections by their weights (each gets
+// at least one; largest remainders take the rest).
+static bool split_ctas(const double *w, int n, int32_t ctas, int32_t *begin) {
+    if (n < 1 || n > LORA_MAX_PROJ || ctas < n) return false;
+    double total = 0.0;
+    for (int q = 0; q < n; ++q) total += w[q] > 0.0 ? w[q] : 0.0;
+    int32_t cnt[LORA_MAX_PROJ];
+    double rem[LORA_MAX_PROJ];
+    int32_t used = 0;
+    for (int q = 0; q < n; ++q) {
+        const double share = total > 0.0 ? (ctas - n) * (w[q] > 0.0 ? w[q] : 0.0) / total : 0.0;
+        cnt[q] = 1 + static_cast<int32_t>(share);
+        rem[q] = share - static_cast<int32_t>(share);
+        used += cnt[q];
+    }
+    while (used < ctas) {
+        int best = 0;
+        for (int q = 1; q < n; ++q)
+            if (rem[q] > rem[best]) best = q;
+        ++cnt[best];
+        rem[best] = -1.0;
+        ++used;
+    }
+    begin[0] = 0;
+    for (int q = 0; q < n; ++q) begin[q + 1] = begin[q] + cnt[q];
+    return begin[n] == ctas;
 }
 
-cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView &v, cudaStream_t stream) {
+cudaError_t launch_pipe_shrink(const ForwardPlan &plan, const ProjView *const *vs, int n, cudaStream_t stream) {
     if (plan.M <= 0) return cudaSuccess;
-    if (!pipe_grouped_supported(plan.M, v.max_rank) || plan.v_parts < 1 || plan.v_parts > kMaxVPlanes)
-        return cudaErrorInvalidValue;
-    PipeExpandParams p;
-    p.M = plan.M;
-    p.N = v.N;
-    p.row_slot = plan.row_slot;
-    p.b_arena = static_cast<const __nv_bfloat16 *>(v.b_arena);
-    p.table = v.table;
-    p.ranks = v.ranks;
-    p.scales = v.scales;
-    p.max_slots = v.max_slots;
-    p.bps = v.bps;
-    p.num_blocks = v.num_blocks;
-    p.V = v.V;
-    p.ldv = v.max_rank;
-    p.ksplit = 1;  // as the shrink writes it
-    p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
-    p.vslot_floats = kChunkRows * v.max_rank;
-    p.ycorr = v.ycorr;
-    p.group = pipe_group_of(plan, v);
-    if (!p.group) return cudaErrorInvalidValue;
-    p.status = plan.status;
-    const size_t vbytes = sizeof(float) * static_cast<size_t>(p.vslot_floats);
+    if (n < 1 || n > LORA_MAX_PROJ || plan.v_parts < 1 || plan.v_parts > kMaxVPlanes) return cudaErrorInvalidValue;
+    PipeMulti<PipeShrinkParams> m = {};
+    m.n_proj = n;
+    double w[LORA_MAX_PROJ];
+    for (int q = 0; q < n; ++q) {
+        const ProjView &v = *vs[q];
+        if (!pipe_grouped_supported(plan.M, v.max_rank)) return cudaErrorInvalidValue;
+        PipeShrinkParams &p = m.proj[q];
+        p.M = plan.M;
+        p.K = plan.K;
+        p.ldx = plan.ldx;
+        p.x = static_cast<const __nv_bfloat16 *>(plan.x);
+        p.row_slot = plan.row_slot;
+        p.a_arena = static_cast<const __nv_bfloat16 *>(v.a_arena);
+        p.table = v.table;
+        p.ranks = v.ranks;
+        p.max_slots = v.max_slots;
+        p.bps = v.bps;
+        p.num_blocks = v.num_blocks;
+        p.V = v.V;
+        p.ldv = v.max_rank;
+        // one item covers all of K (in kShrStageK stages), so V is one plane:
+        // the expand then fetches one V piece per item instead of one per slice
+        p.ksplit = 1;
+        p.kc_len = pipe_kc_len(plan.K, 1);
+        p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
+        p.counters = plan.counters;
+        p.n_counters = plan.n_counters;
+        p.group = pipe_group_of(plan, v);
+        if (!p.group) return cudaErrorInvalidValue;
+        p.status = plan.status;
+        w[q] = static_cast<double>(v.max_rank);  // the A bytes a row's adapter brings, at most
+    }
+    if (!split_ctas(w, n, device_sm_count(), m.cta_begin)) return cudaErrorInvalidValue;
+    return launch_pipe(pipe_shrink_kernel, m, kPipeThreads, kShrSmem, kShrSmem, stream);
+}
+
+cudaError_t launch_pipe_expand(const ForwardPlan &plan, const ProjView *const *vs, int n, cudaStream_t stream) {
+    if (plan.M <= 0) return cudaSuccess;
+    if (n < 1 || n > LORA_MAX_PROJ || plan.v_parts < 1 || plan.v_parts > kMaxVPlanes) return cudaErrorInvalidValue;
+    PipeMulti<PipeExpandParams> m = {};
+    m.n_proj = n;
+    double w[LORA_MAX_PROJ];
+    size_t smem = 0;
     const size_t room = kExpSmemMax - static_cast<size_t>(kExpStages) * kExpStageBytes;
-    p.n_vslots = static_cast<int32_t>(room / vbytes < kExpMaxVSlots ? room / vbytes : kExpMaxVSlots);
-    if (p.n_vslots < 2) return cudaErrorInvalidValue;
-    const size_t smem = static_cast<size_t>(kExpStages) * kExpStageBytes + p.n_vslots * vbytes;
-    return launch_pipe(pipe_expand_kernel, p, kExpThreads, smem, kExpSmemMax, stream);
+    for (int q = 0; q < n; ++q) {
+        const ProjView &v = *vs[q];
+        if (!pipe_grouped_supported(plan.M, v.max_rank)) return cudaErrorInvalidValue;
+        PipeExpandParams &p = m.proj[q];
+        p.M = plan.M;
+        p.N = v.N;
+        p.row_slot = plan.row_slot;
+        p.b_arena = static_cast<const __nv_bfloat16 *>(v.b_arena);
+        p.table = v.table;
+        p.ranks = v.ranks;
+        p.scales = v.scales;
+        p.max_slots = v.max_slots;
+        p.bps = v.bps;
+        p.num_blocks = v.num_blocks;
+        p.V = v.V;
+        p.ldv = v.max_rank;
+        p.ksplit = 1;  // as the shrink writes it
+        p.plane_stride = static_cast<size_t>(plan.M) * v.max_rank;
+        p.vslot_floats = kChunkRows * v.max_rank;
+        p.ycorr = v.ycorr;
+        p.group = pipe_group_of(plan, v);
+        if (!p.group) return cudaErrorInvalidValue;
+        p.status = plan.status;
+        const size_t vbytes = sizeof(float) * static_cast<size_t>(p.vslot_floats);
+        p.n_vslots = static_cast<int32_t>(room / vbytes < kExpMaxVSlots ? room / vbytes : kExpMaxVSlots);
+        if (p.n_vslots < 2) return cudaErrorInvalidValue;
+        const size_t need = static_cast<size_t>(kExpStages) * kExpStageBytes + p.n_vslots * vbytes;
+        smem = need > smem ? need : smem;
+        w[q] = static_cast<double>(v.N) * v.max_rank;  // the B bytes a row's adapter brings, at most
+    }
+    if (!split_ctas(w, n, device_sm_count(), m.cta_begin)) return cudaErrorInvalidValue;
+    return launch_pipe(pipe_expand_kernel, m, kExpThreads, smem, kExpSmemMax, stream);
 }
 
 }  // namespace lora
