@@ -382,8 +382,10 @@ __device__ __forceinline__ const P &pipe_projection(const PipeMulti<P> &m, int32
     return m.proj[q];
 }
 
-// Work items u = (chunk, rank block jb, K slice kc), kc fastest; the CTA takes
-// items [u_lo, u_hi).  An item is streamed in stages of kShrStageK k: the
+// Work items u = (chunk, rank block jb, K slice kc), kc fastest, each costing
+// the row copies of its stages (16 A rows and the chunk's x rows); the CTA
+// takes the items whose cost starts in its equal share.  An item is streamed
+// in stages of kShrStageK k: the
 // block's 16 A rows and the chunk's x rows.  Consumer warp w takes the
 // stage's 16-k steps w, w + 8, ...; at the item's last stage the warps' 16 x
 // 16 partial tiles are summed through shared memory and stored to plane kc.
@@ -418,40 +420,52 @@ pipe_shrink_kernel(const __grid_constant__ PipeMulti<PipeShrinkParams> pm) {
     }
     load_group_table(gs, p.group, p.M);
     const int32_t C = gs.n_chunks;
-    for (int32_t c = tid; c < C; c += kPipeThreads) gs.c_pre[c] = gs.c_nblk[c] * p.ksplit;
+    // an item's cost: the row copies of its stages, the block's 16 A rows
+    // and the chunk's x rows
+    for (int32_t c = tid; c < C; c += kPipeThreads)
+        gs.c_pre[c] = gs.c_nblk[c] * p.ksplit * (LORA_BLOCK_ROWS + gs.c_begin[c + 1] - gs.c_begin[c]);
     __syncthreads();
     const int32_t total = cta_scan_inplace(gs.c_pre, C, gs.warp_tot);
     if (tid == 0) gs.c_pre[C] = total;
     __syncthreads();
-    const int32_t u_lo = static_cast<int32_t>(static_cast<int64_t>(cta) * total / ncta);
-    const int32_t u_hi = static_cast<int32_t>(static_cast<int64_t>(cta + 1) * total / ncta);
+    // this CTA's items: those whose cost starts in [w_lo, w_hi)
+    const int64_t w_lo = static_cast<int64_t>(cta) * total / ncta;
+    const int64_t w_hi = static_cast<int64_t>(cta + 1) * total / ncta;
 
     if (warp == kPipeConsumerWarps) {
         // ---- producer warp: lanes 0-15 copy the A rows, lanes 16-31 the x rows
-        int32_t ch = 0;
-        {
-            int32_t lo = 0, hi = C - 1;  // the last chunk with c_pre <= u_lo holds item u_lo
+        int32_t ch = 0, i = 0;  // the chunk of the CTA's first item and the item's index in it
+        if (C > 0) {
+            int32_t lo = 0, hi = C - 1;  // the last chunk whose cost starts at or before w_lo
             while (lo < hi) {
                 const int32_t mid = (lo + hi + 1) >> 1;
-                if (gs.c_pre[mid] <= u_lo) lo = mid;
+                if (gs.c_pre[mid] <= w_lo) lo = mid;
                 else hi = mid - 1;
             }
             ch = lo;
+            const int32_t w = LORA_BLOCK_ROWS + gs.c_begin[ch + 1] - gs.c_begin[ch];
+            i = static_cast<int32_t>((w_lo - gs.c_pre[ch] + w - 1) / w);
         }
         int32_t it = 0;
         bool ok = true;
-        int32_t cur_ch = -1, blk_lane = 0, blk_next = chunk_block_id(gs, ch, C, p.table, p.bps, lane);
-        for (int32_t u = u_lo; u < u_hi && ok; ++u) {
-            while (gs.c_pre[ch + 1] <= u) ++ch;
-            if (ch != cur_ch) {  // a new chunk: its ids were loaded one chunk ago
-                if (ch == cur_ch + 1 || cur_ch < 0) blk_lane = blk_next;
-                else blk_lane = chunk_block_id(gs, ch, C, p.table, p.bps, lane);
-                cur_ch = ch;
-                blk_next = chunk_block_id(gs, ch + 1, C, p.table, p.bps, lane);
-            }
-            const int32_t local = u - gs.c_pre[ch];
-            const int32_t jb = local / p.ksplit, kc = local - jb * p.ksplit;
+        // blk_next: the block ids of chunk next_ch, loaded one chunk ahead
+        int32_t cur_ch = -1, blk_lane = 0, next_ch = ch, blk_next = chunk_block_id(gs, ch, C, p.table, p.bps, lane);
+        while (ok && ch < C) {
             const int32_t p0 = gs.c_begin[ch], R = gs.c_begin[ch + 1] - p0;
+            if (i >= gs.c_nblk[ch] * p.ksplit) {  // past the chunk's items (none for rows without an adapter)
+                ++ch;
+                i = 0;
+                continue;
+            }
+            if (gs.c_pre[ch] + static_cast<int64_t>(i) * (LORA_BLOCK_ROWS + R) >= w_hi) break;
+            const int32_t local = i++;
+            if (ch != cur_ch) {  // a new chunk: its ids were loaded one chunk ago, unless chunks were skipped
+                blk_lane = ch == next_ch ? blk_next : chunk_block_id(gs, ch, C, p.table, p.bps, lane);
+                cur_ch = ch;
+                next_ch = ch + 1;
+                blk_next = chunk_block_id(gs, next_ch, C, p.table, p.bps, lane);
+            }
+            const int32_t jb = local / p.ksplit, kc = local - jb * p.ksplit;
             const int32_t blk = __shfl_sync(0xffffffffu, blk_lane, jb);
             if (blk < 0 || blk >= p.num_blocks) continue;  // reported by the expand, which zeroes these rows
             const int32_t xr = lane - LORA_BLOCK_ROWS;
